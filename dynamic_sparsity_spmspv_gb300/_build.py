@@ -1,0 +1,69 @@
+"""Builds libdbspmspv.so in-tree (dynamic_sparsity_spmspv_gb300/_build/).
+
+nvcc compiles the CUDA translation unit for sm_103a only; g++ compiles the
+host builder; both run in parallel and nvcc links the shared library against
+the static CUDA runtime.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(PKG, "csrc")
+OUT = os.path.join(PKG, "_build")
+LIB = os.path.join(OUT, "libdbspmspv.so")
+INCLUDE = os.path.join(os.path.dirname(PKG), "include")
+
+CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+SOURCES_CU = ["kernels.cu"]
+SOURCES_CPP = ["matrix.cpp"]
+HEADERS = ["format.h", "internal.h"]
+
+
+def _newest_input() -> float:
+    paths = [os.path.join(CSRC, f) for f in SOURCES_CU + SOURCES_CPP + HEADERS]
+    paths.append(os.path.join(INCLUDE, "dbspmspv.h"))
+    return max(os.path.getmtime(p) for p in paths)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    os.makedirs(OUT, exist_ok=True)
+    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
+        return LIB
+    procs = []
+    objs = []
+    for src in SOURCES_CU:
+        obj = os.path.join(OUT, src + ".o")
+        cmd = [NVCC, *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
+               "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+        objs.append(obj)
+    for src in SOURCES_CPP:
+        obj = os.path.join(OUT, src + ".o")
+        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-pthread", "-Wall", "-I", INCLUDE,
+               "-I", os.path.join(CUDA_HOME, "include"), "-c", os.path.join(CSRC, src), "-o", obj]
+        procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+        objs.append(obj)
+    failed = []
+    for cmd, p in procs:
+        out, _ = p.communicate()
+        if verbose or p.returncode != 0:
+            print(out.decode(errors="replace"))
+        if p.returncode != 0:
+            failed.append(" ".join(cmd))
+    if failed:
+        raise RuntimeError("dbspmspv build failed:\n" + "\n".join(failed))
+    tmp = LIB + f".tmp{os.getpid()}"
+    subprocess.check_call([NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-lpthread"])
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force=True, verbose=True))

@@ -1,0 +1,47 @@
+// Internal structures of the dbspmspv library (not part of the C ABI).
+#pragma once
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/dbspmspv.h"
+#include "format.h"
+
+namespace dbs {
+
+struct alignas(8) U2 { uint32_t x, y; };
+struct alignas(16) U4 { uint32_t x, y, z, w; };
+
+// Host copy of the blocked format (kept with keep_host or host_only).
+struct HostFormat {
+    std::vector<uint32_t> rb_ptr;     // nbr + 1
+    std::vector<U2> blk_desc;         // B: {col block, meta}
+    std::vector<uint32_t> blk_ref;    // B
+    std::vector<uint32_t> cb_ptr;     // nbc + 1
+    std::vector<U2> csc_desc;         // B: {row block, meta}
+    std::vector<uint32_t> csc_ref;    // B
+    std::vector<uint32_t> csc2csr;    // B (host only)
+    std::vector<U4> payload;          // P
+    std::vector<U4> tiles;            // T: {p0, p1, rb0, span}
+};
+
+}  // namespace dbs
+
+struct dbs_matrix {
+    int64_t m = 0, n = 0, nnz = 0;
+    int64_t nbr = 0, nbc = 0, B = 0, P = 0, T = 0;
+    bool valued = false;
+    bool on_device = false;
+    int device = -1;
+    // device copies (NULL when host_only)
+    uint32_t *d_rb_ptr = nullptr;
+    dbs::U2 *d_blk_desc = nullptr;
+    uint32_t *d_blk_ref = nullptr;
+    uint32_t *d_cb_ptr = nullptr;
+    dbs::U2 *d_csc_desc = nullptr;
+    uint32_t *d_csc_ref = nullptr;
+    dbs::U4 *d_payload = nullptr;
+    dbs::U4 *d_tiles = nullptr;
+    dbs::HostFormat *host = nullptr;
+    dbs_matrix_info info{};
+};

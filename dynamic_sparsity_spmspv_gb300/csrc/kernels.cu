@@ -1,0 +1,1277 @@
+// CUDA kernels (sm_103a) and the execution part of the C ABI: workspace,
+// SpMSpV with sparse or dense x, DB-BFS, statistics, self-test.
+//
+// DB-SpMSpV (Cong et al., ICPP '26):
+//   4.1      vector metadata on the GPU: blk_x_mask per 16-element block and
+//            the nonzero-block count, joined to the SpMSpV by a grid-level
+//            barrier inside one launch (no host round trip);
+//   3.3.1    high-level path: push iff N_nzblk / N_blk < th3, decided on the
+//            device; low-level microkernel from block type and blk_x_mask;
+//   3.3.2    push: matrix-block tasks flattened over the active column blocks
+//            (a warp takes 32 CSC positions); pull: load-weighted tiles of
+//            consecutive primary blocks, one CTA each;
+//   3.3.3    hierarchical writeback: microkernel registers / warp shuffles ->
+//            shared-memory row accumulators -> global;
+//   Alg. 2   ForceCSR row-wise microkernel (two lanes per row);
+//   Alg. 3   ForceCSC column-wise microkernel (half-warps over column ranges);
+//   Alg. 4   Dense microkernel -- here over a column-major block, so pull and
+//            push both read only the active columns' 64-byte runs;
+//   Alg. 5   Boolean reachability with the visited mask; here one lane per
+//            block computes the found-row mask with bit operations;
+//   4.2      DB-BFS: the level loop runs inside one cooperative launch.
+//
+// Every device-side wait is a grid barrier with a time bound; on expiry the
+// kernel latches DBS_ERR_TIMEOUT in the workspace and returns.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <new>
+
+#include "internal.h"
+
+using namespace dbs;
+
+namespace {
+
+constexpr int NT = 256;              // threads per CTA
+constexpr int NW = NT / 32;          // warps per CTA
+constexpr uint32_t FULL = 0xFFFFFFFFu;
+constexpr uint32_t HEAVY_CAP = 1040; // heavy blocks per pull tile (weight cap 2048 / 2 + slack)
+constexpr uint32_t CTILE = 4096;     // row blocks per compaction tile (256 threads x 16)
+
+struct Ctrl {
+    unsigned int bar_count;
+    unsigned int bar_gen;
+    unsigned int err;
+    unsigned int path;
+    unsigned int n_act[3];
+    unsigned int n_chunk[3];
+    unsigned int tile_next[3];
+    unsigned int bfs_levels;
+    unsigned int bfs_push_levels;
+    unsigned int pad0;
+    unsigned long long x_active;
+    unsigned long long visited;
+    unsigned long long hits;
+    unsigned long long touched;
+    unsigned long long bytes;
+    unsigned long long nzblk;
+    unsigned long long y_nnz;
+    unsigned long long reached;
+};
+
+struct KParams {
+    // matrix
+    int32_t m, n, nbr, nbc;
+    uint32_t B, T;
+    int valued;
+    const uint32_t *__restrict__ rb_ptr;
+    const uint2 *__restrict__ blk_desc;
+    const uint32_t *__restrict__ blk_ref;
+    const uint32_t *__restrict__ cb_ptr;
+    const uint2 *__restrict__ csc_desc;
+    const uint32_t *__restrict__ csc_ref;
+    const uint4 *__restrict__ payload;
+    const uint4 *__restrict__ tiles;
+    // call
+    int path_force;
+    const int32_t *x_idx;
+    const float *x_val;
+    long long x_nnz;
+    const float *x_in;        // dense x (dense mode)
+    const float *xv;          // x values read by the microkernels
+    const uint32_t *uvis32;   // caller's visited mask (Boolean SpMSpV), or NULL
+    int32_t *y_idx;
+    float *y_val;
+    long long *y_nnz;
+    float *y_dense;
+    long long bfs_src;
+    int32_t *levels;
+    // workspace
+    float *x_dense;
+    uint32_t *xm32;
+    uint32_t *act[3];
+    uint2 *chunks[3];
+    float *y_acc;
+    uint32_t *yrm32;
+    uint32_t *ctile_cnt;
+    uint32_t n_ctiles;
+    uint32_t *bvis32;
+    uint32_t *fm32[2];
+    Ctrl *ctrl;
+    int slot;                 // counter slot of this call (dense mode alternates 0/1)
+    double th3;
+    int local_pull_min;
+    int stats;
+    long long timeout_ns;
+};
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(unsigned *p, unsigned v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ unsigned ld_cg(const unsigned *p) { return __ldcg(p); }
+
+// 16-bit block masks packed two per 32-bit word (block b in word b >> 1).
+__device__ __forceinline__ uint32_t mask16(const uint32_t *w, uint32_t b)
+{
+    return (__ldcg(w + (b >> 1)) >> ((b & 1u) << 4)) & 0xFFFFu;
+}
+__device__ __forceinline__ uint32_t or16(uint32_t *w, uint32_t b, uint32_t bits)
+{
+    uint32_t sh = (b & 1u) << 4;
+    return (atomicOr(w + (b >> 1), bits << sh) >> sh) & 0xFFFFu;
+}
+
+// Bounded grid barrier.  Returns false (and every caller must return) when
+// the wait timed out or another block latched an error.
+__device__ bool grid_sync(const KParams &P)
+{
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Ctrl *c = P.ctrl;
+        int ok = 1;
+        unsigned gen = ld_acquire(&c->bar_gen);
+        __threadfence();
+        unsigned arrived = atomicAdd(&c->bar_count, 1u);
+        if (arrived == gridDim.x - 1) {
+            atomicExch(&c->bar_count, 0u);
+            __threadfence();
+            st_release(&c->bar_gen, gen + 1);
+        } else {
+            unsigned long long t0 = globaltimer();
+            unsigned ns = 32;
+            while (ld_acquire(&c->bar_gen) == gen) {
+                if (ld_cg(&c->err) != 0u) { ok = 0; break; }
+                if ((long long)(globaltimer() - t0) > P.timeout_ns) {
+                    atomicCAS(&c->err, 0u, (unsigned)DBS_ERR_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(ns);
+                if (ns < 1024) ns <<= 1;
+            }
+        }
+        if (ok && ld_cg(&c->err) != 0u) ok = 0;
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+__device__ __forceinline__ void latch_error(const KParams &P, unsigned code)
+{
+    atomicCAS(&P.ctrl->err, 0u, code);
+}
+
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_up_sync(FULL, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+// Block-wide exclusive scan of one value per thread; returns the prefix and
+// stores the total in *total.  All threads must call it.
+__device__ uint32_t block_excl_scan(uint32_t v, uint32_t *total)
+{
+    __shared__ uint32_t s_w[NW];
+    __shared__ uint32_t s_tot;
+    int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t inc = warp_incl_scan(v, lane);
+    if (lane == 31) s_w[w] = inc;
+    __syncthreads();
+    if (w == 0) {
+        uint32_t x = lane < NW ? s_w[lane] : 0u;
+        uint32_t xi = warp_incl_scan(x, lane);
+        if (lane < NW) s_w[lane] = xi - x;
+        if (lane == NW - 1) s_tot = xi;
+    }
+    __syncthreads();
+    uint32_t r = s_w[w] + inc - v;
+    *total = s_tot;
+    __syncthreads();
+    return r;
+}
+
+// Appends column block cb to the active list of `slot` and its CSC range to
+// the push task list (32 positions per task): the flattened matrix-block
+// tasks of Section 3.3.2.
+__device__ void append_active(const KParams &P, int slot, uint32_t cb)
+{
+    Ctrl *c = P.ctrl;
+    uint32_t i = atomicAdd(&c->n_act[slot], 1u);
+    P.act[slot][i] = cb;
+    uint32_t s = __ldg(P.cb_ptr + cb), e = __ldg(P.cb_ptr + cb + 1);
+    if (e <= s) return;
+    uint32_t nch = (e - s + PUSH_CHUNK - 1) / PUSH_CHUNK;
+    uint32_t base = atomicAdd(&c->n_chunk[slot], nch);
+    for (uint32_t k = 0; k < nch; ++k) P.chunks[slot][base + k] = make_uint2(s + k * PUSH_CHUNK, cb);
+}
+
+// ------------------------------------------------------------ microkernels
+// fp32 warp microkernels: the whole warp works on one block with uniform
+// arguments; on return lane l (and l + 16) holds row (l & 15)'s partial sum
+// and whether that row met an active entry.
+
+struct RowOut {
+    float sum;
+    uint32_t touched;
+};
+
+// x values: a generic load, because push passes the vector block cached in
+// shared memory and pull passes global memory written earlier in the launch
+// (never read before that point, so no stale L1 line can exist).
+__device__ __forceinline__ float xval(const float *xb, uint32_t c) { return xb[c]; }
+
+// Algorithm 3 structure (column-organised payloads: Dense, ForceCSC): lane
+// (row r, half h) walks the active columns of its half.
+template <uint32_t FMT>
+__device__ __forceinline__ RowOut mk_colwise(const uint8_t *__restrict__ b, uint32_t nnz, uint32_t act,
+                                             const float *xb, int lane, uint32_t *nread)
+{
+    const uint32_t r = lane & 15, h = lane >> 4;
+    const uint16_t *cmask = reinterpret_cast<const uint16_t *>(b + (FMT == FMT_DENSE ? 0u : OFF_MASK));
+    const float *vals = reinterpret_cast<const float *>(b + val_offset(FMT, nnz));
+    uint32_t a = act & (h ? 0xFF00u : 0x00FFu);
+    float sum = 0.0f;
+    uint32_t t = 0, cnt = 0;
+    while (a) {
+        uint32_t c = __ffs(a) - 1u;
+        a &= a - 1u;
+        uint32_t cm = __ldg(cmask + c);
+        if ((cm >> r) & 1u) {
+            uint32_t idx = FMT == FMT_DENSE ? c * 16u + r : (uint32_t)__ldg(b + OFF_PTR + c) + __popc(cm & ((1u << r) - 1u));
+            sum = fmaf(__ldg(vals + idx), xval(xb, c), sum);
+            t = 1u;
+            ++cnt;
+        }
+    }
+    sum += __shfl_xor_sync(FULL, sum, 16);
+    t |= __shfl_xor_sync(FULL, t, 16);
+    *nread = cnt;
+    return RowOut{sum, t};
+}
+
+// Algorithm 2 (row-organised payloads: ForceCSR, patched CSR in pull mode):
+// two lanes per row take alternate active entries; results move to lane r.
+template <uint32_t FMT>
+__device__ __forceinline__ RowOut mk_rowwise(const uint8_t *__restrict__ b, uint32_t nnz, uint32_t act,
+                                             const float *xb, int lane, uint32_t *nread)
+{
+    const uint32_t row = lane >> 1, sub = lane & 1;
+    const uint32_t rm = __ldg(reinterpret_cast<const uint16_t *>(b + OFF_MASK) + row);
+    const uint32_t base = __ldg(b + OFF_PTR + row);
+    const float *vals = reinterpret_cast<const float *>(b + val_offset(FMT, nnz));
+    uint32_t a = rm & act, k = 0, cnt = 0;
+    float sum = 0.0f;
+    while (a) {
+        uint32_t c = __ffs(a) - 1u;
+        if ((k & 1u) == sub) {
+            uint32_t off = __popc(rm & ((1u << c) - 1u));
+            sum = fmaf(__ldg(vals + base + off), xval(xb, c), sum);
+            ++cnt;
+        }
+        a &= a - 1u;
+        ++k;
+    }
+    sum += __shfl_xor_sync(FULL, sum, 1);
+    uint32_t t = (rm & act) != 0u;
+    const int src = (lane & 15) << 1;
+    float s2 = __shfl_sync(FULL, sum, src);
+    uint32_t t2 = __shfl_sync(FULL, t, src);
+    *nread = cnt;
+    return RowOut{s2, t2};
+}
+
+// Patched CSR in push mode (Section 3.3.3): for each active column walk its
+// row_idx_csc2csr bytes (row, offset within the row) and read the value from
+// the row-ordered array; two columns per step (one per half-warp).
+__device__ __forceinline__ RowOut mk_pcsr_col(const uint8_t *__restrict__ b, uint32_t nnz, uint32_t act,
+                                              const float *xb, int lane, float *wacc, uint32_t *nread)
+{
+    if (lane < 16) wacc[lane] = 0.0f;
+    __syncwarp();
+    const float *vals = reinterpret_cast<const float *>(b + val_offset(FMT_PCSR, nnz));
+    uint32_t a = act, rows = 0, cnt = 0;
+    const uint32_t h = lane >> 4, l = lane & 15;
+    while (a) {
+        uint32_t c0 = __ffs(a) - 1u;
+        a &= a - 1u;
+        uint32_t c1 = a ? __ffs(a) - 1u : 16u;
+        if (a) a &= a - 1u;
+        uint32_t c = h ? c1 : c0;
+        if (c < 16u) {
+            uint32_t s = __ldg(b + OFF_PCOLPTR + c);
+            uint32_t e = c == 15u ? nnz : (uint32_t)__ldg(b + OFF_PCOLPTR + c + 1);
+            uint32_t k = s + l;
+            if (k < e) {
+                uint32_t code = __ldg(b + OFF_RCSC + k);
+                uint32_t row = code >> 4, off = code & 15u;
+                float v = __ldg(vals + __ldg(b + OFF_PTR + row) + off) * xval(xb, c);
+                atomicAdd(&wacc[row], v);
+                rows |= 1u << row;
+                ++cnt;
+            }
+        }
+    }
+    __syncwarp();
+    rows = __reduce_or_sync(FULL, rows);
+    float s = wacc[lane & 15];
+    __syncwarp();
+    *nread = cnt;
+    return RowOut{s, (rows >> (lane & 15)) & 1u};
+}
+
+// Dispatch of the fp32 warp microkernel for a non-COO block (Section 3.3.1:
+// by blocks_type and blk_x_mask).
+__device__ __forceinline__ RowOut mk_heavy(const KParams &P, const uint8_t *b, uint32_t meta, uint32_t act,
+                                           const float *xb, int lane, float *wacc, uint32_t *bytes)
+{
+    const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
+    uint32_t nr = 0;
+    RowOut o;
+    uint32_t fixed;
+    if (fmt == FMT_DENSE) { o = mk_colwise<FMT_DENSE>(b, nnz, act, xb, lane, &nr); fixed = 32; }
+    else if (fmt == FMT_FCSC) { o = mk_colwise<FMT_FCSC>(b, nnz, act, xb, lane, &nr); fixed = 48; }
+    else if (fmt == FMT_FCSR) { o = mk_rowwise<FMT_FCSR>(b, nnz, act, xb, lane, &nr); fixed = 48; }
+    else if ((int)__popc(act) >= P.local_pull_min) { o = mk_rowwise<FMT_PCSR>(b, nnz, act, xb, lane, &nr); fixed = 48; }
+    else { o = mk_pcsr_col(b, nnz, act, xb, lane, wacc, &nr); fixed = 64; nr *= 2; /* rcsc byte + value */ }
+    if (P.stats) {
+        uint32_t tot = __reduce_add_sync(FULL, nr);
+        // Dense reads whole 64-byte column runs; the others read values and codes
+        *bytes = fixed + (fmt == FMT_DENSE ? 64u * __popc(act) : 4u * tot);
+    }
+    return o;
+}
+
+// COO block, one lane: scan the packed coordinates (Section 3.3.3).  Adds the
+// products through `add(row, value)` and returns the touched-row bits.
+template <class Add>
+__device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint32_t nnz, uint32_t act,
+                                            const float *xb, bool valued, Add add)
+{
+    const float *vals = reinterpret_cast<const float *>(b + val_offset(FMT_COO, nnz));
+    uint32_t rows = 0;
+    for (uint32_t k = 0; k < nnz; ++k) {
+        uint32_t e = __ldg(b + k);
+        uint32_t c = e & 15u;
+        if ((act >> c) & 1u) {
+            uint32_t r = e >> 4;
+            rows |= 1u << r;
+            if (valued) add(r, __ldg(vals + k) * xval(xb, c));
+        }
+    }
+    return rows;
+}
+
+// Boolean microkernel, one lane (Algorithm 5 semantics): the rows of the
+// block reached from its active columns.
+__device__ __forceinline__ uint32_t bool_found(const uint8_t *__restrict__ b, uint32_t meta, uint32_t act)
+{
+    const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
+    uint32_t f = 0;
+    if (fmt == FMT_COO) {
+        for (uint32_t k = 0; k < nnz; ++k) {
+            uint32_t e = __ldg(b + k);
+            if ((act >> (e & 15u)) & 1u) f |= 1u << (e >> 4);
+        }
+    } else {
+        const uint4 *m4 = reinterpret_cast<const uint4 *>(b + (fmt == FMT_DENSE ? 0u : OFF_MASK));
+        uint4 lo = __ldg(m4), hi = __ldg(m4 + 1);
+        uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        if (fmt == FMT_DENSE || fmt == FMT_FCSC) {          // column masks: OR the active columns
+            uint32_t a = act;
+            while (a) {
+                uint32_t c = __ffs(a) - 1u;
+                a &= a - 1u;
+                f |= (w[c >> 1] >> ((c & 1u) << 4)) & 0xFFFFu;
+            }
+        } else {                                            // row masks: rows meeting an active column
+#pragma unroll
+            for (uint32_t r = 0; r < 16; ++r)
+                if ((w[r >> 1] >> ((r & 1u) << 4)) & act) f |= 1u << r;
+        }
+    }
+    return f;
+}
+
+__device__ __forceinline__ uint32_t bool_bytes(uint32_t meta)
+{
+    uint32_t fmt = meta_fmt(meta);
+    return fmt == FMT_COO ? meta_nnz(meta) : 32u;
+}
+
+// ------------------------------------------------------------- traversal
+
+struct Smem {
+    uint32_t rbp[TILE_MAX_SPAN + 1];
+    float y[TILE_MAX_SPAN * 16];
+    uint32_t rm[TILE_MAX_SPAN];
+    uint32_t vis[TILE_MAX_SPAN];
+    uint4 heavy[HEAVY_CAP];
+    float wacc[NW][16];
+    float wx[NW][16];
+    uint32_t nheavy;
+    uint32_t tile;
+    unsigned long long st[4];   // visited, hits, touched, bytes
+};
+
+__device__ __forceinline__ void stat_add(Smem &S, int i, unsigned long long v)
+{
+    if (v) atomicAdd(&S.st[i], v);
+}
+
+// Pull (Section 3.3.2): CTAs take tiles of consecutive primary blocks.
+// SR 0 = plus-times, 1 = Boolean.  DOUT: dense output y.  BFS: first touch
+// of a next-frontier row block appends it to the list of slot `nslot`.
+template <int SR, bool DOUT, bool BFS>
+__device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const uint32_t *vis,
+                           uint32_t *out_rm, int tslot, int nslot)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float *xv = P.xv;
+    for (;;) {
+        if (tid == 0) S.tile = atomicAdd(&P.ctrl->tile_next[tslot], 1u);
+        __syncthreads();
+        const uint32_t t = S.tile;
+        if (t >= P.T) break;
+        const uint4 td = __ldg(P.tiles + t);
+        const uint32_t p0 = td.x, p1 = td.y, rb0 = td.z, span = td.w;
+        if (tid <= (int)span) S.rbp[tid] = __ldg(P.rb_ptr + rb0 + tid);
+        for (uint32_t i = tid; i < span * 16u; i += NT) S.y[i] = 0.0f;
+        if (tid < (int)span) {
+            S.rm[tid] = 0u;
+            S.vis[tid] = vis ? mask16(vis, rb0 + tid) : 0u;
+        }
+        if (tid == 0) S.nheavy = 0u;
+        __syncthreads();
+
+        // Stage 1: scan the tile's block descriptors, test them against the
+        // vector-block masks, run COO / Boolean blocks in place, queue the rest.
+        unsigned long long c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
+        for (uint32_t p = p0 + tid; p < p1; p += NT) {
+            uint32_t lo = 0, hi = span - 1u;
+            while (lo < hi) {
+                uint32_t mid = (lo + hi + 1u) >> 1;
+                if (S.rbp[mid] <= p) lo = mid; else hi = mid - 1u;
+            }
+            const uint32_t lrb = lo;
+            if (SR == 1 && S.vis[lrb] == 0xFFFFu) continue;   // row block fully visited
+            const uint2 d = __ldg(P.blk_desc + p);
+            const uint32_t col = d.x, meta = d.y;
+            const uint32_t xmb = mask16(xm, col);
+            c_bytes += 8;
+            if (!xmb) continue;
+            ++c_vis;
+            c_touch += meta_nnz(meta);
+            const uint32_t act = meta_cmask(meta) & xmb;
+            if (!act) continue;
+            ++c_hit;
+            const uint32_t ref = __ldg(P.blk_ref + p);
+            const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + ref);
+            c_bytes += 4;
+            if (SR == 1) {
+                uint32_t f = bool_found(b, meta, act);
+                if (f) atomicOr(&S.rm[lrb], f);
+                c_bytes += bool_bytes(meta);
+            } else if (meta_fmt(meta) == FMT_COO) {
+                const uint32_t nnz = meta_nnz(meta);
+                float *sy = &S.y[lrb * 16u];
+                uint32_t rows = coo_lane(b, nnz, act, xv + (size_t)col * 16u, true,
+                                         [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
+                if (rows) atomicOr(&S.rm[lrb], rows);
+                c_bytes += val_offset(FMT_COO, nnz) + 4u * nnz;
+            } else {
+                uint32_t slot = atomicAdd(&S.nheavy, 1u);
+                if (slot < HEAVY_CAP) S.heavy[slot] = make_uint4(ref, meta, col, lrb);
+                else latch_error(P, DBS_ERR_INTERNAL);
+            }
+        }
+        __syncthreads();
+
+        // Stage 2 (plus-times): warps run the queued blocks' microkernels.
+        if (SR == 0) {
+            const uint32_t nh = min(S.nheavy, HEAVY_CAP);
+            for (uint32_t i = warp; i < nh; i += NW) {
+                const uint4 h = S.heavy[i];
+                const uint32_t act = meta_cmask(h.y) & mask16(xm, h.z);
+                uint32_t by = 0;
+                RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + h.x), h.y, act,
+                                    xv + (size_t)h.z * 16u, lane, S.wacc[warp], &by);
+                if (lane < 16 && o.touched) atomicAdd(&S.y[h.w * 16u + lane], o.sum);
+                uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
+                if (lane == 0) {
+                    if (bits) atomicOr(&S.rm[h.w], bits);
+                    c_bytes += by;
+                }
+            }
+            __syncthreads();
+        }
+
+        // Stage 3: write the tile's row blocks back.  A row block entirely
+        // inside the tile is stored; one shared with a neighbour tile is added.
+        for (uint32_t i = tid; i < span * 16u; i += NT) {
+            const uint32_t lrb = i >> 4, r = i & 15u, rb = rb0 + lrb;
+            const uint32_t rm = S.rm[lrb];
+            const bool partial = S.rbp[lrb] < p0 || S.rbp[lrb + 1] > p1;
+            if (SR == 0) {
+                if ((rm >> r) & 1u) {
+                    float *dst = DOUT ? P.y_dense : P.y_acc;
+                    const size_t row = (size_t)rb * 16u + r;
+                    if (partial) atomicAdd(dst + row, S.y[i]);
+                    else dst[row] = S.y[i];
+                }
+                if (!DOUT && r == 0 && rm) or16(out_rm, rb, rm);
+            } else if (r == 0 && rm) {
+                uint32_t f = rm & ~S.vis[lrb];
+                if (f) {
+                    uint32_t old = or16(out_rm, rb, f);
+                    if (BFS && old == 0u) append_active(P, nslot, rb);
+                }
+            }
+        }
+        if (P.stats) {
+            stat_add(S, 0, c_vis);
+            stat_add(S, 1, c_hit);
+            stat_add(S, 2, c_touch);
+            stat_add(S, 3, c_bytes + (tid == 0 ? 16u + 4u * (span + 1u) : 0u));
+        }
+        __syncthreads();
+    }
+}
+
+// Push (Section 3.3.2): warps take tasks of 32 consecutive CSC positions of
+// one active column block; the active vector block is cached in shared memory
+// (Section 3.3.3) and each block's rows are written back with atomics.
+template <int SR, bool DOUT, bool BFS>
+__device__ void push_tasks(const KParams &P, Smem &S, const uint32_t *xm, const uint32_t *vis,
+                           uint32_t *out_rm, int cslot, int nslot)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t nch = ld_cg(&P.ctrl->n_chunk[cslot]);
+    const uint32_t gw = blockIdx.x * NW + warp, nwarps = gridDim.x * NW;
+    float *wx = S.wx[warp];
+    unsigned long long c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
+    for (uint32_t ci = gw; ci < nch; ci += nwarps) {
+        const uint2 ch = __ldcg(P.chunks[cslot] + ci);
+        const uint32_t q0 = ch.x, c = ch.y;
+        const uint32_t q1 = min(q0 + PUSH_CHUNK, __ldg(P.cb_ptr + c + 1));
+        const uint32_t xmb = mask16(xm, c);
+        if (SR == 0) {
+            if (lane < 16) {
+                const size_t j = (size_t)c * 16u + lane;
+                wx[lane] = j < (size_t)P.n ? __ldcg(P.xv + j) : 0.0f;
+            }
+            __syncwarp();
+        }
+        const uint32_t q = q0 + lane;
+        uint32_t rb = 0, meta = 0, act = 0, vm = 0, ref = 0;
+        if (q < q1) {
+            const uint2 d = __ldg(P.csc_desc + q);
+            rb = d.x;
+            meta = d.y;
+            act = meta_cmask(meta) & xmb;
+            ++c_vis;
+            c_touch += meta_nnz(meta);
+            c_bytes += 8;
+            if (SR == 1 && vis && act) {
+                vm = mask16(vis, rb);
+                if (vm == 0xFFFFu) act = 0;
+            }
+            if (act) {
+                ref = __ldg(P.csc_ref + q);
+                ++c_hit;
+                c_bytes += 4;
+            }
+        }
+        const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + ref);
+        if (SR == 1) {
+            if (act) {
+                uint32_t f = bool_found(b, meta, act) & ~vm;
+                c_bytes += bool_bytes(meta);
+                if (f) {
+                    uint32_t old = or16(out_rm, rb, f);
+                    if (BFS && old == 0u) append_active(P, nslot, rb);
+                }
+            }
+        } else {
+            float *y = DOUT ? P.y_dense : P.y_acc;
+            if (act && meta_fmt(meta) == FMT_COO) {
+                const uint32_t nnz = meta_nnz(meta);
+                float *yr = y + (size_t)rb * 16u;
+                uint32_t rows = coo_lane(b, nnz, act, wx, true, [&](uint32_t r, float v) { atomicAdd(yr + r, v); });
+                if (!DOUT && rows) or16(out_rm, rb, rows);
+                c_bytes += val_offset(FMT_COO, nnz) + 4u * nnz;
+            }
+            uint32_t heavy = __ballot_sync(FULL, act && meta_fmt(meta) != FMT_COO);
+            while (heavy) {
+                const int L = __ffs(heavy) - 1;
+                heavy &= heavy - 1u;
+                const uint32_t h_ref = __shfl_sync(FULL, ref, L);
+                const uint32_t h_meta = __shfl_sync(FULL, meta, L);
+                const uint32_t h_rb = __shfl_sync(FULL, rb, L);
+                const uint32_t h_act = __shfl_sync(FULL, act, L);
+                uint32_t by = 0;
+                RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + h_ref), h_meta, h_act, wx,
+                                    lane, S.wacc[warp], &by);
+                if (lane < 16 && o.touched) atomicAdd(y + (size_t)h_rb * 16u + lane, o.sum);
+                uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
+                if (lane == 0) {
+                    if (!DOUT && bits) or16(out_rm, h_rb, bits);
+                    c_bytes += by;
+                }
+            }
+            __syncwarp();
+        }
+    }
+    if (P.stats) {
+        c_vis = __reduce_add_sync(FULL, (unsigned)c_vis);
+        c_hit = __reduce_add_sync(FULL, (unsigned)c_hit);
+        c_touch = __reduce_add_sync(FULL, (unsigned)c_touch);
+        c_bytes = __reduce_add_sync(FULL, (unsigned)c_bytes);
+        if (lane == 0) {
+            stat_add(S, 0, c_vis);
+            stat_add(S, 1, c_hit);
+            stat_add(S, 2, c_touch);
+            stat_add(S, 3, c_bytes);
+        }
+    }
+}
+
+__device__ __forceinline__ bool choose_push(const KParams &P, uint32_t n_act)
+{
+    if (P.path_force == DBS_PATH_PUSH) return true;
+    if (P.path_force == DBS_PATH_PULL) return false;
+    if (P.nbc == 0) return true;
+    return (double)n_act / (double)P.nbc < P.th3;   // Section 3.3.1: xb_sparsity < th3
+}
+
+__device__ __forceinline__ void stats_begin(Smem &S)
+{
+    if (threadIdx.x < 4) S.st[threadIdx.x] = 0ull;
+}
+__device__ __forceinline__ void stats_flush(const KParams &P, Smem &S)
+{
+    __syncthreads();
+    if (P.stats && threadIdx.x == 0) {
+        if (S.st[0]) atomicAdd(&P.ctrl->visited, S.st[0]);
+        if (S.st[1]) atomicAdd(&P.ctrl->hits, S.st[1]);
+        if (S.st[2]) atomicAdd(&P.ctrl->touched, S.st[2]);
+        if (S.st[3]) atomicAdd(&P.ctrl->bytes, S.st[3]);
+    }
+}
+
+__device__ __forceinline__ void reset_stats(const KParams &P)
+{
+    Ctrl *c = P.ctrl;
+    c->x_active = 0; c->visited = 0; c->hits = 0; c->touched = 0; c->bytes = 0;
+    c->nzblk = 0; c->y_nnz = 0; c->reached = 0;
+}
+
+// ------------------------------------------------------------- kernels
+
+// One SpMSpV with a sparse x (index list + values) and a sparse output.
+// Phases: metadata | traversal | compaction counts | compaction writes.
+template <int SR>
+__global__ void __launch_bounds__(NT) k_spmspv_sparse(KParams P)
+{
+    __shared__ Smem S;
+    if (ld_cg(&P.ctrl->err) != 0u) return;
+    const int tid = threadIdx.x;
+    const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
+    stats_begin(S);
+    if (blockIdx.x == 0 && tid == 0 && P.stats) reset_stats(P);
+
+    // Phase 1 (Section 4.1): scatter x, build blk_x_mask, count and list the
+    // nonzero vector blocks (first setter of a block appends it).
+    unsigned act_cnt = 0;
+    for (size_t e = gtid; e < (size_t)P.x_nnz; e += gsz) {
+        const uint32_t j = (uint32_t)__ldg(P.x_idx + e);
+        const float v = P.x_val ? __ldg(P.x_val + e) : 1.0f;
+        if (!(v != 0.0f)) continue;
+        ++act_cnt;
+        if (SR == 0) P.x_dense[j] = v;
+        const uint32_t sh = j & 31u;
+        const uint32_t old = atomicOr(P.xm32 + (j >> 5), 1u << sh);
+        if (((old >> (sh & 16u)) & 0xFFFFu) == 0u) append_active(P, 0, j >> 4);
+    }
+    if (P.stats) {
+        act_cnt = __reduce_add_sync(FULL, act_cnt);
+        if ((tid & 31) == 0 && act_cnt) atomicAdd(&P.ctrl->x_active, (unsigned long long)act_cnt);
+    }
+    if (!grid_sync(P)) return;
+
+    // Phase 2 (Section 3.3.1): device-side path choice, then traversal.
+    const uint32_t n_act = ld_cg(&P.ctrl->n_act[0]);
+    const bool push = choose_push(P, n_act);
+    if (push) push_tasks<SR, false, false>(P, S, P.xm32, P.uvis32, P.yrm32, 0, 0);
+    else pull_tiles<SR, false, false>(P, S, P.xm32, P.uvis32, P.yrm32, 0, 0);
+    stats_flush(P, S);
+    if (!grid_sync(P)) return;
+
+    // Phase 3: clear x, count output rows per compaction tile, reset counters.
+    for (size_t e = gtid; e < (size_t)P.x_nnz; e += gsz) {
+        const uint32_t j = (uint32_t)__ldg(P.x_idx + e);
+        if (SR == 0) P.x_dense[j] = 0.0f;
+        P.xm32[j >> 5] = 0u;
+    }
+    const uint16_t *yrm16 = reinterpret_cast<const uint16_t *>(P.yrm32);
+    for (uint32_t ct = blockIdx.x; ct < P.n_ctiles; ct += gridDim.x) {
+        const uint4 *w4 = reinterpret_cast<const uint4 *>(yrm16 + (size_t)ct * CTILE + tid * 16u);
+        uint4 a = __ldcg(w4), b = __ldcg(w4 + 1);
+        uint32_t cnt = __popc(a.x) + __popc(a.y) + __popc(a.z) + __popc(a.w) + __popc(b.x) + __popc(b.y) +
+                       __popc(b.z) + __popc(b.w);
+        uint32_t tot;
+        block_excl_scan(cnt, &tot);
+        if (tid == 0) P.ctile_cnt[ct] = tot;
+    }
+    if (blockIdx.x == 0 && tid == 0) {
+        Ctrl *c = P.ctrl;
+        c->path = push ? 1u : 2u;
+        if (P.stats) c->nzblk = n_act;
+        c->n_act[0] = 0u;
+        c->n_chunk[0] = 0u;
+        c->tile_next[0] = 0u;
+    }
+    if (!grid_sync(P)) return;
+
+    // Phase 4: ascending output (Section 2.1 "then compaction"); clear the
+    // accumulator and the row masks for the next call.
+    uint32_t *yrm_w = P.yrm32;
+    for (uint32_t ct = blockIdx.x; ct < P.n_ctiles; ct += gridDim.x) {
+        uint32_t base = 0;
+        for (uint32_t k = tid; k < ct; k += NT) base += __ldcg(P.ctile_cnt + k);
+        uint32_t tmp;
+        base = block_excl_scan(base, &tmp);
+        base = tmp;   // sum over all threads = prefix of this tile
+        uint4 *w4 = reinterpret_cast<uint4 *>(yrm_w) + ((size_t)ct * CTILE + tid * 16u) / 8u;
+        uint4 a = __ldcg(w4), b = __ldcg(w4 + 1);
+        uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cnt += __popc(w[i]);
+        uint32_t tile_tot;
+        uint32_t o = base + block_excl_scan(cnt, &tile_tot);
+        const uint32_t rb_base = ct * CTILE + tid * 16u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t bits = w[i];
+            while (bits) {
+                uint32_t k = __ffs(bits) - 1u;
+                bits &= bits - 1u;
+                const uint32_t row = (rb_base + 2u * i + (k >> 4)) * 16u + (k & 15u);
+                P.y_idx[o] = (int32_t)row;
+                if (SR == 0) {
+                    P.y_val[o] = __ldcg(P.y_acc + row);
+                    P.y_acc[row] = 0.0f;
+                }
+                ++o;
+            }
+        }
+        if (a.x | a.y | a.z | a.w) w4[0] = make_uint4(0, 0, 0, 0);
+        if (b.x | b.y | b.z | b.w) w4[1] = make_uint4(0, 0, 0, 0);
+        if (ct == P.n_ctiles - 1 && tid == 0) {
+            *P.y_nnz = (long long)(base + tile_tot);
+            if (P.stats) P.ctrl->y_nnz = base + tile_tot;
+        }
+    }
+    if (P.n_ctiles == 0 && blockIdx.x == 0 && tid == 0) *P.y_nnz = 0;
+}
+
+// One SpMSpV with a dense x and a dense y (Section 4.3, DB-Decoding): the
+// vector masks come from warp ballots (Section 4.1).  Counter slot P.slot is
+// used by this call; the other slot is reset for the next call.
+__global__ void __launch_bounds__(NT) k_spmspv_dense(KParams P)
+{
+    __shared__ Smem S;
+    __shared__ uint32_t s_cnt[NW];
+    __shared__ uint32_t s_base;
+    if (ld_cg(&P.ctrl->err) != 0u) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
+    stats_begin(S);
+    if (blockIdx.x == 0 && tid == 0 && P.stats) reset_stats(P);
+    for (size_t i = gtid; i < (size_t)P.m; i += gsz) P.y_dense[i] = 0.0f;
+
+    // Phase 1: each warp reads 32 x values, ballots their nonzero pattern and
+    // splits it into the two 16-bit block masks; nonzero blocks are counted
+    // per warp, per CTA, and added to the global count once per CTA.
+    const uint32_t nwords = (uint32_t)((P.n + 31) / 32);
+    const uint32_t wstep = gridDim.x * NW;
+    unsigned act_cnt = 0;
+    for (uint32_t w0 = blockIdx.x * NW; w0 < nwords; w0 += wstep) {
+        const uint32_t w = w0 + warp;
+        uint32_t bal = 0, nb = 0;
+        if (w < nwords) {
+            const size_t j = (size_t)w * 32u + lane;
+            const float v = j < (size_t)P.n ? __ldg(P.x_in + j) : 0.0f;
+            bal = __ballot_sync(FULL, v != 0.0f);
+            if (lane == 0) P.xm32[w] = bal;
+            nb = ((bal & 0xFFFFu) != 0u) + ((bal >> 16) != 0u);
+            act_cnt += __popc(bal);
+        }
+        if (lane == 0) s_cnt[warp] = nb;
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t tot = 0;
+            for (int k = 0; k < NW; ++k) { uint32_t c = s_cnt[k]; s_cnt[k] = tot; tot += c; }
+            s_base = tot ? atomicAdd(&P.ctrl->n_act[P.slot], tot) : 0u;
+        }
+        __syncthreads();
+        if (w < nwords && lane == 0 && nb) {
+            uint32_t pos = s_base + s_cnt[warp];
+            for (uint32_t h = 0; h < 2; ++h) {
+                if (!((bal >> (16 * h)) & 0xFFFFu)) continue;
+                const uint32_t cb = 2u * w + h;
+                P.act[P.slot][pos++] = cb;
+                const uint32_t s = __ldg(P.cb_ptr + cb), e = __ldg(P.cb_ptr + cb + 1);
+                if (e > s) {
+                    const uint32_t nch = (e - s + PUSH_CHUNK - 1) / PUSH_CHUNK;
+                    const uint32_t base = atomicAdd(&P.ctrl->n_chunk[P.slot], nch);
+                    for (uint32_t k = 0; k < nch; ++k)
+                        P.chunks[P.slot][base + k] = make_uint2(s + k * PUSH_CHUNK, cb);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (P.stats && lane == 0 && act_cnt) atomicAdd(&P.ctrl->x_active, (unsigned long long)act_cnt);
+    if (!grid_sync(P)) return;
+
+    const uint32_t n_act = ld_cg(&P.ctrl->n_act[P.slot]);
+    const bool push = choose_push(P, n_act);
+    if (push) push_tasks<0, true, false>(P, S, P.xm32, nullptr, nullptr, P.slot, 0);
+    else pull_tiles<0, true, false>(P, S, P.xm32, nullptr, nullptr, P.slot, 0);
+    stats_flush(P, S);
+    if (blockIdx.x == 0 && tid == 0) {
+        Ctrl *c = P.ctrl;
+        const int o = P.slot ^ 1;
+        c->n_act[o] = 0u;
+        c->n_chunk[o] = 0u;
+        c->tile_next[o] = 0u;
+        c->path = push ? 1u : 2u;
+        if (P.stats) c->nzblk = n_act;
+    }
+}
+
+// DB-BFS (Section 4.2): the frontier is the vector-block mask; each level is
+// next = (A or.and frontier) and not visited, on the path chosen from the
+// frontier's nonzero-block ratio.  Lists and counters rotate over three
+// slots so each level needs two grid barriers.
+__global__ void __launch_bounds__(NT) k_bfs(KParams P)
+{
+    __shared__ Smem S;
+    if (ld_cg(&P.ctrl->err) != 0u) return;
+    const int tid = threadIdx.x;
+    const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
+    stats_begin(S);
+    const uint32_t nwords = (uint32_t)((P.nbc + 1) / 2);
+    for (size_t v = gtid; v < (size_t)P.n; v += gsz) P.levels[v] = -1;
+    for (size_t w = gtid; w < nwords; w += gsz) {
+        uint32_t vis = 0;
+        // rows beyond m in the last row block count as visited
+        for (uint32_t h = 0; h < 2; ++h) {
+            const uint32_t rb = 2u * (uint32_t)w + h;
+            if (rb >= (uint32_t)P.nbr) { vis |= 0xFFFFu << (16 * h); continue; }
+            const int64_t r0 = (int64_t)rb * 16;
+            if (r0 + 16 > P.m) vis |= ((0xFFFFu << (uint32_t)(P.m - r0)) & 0xFFFFu) << (16 * h);
+        }
+        P.bvis32[w] = vis;
+        P.fm32[0][w] = 0u;
+        P.fm32[1][w] = 0u;
+    }
+    if (blockIdx.x == 0 && tid == 0) {
+        Ctrl *c = P.ctrl;
+        for (int s = 0; s < 3; ++s) { c->n_act[s] = 0u; c->n_chunk[s] = 0u; c->tile_next[s] = 0u; }
+        reset_stats(P);
+        c->bfs_levels = 0u;
+        c->bfs_push_levels = 0u;
+    }
+    if (!grid_sync(P)) return;
+    if (blockIdx.x == 0 && tid == 0) {
+        const uint32_t s = (uint32_t)P.bfs_src;
+        P.levels[s] = 0;
+        or16(P.fm32[0], s >> 4, 1u << (s & 15u));
+        or16(P.bvis32, s >> 4, 1u << (s & 15u));
+        append_active(P, 0, s >> 4);
+    }
+    if (!grid_sync(P)) return;
+
+    unsigned long long reached = 1, nz_sum = 0;
+    uint32_t push_levels = 0, L = 1;
+    for (;; ++L) {
+        const int cur = (int)((L - 1) % 3), nxt = (int)(L % 3), old = (int)((L + 1) % 3);
+        uint32_t *fcur = P.fm32[(L - 1) & 1], *fnext = P.fm32[L & 1];
+        const uint32_t n_act = ld_cg(&P.ctrl->n_act[cur]);
+        if (n_act == 0u) break;
+        nz_sum += n_act;
+        const bool push = choose_push(P, n_act);
+        push_levels += push;
+        if (push) push_tasks<1, false, true>(P, S, fcur, P.bvis32, fnext, cur, nxt);
+        else pull_tiles<1, false, true>(P, S, fcur, P.bvis32, fnext, cur, nxt);
+        if (!grid_sync(P)) return;
+
+        // level update: visited |= next, levels of the new vertices, clear
+        // the old frontier, reset the slot two levels back.
+        const uint32_t n_next = ld_cg(&P.ctrl->n_act[nxt]);
+        for (size_t i = gtid; i < n_next; i += gsz) {
+            const uint32_t rb = __ldcg(P.act[nxt] + i);
+            const uint32_t f = mask16(fnext, rb);
+            or16(P.bvis32, rb, f);
+            uint32_t bits = f;
+            while (bits) {
+                const uint32_t r = __ffs(bits) - 1u;
+                bits &= bits - 1u;
+                P.levels[rb * 16u + r] = (int32_t)L;
+            }
+        }
+        if (P.stats) {
+            unsigned long long cnt = 0;
+            for (size_t i = gtid; i < n_next; i += gsz) cnt += __popc(mask16(fnext, __ldcg(P.act[nxt] + i)));
+            cnt = __reduce_add_sync(FULL, (unsigned)cnt);
+            if ((tid & 31) == 0 && cnt) atomicAdd(&P.ctrl->reached, cnt);
+        }
+        for (size_t i = gtid; i < n_act; i += gsz) {
+            const uint32_t rb = __ldcg(P.act[cur] + i);
+            atomicAnd(fcur + (rb >> 1), ~(0xFFFFu << ((rb & 1u) << 4)));
+        }
+        if (blockIdx.x == 0 && tid == 0) {
+            Ctrl *c = P.ctrl;
+            c->n_act[old] = 0u;
+            c->n_chunk[old] = 0u;
+            c->tile_next[old] = 0u;
+        }
+        if (!grid_sync(P)) return;
+    }
+    stats_flush(P, S);
+    if (blockIdx.x == 0 && tid == 0) {
+        Ctrl *c = P.ctrl;
+        c->bfs_levels = L - 1u;   // the loop stops when frontier L-1 is empty
+        c->bfs_push_levels = push_levels;
+        c->path = 0u;
+        c->nzblk = nz_sum;
+        if (P.stats) c->reached += reached;
+    }
+}
+
+// Withholds block 0 from the barrier so every other block's wait expires.
+__global__ void __launch_bounds__(NT) k_selftest_wait(KParams P)
+{
+    if (blockIdx.x == 0) return;
+    grid_sync(P);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host
+
+struct dbs_workspace {
+    const dbs_matrix *A = nullptr;
+    int device = -1;
+    int sms = 0;
+    int grid_sparse[2] = {0, 0};
+    int grid_dense = 0, grid_bfs = 0;
+    int call_count = 0;
+    dbs_exec_opts opts{};
+    float *x_dense = nullptr;
+    uint32_t *xm32 = nullptr;
+    uint32_t *act[3] = {nullptr, nullptr, nullptr};
+    uint2 *chunks[3] = {nullptr, nullptr, nullptr};
+    float *y_acc = nullptr;
+    uint32_t *yrm32 = nullptr;
+    uint32_t *ctile_cnt = nullptr;
+    uint32_t n_ctiles = 0;
+    uint32_t *bvis32 = nullptr;
+    uint32_t *fm32[2] = {nullptr, nullptr};
+    Ctrl *ctrl = nullptr;
+    bool last_was_bfs = false;
+};
+
+namespace {
+
+void ws_free(dbs_workspace *w)
+{
+    cudaFree(w->x_dense); cudaFree(w->xm32); cudaFree(w->y_acc); cudaFree(w->yrm32);
+    cudaFree(w->ctile_cnt); cudaFree(w->bvis32); cudaFree(w->fm32[0]); cudaFree(w->fm32[1]);
+    cudaFree(w->ctrl);
+    for (int s = 0; s < 3; ++s) { cudaFree(w->act[s]); cudaFree(w->chunks[s]); }
+}
+
+template <class T>
+bool dalloc(T **p, size_t count)
+{
+    size_t bytes = std::max<size_t>(count * sizeof(T), 16);
+    if (cudaMalloc((void **)p, bytes) != cudaSuccess) { cudaGetLastError(); *p = nullptr; return false; }
+    if (cudaMemset(*p, 0, bytes) != cudaSuccess) { cudaGetLastError(); return false; }
+    return true;
+}
+
+KParams make_params(const dbs_matrix *A, dbs_workspace *w)
+{
+    KParams P{};
+    P.m = (int32_t)A->m; P.n = (int32_t)A->n; P.nbr = (int32_t)A->nbr; P.nbc = (int32_t)A->nbc;
+    P.B = (uint32_t)A->B; P.T = (uint32_t)A->T; P.valued = A->valued;
+    P.rb_ptr = A->d_rb_ptr;
+    P.blk_desc = reinterpret_cast<const uint2 *>(A->d_blk_desc);
+    P.blk_ref = A->d_blk_ref;
+    P.cb_ptr = A->d_cb_ptr;
+    P.csc_desc = reinterpret_cast<const uint2 *>(A->d_csc_desc);
+    P.csc_ref = A->d_csc_ref;
+    P.payload = reinterpret_cast<const uint4 *>(A->d_payload);
+    P.tiles = reinterpret_cast<const uint4 *>(A->d_tiles);
+    P.x_dense = w->x_dense; P.xm32 = w->xm32;
+    for (int s = 0; s < 3; ++s) { P.act[s] = w->act[s]; P.chunks[s] = w->chunks[s]; }
+    P.y_acc = w->y_acc; P.yrm32 = w->yrm32; P.ctile_cnt = w->ctile_cnt; P.n_ctiles = w->n_ctiles;
+    P.bvis32 = w->bvis32; P.fm32[0] = w->fm32[0]; P.fm32[1] = w->fm32[1];
+    P.ctrl = w->ctrl;
+    P.th3 = w->opts.th3;
+    P.local_pull_min = w->opts.local_pull_min;
+    P.stats = w->opts.collect_stats;
+    P.timeout_ns = w->opts.wait_timeout_ns;
+    return P;
+}
+
+dbs_status launch(const void *fn, int grid, KParams &P, cudaStream_t s)
+{
+    void *args[] = {&P};
+    cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NT), args, 0, s);
+    if (e != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+    return DBS_OK;
+}
+
+int coop_grid(const void *fn, int sms)
+{
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, NT, 0) != cudaSuccess) { cudaGetLastError(); return 0; }
+    return nb * sms;
+}
+
+dbs_status check_ready(const dbs_matrix *A, dbs_workspace *w)
+{
+    if (!A || !w || w->A != A || !A->on_device) return DBS_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+    if (dev != w->device) return DBS_ERR_INVALID_ARG;
+    return DBS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void dbs_exec_opts_default(dbs_exec_opts *o)
+{
+    if (!o) return;
+    o->th3 = 0.01;
+    o->local_pull_min = 8;
+    o->collect_stats = 0;
+    o->wait_timeout_ns = 2000000000LL;
+}
+
+dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
+{
+    if (!A || !out || !A->on_device) return DBS_ERR_INVALID_ARG;
+    dbs_workspace *w = new (std::nothrow) dbs_workspace();
+    if (!w) return DBS_ERR_OOM;
+    w->A = A;
+    dbs_exec_opts_default(&w->opts);
+    if (cudaGetDevice(&w->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&w->sms, cudaDevAttrMultiProcessorCount, w->device) != cudaSuccess) {
+        cudaGetLastError();
+        delete w;
+        return DBS_ERR_CUDA;
+    }
+    const size_t nbc = (size_t)A->nbc, nbr = (size_t)A->nbr;
+    const size_t chunk_cap = (size_t)A->B / PUSH_CHUNK + nbc + 1;
+    w->n_ctiles = (uint32_t)((nbr + CTILE - 1) / CTILE);
+    const size_t yrm_words = std::max<size_t>(1, (size_t)w->n_ctiles) * CTILE / 2 + 8;
+    bool ok = dalloc(&w->x_dense, nbc * 16 + 16) && dalloc(&w->xm32, nbc / 2 + 8) &&
+              dalloc(&w->y_acc, nbr * 16 + 16) && dalloc(&w->yrm32, yrm_words) &&
+              dalloc(&w->ctile_cnt, (size_t)w->n_ctiles + 1) && dalloc(&w->bvis32, nbr / 2 + 8) &&
+              dalloc(&w->fm32[0], nbc / 2 + 8) && dalloc(&w->fm32[1], nbc / 2 + 8) && dalloc(&w->ctrl, 1);
+    for (int s = 0; s < 3 && ok; ++s) ok = dalloc(&w->act[s], nbc + 1) && dalloc(&w->chunks[s], chunk_cap);
+    if (!ok) { ws_free(w); delete w; return DBS_ERR_OOM; }
+    w->grid_sparse[0] = coop_grid((const void *)k_spmspv_sparse<0>, w->sms);
+    w->grid_sparse[1] = coop_grid((const void *)k_spmspv_sparse<1>, w->sms);
+    w->grid_dense = coop_grid((const void *)k_spmspv_dense, w->sms);
+    w->grid_bfs = coop_grid((const void *)k_bfs, w->sms);
+    if (!w->grid_sparse[0] || !w->grid_sparse[1] || !w->grid_dense || !w->grid_bfs) {
+        ws_free(w);
+        delete w;
+        return DBS_ERR_CUDA;
+    }
+    *out = w;
+    return DBS_OK;
+}
+
+dbs_status dbs_workspace_destroy(dbs_workspace *w)
+{
+    if (!w) return DBS_OK;
+    ws_free(w);
+    delete w;
+    return DBS_OK;
+}
+
+dbs_status dbs_workspace_set_opts(dbs_workspace *w, const dbs_exec_opts *o)
+{
+    if (!w || !o) return DBS_ERR_INVALID_ARG;
+    if (!(o->th3 >= 0.0) || o->local_pull_min < 0 || o->wait_timeout_ns <= 0) return DBS_ERR_INVALID_ARG;
+    w->opts = *o;
+    return DBS_OK;
+}
+
+dbs_status dbs_workspace_check(dbs_workspace *w, void *stream)
+{
+    if (!w) return DBS_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+    Ctrl c;
+    if (cudaMemcpy(&c, w->ctrl, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return DBS_ERR_CUDA;
+    }
+    if (c.err == 0u) return DBS_OK;
+    // A failed call can leave barrier, counters and scratch half-updated:
+    // reset all of them.
+    const dbs_matrix *A = w->A;
+    bool ok = cudaMemset(w->ctrl, 0, sizeof(Ctrl)) == cudaSuccess &&
+              cudaMemset(w->x_dense, 0, ((size_t)A->nbc * 16 + 16) * sizeof(float)) == cudaSuccess &&
+              cudaMemset(w->xm32, 0, ((size_t)A->nbc / 2 + 8) * 4) == cudaSuccess &&
+              cudaMemset(w->y_acc, 0, ((size_t)A->nbr * 16 + 16) * sizeof(float)) == cudaSuccess &&
+              cudaMemset(w->yrm32, 0, (std::max<size_t>(1, w->n_ctiles) * CTILE / 2 + 8) * 4) == cudaSuccess &&
+              cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) { cudaGetLastError(); return DBS_ERR_CUDA; }
+    return (dbs_status)c.err;
+}
+
+dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx, const float *x_val,
+                      int64_t x_nnz, const uint16_t *visited_mask, int32_t *y_idx, float *y_val,
+                      int64_t *y_nnz, dbs_path path, dbs_workspace *w, void *stream)
+{
+    dbs_status st = check_ready(A, w);
+    if (st != DBS_OK) return st;
+    if (sr != DBS_PLUS_TIMES_F32 && sr != DBS_OR_AND_BOOL) return DBS_ERR_INVALID_ARG;
+    if (path < DBS_PATH_AUTO || path > DBS_PATH_PULL) return DBS_ERR_INVALID_ARG;
+    if (x_nnz < 0 || x_nnz > A->n || (x_nnz > 0 && !x_idx) || !y_idx || !y_nnz) return DBS_ERR_INVALID_ARG;
+    if (sr == DBS_PLUS_TIMES_F32) {
+        if (!A->valued) return DBS_ERR_UNSUPPORTED;
+        if ((x_nnz > 0 && !x_val) || !y_val || visited_mask) return DBS_ERR_INVALID_ARG;
+    }
+    if (reinterpret_cast<uintptr_t>(visited_mask) & 3u) return DBS_ERR_INVALID_ARG;
+    KParams P = make_params(A, w);
+    P.path_force = (int)path;
+    P.x_idx = x_idx;
+    P.x_val = x_val;
+    P.x_nnz = x_nnz;
+    P.xv = w->x_dense;
+    P.uvis32 = reinterpret_cast<const uint32_t *>(visited_mask);
+    P.y_idx = y_idx;
+    P.y_val = y_val;
+    P.y_nnz = reinterpret_cast<long long *>(y_nnz);
+    const void *fn = sr == DBS_PLUS_TIMES_F32 ? (const void *)k_spmspv_sparse<0> : (const void *)k_spmspv_sparse<1>;
+    w->last_was_bfs = false;
+    return launch(fn, w->grid_sparse[sr == DBS_PLUS_TIMES_F32 ? 0 : 1], P, (cudaStream_t)stream);
+}
+
+dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_path path, dbs_workspace *w,
+                            void *stream)
+{
+    dbs_status st = check_ready(A, w);
+    if (st != DBS_OK) return st;
+    if (!A->valued) return DBS_ERR_UNSUPPORTED;
+    if ((A->n > 0 && !x) || (A->m > 0 && !y) || path < DBS_PATH_AUTO || path > DBS_PATH_PULL)
+        return DBS_ERR_INVALID_ARG;
+    KParams P = make_params(A, w);
+    P.path_force = (int)path;
+    P.x_in = x;
+    P.xv = x;
+    P.y_dense = y;
+    P.slot = w->call_count & 1;
+    w->call_count++;
+    w->last_was_bfs = false;
+    return launch((const void *)k_spmspv_dense, w->grid_dense, P, (cudaStream_t)stream);
+}
+
+dbs_status dbs_bfs(const dbs_matrix *A, int64_t src, int32_t *levels, int32_t *nlevels_host, dbs_path path,
+                   dbs_workspace *w, void *stream)
+{
+    dbs_status st = check_ready(A, w);
+    if (st != DBS_OK) return st;
+    if (A->m != A->n || src < 0 || src >= A->n || !levels || path < DBS_PATH_AUTO || path > DBS_PATH_PULL)
+        return DBS_ERR_INVALID_ARG;
+    KParams P = make_params(A, w);
+    P.path_force = (int)path;
+    P.bfs_src = src;
+    P.levels = levels;
+    cudaStream_t s = (cudaStream_t)stream;
+    // The dense-x kernel alternates counter slots; BFS resets all of them
+    // itself, so the next dense call may start from either slot.
+    w->call_count = 0;
+    w->last_was_bfs = true;
+    st = launch((const void *)k_bfs, w->grid_bfs, P, s);
+    if (st != DBS_OK || !nlevels_host) return st;
+    Ctrl c;
+    if (cudaMemcpyAsync(&c, w->ctrl, sizeof(Ctrl), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return DBS_ERR_CUDA;
+    }
+    if (c.err) return (dbs_status)c.err;
+    *nlevels_host = (int32_t)c.bfs_levels;
+    return DBS_OK;
+}
+
+dbs_status dbs_last_stats(dbs_workspace *w, void *stream, dbs_stats *out)
+{
+    if (!w || !out) return DBS_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+    Ctrl c;
+    if (cudaMemcpy(&c, w->ctrl, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return DBS_ERR_CUDA;
+    }
+    *out = dbs_stats{};
+    out->path = (int32_t)c.path;
+    out->status = (int32_t)c.err;
+    out->n_nzblk = (int64_t)c.nzblk;
+    out->n_blk = w->A->nbc;
+    out->x_active = (int64_t)c.x_active;
+    out->visited_blocks = (int64_t)c.visited;
+    out->hit_blocks = (int64_t)c.hits;
+    out->touched_nnz = (int64_t)c.touched;
+    out->bytes_alg = (int64_t)c.bytes;
+    out->y_nnz = w->last_was_bfs ? (int64_t)c.reached : (int64_t)c.y_nnz;
+    out->bfs_levels = (int32_t)c.bfs_levels;
+    out->bfs_push_levels = (int32_t)c.bfs_push_levels;
+    return DBS_OK;
+}
+
+dbs_status dbs_selftest_wait_timeout(dbs_workspace *w, void *stream)
+{
+    if (!w) return DBS_ERR_INVALID_ARG;
+    KParams P = make_params(w->A, w);
+    int grid = std::min(w->grid_bfs, 2 * w->sms);
+    if (grid < 2) return DBS_ERR_UNSUPPORTED;
+    return launch((const void *)k_selftest_wait, grid, P, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,264 @@
+/*
+ * dbspmspv.h -- C ABI of a GB300 (sm_103a) implementation of DB-SpMSpV:
+ * dual-view blocked sparse-matrix x sparse-vector multiplication y = A x for
+ * a reusable matrix A and an input vector x that changes on every call.
+ *
+ * Method: Cong et al., "DB-SpMSpV: Dual-View Blocked Sparse Matrix-Sparse
+ * Vector Multiplication for Dynamic GPU Workloads", ICPP '26.
+ *   - build once, call many times with a changing x (Sections 1 and 4.3;
+ *     "the DB-format conversion is performed offline and reused", Section 5.5);
+ *   - 16x16 blocks, block-CSR and block-CSC views over one payload (3.2.1);
+ *   - vector-block masks and nonzero-block statistics built on the GPU (4.1);
+ *   - push/pull selection by nonzero-vector-block ratio, th3 = 0.01 (3.3.1);
+ *   - per-block microkernels chosen from block type and blk_x_mask (3.3.1,
+ *     3.3.3, Algorithms 2-4);
+ *   - load-weighted pull tiles and flattened push tasks (3.3.2);
+ *   - Boolean or/and semiring with a visited mask and DB-BFS (4.2, Alg. 5).
+ *
+ * Conventions (apply to every function below):
+ *   - Every function returns a dbs_status; nothing aborts, throws or traps.
+ *   - "stream" is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls marked ASYNC only enqueue work on that stream and return;
+ *     their device outputs are valid once the stream reaches that point.
+ *     Device-side failures of an ASYNC call (a bounded wait that timed out)
+ *     are latched in the workspace and reported by dbs_workspace_check().
+ *   - "device" pointers are CUDA global-memory pointers on the current device;
+ *     "host" pointers are ordinary CPU memory.  The caller owns every input
+ *     and output buffer; the library owns the matrix and the workspace.
+ *   - A(i, j) stored means x_j contributes to y_i; push walks column j.
+ *   - x_j is active iff it is listed and its value is != 0 (so -0.0 is
+ *     inactive and NaN is active); with no values every listed index is
+ *     active.  Listed indices must be unique and in [0, n).
+ *   - Output pattern is structural: y_i is produced iff some stored A(i, j)
+ *     has an active x_j, even when the values cancel to zero.
+ *   - Limits: m, n < 2^31; nonzero 16x16 blocks < 2^32; payload < 64 GiB.
+ */
+#ifndef DBSPMSPV_H
+#define DBSPMSPV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DBS_OK = 0,
+    DBS_ERR_INVALID_ARG = 1,   /* bad pointer, size, index, duplicate or option */
+    DBS_ERR_OOM = 2,           /* host or device allocation failed (nothing leaked) */
+    DBS_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+    DBS_ERR_TIMEOUT = 4,       /* a bounded device-side wait gave up */
+    DBS_ERR_UNSUPPORTED = 5,   /* valid request this build does not serve */
+    DBS_ERR_INTERNAL = 6       /* a device-side capacity or consistency check failed */
+} dbs_status;
+
+typedef enum {
+    DBS_PLUS_TIMES_F32 = 0,    /* y_i = sum_j A(i,j) * x_j in fp32 */
+    DBS_OR_AND_BOOL = 1        /* y_i = OR_j (A(i,j) and x_j active) and not visited_i */
+} dbs_semiring;
+
+typedef enum {
+    DBS_PATH_AUTO = 0,         /* push iff N_nzblk / N_blk < th3 (Section 3.3.1) */
+    DBS_PATH_PUSH = 1,         /* column-driven over the block-CSC view */
+    DBS_PATH_PULL = 2          /* row-driven over the block-CSR view */
+} dbs_path;
+
+/* Low-level block formats (Section 3.2.1, Figure 5(b), Figure 6). */
+typedef enum {
+    DBS_FMT_COO = 0,           /* packed 4+4-bit coordinates + values (nnz < th0) */
+    DBS_FMT_DENSE = 1,         /* 256 values + column masks (nnz > th1) */
+    DBS_FMT_FORCE_CSR = 2,     /* row_ptr + row_mask + values in row order */
+    DBS_FMT_FORCE_CSC = 3,     /* col_ptr + col_mask + values in column order */
+    DBS_FMT_PATCHED_CSR = 4    /* ForceCSR + col_ptr + row_idx_csc2csr bytes */
+} dbs_format;
+#define DBS_FMT_AUTO (-1)
+#define DBS_NUM_FORMATS 5
+
+/* Build options.  dbs_build_opts_default() fills the paper's settings. */
+typedef struct {
+    int32_t th0;               /* nnz < th0 -> COO (paper: 32) */
+    int32_t th1;               /* nnz > th1 -> Dense (paper: 128) */
+    double th2;                /* skew ratio above which a block is ForceCSR/ForceCSC (paper: 2.0) */
+    int32_t force_format;      /* DBS_FMT_AUTO, or one dbs_format for every block (ablation) */
+    int32_t tile_weight;       /* pull tile weight cap; block weights Dense 4, ForceCSR /
+                                  ForceCSC / patched CSR 2, COO 1 (Section 3.3.2).
+                                  0 = sized from the matrix and the GPU's SM count. */
+    int32_t tile_max_row_blocks; /* row blocks one pull tile may span (1..64); 1 with
+                                  tile_weight 16 reproduces the paper's segments. 0 = 64 */
+    int32_t keep_host;         /* keep a host copy of the blocked format (export) */
+    int32_t host_only;         /* build the format on the host only; no device memory
+                                  is touched (the matrix can be inspected and exported
+                                  but not multiplied).  For CPU-side checks. */
+    int32_t num_threads;       /* host builder threads; 0 = all hardware threads */
+} dbs_build_opts;
+
+void dbs_build_opts_default(dbs_build_opts *opts);
+
+/* Execution options of a workspace.  dbs_exec_opts_default() fills them. */
+typedef struct {
+    double th3;                /* push iff N_nzblk < th3 * N_blk (paper: 0.01) */
+    int32_t local_pull_min;    /* patched-CSR blocks use the row-wise (pull) microkernel
+                                  when popc(active block columns) >= this; else the
+                                  column-wise (push) one.  Unstated in the paper; 8. */
+    int32_t collect_stats;     /* 1: count visited / hit blocks, touched nnz and
+                                  algorithmic bytes on the device (a few atomics per CTA) */
+    int64_t wait_timeout_ns;   /* bound on every device-side wait (grid barriers);
+                                  default 2 s.  On expiry the kernel latches
+                                  DBS_ERR_TIMEOUT and returns. */
+} dbs_exec_opts;
+
+void dbs_exec_opts_default(dbs_exec_opts *opts);
+
+typedef struct dbs_matrix dbs_matrix;        /* opaque; library-owned device memory */
+typedef struct dbs_workspace dbs_workspace;  /* opaque; per-stream scratch */
+
+/* Section 3.2.1 (the DB format), Section 3.3.2 (pull segments), Section 5.5
+ * (offline conversion).  Builds the blocked dual-view matrix from CSR.
+ *   m, n        rows and columns (0 <= m, n < 2^31)
+ *   nnz         number of stored entries (= row_ptr[m])
+ *   row_ptr     int64[m+1], non-decreasing, row_ptr[0] = 0
+ *   col_idx     int32[nnz], in [0, n), unique within a row (any order)
+ *   vals        float32[nnz], or NULL for a pattern-only matrix (Boolean
+ *               semiring only)
+ *   inputs_on_device  0: the three arrays are host pointers; 1: device pointers
+ *   opts        NULL = dbs_build_opts_default()
+ *   stream      stream for the upload (the call synchronizes it before returning)
+ *   out         receives the matrix; unchanged on error
+ * SYNCHRONOUS.  Errors: DBS_ERR_INVALID_ARG (bad sizes, out-of-range or
+ * duplicate column, non-monotone row_ptr, bad option), DBS_ERR_OOM, DBS_ERR_CUDA.
+ * On error nothing is leaked. */
+dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t *row_ptr,
+                                const int32_t *col_idx, const float *vals, int inputs_on_device,
+                                const dbs_build_opts *opts, void *stream, dbs_matrix **out);
+
+/* Frees everything the matrix owns.  NULL is accepted.  The caller must make
+ * sure no enqueued call still uses it. */
+dbs_status dbs_matrix_destroy(dbs_matrix *A);
+
+/* Section 5.5, Table 4: storage of the blocked format next to plain CSR and
+ * CSR + CSC (4-byte indices; 4-byte values when valued). */
+typedef struct {
+    int64_t m, n, nnz;
+    int64_t nbr, nbc;                       /* ceil(m/16), ceil(n/16) */
+    int64_t nblocks;                        /* nonzero 16x16 blocks */
+    int64_t blocks_by_format[DBS_NUM_FORMATS];
+    int64_t nnz_by_format[DBS_NUM_FORMATS];
+    int64_t ntiles;                         /* pull tiles */
+    int64_t payload_bytes;                  /* low-level block payload */
+    int64_t view_bytes;                     /* high-level views, tiles, pointers */
+    int64_t total_bytes;                    /* payload + views (device footprint) */
+    int64_t csr_bytes;                      /* plain CSR of the same matrix */
+    int64_t csr_csc_bytes;                  /* CSR + CSC duplication */
+    int32_t valued;                         /* 1 if built with values */
+    int32_t on_device;                      /* 0 for host_only builds */
+    double build_seconds;                   /* host time of the conversion */
+} dbs_matrix_info;
+
+/* Fills *out.  Host-only, no synchronization. */
+dbs_status dbs_matrix_info_get(const dbs_matrix *A, dbs_matrix_info *out);
+
+/* Figure 5(b): exports the high-level views to caller-allocated HOST arrays
+ * (any pointer may be NULL to skip it):
+ *   blk_row_ptr int64[nbr+1], blk_col_idx int64[B]      block-CSR view
+ *   blk_col_ptr int64[nbc+1], blk_row_idx int64[B]      block-CSC view
+ *   blk_csc2csr int64[B]     CSC position -> primary (block-CSR) block id
+ *   blk_nnz int32[B], blk_format int32[B]               per primary block
+ * Uses the host copy when present, else copies from the device (synchronous). */
+dbs_status dbs_matrix_export_views(const dbs_matrix *A, int64_t *blk_row_ptr, int64_t *blk_col_idx,
+                                   int64_t *blk_col_ptr, int64_t *blk_row_idx,
+                                   int64_t *blk_csc2csr, int32_t *blk_nnz, int32_t *blk_format);
+
+/* Decodes the low-level payload back to CSR (HOST arrays, row_ptr int64[m+1],
+ * col_idx int32[nnz], vals float32[nnz] or NULL) with columns ascending per
+ * row.  A round trip returns the input bit for bit.  Synchronous. */
+dbs_status dbs_matrix_export_csr(const dbs_matrix *A, int64_t *row_ptr, int32_t *col_idx,
+                                 float *vals);
+
+/* Scratch for SpMSpV and BFS on one matrix: a dense copy of x, the vector-block
+ * masks, active lists, push task list, the output accumulator, counters and
+ * the grid-barrier state.  Calls sharing a workspace must be ordered on one
+ * stream.  Every call leaves the scratch cleared for the next one. */
+dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out);
+dbs_status dbs_workspace_destroy(dbs_workspace *ws);
+dbs_status dbs_workspace_set_opts(dbs_workspace *ws, const dbs_exec_opts *opts);
+
+/* Synchronizes the stream, returns the status latched by the device since the
+ * last check (DBS_OK, DBS_ERR_TIMEOUT or DBS_ERR_INTERNAL) and clears it, so
+ * the workspace can be used again.  Calls enqueued after a latched error do
+ * no work and leave their outputs untouched. */
+dbs_status dbs_workspace_check(dbs_workspace *ws, void *stream);
+
+/* Sections 3.3.1-3.3.3 and 4.1: one SpMSpV y = A x with a sparse x.  ASYNC.
+ *   sr            DBS_PLUS_TIMES_F32 (matrix must be valued) or DBS_OR_AND_BOOL
+ *   x_idx         device int32[x_nnz], unique indices in [0, n)
+ *   x_val         device float32[x_nnz]; NULL = every listed index active
+ *                 (required non-NULL for plus-times)
+ *   x_nnz         host count (0 allowed)
+ *   visited_mask  Boolean only: device uint16[ceil(m/16)], bit r of word b set
+ *                 = row 16b+r is excluded from y (Algorithm 5); NULL = none
+ *   y_idx         device int32[m] capacity: ascending output row indices
+ *   y_val         device float32[m] capacity for plus-times; NULL for Boolean
+ *   y_nnz         device int64[1]: number of output entries
+ *   path          DBS_PATH_AUTO / _PUSH / _PULL
+ * Errors returned immediately: DBS_ERR_INVALID_ARG, DBS_ERR_UNSUPPORTED
+ * (plus-times on a pattern-only matrix), DBS_ERR_CUDA (launch failure). */
+dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx,
+                      const float *x_val, int64_t x_nnz, const uint16_t *visited_mask,
+                      int32_t *y_idx, float *y_val, int64_t *y_nnz, dbs_path path,
+                      dbs_workspace *ws, void *stream);
+
+/* Section 4.3 (DB-Decoding): x given as a dense device float32[n] whose zero
+ * entries are inactive; the vector-block masks are built from it with warp
+ * ballots (Section 4.1).  y is a dense device float32[m]; rows with no active
+ * contribution are written as 0.  Plus-times only.  ASYNC. */
+dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_path path,
+                            dbs_workspace *ws, void *stream);
+
+/* Section 4.2 (DB-BFS): level-synchronous BFS from src on a square matrix;
+ * each level is next = (A or.and frontier) and not visited, with push/pull
+ * re-chosen per level (or forced by path).  The whole level loop runs on the
+ * device.  levels: device int32[n], level of each vertex or -1 if unreached.
+ * nlevels_host: optional host int32*; if non-NULL the call synchronizes the
+ * stream and stores the number of levels (max level + 1).  ASYNC otherwise. */
+dbs_status dbs_bfs(const dbs_matrix *A, int64_t src, int32_t *levels, int32_t *nlevels_host,
+                   dbs_path path, dbs_workspace *ws, void *stream);
+
+/* Statistics of the last call on this workspace.  Synchronizes the stream.
+ * Counts other than path/N_nzblk/y_nnz are filled only with collect_stats. */
+typedef struct {
+    int32_t path;               /* 1 push, 2 pull (BFS: last level) */
+    int32_t status;             /* latched device status (not cleared here) */
+    int64_t n_nzblk;            /* nonzero vector blocks of x (BFS: summed over levels) */
+    int64_t n_blk;              /* ceil(n/16) */
+    int64_t x_active;           /* active x entries */
+    int64_t visited_blocks;     /* matrix blocks whose column block is nonzero in x */
+    int64_t hit_blocks;         /* visited blocks whose columns intersect x's mask */
+    int64_t touched_nnz;        /* nnz of visited blocks */
+    int64_t bytes_alg;          /* algorithmic bytes: the bytes of views, block payload
+                                   slices, vector and output that the chosen path must
+                                   move for this x (a lower bound on DRAM traffic) */
+    int64_t y_nnz;              /* output entries (BFS: vertices reached) */
+    int32_t bfs_levels;         /* BFS: number of levels */
+    int32_t bfs_push_levels;    /* BFS: levels run on the push path */
+} dbs_stats;
+
+dbs_status dbs_last_stats(dbs_workspace *ws, void *stream, dbs_stats *out);
+
+/* Self-test of the bounded device wait: launches the grid barrier with one
+ * block withheld, so every other block's wait expires after
+ * opts.wait_timeout_ns; the kernel latches DBS_ERR_TIMEOUT and returns.
+ * dbs_workspace_check() then reports it.  No GPU fault is involved. */
+dbs_status dbs_selftest_wait_timeout(dbs_workspace *ws, void *stream);
+
+/* Human-readable name of a status. */
+const char *dbs_status_string(dbs_status s);
+
+/* Library version string, e.g. "dbspmspv 0.1 sm_103a". */
+const char *dbs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DBSPMSPV_H */
