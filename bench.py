@@ -1,0 +1,465 @@
+#!/usr/bin/env python
+"""Benchmark of the DB-SpMSpV hot path on one GB300 (or N replicas).
+
+Workload (default): R-MAT scale 20 (2^20 vertices, edge factor 16, a/b/c/d =
+.57/.19/.19/.05), symmetrised, duplicates and self-loops removed, pattern
+only.  One step = one Boolean SpMSpV at each input density in
+{0.01%, 0.1%, 1%, 10%, 50%} (auto push/pull) + one DB-BFS from the next of 16
+random non-isolated sources.  Inputs are resident in HBM before timing; L2 is
+flushed (256 MiB write) before every call, outside the timed regions; every
+call is timed with CUDA events on its stream.
+
+Metric: touched nnz per second (nnz of the matrix blocks whose column block
+is active in x, summed over the step's SpMSpV calls and BFS levels).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same workload on its own GPU (replicas, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DENSITIES = (1e-4, 1e-3, 1e-2, 1e-1, 5e-1)
+N_SOURCES = 16
+POOL = 32                      # distinct x per density, cycled over the steps
+FLUSH_BYTES = 256 << 20        # > 2x the 129 MB L2
+METRIC = "SpMSpV touched-nnz/s and HBM GB/s vs input density (1 GB300); DB-BFS GTEPS"
+UNIT = "touched-nnz/s"
+WORKLOAD = ("rmat-s20-ef16 (2^20 vertices, a/b/c/d .57/.19/.19/.05, symmetrised, pattern only); "
+            "Boolean SpMSpV at x density 0.01%/0.1%/1%/10%/50% + DB-BFS from 16 sources")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                       "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except Exception:
+            self.p.kill()
+            out = ""
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9 or f[0] != str(self.gpu):
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def build_workload(scale: int, seed_tag: int):
+    import synth
+    A = synth.config("rmat", "full") if scale == 20 else synth.rmat_graph(scale, 16, seed=44)
+    xs = {}
+    for d in DENSITIES:
+        k = max(1, int(round(d * A.n)))
+        xs[d] = [synth.x_uniform(A.n, k, [44, seed_tag, int(d * 1e6), i], valued=False) for i in range(POOL)]
+    sources = synth.bfs_sources(A, N_SOURCES, [44, 7])
+    return A, xs, sources
+
+
+class TouchedCounter:
+    """touched nnz = sum of nnz over the blocks whose column block holds an
+    active x entry; a BFS level touches the blocks of its frontier's column
+    blocks.  Independent of the path taken."""
+
+    def __init__(self, views):
+        nbc = len(views["blk_col_ptr"]) - 1
+        self.nbc = nbc
+        self.per_cb = np.zeros(nbc, np.int64)
+        np.add.at(self.per_cb, views["blk_col_idx"], views["blk_nnz"].astype(np.int64))
+
+    def spmspv(self, idx) -> int:
+        act = np.zeros(self.nbc, bool)
+        act[np.asarray(idx) // 16] = True
+        return int(self.per_cb[act].sum())
+
+    def bfs(self, levels) -> int:
+        reached = np.nonzero(levels >= 0)[0]
+        lv = levels[reached]
+        cb = reached // 16
+        key = np.sort(lv.astype(np.int64) * self.nbc + cb)       # (level, column block) pairs
+        if key.size:
+            key = key[np.r_[True, key[1:] != key[:-1]]]
+        return int(self.per_cb[key % self.nbc].sum())
+
+
+def cpu_baseline(A, xs, sources, touched_x, touched_bfs, budget_s: float):
+    """The oracle as it stands, single-threaded, on a bounded sample of the
+    same step (densities cycled, then BFS sources)."""
+    import oracle
+    O = oracle.Oracle(A)
+    t_total, units, calls, bfs_runs = 0.0, 0, 0, 0
+    i = 0
+    while t_total < budget_s and i < POOL:
+        for d in DENSITIES:
+            x = xs[d][i]
+            t0 = time.perf_counter()
+            O.spmspv(x, oracle.OR_AND)
+            t_total += time.perf_counter() - t0
+            units += touched_x[d][i]
+            calls += 1
+        src = int(sources[i % len(sources)])
+        t0 = time.perf_counter()
+        O.bfs_queue(src)
+        t_total += time.perf_counter() - t0
+        units += touched_bfs[i % len(sources)]
+        bfs_runs += 1
+        i += 1
+    return {"value": units / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{i} steps: {calls} oracle SpMSpV calls (push scatter, fp64 C, 1 thread) at the 5 densities "
+                      f"+ {bfs_runs} queue BFS; {t_total:.1f} s of CPU time; units = the same touched nnz"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed on this host's cores."""
+    ws_, rank, _ = _dist()
+    if rank != 0:
+        return
+    A, xs, sources = build_workload(args.scale, 0)
+    import oracle
+    O = oracle.Oracle(A)
+    # touched nnz per x from the block views (same definition as the GPU arm)
+    counter = TouchedCounter(oracle.block_views(A))
+    touched = lambda x: counter.spmspv(x.idx)  # noqa: E731
+    bfs_touched = counter.bfs
+
+    # A reference step is a bounded sample of the workload: the SpMSpV call at
+    # one density (cycling), plus the queue BFS every fifth step, so five
+    # consecutive steps cover one full step of the GPU arm.
+    steps_total = args.warmup + args.steps
+    t_step, units = [], []
+    for s in range(steps_total):
+        i = (s // len(DENSITIES)) % POOL
+        d = DENSITIES[s % len(DENSITIES)]
+        t0 = time.perf_counter()
+        O.spmspv(xs[d][i], oracle.OR_AND)
+        lev = None
+        if s % len(DENSITIES) == len(DENSITIES) - 1:
+            lev = O.bfs_queue(int(sources[(s // len(DENSITIES)) % len(sources)]))
+        dt = time.perf_counter() - t0
+        u = touched(xs[d][i]) + (bfs_touched(lev) if lev is not None else 0)
+        if s >= args.warmup:
+            t_step.append(dt)
+            units.append(u)
+    T = sum(t_step)
+    value = sum(units) / T
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * T / len(t_step), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bool", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "densities": list(DENSITIES), "bfs_sources": N_SOURCES},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} steps, each one oracle SpMSpV at one of the 5 densities "
+                                       "(cycling) plus a queue BFS every 5th step; fp64 C, 1 thread"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--scale", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import dynamic_sparsity_spmspv_gb300 as dbs
+
+    A, xs, sources = build_workload(args.scale, 0)
+    M = dbs.DBMatrix.from_csr(A)
+    info = M.info()
+    ws = dbs.Workspace(M, collect_stats=1)
+    stream = torch.cuda.current_stream()
+
+    x_dev = {d: [torch.from_numpy(x.idx).to(dev) for x in xs[d]] for d in DENSITIES}
+    y_idx = torch.empty(A.m, dtype=torch.int32, device=dev)
+    y_nnz = torch.empty(1, dtype=torch.int64, device=dev)
+    levels = torch.empty(A.n, dtype=torch.int32, device=dev)
+
+    # Units: touched nnz = nnz of the blocks whose column block is active in
+    # x (for BFS: in each level's frontier), from the library's block views.
+    counter = TouchedCounter(M.export_views())
+    # untimed pass with device statistics: algorithmic bytes and path
+    touched_x = {d: [counter.spmspv(x.idx) for x in xs[d]] for d in DENSITIES}
+    bytes_x = {d: [] for d in DENSITIES}
+    path_x = {d: [] for d in DENSITIES}
+    for d in DENSITIES:
+        for xi in x_dev[d]:
+            dbs.spmspv(M, xi, None, semiring="or_and", ws=ws, y_idx=y_idx, y_nnz=y_nnz)
+            st = ws.stats()
+            bytes_x[d].append(st["bytes_alg"])
+            path_x[d].append(st["path"])
+    touched_bfs, bytes_bfs, edges_bfs, nlev_bfs, push_lev = [], [], [], [], []
+    deg = np.diff(A.row_ptr)
+    for src in sources:
+        _, nl = dbs.bfs(M, int(src), levels=levels, ws=ws)
+        st = ws.stats()
+        bytes_bfs.append(st["bytes_alg"])
+        lev = levels.cpu().numpy()
+        touched_bfs.append(counter.bfs(lev))
+        edges_bfs.append(int(deg[lev >= 0].sum()) // 2)
+        nlev_bfs.append(nl)
+        push_lev.append(st["bfs_push_levels"])
+    assert ws.check() == 0
+    ws.set_opts(dbs.exec_opts(collect_stats=0))
+
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush(i):
+        flush_buf.fill_(float(i & 7))
+
+    def step(s, ev, rec):
+        i = s % POOL
+        for d in DENSITIES:
+            flush(s)
+            e0, e1 = ev.pop(), ev.pop()
+            e0.record(stream)
+            dbs.spmspv(M, x_dev[d][i], None, semiring="or_and", ws=ws, y_idx=y_idx, y_nnz=y_nnz)
+            e1.record(stream)
+            rec.append(("spmspv", d, i, e0, e1))
+        flush(s)
+        e0, e1 = ev.pop(), ev.pop()
+        e0.record(stream)
+        dbs.bfs(M, int(sources[s % N_SOURCES]), levels=levels, ws=ws, sync=False)
+        e1.record(stream)
+        rec.append(("bfs", None, s % N_SOURCES, e0, e1))
+
+    def new_events(n):
+        return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+    for s in range(args.warmup):
+        step(s, new_events(12), [])
+    torch.cuda.synchronize()
+
+    calls_per_step = len(DENSITIES) + 1
+    ev = new_events(2 * calls_per_step * args.steps)
+    rec = []
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        step(args.warmup + s, ev, rec)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    assert ws.check() == 0
+
+    t_sp = {d: 0.0 for d in DENSITIES}
+    n_sp = {d: 0 for d in DENSITIES}
+    units_sp = {d: 0 for d in DENSITIES}
+    bytes_sp = {d: 0 for d in DENSITIES}
+    t_bfs = 0.0
+    units_bfs = edges = bytes_b = 0
+    for kind, d, i, e0, e1 in rec:
+        ms = e0.elapsed_time(e1)
+        if kind == "spmspv":
+            t_sp[d] += ms
+            n_sp[d] += 1
+            units_sp[d] += touched_x[d][i]
+            bytes_sp[d] += bytes_x[d][i]
+        else:
+            t_bfs += ms
+            units_bfs += touched_bfs[i]
+            edges += edges_bfs[i]
+            bytes_b += bytes_bfs[i]
+    t_total_ms = sum(t_sp.values()) + t_bfs
+    units_total = sum(units_sp.values()) + units_bfs
+    t_max = t_total_ms
+    if world > 1:
+        tt = torch.tensor([t_total_ms], device=dev)
+        uu = torch.tensor([float(units_total)], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(uu, op=torch.distributed.ReduceOp.SUM)
+        t_max, units_total = float(tt.item()), float(uu.item())
+    value = units_total / (t_max * 1e-3)
+
+    peak, peak_kind = _peaks()
+    per_density = []
+    for d in DENSITIES:
+        t = t_sp[d] / max(n_sp[d], 1)
+        per_density.append({
+            "density": d, "us_per_call": 1e3 * t,
+            "touched_nnz_per_s": units_sp[d] / (t_sp[d] * 1e-3),
+            "bytes_alg_per_call": bytes_sp[d] / max(n_sp[d], 1),
+            "gbs": bytes_sp[d] / (t_sp[d] * 1e-3) / 1e9,
+            "frac_of_measured_hbm": bytes_sp[d] / (t_sp[d] * 1e-3) / 1e9 / peak,
+            "path": "push" if statistics.mode(path_x[d]) == 1 else "pull"})
+    bfs_info = {"gteps_harmonic": None, "ms_per_bfs": t_bfs / args.steps,
+                "gteps": edges / (t_bfs * 1e-3) / 1e9, "levels_mean": float(np.mean(nlev_bfs)),
+                "push_levels_mean": float(np.mean(push_lev)),
+                "gbs": bytes_b / (t_bfs * 1e-3) / 1e9}
+    # harmonic mean of per-source GTEPS from per-call times
+    per_src_t = {}
+    for kind, d, i, e0, e1 in rec:
+        if kind == "bfs":
+            per_src_t.setdefault(i, []).append(e0.elapsed_time(e1))
+    if per_src_t:
+        g = [edges_bfs[i] / (np.mean(v) * 1e-3) / 1e9 for i, v in per_src_t.items()]
+        bfs_info["gteps_harmonic"] = len(g) / sum(1.0 / x for x in g)
+
+    # dominant kernel: the launch kind with the largest share of the step time
+    t_spmspv_all = sum(t_sp.values())
+    if t_spmspv_all >= t_bfs:
+        dom, dom_bytes, dom_t, dom_n = "k_spmspv_sparse<or_and>", sum(bytes_sp.values()), t_spmspv_all, sum(n_sp.values())
+    else:
+        dom, dom_bytes, dom_t, dom_n = "k_bfs", bytes_b, t_bfs, args.steps
+    achieved = dom_bytes / dom_n / (dom_t / dom_n * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                "bytes_alg_per_launch": dom_bytes / dom_n, "us_per_launch": 1e3 * dom_t / dom_n,
+                "share_of_step": dom_t / t_total_ms}
+
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bool", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "densities": list(DENSITIES), "bfs_sources": N_SOURCES,
+                      "x_pool_per_density": POOL, "l2": "flushed (256 MiB write) before every call, outside timing",
+                      "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                      "matrix": {"n": A.n, "nnz": A.nnz, "blocks": info["nblocks"], "tiles": info["ntiles"],
+                                 "device_bytes": info["total_bytes"]}},
+           "gpu_launches": calls_per_step * args.steps,
+           "roofline": roofline, "per_density": per_density, "bfs": bfs_info, "clocks": clocks,
+           "wall_s_timed_region": wall}
+
+    # end to end through the public API with host buffers
+    if not args.no_e2e:
+        pin = {d: [torch.from_numpy(x.idx).pin_memory() for x in xs[d]] for d in DENSITIES}
+        xbuf = torch.empty(A.n, dtype=torch.int32, device=dev)
+        lev_host = torch.empty(A.n, dtype=torch.int32).pin_memory()
+        yh = torch.empty(A.m, dtype=torch.int32).pin_memory()
+        ynh = torch.empty(1, dtype=torch.int64).pin_memory()
+        h2d = d2h = 0
+        e2e_ms, e2e_units = 0.0, 0
+        ksteps = max(10, args.steps // 4)
+        for s in range(args.warmup + ksteps):
+            i = s % POOL
+            timed = s >= args.warmup
+            step_ms = 0.0
+            for d in DENSITIES:
+                flush(s)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                k = pin[d][i].numel()
+                xbuf[:k].copy_(pin[d][i], non_blocking=True)
+                dbs.spmspv(M, xbuf[:k], None, semiring="or_and", ws=ws, y_idx=y_idx, y_nnz=y_nnz)
+                ynh.copy_(y_nnz, non_blocking=True)
+                stream.synchronize()
+                ny = int(ynh.item())
+                yh[:ny].copy_(y_idx[:ny], non_blocking=True)
+                e1.record(stream)
+                e1.synchronize()
+                step_ms += e0.elapsed_time(e1)
+                if timed:
+                    h2d += 4 * k
+                    d2h += 8 + 4 * ny
+                    e2e_units += touched_x[d][i]
+            flush(s)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dbs.bfs(M, int(sources[s % N_SOURCES]), levels=levels, ws=ws, sync=False)
+            lev_host.copy_(levels, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            step_ms += e0.elapsed_time(e1)
+            if timed:
+                d2h += 4 * A.n
+                e2e_units += touched_bfs[s % N_SOURCES]
+                e2e_ms += step_ms
+        out["e2e"] = {"value": e2e_units / (e2e_ms * 1e-3), "unit": UNIT,
+                      "h2d_bytes_per_step": h2d // ksteps, "d2h_bytes_per_step": d2h // ksteps,
+                      "steps": ksteps, "ms_per_step": e2e_ms / ksteps}
+
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(A, xs, sources, touched_x, touched_bfs, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -46,7 +46,6 @@ struct Ctrl {
     unsigned int path;
     unsigned int n_act[3];
     unsigned int n_chunk[3];
-    unsigned int tile_next[3];
     unsigned int bfs_levels;
     unsigned int bfs_push_levels;
     unsigned int pad0;
@@ -89,7 +88,8 @@ struct KParams {
     int32_t *levels;
     // workspace
     float *x_dense;
-    uint32_t *xm32;
+    uint32_t *xm32;           // sparse-x masks: zero between calls
+    uint32_t *dxm32;          // dense-x masks: fully rewritten by every dense call
     uint32_t *act[3];
     uint2 *chunks[3];
     float *y_acc;
@@ -396,15 +396,12 @@ __device__ __forceinline__ uint32_t bool_found(const uint8_t *__restrict__ b, ui
         }
     } else {
         const uint4 *m4 = reinterpret_cast<const uint4 *>(b + (fmt == FMT_DENSE ? 0u : OFF_MASK));
-        uint4 lo = __ldg(m4), hi = __ldg(m4 + 1);
-        uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        const uint4 lo = __ldg(m4), hi = __ldg(m4 + 1);
+        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
         if (fmt == FMT_DENSE || fmt == FMT_FCSC) {          // column masks: OR the active columns
-            uint32_t a = act;
-            while (a) {
-                uint32_t c = __ffs(a) - 1u;
-                a &= a - 1u;
-                f |= (w[c >> 1] >> ((c & 1u) << 4)) & 0xFFFFu;
-            }
+#pragma unroll
+            for (uint32_t c = 0; c < 16; ++c)
+                if ((act >> c) & 1u) f |= (w[c >> 1] >> ((c & 1u) << 4)) & 0xFFFFu;
         } else {                                            // row masks: rows meeting an active column
 #pragma unroll
             for (uint32_t r = 0; r < 16; ++r)
@@ -440,21 +437,56 @@ __device__ __forceinline__ void stat_add(Smem &S, int i, unsigned long long v)
     if (v) atomicAdd(&S.st[i], v);
 }
 
-// Pull (Section 3.3.2): CTAs take tiles of consecutive primary blocks.
+// Byte i (0..15) / 32-bit word i (0..3) of a 16-byte payload chunk.
+__device__ __forceinline__ uint32_t chunk_word(const uint4 &c, uint32_t i)
+{
+    return i == 0 ? c.x : i == 1 ? c.y : i == 2 ? c.z : c.w;
+}
+__device__ __forceinline__ uint32_t chunk_byte(const uint4 &c, uint32_t i)
+{
+    return (chunk_word(c, i >> 2) >> ((i & 3u) << 3)) & 0xFFu;
+}
+
+// COO block whose payload fits in its first 16-byte chunk (already loaded):
+// Boolean up to 16 entries, plus-times up to 3 (coordinates, then values at
+// align4(nnz)).  Returns the touched (Boolean: found) rows.
+template <int SR>
+__device__ __forceinline__ uint32_t coo_chunk(const uint4 &c, uint32_t nnz, uint32_t act, const float *xb,
+                                              float *sy)
+{
+    uint32_t rows = 0;
+    const uint32_t vw = (nnz + 3u) >> 2;
+    for (uint32_t k = 0; k < nnz; ++k) {
+        const uint32_t e = chunk_byte(c, k);
+        const uint32_t col = e & 15u;
+        if ((act >> col) & 1u) {
+            const uint32_t r = e >> 4;
+            rows |= 1u << r;
+            if (SR == 0) atomicAdd(&sy[r], __uint_as_float(chunk_word(c, vw + k)) * xval(xb, col));
+        }
+    }
+    return rows;
+}
+
+// Pull (Section 3.3.2): CTAs take tiles of consecutive primary blocks in a
+// static order, prefetching the next tile's descriptor.  Stage 1 runs in
+// batches of PB blocks per thread whose descriptor, mask, payload-reference
+// and first-chunk loads are each issued together, so every thread keeps
+// several independent requests in flight (the role of the paper's
+// double-buffered asynchronous prefetch).
 // SR 0 = plus-times, 1 = Boolean.  DOUT: dense output y.  BFS: first touch
 // of a next-frontier row block appends it to the list of slot `nslot`.
 template <int SR, bool DOUT, bool BFS>
 __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const uint32_t *vis,
-                           uint32_t *out_rm, int tslot, int nslot)
+                           uint32_t *out_rm, int nslot)
 {
+    constexpr int PB = 4;
+    constexpr int NBATCH = (int)TILE_MAX_BLOCKS / (NT * PB);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float *xv = P.xv;
-    for (;;) {
-        if (tid == 0) S.tile = atomicAdd(&P.ctrl->tile_next[tslot], 1u);
-        __syncthreads();
-        const uint32_t t = S.tile;
-        if (t >= P.T) break;
-        const uint4 td = __ldg(P.tiles + t);
+    uint32_t t = blockIdx.x;
+    uint4 td = t < P.T ? __ldg(P.tiles + t) : make_uint4(0, 0, 0, 0);
+    for (; t < P.T; t += gridDim.x) {
         const uint32_t p0 = td.x, p1 = td.y, rb0 = td.z, span = td.w;
         if (tid <= (int)span) S.rbp[tid] = __ldg(P.rb_ptr + rb0 + tid);
         for (uint32_t i = tid; i < span * 16u; i += NT) S.y[i] = 0.0f;
@@ -464,46 +496,75 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
         }
         if (tid == 0) S.nheavy = 0u;
         __syncthreads();
+        const uint32_t tn = t + gridDim.x;
+        const uint4 td_next = tn < P.T ? __ldg(P.tiles + tn) : make_uint4(0, 0, 0, 0);
 
-        // Stage 1: scan the tile's block descriptors, test them against the
-        // vector-block masks, run COO / Boolean blocks in place, queue the rest.
+        // Stage 1: block descriptors against the vector-block masks; COO and
+        // Boolean blocks are finished in place, the rest are queued.
         unsigned long long c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
-        for (uint32_t p = p0 + tid; p < p1; p += NT) {
-            uint32_t lo = 0, hi = span - 1u;
+        uint32_t lo = 0;
+        {
+            uint32_t hi = span - 1u;
+            const uint32_t p = p0 + tid;
             while (lo < hi) {
                 uint32_t mid = (lo + hi + 1u) >> 1;
                 if (S.rbp[mid] <= p) lo = mid; else hi = mid - 1u;
             }
-            const uint32_t lrb = lo;
-            if (SR == 1 && S.vis[lrb] == 0xFFFFu) continue;   // row block fully visited
-            const uint2 d = __ldg(P.blk_desc + p);
-            const uint32_t col = d.x, meta = d.y;
-            const uint32_t xmb = mask16(xm, col);
-            c_bytes += 8;
-            if (!xmb) continue;
-            ++c_vis;
-            c_touch += meta_nnz(meta);
-            const uint32_t act = meta_cmask(meta) & xmb;
-            if (!act) continue;
-            ++c_hit;
-            const uint32_t ref = __ldg(P.blk_ref + p);
-            const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + ref);
-            c_bytes += 4;
-            if (SR == 1) {
-                uint32_t f = bool_found(b, meta, act);
-                if (f) atomicOr(&S.rm[lrb], f);
-                c_bytes += bool_bytes(meta);
-            } else if (meta_fmt(meta) == FMT_COO) {
-                const uint32_t nnz = meta_nnz(meta);
-                float *sy = &S.y[lrb * 16u];
-                uint32_t rows = coo_lane(b, nnz, act, xv + (size_t)col * 16u, true,
-                                         [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
-                if (rows) atomicOr(&S.rm[lrb], rows);
-                c_bytes += val_offset(FMT_COO, nnz) + 4u * nnz;
-            } else {
-                uint32_t slot = atomicAdd(&S.nheavy, 1u);
-                if (slot < HEAVY_CAP) S.heavy[slot] = make_uint4(ref, meta, col, lrb);
-                else latch_error(P, DBS_ERR_INTERNAL);
+        }
+#pragma unroll 1
+        for (int bt = 0; bt < NBATCH; ++bt) {
+            if (p0 + tid + (uint32_t)(bt * PB * NT) >= p1) break;
+            uint2 d[PB];
+            uint32_t lr[PB], act[PB], ref[PB];
+            uint4 c0[PB];
+#pragma unroll
+            for (int k = 0; k < PB; ++k) {
+                const uint32_t p = p0 + tid + (uint32_t)((bt * PB + k) * NT);
+                d[k] = p < p1 ? __ldg(P.blk_desc + p) : make_uint2(0u, 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < PB; ++k) {
+                const uint32_t p = p0 + tid + (uint32_t)((bt * PB + k) * NT);
+                while (lo + 1u < span && S.rbp[lo + 1u] <= p) ++lo;
+                lr[k] = lo;
+                const bool ok = p < p1 && !(SR == 1 && S.vis[lo] == 0xFFFFu);
+                act[k] = ok ? mask16(xm, d[k].x) : 0u;
+                if (p < p1) c_bytes += 8;
+            }
+#pragma unroll
+            for (int k = 0; k < PB; ++k) {
+                const uint32_t p = p0 + tid + (uint32_t)((bt * PB + k) * NT);
+                if (act[k]) { ++c_vis; c_touch += meta_nnz(d[k].y); }
+                act[k] &= meta_cmask(d[k].y);
+                ref[k] = act[k] ? __ldg(P.blk_ref + p) : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < PB; ++k) c0[k] = act[k] ? __ldg(P.payload + ref[k]) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int k = 0; k < PB; ++k) {
+                if (!act[k]) continue;
+                const uint32_t meta = d[k].y, fmt = meta_fmt(meta), nnz = meta_nnz(meta), col = d[k].x;
+                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + ref[k]);
+                ++c_hit;
+                c_bytes += 4;
+                uint32_t rows = 0;
+                if (fmt == FMT_COO && nnz <= (SR == 1 ? 16u : 3u)) {
+                    rows = coo_chunk<SR>(c0[k], nnz, act[k], xv + (size_t)col * 16u, &S.y[lr[k] * 16u]);
+                    c_bytes += SR == 1 ? nnz : 5u * nnz;
+                } else if (SR == 1) {
+                    rows = bool_found(b, meta, act[k]);
+                    c_bytes += bool_bytes(meta);
+                } else if (fmt == FMT_COO) {
+                    float *sy = &S.y[lr[k] * 16u];
+                    rows = coo_lane(b, nnz, act[k], xv + (size_t)col * 16u, true,
+                                    [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
+                    c_bytes += val_offset(FMT_COO, nnz) + 4u * nnz;
+                } else {
+                    uint32_t slot = atomicAdd(&S.nheavy, 1u);
+                    if (slot < HEAVY_CAP) S.heavy[slot] = make_uint4(ref[k], meta, col, lr[k]);
+                    else latch_error(P, DBS_ERR_INTERNAL);
+                }
+                if (rows) atomicOr(&S.rm[lr[k]], rows);
             }
         }
         __syncthreads();
@@ -532,6 +593,7 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
         for (uint32_t i = tid; i < span * 16u; i += NT) {
             const uint32_t lrb = i >> 4, r = i & 15u, rb = rb0 + lrb;
             const uint32_t rm = S.rm[lrb];
+            if (!rm) continue;
             const bool partial = S.rbp[lrb] < p0 || S.rbp[lrb + 1] > p1;
             if (SR == 0) {
                 if ((rm >> r) & 1u) {
@@ -540,8 +602,8 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
                     if (partial) atomicAdd(dst + row, S.y[i]);
                     else dst[row] = S.y[i];
                 }
-                if (!DOUT && r == 0 && rm) or16(out_rm, rb, rm);
-            } else if (r == 0 && rm) {
+                if (!DOUT && r == 0) or16(out_rm, rb, rm);
+            } else if (r == 0) {
                 uint32_t f = rm & ~S.vis[lrb];
                 if (f) {
                     uint32_t old = or16(out_rm, rb, f);
@@ -555,6 +617,7 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
             stat_add(S, 2, c_touch);
             stat_add(S, 3, c_bytes + (tid == 0 ? 16u + 4u * (span + 1u) : 0u));
         }
+        td = td_next;
         __syncthreads();
     }
 }
@@ -692,7 +755,7 @@ __device__ __forceinline__ void reset_stats(const KParams &P)
 // One SpMSpV with a sparse x (index list + values) and a sparse output.
 // Phases: metadata | traversal | compaction counts | compaction writes.
 template <int SR>
-__global__ void __launch_bounds__(NT) k_spmspv_sparse(KParams P)
+__global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
 {
     __shared__ Smem S;
     if (ld_cg(&P.ctrl->err) != 0u) return;
@@ -706,13 +769,17 @@ __global__ void __launch_bounds__(NT) k_spmspv_sparse(KParams P)
     unsigned act_cnt = 0;
     for (size_t e = gtid; e < (size_t)P.x_nnz; e += gsz) {
         const uint32_t j = (uint32_t)__ldg(P.x_idx + e);
+        if (j >= (uint32_t)P.n) {                 // also catches negative indices
+            latch_error(P, DBS_ERR_INVALID_ARG);
+            continue;
+        }
         const float v = P.x_val ? __ldg(P.x_val + e) : 1.0f;
         if (!(v != 0.0f)) continue;
         ++act_cnt;
         if (SR == 0) P.x_dense[j] = v;
         const uint32_t sh = j & 31u;
         const uint32_t old = atomicOr(P.xm32 + (j >> 5), 1u << sh);
-        if (((old >> (sh & 16u)) & 0xFFFFu) == 0u) append_active(P, 0, j >> 4);
+        if (((old >> (sh & 16u)) & 0xFFFFu) == 0u) append_active(P, P.slot, j >> 4);
     }
     if (P.stats) {
         act_cnt = __reduce_add_sync(FULL, act_cnt);
@@ -721,16 +788,17 @@ __global__ void __launch_bounds__(NT) k_spmspv_sparse(KParams P)
     if (!grid_sync(P)) return;
 
     // Phase 2 (Section 3.3.1): device-side path choice, then traversal.
-    const uint32_t n_act = ld_cg(&P.ctrl->n_act[0]);
+    const uint32_t n_act = ld_cg(&P.ctrl->n_act[P.slot]);
     const bool push = choose_push(P, n_act);
-    if (push) push_tasks<SR, false, false>(P, S, P.xm32, P.uvis32, P.yrm32, 0, 0);
-    else pull_tiles<SR, false, false>(P, S, P.xm32, P.uvis32, P.yrm32, 0, 0);
+    if (push) push_tasks<SR, false, false>(P, S, P.xm32, P.uvis32, P.yrm32, P.slot, 0);
+    else pull_tiles<SR, false, false>(P, S, P.xm32, P.uvis32, P.yrm32, 0);
     stats_flush(P, S);
     if (!grid_sync(P)) return;
 
     // Phase 3: clear x, count output rows per compaction tile, reset counters.
     for (size_t e = gtid; e < (size_t)P.x_nnz; e += gsz) {
         const uint32_t j = (uint32_t)__ldg(P.x_idx + e);
+        if (j >= (uint32_t)P.n) continue;
         if (SR == 0) P.x_dense[j] = 0.0f;
         P.xm32[j >> 5] = 0u;
     }
@@ -748,9 +816,9 @@ __global__ void __launch_bounds__(NT) k_spmspv_sparse(KParams P)
         Ctrl *c = P.ctrl;
         c->path = push ? 1u : 2u;
         if (P.stats) c->nzblk = n_act;
-        c->n_act[0] = 0u;
-        c->n_chunk[0] = 0u;
-        c->tile_next[0] = 0u;
+        // counters of both slots are clean for the next call, whichever slot it uses
+        c->n_act[0] = 0u; c->n_act[1] = 0u;
+        c->n_chunk[0] = 0u; c->n_chunk[1] = 0u;
     }
     if (!grid_sync(P)) return;
 
@@ -800,7 +868,7 @@ __global__ void __launch_bounds__(NT) k_spmspv_sparse(KParams P)
 // One SpMSpV with a dense x and a dense y (Section 4.3, DB-Decoding): the
 // vector masks come from warp ballots (Section 4.1).  Counter slot P.slot is
 // used by this call; the other slot is reset for the next call.
-__global__ void __launch_bounds__(NT) k_spmspv_dense(KParams P)
+__global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
 {
     __shared__ Smem S;
     __shared__ uint32_t s_cnt[NW];
@@ -825,7 +893,7 @@ __global__ void __launch_bounds__(NT) k_spmspv_dense(KParams P)
             const size_t j = (size_t)w * 32u + lane;
             const float v = j < (size_t)P.n ? __ldg(P.x_in + j) : 0.0f;
             bal = __ballot_sync(FULL, v != 0.0f);
-            if (lane == 0) P.xm32[w] = bal;
+            if (lane == 0) P.dxm32[w] = bal;
             nb = ((bal & 0xFFFFu) != 0u) + ((bal >> 16) != 0u);
             act_cnt += __popc(bal);
         }
@@ -859,15 +927,14 @@ __global__ void __launch_bounds__(NT) k_spmspv_dense(KParams P)
 
     const uint32_t n_act = ld_cg(&P.ctrl->n_act[P.slot]);
     const bool push = choose_push(P, n_act);
-    if (push) push_tasks<0, true, false>(P, S, P.xm32, nullptr, nullptr, P.slot, 0);
-    else pull_tiles<0, true, false>(P, S, P.xm32, nullptr, nullptr, P.slot, 0);
+    if (push) push_tasks<0, true, false>(P, S, P.dxm32, nullptr, nullptr, P.slot, 0);
+    else pull_tiles<0, true, false>(P, S, P.dxm32, nullptr, nullptr, 0);
     stats_flush(P, S);
     if (blockIdx.x == 0 && tid == 0) {
         Ctrl *c = P.ctrl;
         const int o = P.slot ^ 1;
         c->n_act[o] = 0u;
         c->n_chunk[o] = 0u;
-        c->tile_next[o] = 0u;
         c->path = push ? 1u : 2u;
         if (P.stats) c->nzblk = n_act;
     }
@@ -877,7 +944,7 @@ __global__ void __launch_bounds__(NT) k_spmspv_dense(KParams P)
 // next = (A or.and frontier) and not visited, on the path chosen from the
 // frontier's nonzero-block ratio.  Lists and counters rotate over three
 // slots so each level needs two grid barriers.
-__global__ void __launch_bounds__(NT) k_bfs(KParams P)
+__global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
 {
     __shared__ Smem S;
     if (ld_cg(&P.ctrl->err) != 0u) return;
@@ -901,7 +968,7 @@ __global__ void __launch_bounds__(NT) k_bfs(KParams P)
     }
     if (blockIdx.x == 0 && tid == 0) {
         Ctrl *c = P.ctrl;
-        for (int s = 0; s < 3; ++s) { c->n_act[s] = 0u; c->n_chunk[s] = 0u; c->tile_next[s] = 0u; }
+        for (int s = 0; s < 3; ++s) { c->n_act[s] = 0u; c->n_chunk[s] = 0u; }
         reset_stats(P);
         c->bfs_levels = 0u;
         c->bfs_push_levels = 0u;
@@ -927,7 +994,7 @@ __global__ void __launch_bounds__(NT) k_bfs(KParams P)
         const bool push = choose_push(P, n_act);
         push_levels += push;
         if (push) push_tasks<1, false, true>(P, S, fcur, P.bvis32, fnext, cur, nxt);
-        else pull_tiles<1, false, true>(P, S, fcur, P.bvis32, fnext, cur, nxt);
+        else pull_tiles<1, false, true>(P, S, fcur, P.bvis32, fnext, nxt);
         if (!grid_sync(P)) return;
 
         // level update: visited |= next, levels of the new vertices, clear
@@ -958,13 +1025,15 @@ __global__ void __launch_bounds__(NT) k_bfs(KParams P)
             Ctrl *c = P.ctrl;
             c->n_act[old] = 0u;
             c->n_chunk[old] = 0u;
-            c->tile_next[old] = 0u;
         }
         if (!grid_sync(P)) return;
     }
     stats_flush(P, S);
     if (blockIdx.x == 0 && tid == 0) {
         Ctrl *c = P.ctrl;
+        // Every block has passed the last barrier and reads only n_act[cur],
+        // which is already 0: all slots can be cleared for the next call.
+        for (int s = 0; s < 3; ++s) { c->n_act[s] = 0u; c->n_chunk[s] = 0u; }
         c->bfs_levels = L - 1u;   // the loop stops when frontier L-1 is empty
         c->bfs_push_levels = push_levels;
         c->path = 0u;
@@ -974,7 +1043,7 @@ __global__ void __launch_bounds__(NT) k_bfs(KParams P)
 }
 
 // Withholds block 0 from the barrier so every other block's wait expires.
-__global__ void __launch_bounds__(NT) k_selftest_wait(KParams P)
+__global__ void __launch_bounds__(NT, 4) k_selftest_wait(KParams P)
 {
     if (blockIdx.x == 0) return;
     grid_sync(P);
@@ -994,6 +1063,7 @@ struct dbs_workspace {
     dbs_exec_opts opts{};
     float *x_dense = nullptr;
     uint32_t *xm32 = nullptr;
+    uint32_t *dxm32 = nullptr;
     uint32_t *act[3] = {nullptr, nullptr, nullptr};
     uint2 *chunks[3] = {nullptr, nullptr, nullptr};
     float *y_acc = nullptr;
@@ -1010,7 +1080,7 @@ namespace {
 
 void ws_free(dbs_workspace *w)
 {
-    cudaFree(w->x_dense); cudaFree(w->xm32); cudaFree(w->y_acc); cudaFree(w->yrm32);
+    cudaFree(w->x_dense); cudaFree(w->xm32); cudaFree(w->dxm32); cudaFree(w->y_acc); cudaFree(w->yrm32);
     cudaFree(w->ctile_cnt); cudaFree(w->bvis32); cudaFree(w->fm32[0]); cudaFree(w->fm32[1]);
     cudaFree(w->ctrl);
     for (int s = 0; s < 3; ++s) { cudaFree(w->act[s]); cudaFree(w->chunks[s]); }
@@ -1038,7 +1108,7 @@ KParams make_params(const dbs_matrix *A, dbs_workspace *w)
     P.csc_ref = A->d_csc_ref;
     P.payload = reinterpret_cast<const uint4 *>(A->d_payload);
     P.tiles = reinterpret_cast<const uint4 *>(A->d_tiles);
-    P.x_dense = w->x_dense; P.xm32 = w->xm32;
+    P.x_dense = w->x_dense; P.xm32 = w->xm32; P.dxm32 = w->dxm32;
     for (int s = 0; s < 3; ++s) { P.act[s] = w->act[s]; P.chunks[s] = w->chunks[s]; }
     P.y_acc = w->y_acc; P.yrm32 = w->yrm32; P.ctile_cnt = w->ctile_cnt; P.n_ctiles = w->n_ctiles;
     P.bvis32 = w->bvis32; P.fm32[0] = w->fm32[0]; P.fm32[1] = w->fm32[1];
@@ -1105,6 +1175,7 @@ dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
     w->n_ctiles = (uint32_t)((nbr + CTILE - 1) / CTILE);
     const size_t yrm_words = std::max<size_t>(1, (size_t)w->n_ctiles) * CTILE / 2 + 8;
     bool ok = dalloc(&w->x_dense, nbc * 16 + 16) && dalloc(&w->xm32, nbc / 2 + 8) &&
+              dalloc(&w->dxm32, nbc / 2 + 8) &&
               dalloc(&w->y_acc, nbr * 16 + 16) && dalloc(&w->yrm32, yrm_words) &&
               dalloc(&w->ctile_cnt, (size_t)w->n_ctiles + 1) && dalloc(&w->bvis32, nbr / 2 + 8) &&
               dalloc(&w->fm32[0], nbc / 2 + 8) && dalloc(&w->fm32[1], nbc / 2 + 8) && dalloc(&w->ctrl, 1);
@@ -1188,6 +1259,8 @@ dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx
     P.y_val = y_val;
     P.y_nnz = reinterpret_cast<long long *>(y_nnz);
     const void *fn = sr == DBS_PLUS_TIMES_F32 ? (const void *)k_spmspv_sparse<0> : (const void *)k_spmspv_sparse<1>;
+    P.slot = w->call_count & 1;
+    w->call_count++;
     w->last_was_bfs = false;
     return launch(fn, w->grid_sparse[sr == DBS_PLUS_TIMES_F32 ? 0 : 1], P, (cudaStream_t)stream);
 }
@@ -1223,8 +1296,9 @@ dbs_status dbs_bfs(const dbs_matrix *A, int64_t src, int32_t *levels, int32_t *n
     P.bfs_src = src;
     P.levels = levels;
     cudaStream_t s = (cudaStream_t)stream;
-    // The dense-x kernel alternates counter slots; BFS resets all of them
-    // itself, so the next dense call may start from either slot.
+    // Counter slots: a dense-x call leaves its own slot dirty and clears the
+    // other, so calls alternate slots; sparse-x and BFS calls leave every
+    // slot clear.
     w->call_count = 0;
     w->last_was_bfs = true;
     st = launch((const void *)k_bfs, w->grid_bfs, P, s);

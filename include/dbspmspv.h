@@ -202,7 +202,10 @@ dbs_status dbs_workspace_check(dbs_workspace *ws, void *stream);
  *   y_nnz         device int64[1]: number of output entries
  *   path          DBS_PATH_AUTO / _PUSH / _PULL
  * Errors returned immediately: DBS_ERR_INVALID_ARG, DBS_ERR_UNSUPPORTED
- * (plus-times on a pattern-only matrix), DBS_ERR_CUDA (launch failure). */
+ * (plus-times on a pattern-only matrix), DBS_ERR_CUDA (launch failure).
+ * An index outside [0, n) is skipped by the kernel and latched as
+ * DBS_ERR_INVALID_ARG (dbs_workspace_check); the call's outputs are then
+ * undefined.  With repeated indices one of their values is used. */
 dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx,
                       const float *x_val, int64_t x_nnz, const uint16_t *visited_mask,
                       int32_t *y_idx, float *y_val, int64_t *y_nnz, dbs_path path,

@@ -1,0 +1,105 @@
+"""GPU parity at the workloads' full sizes, through the same API and defaults
+the benchmark times.  The oracle is fast enough to check every output entry
+(and every BFS level) at these sizes, so nothing is sampled."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+import __graft_entry__  # noqa: E402
+
+__graft_entry__.build()
+import dynamic_sparsity_spmspv_gb300 as dbs  # noqa: E402
+from test_gpu_parity import assert_parity, _t  # noqa: E402
+
+PATHS = ("auto", "push", "pull")
+
+
+@pytest.fixture(scope="module")
+def full():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            cache.clear()
+            A = synth.config(name, "full")
+            cache[name] = (A, oracle.Oracle(A), dbs.DBMatrix.from_csr(A))
+        return cache[name]
+    return get
+
+
+def test_er_full(full):
+    A, O, M = full("er")
+    ws = dbs.Workspace(M)
+    for i in range(8):
+        x = synth.x_uniform(A.n, 41, [43, i])          # 1% of 4096, U[-1, 1]
+        for path in PATHS:
+            assert_parity(A, O, M, ws, x, path=path)
+
+
+def test_rmat_full_sweep_and_bfs(full):
+    A, O, M = full("rmat")
+    ws = dbs.Workspace(M, collect_stats=1)
+    expected_path = {1e-4: 1, 1e-3: 2, 1e-2: 2, 1e-1: 2, 5e-1: 2}
+    for d, p_exp in expected_path.items():
+        x = synth.x_uniform(A.n, int(round(d * A.n)), [44, 0, int(d * 1e6), 0], valued=False)
+        for path in PATHS:
+            assert_parity(A, O, M, ws, x, "or_and", path=path)
+            if path == "auto":
+                assert ws.stats()["path"] == p_exp, d
+    for i, src in enumerate(synth.bfs_sources(A, 16, [44, 7])):
+        ref = O.bfs_queue(int(src))
+        for path in (PATHS if i < 2 else ("auto",)):
+            lev, nl = dbs.bfs(M, int(src), ws=ws, path=path)
+            np.testing.assert_array_equal(lev.cpu().numpy(), ref)
+            assert nl == int(ref.max()) + 1
+
+
+def test_fem_full(full):
+    A, O, M = full("fem")
+    assert A.nnz == 382 ** 3
+    ws = dbs.Workspace(M)
+    for f in (1e-3, 1e-2, 1e-1):
+        x = synth.x_clusters(A.n, f, [45, int(f * 1e4)])
+        for path in PATHS:
+            assert_parity(A, O, M, ws, x, path=path)
+
+
+def test_llm_full_dense_and_sparse_x(full):
+    A, O, M = full("llm")
+    assert A.nnz == 4096 * 5504
+    ws = dbs.Workspace(M)
+    for t in range(12):
+        xd = synth.x_relu_topk(A.n, 1101, [46, t])
+        nz = np.nonzero(xd)[0].astype(np.int32)
+        x = synth.SparseVec(A.n, nz, xd[nz])
+        ri, rv, rs = O.spmspv(x)
+        for path in PATHS:
+            y = dbs.spmspv_dense(M, _t(xd), ws=ws, path=path).cpu().numpy()
+            assert ws.check() == 0
+            assert oracle.tolerance_ok(y[ri], rv, rs).all()
+            rest = np.ones(A.m, bool)
+            rest[ri] = False
+            assert (y[rest] == 0).all()
+        if t < 3:
+            for path in PATHS:
+                assert_parity(A, O, M, ws, x, path=path)
+
+
+def test_grid_hubs_full_bfs(full):
+    A, O, M = full("grid")
+    ws = dbs.Workspace(M)
+    for i, src in enumerate(synth.bfs_sources(A, 8, [47, 7])):
+        ref = O.bfs_queue(int(src))
+        for path in (PATHS if i == 0 else ("auto",)):
+            lev, nl = dbs.bfs(M, int(src), ws=ws, path=path)
+            np.testing.assert_array_equal(lev.cpu().numpy(), ref)
+            assert nl == int(ref.max()) + 1
+    x = synth.x_uniform(A.n, A.n // 1000, [47, 1], valued=False)
+    for path in PATHS:
+        assert_parity(A, O, M, ws, x, "or_and", path=path)

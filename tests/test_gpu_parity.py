@@ -213,7 +213,8 @@ def test_selector_boundary():
     ws = dbs.Workspace(M, collect_stats=1)
     O = oracle.Oracle(A)
     for nzb, expect in ((63, 1), (64, 2), (65, 2), (1, 1)):
-        blocks = np.arange(nzb) * 100
+        blocks = np.arange(nzb) * 97                   # all < 6400 column blocks
+        assert blocks.max() * 16 + 3 < n
         x = synth.SparseVec(n, (blocks * 16 + 3).astype(np.int32), np.ones(nzb, np.float32))
         assert_parity(A, O, M, ws, x)
         st = ws.stats()
@@ -243,6 +244,37 @@ def test_workspace_reuse_alternating_paths(small):
     for i in range(12):
         x = synth.x_uniform(A.n, [3, 700, 40, 70][i % 4], [i, 9])
         assert_parity(A, O, M, ws, x, path=PATHS[i % 3])
+
+
+def test_mixed_call_sequence_on_one_workspace():
+    """Dense-x, sparse-x, Boolean and BFS calls interleaved on one workspace:
+    each call must leave the scratch as the next one expects."""
+    A = synth.random_csr(900, 900, 0.01, 21)
+    A = synth.csr_from_coo(900, 900, *[np.r_[a, b] for a, b in zip(
+        (np.repeat(np.arange(900), np.diff(A.row_ptr)), A.col_idx, A.vals),
+        (A.col_idx, np.repeat(np.arange(900), np.diff(A.row_ptr)), A.vals))], dedupe=True)
+    O = oracle.Oracle(A)
+    M = dbs.DBMatrix.from_csr(A)
+    ws = dbs.Workspace(M)
+    ops = ["dense", "sparse", "dense", "dense", "bool", "bfs", "sparse", "dense", "bfs", "dense",
+           "sparse", "sparse", "bool", "dense", "bfs", "bfs", "sparse"]
+    for i, op in enumerate(ops):
+        path = PATHS[i % 3]
+        if op == "dense":
+            xd = synth.x_relu_topk(A.n, [5, 90, 400][i % 3], [i, 77])
+            nz = np.nonzero(xd)[0].astype(np.int32)
+            ri, rv, rs = O.spmspv(synth.SparseVec(A.n, nz, xd[nz]))
+            y = dbs.spmspv_dense(M, _t(xd), ws=ws, path=path).cpu().numpy()
+            assert oracle.tolerance_ok(y[ri], rv, rs).all(), (i, op)
+        elif op == "sparse":
+            assert_parity(A, O, M, ws, synth.x_uniform(A.n, [3, 50, 600][i % 3], [i, 78]), path=path)
+        elif op == "bool":
+            x = synth.x_uniform(A.n, [7, 200, 30][i % 3], [i, 79], valued=False)
+            assert_parity(A, O, M, ws, x, "or_and", path=path)
+        else:
+            lev, nl = dbs.bfs(M, i * 37 % A.n, ws=ws, path=path)
+            np.testing.assert_array_equal(lev.cpu().numpy(), O.bfs_queue(i * 37 % A.n))
+        assert ws.check() == 0
 
 
 @pytest.mark.parametrize("name", ["llm", "er", "fem"])
@@ -310,6 +342,17 @@ def test_wait_timeout_is_reported_and_recovers(small):
     assert ws.check() == 4                          # DBS_ERR_TIMEOUT, then cleared
     assert ws.check() == 0
     assert_parity(A, O, M, ws, synth.x_uniform(A.n, 30, 1))
+
+
+def test_out_of_range_x_index_is_reported(small):
+    """The kernel bounds-checks every listed index: an index >= n is skipped
+    and latched as DBS_ERR_INVALID_ARG instead of being read."""
+    A, O, M = small["er"]
+    ws = dbs.Workspace(M)
+    for sr, val in (("plus_times", np.array([1.0, 2.0], np.float32)), ("or_and", None)):
+        dbs.spmspv(M, _t(np.array([3, A.n + 5], np.int32)), _t(val), semiring=sr, ws=ws)
+        assert ws.check() == 1
+        assert_parity(A, O, M, ws, synth.x_uniform(A.n, 20, 3))     # workspace usable again
 
 
 def test_error_returns(small):
