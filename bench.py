@@ -261,13 +261,15 @@ def main():
     touched_x = {d: [counter.spmspv(x.idx) for x in xs[d]] for d in DENSITIES}
     bytes_x = {d: [] for d in DENSITIES}
     path_x = {d: [] for d in DENSITIES}
+    phase_x = {d: [] for d in DENSITIES}
     for d in DENSITIES:
         for xi in x_dev[d]:
             dbs.spmspv(M, xi, None, semiring="or_and", ws=ws, y_idx=y_idx, y_nnz=y_nnz)
             st = ws.stats()
             bytes_x[d].append(st["bytes_alg"])
             path_x[d].append(st["path"])
-    touched_bfs, bytes_bfs, edges_bfs, nlev_bfs, push_lev = [], [], [], [], []
+            phase_x[d].append(st["phase_ns"])
+    touched_bfs, bytes_bfs, edges_bfs, nlev_bfs, push_lev, phase_bfs = [], [], [], [], [], []
     deg = np.diff(A.row_ptr)
     for src in sources:
         _, nl = dbs.bfs(M, int(src), levels=levels, ws=ws)
@@ -278,6 +280,7 @@ def main():
         edges_bfs.append(int(deg[lev >= 0].sum()) // 2)
         nlev_bfs.append(nl)
         push_lev.append(st["bfs_push_levels"])
+        phase_bfs.append(st["phase_ns"])
     assert ws.check() == 0
     ws.set_opts(dbs.exec_opts(collect_stats=0))
 
@@ -367,11 +370,15 @@ def main():
             "bytes_alg_per_call": bytes_sp[d] / max(n_sp[d], 1),
             "gbs": bytes_sp[d] / (t_sp[d] * 1e-3) / 1e9,
             "frac_of_measured_hbm": bytes_sp[d] / (t_sp[d] * 1e-3) / 1e9 / peak,
-            "path": "push" if statistics.mode(path_x[d]) == 1 else "pull"})
+            "path": "push" if statistics.mode(path_x[d]) == 1 else "pull",
+            "device_phase_us_with_stats": [round(float(np.mean([p[i] for p in phase_x[d]])) / 1e3, 2)
+                                           for i in range(3)]})
     bfs_info = {"gteps_harmonic": None, "ms_per_bfs": t_bfs / args.steps,
                 "gteps": edges / (t_bfs * 1e-3) / 1e9, "levels_mean": float(np.mean(nlev_bfs)),
                 "push_levels_mean": float(np.mean(push_lev)),
-                "gbs": bytes_b / (t_bfs * 1e-3) / 1e9}
+                "gbs": bytes_b / (t_bfs * 1e-3) / 1e9,
+                "device_phase_us_with_stats": [round(float(np.mean([p[i] for p in phase_bfs])) / 1e3, 2)
+                                               for i in range(3)]}
     # harmonic mean of per-source GTEPS from per-call times
     per_src_t = {}
     for kind, d, i, e0, e1 in rec:

@@ -183,7 +183,9 @@ class Workspace:
     def stats(self, stream=None) -> dict:
         s = dbs_stats()
         _lib.check("dbs_last_stats", _lib.load().dbs_last_stats(self._h, _stream_handle(stream), ctypes.byref(s)))
-        return {f: getattr(s, f) for f, _ in s._fields_}
+        d = {f: getattr(s, f) for f, _ in s._fields_}
+        d["phase_ns"] = list(s.phase_ns)
+        return d
 
     def selftest_wait_timeout(self, stream=None):
         _lib.check("dbs_selftest_wait_timeout",

@@ -42,7 +42,7 @@ class dbs_stats(ctypes.Structure):
     _fields_ = [("path", I32), ("status", I32), ("n_nzblk", I64), ("n_blk", I64),
                 ("x_active", I64), ("visited_blocks", I64), ("hit_blocks", I64),
                 ("touched_nnz", I64), ("bytes_alg", I64), ("y_nnz", I64),
-                ("bfs_levels", I32), ("bfs_push_levels", I32)]
+                ("bfs_levels", I32), ("bfs_push_levels", I32), ("phase_ns", I64 * 3)]
 
 
 # name -> (restype, argtypes)

@@ -15,10 +15,22 @@
 //                         This is the paper's csc2csr mapping resolved to the
 //                         shared payload, so push reaches a block in one load.
 //   payload  uint4[P]     the low-level blocks, 16-byte aligned
-//   tiles    uint4[T]     pull work units {p0, p1, rb0, span} (Section 3.3.2)
+//   tiles    uint4[T]     pull work units {p0, p1, rb0, span | flags << 16} (Section 3.3.2)
+//   tile_ref u32[T]       payload offset of each tile's first block
 //
-// meta word: bits 0-15 column-occupancy mask of the block (bit c = local
-// column c holds an entry), bits 16-18 format, bits 24-31 nnz - 1.
+// blk_desc.x holds the column block in bits 0-26 and, in bits 27-31, the
+// block's row block relative to the first row block of its pull tile, so a
+// pull task needs no row-block search.  Tile flag bit 0: the tile holds at
+// least one block with a payload (not inline).
+//
+// meta word (the same word in both views):
+//   stored block:  bits 0-15 column-occupancy mask (bit c = local column c
+//                  holds an entry), bits 16-18 format, bits 19-26 nnz - 1,
+//                  bit 31 = 0;
+//   inline block:  a pattern-only COO block with at most 3 entries keeps its
+//                  coordinates in the word itself and has no payload:
+//                  bits 0-23 coordinates (byte k = row << 4 | col of entry k;
+//                  unused bytes repeat entry 0), bits 24-25 nnz - 1, bit 31 = 1.
 //
 // Payload layouts (bytes from the 16-byte aligned start; bit k of a row mask
 // is local column k, bit k of a column mask is local row k, as in Figure 5's
@@ -47,20 +59,49 @@ namespace dbs {
 constexpr int BS = 16;
 constexpr uint32_t FMT_COO = 0, FMT_DENSE = 1, FMT_FCSR = 2, FMT_FCSC = 3, FMT_PCSR = 4;
 
-// Pull tiles: at most this many blocks (one CTA pass of 256 threads x 8) and
-// this many row blocks (shared-memory row accumulators).
-constexpr uint32_t TILE_MAX_BLOCKS = 2048;
-constexpr uint32_t TILE_MAX_SPAN = 64;
+// Pull tiles (one warp task each): at most this many blocks (32 lanes x 8) and
+// this many row blocks (the warp's shared-memory row accumulators).
+constexpr uint32_t TILE_MAX_BLOCKS = 256;
+constexpr uint32_t TILE_MAX_SPAN = 32;
 // Push tasks: CSC positions per work item (one warp, one position per lane).
 constexpr uint32_t PUSH_CHUNK = 32;
 
+constexpr uint32_t DESC_COL_MASK = 0x07FFFFFFu;   // column block bits of blk_desc.x
+constexpr uint32_t DESC_LRB_SHIFT = 27;            // local row block bits of blk_desc.x
+constexpr uint32_t TILE_HAS_STORED = 1u << 16;     // flag in tiles[].w
+
+constexpr uint32_t META_INLINE = 0x80000000u;
+constexpr uint32_t INLINE_MAX_NNZ = 3;
+
 DBS_HD uint32_t meta_pack(uint32_t cmask, uint32_t fmt, uint32_t nnz)
 {
-    return (cmask & 0xFFFFu) | (fmt << 16) | ((nnz - 1u) << 24);
+    return (cmask & 0xFFFFu) | (fmt << 16) | ((nnz - 1u) << 19);
 }
-DBS_HD uint32_t meta_cmask(uint32_t m) { return m & 0xFFFFu; }
-DBS_HD uint32_t meta_fmt(uint32_t m) { return (m >> 16) & 7u; }
-DBS_HD uint32_t meta_nnz(uint32_t m) { return (m >> 24) + 1u; }
+// coords: nnz (1..3) bytes row << 4 | col
+DBS_HD uint32_t meta_pack_inline(const uint8_t *coords, uint32_t nnz)
+{
+    uint32_t w = 0;
+    for (uint32_t k = 0; k < 3u; ++k) w |= (uint32_t)coords[k < nnz ? k : 0u] << (8u * k);
+    return META_INLINE | ((nnz - 1u) << 24) | w;
+}
+DBS_HD bool meta_inline(uint32_t m) { return (m & META_INLINE) != 0u; }
+DBS_HD uint32_t meta_fmt(uint32_t m) { return meta_inline(m) ? FMT_COO : (m >> 16) & 7u; }
+DBS_HD uint32_t meta_nnz(uint32_t m) { return meta_inline(m) ? ((m >> 24) & 3u) + 1u : ((m >> 19) & 0xFFu) + 1u; }
+DBS_HD uint32_t meta_cmask(uint32_t m)
+{
+    return meta_inline(m) ? (1u << (m & 15u)) | (1u << ((m >> 8) & 15u)) | (1u << ((m >> 16) & 15u))
+                          : m & 0xFFFFu;
+}
+// Rows of an inline block reached from the active columns `act`.
+DBS_HD uint32_t meta_inline_found(uint32_t m, uint32_t act)
+{
+    uint32_t f = 0;
+    for (uint32_t k = 0; k < 3u; ++k) {
+        const uint32_t e = (m >> (8u * k)) & 0xFFu;
+        f |= ((act >> (e & 15u)) & 1u) << (e >> 4);
+    }
+    return f;
+}
 
 // Section 3.3.2: Dense 4, ForceCSR / ForceCSC / (patched) CSR 2, COO 1.
 DBS_HD uint32_t fmt_weight(uint32_t fmt)
@@ -81,6 +122,11 @@ DBS_HD uint32_t payload_bytes(uint32_t fmt, uint32_t nnz, bool valued)
 DBS_HD uint32_t payload_units(uint32_t fmt, uint32_t nnz, bool valued)
 {
     return (payload_bytes(fmt, nnz, valued) + 15u) >> 4;
+}
+// Payload units of a block given its meta word (0 for inline blocks).
+DBS_HD uint32_t meta_units(uint32_t m, bool valued)
+{
+    return meta_inline(m) ? 0u : payload_units(meta_fmt(m), meta_nnz(m), valued);
 }
 
 // Offsets of the structural arrays.

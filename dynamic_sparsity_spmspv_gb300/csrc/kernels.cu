@@ -36,16 +36,16 @@ namespace {
 constexpr int NT = 256;              // threads per CTA
 constexpr int NW = NT / 32;          // warps per CTA
 constexpr uint32_t FULL = 0xFFFFFFFFu;
-constexpr uint32_t HEAVY_CAP = 1040; // heavy blocks per pull tile (weight cap 2048 / 2 + slack)
-constexpr uint32_t CTILE = 4096;     // row blocks per compaction tile (256 threads x 16)
+constexpr uint32_t CTILE = 2 * NT;   // row blocks per compaction tile (one mask word per thread)
 
 struct Ctrl {
     unsigned int bar_count;
     unsigned int bar_gen;
     unsigned int err;
     unsigned int path;
-    unsigned int n_act[3];
-    unsigned int n_chunk[3];
+    unsigned int n_blk[3];      // nonzero vector blocks (N_nzblk) of the slot's vector
+    unsigned int n_act[3];      // push list length of the slot
+    unsigned int n_chunk[3];    // push task count of the slot
     unsigned int bfs_levels;
     unsigned int bfs_push_levels;
     unsigned int pad0;
@@ -57,6 +57,7 @@ struct Ctrl {
     unsigned long long nzblk;
     unsigned long long y_nnz;
     unsigned long long reached;
+    unsigned long long t_phase[4];   // device timestamps: start, metadata done, traversal done, end
 };
 
 struct KParams {
@@ -72,6 +73,7 @@ struct KParams {
     const uint32_t *__restrict__ csc_ref;
     const uint4 *__restrict__ payload;
     const uint4 *__restrict__ tiles;
+    const uint32_t *__restrict__ tile_ref;
     // call
     int path_force;
     const int32_t *x_idx;
@@ -212,19 +214,67 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t *total)
     return r;
 }
 
-// Appends column block cb to the active list of `slot` and its CSC range to
-// the push task list (32 positions per task): the flattened matrix-block
-// tasks of Section 3.3.2.
-__device__ void append_active(const KParams &P, int slot, uint32_t cb)
+// Push list construction (Section 3.3.2: matrix-block tasks flattened over
+// the active column blocks).  Every thread of the CTA calls this together;
+// thread t appends column block cb if `want`.  The CTA reserves its list
+// entries and its tasks (32 CSC positions each) with one atomic per counter
+// and then writes the tasks with all its threads, so a column block with
+// thousands of tasks does not serialise on one thread.
+struct ListStage {
+    uint32_t cb[NT];
+    uint32_t q0[NT];
+    uint32_t cstart[NT + 1];
+    uint32_t base_a, base_c;
+};
+
+__device__ void cta_append(const KParams &P, ListStage &L, int slot, bool want, uint32_t cb)
 {
-    Ctrl *c = P.ctrl;
-    uint32_t i = atomicAdd(&c->n_act[slot], 1u);
-    P.act[slot][i] = cb;
-    uint32_t s = __ldg(P.cb_ptr + cb), e = __ldg(P.cb_ptr + cb + 1);
-    if (e <= s) return;
-    uint32_t nch = (e - s + PUSH_CHUNK - 1) / PUSH_CHUNK;
-    uint32_t base = atomicAdd(&c->n_chunk[slot], nch);
-    for (uint32_t k = 0; k < nch; ++k) P.chunks[slot][base + k] = make_uint2(s + k * PUSH_CHUNK, cb);
+    const int tid = threadIdx.x;
+    uint32_t s = 0, e = 0;
+    if (want) {
+        s = __ldg(P.cb_ptr + cb);
+        e = __ldg(P.cb_ptr + cb + 1);
+    }
+    const uint32_t nch = want ? (e - s + PUSH_CHUNK - 1) / PUSH_CHUNK : 0u;
+    uint32_t tot_a, tot_c;
+    const uint32_t oa = block_excl_scan(want ? 1u : 0u, &tot_a);
+    const uint32_t oc = block_excl_scan(nch, &tot_c);
+    if (tot_a == 0u) return;
+    if (tid == 0) {
+        L.base_a = atomicAdd(&P.ctrl->n_act[slot], tot_a);
+        L.base_c = tot_c ? atomicAdd(&P.ctrl->n_chunk[slot], tot_c) : 0u;
+        L.cstart[tot_a] = tot_c;
+    }
+    if (want) {
+        L.cb[oa] = cb;
+        L.q0[oa] = s;
+        L.cstart[oa] = oc;
+    }
+    __syncthreads();
+    if (want) P.act[slot][L.base_a + oa] = cb;
+    for (uint32_t t = tid; t < tot_c; t += NT) {
+        uint32_t lo = 0, hi = tot_a - 1u;       // last entry whose tasks start at or before t
+        while (lo < hi) {
+            const uint32_t mid = (lo + hi + 1u) >> 1;
+            if (L.cstart[mid] <= t) lo = mid; else hi = mid - 1u;
+        }
+        P.chunks[slot][L.base_c + t] = make_uint2(L.q0[lo] + (t - L.cstart[lo]) * PUSH_CHUNK, L.cb[lo]);
+    }
+    __syncthreads();
+}
+
+// Sum of one value per thread over the CTA, added to *dst once per CTA.
+template <class T>
+__device__ __forceinline__ void cta_count(T *dst, uint32_t v)
+{
+    uint32_t tot;
+    block_excl_scan(v, &tot);
+    if (threadIdx.x == 0 && tot) atomicAdd(dst, (T)tot);
+}
+
+__device__ __forceinline__ void stamp(const KParams &P, int i)
+{
+    if (P.stats && blockIdx.x == 0 && threadIdx.x == 0) P.ctrl->t_phase[i] = globaltimer();
 }
 
 // ------------------------------------------------------------ microkernels
@@ -387,6 +437,7 @@ __device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint
 // block reached from its active columns.
 __device__ __forceinline__ uint32_t bool_found(const uint8_t *__restrict__ b, uint32_t meta, uint32_t act)
 {
+    if (meta_inline(meta)) return meta_inline_found(meta, act);   // no payload to read
     const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
     uint32_t f = 0;
     if (fmt == FMT_COO) {
@@ -413,221 +464,191 @@ __device__ __forceinline__ uint32_t bool_found(const uint8_t *__restrict__ b, ui
 
 __device__ __forceinline__ uint32_t bool_bytes(uint32_t meta)
 {
-    uint32_t fmt = meta_fmt(meta);
-    return fmt == FMT_COO ? meta_nnz(meta) : 32u;
+    if (meta_inline(meta)) return 0u;
+    return meta_fmt(meta) == FMT_COO ? meta_nnz(meta) : 32u;
 }
 
 // ------------------------------------------------------------- traversal
 
-struct Smem {
-    uint32_t rbp[TILE_MAX_SPAN + 1];
-    float y[TILE_MAX_SPAN * 16];
-    uint32_t rm[TILE_MAX_SPAN];
-    uint32_t vis[TILE_MAX_SPAN];
-    uint4 heavy[HEAVY_CAP];
-    float wacc[NW][16];
-    float wx[NW][16];
-    uint32_t nheavy;
-    uint32_t tile;
-    unsigned long long st[4];   // visited, hits, touched, bytes
+// Per-warp state of a pull task.
+struct WarpPull {
+    uint32_t rm[TILE_MAX_SPAN];       // touched (Boolean: found) rows per row block
+    uint32_t vis[TILE_MAX_SPAN];      // visited rows per row block (Boolean)
+    float y[TILE_MAX_SPAN * 16];      // partial row sums (plus-times)
+    uint4 q[TILE_MAX_BLOCKS];         // hit blocks with a payload: {ref, meta, col, lrb | act << 16}
+    uint32_t nq;
 };
 
+struct Smem {
+    WarpPull wp[NW];
+    float wacc[NW][16];
+    float wx[NW][16];
+    unsigned long long st[4];   // visited, hits, touched, bytes
+    ListStage L;
+};
+
+extern __shared__ __align__(128) unsigned char smem_raw[];
+
+// Statistics: a warp sums its lanes' counts and one lane adds them to the
+// CTA's shared counter (all lanes of the warp must call it).
 __device__ __forceinline__ void stat_add(Smem &S, int i, unsigned long long v)
 {
-    if (v) atomicAdd(&S.st[i], v);
+    const unsigned long long w = __reduce_add_sync(FULL, (unsigned)v);
+    if ((threadIdx.x & 31) == 0 && w) atomicAdd(&S.st[i], w);
 }
 
-// Byte i (0..15) / 32-bit word i (0..3) of a 16-byte payload chunk.
-__device__ __forceinline__ uint32_t chunk_word(const uint4 &c, uint32_t i)
-{
-    return i == 0 ? c.x : i == 1 ? c.y : i == 2 ? c.z : c.w;
-}
-__device__ __forceinline__ uint32_t chunk_byte(const uint4 &c, uint32_t i)
-{
-    return (chunk_word(c, i >> 2) >> ((i & 3u) << 3)) & 0xFFu;
-}
-
-// COO block whose payload fits in its first 16-byte chunk (already loaded):
-// Boolean up to 16 entries, plus-times up to 3 (coordinates, then values at
-// align4(nnz)).  Returns the touched (Boolean: found) rows.
-template <int SR>
-__device__ __forceinline__ uint32_t coo_chunk(const uint4 &c, uint32_t nnz, uint32_t act, const float *xb,
-                                              float *sy)
-{
-    uint32_t rows = 0;
-    const uint32_t vw = (nnz + 3u) >> 2;
-    for (uint32_t k = 0; k < nnz; ++k) {
-        const uint32_t e = chunk_byte(c, k);
-        const uint32_t col = e & 15u;
-        if ((act >> col) & 1u) {
-            const uint32_t r = e >> 4;
-            rows |= 1u << r;
-            if (SR == 0) atomicAdd(&sy[r], __uint_as_float(chunk_word(c, vw + k)) * xval(xb, col));
-        }
-    }
-    return rows;
-}
-
-// Pull (Section 3.3.2): CTAs take tiles of consecutive primary blocks in a
-// static order, prefetching the next tile's descriptor.  Stage 1 runs in
-// batches of PB blocks per thread whose descriptor, mask, payload-reference
-// and first-chunk loads are each issued together, so every thread keeps
-// several independent requests in flight (the role of the paper's
-// double-buffered asynchronous prefetch).
-// SR 0 = plus-times, 1 = Boolean.  DOUT: dense output y.  BFS: first touch
-// of a next-frontier row block appends it to the list of slot `nslot`.
-template <int SR, bool DOUT, bool BFS>
+// Pull (Section 3.3.2): every warp takes tiles of consecutive primary blocks
+// (load-weighted segments of at most 256 blocks and 32 row blocks) and works
+// through them without block-wide synchronisation.  Each lane issues the
+// descriptor loads of its 8 blocks together and then their 8 vector-mask
+// lookups, so many independent requests are in flight per warp.  Inline
+// blocks finish right there; hits with a payload are queued (payload offsets
+// from a warp prefix sum of the block sizes) and drained by the lanes, or by
+// the whole warp for the Dense / Force / patched-CSR microkernels.  Row
+// results gather in the warp's shared-memory accumulators and are written
+// back once per row block (Section 3.3.3).
+// SR 0 = plus-times, 1 = Boolean.  DOUT: dense output y.  L1M: the vector
+// masks may be cached in L1 (they do not change during the launch).
+template <int SR, bool DOUT, bool L1M>
 __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const uint32_t *vis,
-                           uint32_t *out_rm, int nslot)
+                           uint32_t *out_rm)
 {
-    constexpr int PB = 4;
-    constexpr int NBATCH = (int)TILE_MAX_BLOCKS / (NT * PB);
+    constexpr int WK = (int)TILE_MAX_BLOCKS / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    WarpPull &W = S.wp[warp];
     const float *xv = P.xv;
-    uint32_t t = blockIdx.x;
-    uint4 td = t < P.T ? __ldg(P.tiles + t) : make_uint4(0, 0, 0, 0);
-    for (; t < P.T; t += gridDim.x) {
-        const uint32_t p0 = td.x, p1 = td.y, rb0 = td.z, span = td.w;
-        if (tid <= (int)span) S.rbp[tid] = __ldg(P.rb_ptr + rb0 + tid);
-        for (uint32_t i = tid; i < span * 16u; i += NT) S.y[i] = 0.0f;
-        if (tid < (int)span) {
-            S.rm[tid] = 0u;
-            S.vis[tid] = vis ? mask16(vis, rb0 + tid) : 0u;
+    const bool valued = P.valued != 0;
+    const uint32_t nwarps = gridDim.x * NW;
+    unsigned long long c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
+    for (uint32_t t = blockIdx.x * NW + warp; t < P.T; t += nwarps) {
+        const uint4 td = __ldg(P.tiles + t);
+        const uint32_t p0 = td.x, p1 = td.y, rb0 = td.z, span = td.w & 0xFFFFu, nblk = p1 - p0;
+        const bool stored = (td.w & TILE_HAS_STORED) != 0u;
+        uint2 d[WK];
+#pragma unroll
+        for (int k = 0; k < WK; ++k) {
+            const uint32_t li = (uint32_t)(k * 32 + lane);
+            d[k] = li < nblk ? __ldcs(P.blk_desc + p0 + li) : make_uint2(0u, 0u);
         }
-        if (tid == 0) S.nheavy = 0u;
-        __syncthreads();
-        const uint32_t tn = t + gridDim.x;
-        const uint4 td_next = tn < P.T ? __ldg(P.tiles + tn) : make_uint4(0, 0, 0, 0);
+        // first / last row block of the task shared with a neighbour task?
+        uint32_t edge = 0;
+        if (lane == 0) edge = __ldg(P.rb_ptr + rb0) < p0 ? 1u : 0u;
+        if (lane == 1) edge = __ldg(P.rb_ptr + rb0 + span) > p1 ? 2u : 0u;
+        edge = __reduce_or_sync(FULL, edge);
+        if (lane < (int)span) {
+            W.rm[lane] = 0u;
+            if (SR == 1) W.vis[lane] = vis ? mask16(vis, rb0 + lane) : 0u;
+        }
+        if (SR == 0)
+            for (uint32_t i = lane; i < span * 16u; i += 32) W.y[i] = 0.0f;
+        if (lane == 0) W.nq = 0u;
+        __syncwarp();
 
-        // Stage 1: block descriptors against the vector-block masks; COO and
-        // Boolean blocks are finished in place, the rest are queued.
-        unsigned long long c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
-        uint32_t lo = 0;
-        {
-            uint32_t hi = span - 1u;
-            const uint32_t p = p0 + tid;
-            while (lo < hi) {
-                uint32_t mid = (lo + hi + 1u) >> 1;
-                if (S.rbp[mid] <= p) lo = mid; else hi = mid - 1u;
+        uint32_t carry = stored ? __ldg(P.tile_ref + t) : 0u;
+#pragma unroll
+        for (int k = 0; k < WK; ++k) {
+            const uint32_t li = (uint32_t)(k * 32 + lane);
+            const uint32_t meta = d[k].y, col = d[k].x & DESC_COL_MASK, lrb = d[k].x >> DESC_LRB_SHIFT;
+            uint32_t ref = 0;
+            if (stored) {                                     // warp-uniform
+                const uint32_t sz = li < nblk ? meta_units(meta, valued) : 0u;
+                const uint32_t inc = warp_incl_scan(sz, lane);
+                ref = carry + inc - sz;
+                carry += __shfl_sync(FULL, inc, 31);
             }
-        }
-#pragma unroll 1
-        for (int bt = 0; bt < NBATCH; ++bt) {
-            if (p0 + tid + (uint32_t)(bt * PB * NT) >= p1) break;
-            uint2 d[PB];
-            uint32_t lr[PB], act[PB], ref[PB];
-            uint4 c0[PB];
-#pragma unroll
-            for (int k = 0; k < PB; ++k) {
-                const uint32_t p = p0 + tid + (uint32_t)((bt * PB + k) * NT);
-                d[k] = p < p1 ? __ldg(P.blk_desc + p) : make_uint2(0u, 0u);
-            }
-#pragma unroll
-            for (int k = 0; k < PB; ++k) {
-                const uint32_t p = p0 + tid + (uint32_t)((bt * PB + k) * NT);
-                while (lo + 1u < span && S.rbp[lo + 1u] <= p) ++lo;
-                lr[k] = lo;
-                const bool ok = p < p1 && !(SR == 1 && S.vis[lo] == 0xFFFFu);
-                act[k] = ok ? mask16(xm, d[k].x) : 0u;
-                if (p < p1) c_bytes += 8;
-            }
-#pragma unroll
-            for (int k = 0; k < PB; ++k) {
-                const uint32_t p = p0 + tid + (uint32_t)((bt * PB + k) * NT);
-                if (act[k]) { ++c_vis; c_touch += meta_nnz(d[k].y); }
-                act[k] &= meta_cmask(d[k].y);
-                ref[k] = act[k] ? __ldg(P.blk_ref + p) : 0u;
-            }
-#pragma unroll
-            for (int k = 0; k < PB; ++k) c0[k] = act[k] ? __ldg(P.payload + ref[k]) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int k = 0; k < PB; ++k) {
-                if (!act[k]) continue;
-                const uint32_t meta = d[k].y, fmt = meta_fmt(meta), nnz = meta_nnz(meta), col = d[k].x;
-                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + ref[k]);
-                ++c_hit;
-                c_bytes += 4;
-                uint32_t rows = 0;
-                if (fmt == FMT_COO && nnz <= (SR == 1 ? 16u : 3u)) {
-                    rows = coo_chunk<SR>(c0[k], nnz, act[k], xv + (size_t)col * 16u, &S.y[lr[k] * 16u]);
-                    c_bytes += SR == 1 ? nnz : 5u * nnz;
-                } else if (SR == 1) {
-                    rows = bool_found(b, meta, act[k]);
-                    c_bytes += bool_bytes(meta);
-                } else if (fmt == FMT_COO) {
-                    float *sy = &S.y[lr[k] * 16u];
-                    rows = coo_lane(b, nnz, act[k], xv + (size_t)col * 16u, true,
-                                    [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
-                    c_bytes += val_offset(FMT_COO, nnz) + 4u * nnz;
+            const bool skip = li >= nblk || (SR == 1 && vis && W.vis[lrb] == 0xFFFFu);
+            const uint32_t w = skip ? 0u : (L1M ? __ldca(xm + (col >> 1)) : __ldcg(xm + (col >> 1)));
+            const uint32_t m = (w >> ((col & 1u) << 4)) & 0xFFFFu;
+            if (P.stats && m) { ++c_vis; c_touch += meta_nnz(meta); }
+            const uint32_t a = m & meta_cmask(meta);
+            if (a) {
+                if (SR == 1 && meta_inline(meta)) {
+                    atomicOr(&W.rm[lrb], meta_inline_found(meta, a));
                 } else {
-                    uint32_t slot = atomicAdd(&S.nheavy, 1u);
-                    if (slot < HEAVY_CAP) S.heavy[slot] = make_uint4(ref[k], meta, col, lr[k]);
-                    else latch_error(P, DBS_ERR_INTERNAL);
+                    const uint32_t slot = atomicAdd(&W.nq, 1u);
+                    W.q[slot] = make_uint4(ref, meta, col, lrb | (a << 16));
                 }
-                if (rows) atomicOr(&S.rm[lr[k]], rows);
+                if (P.stats) ++c_hit;
             }
         }
-        __syncthreads();
+        __syncwarp();
 
-        // Stage 2 (plus-times): warps run the queued blocks' microkernels.
+        // payload-carrying hits: COO and Boolean blocks one per lane, the
+        // other formats by the whole warp
+        const uint32_t nq = W.nq;
+        for (uint32_t i = lane; i < nq; i += 32) {
+            const uint4 e = W.q[i];
+            const uint32_t meta = e.y, lrb = e.w & 0xFFFFu, a = e.w >> 16;
+            const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + e.x);
+            uint32_t rows = 0;
+            if (SR == 1) {
+                rows = bool_found(b, meta, a);
+                if (P.stats) c_bytes += bool_bytes(meta);
+            } else if (meta_fmt(meta) == FMT_COO) {
+                const uint32_t nnz = meta_nnz(meta);
+                float *sy = &W.y[lrb * 16u];
+                rows = coo_lane(b, nnz, a, xv + (size_t)e.z * 16u, true,
+                                [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
+                if (P.stats) c_bytes += val_offset(FMT_COO, nnz) + 4u * nnz;
+            }
+            if (rows) atomicOr(&W.rm[lrb], rows);
+        }
         if (SR == 0) {
-            const uint32_t nh = min(S.nheavy, HEAVY_CAP);
-            for (uint32_t i = warp; i < nh; i += NW) {
-                const uint4 h = S.heavy[i];
-                const uint32_t act = meta_cmask(h.y) & mask16(xm, h.z);
+            __syncwarp();
+            for (uint32_t i = 0; i < nq; ++i) {
+                const uint4 e = W.q[i];
+                if (meta_fmt(e.y) == FMT_COO) continue;           // warp-uniform
+                const uint32_t lrb = e.w & 0xFFFFu, a = e.w >> 16;
                 uint32_t by = 0;
-                RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + h.x), h.y, act,
-                                    xv + (size_t)h.z * 16u, lane, S.wacc[warp], &by);
-                if (lane < 16 && o.touched) atomicAdd(&S.y[h.w * 16u + lane], o.sum);
-                uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
+                RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + e.x), e.y, a,
+                                    xv + (size_t)e.z * 16u, lane, S.wacc[warp], &by);
+                if (lane < 16 && o.touched) W.y[lrb * 16u + lane] += o.sum;
+                const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
                 if (lane == 0) {
-                    if (bits) atomicOr(&S.rm[h.w], bits);
-                    c_bytes += by;
+                    if (bits) W.rm[lrb] |= bits;
+                    if (P.stats) c_bytes += by;
                 }
+                __syncwarp();
             }
-            __syncthreads();
         }
+        __syncwarp();
 
-        // Stage 3: write the tile's row blocks back.  A row block entirely
-        // inside the tile is stored; one shared with a neighbour tile is added.
-        for (uint32_t i = tid; i < span * 16u; i += NT) {
-            const uint32_t lrb = i >> 4, r = i & 15u, rb = rb0 + lrb;
-            const uint32_t rm = S.rm[lrb];
-            if (!rm) continue;
-            const bool partial = S.rbp[lrb] < p0 || S.rbp[lrb + 1] > p1;
-            if (SR == 0) {
-                if ((rm >> r) & 1u) {
-                    float *dst = DOUT ? P.y_dense : P.y_acc;
-                    const size_t row = (size_t)rb * 16u + r;
-                    if (partial) atomicAdd(dst + row, S.y[i]);
-                    else dst[row] = S.y[i];
-                }
-                if (!DOUT && r == 0) or16(out_rm, rb, rm);
-            } else if (r == 0) {
-                uint32_t f = rm & ~S.vis[lrb];
-                if (f) {
-                    uint32_t old = or16(out_rm, rb, f);
-                    if (BFS && old == 0u) append_active(P, nslot, rb);
-                }
+        // write the task's row blocks back: a row block entirely inside the
+        // task is stored, one shared with a neighbouring task is added
+        if (SR == 1) {
+            if (lane < (int)span) {
+                const uint32_t f = W.rm[lane] & ~W.vis[lane];
+                if (f) or16(out_rm, rb0 + lane, f);
             }
+        } else {
+            for (uint32_t i = lane; i < span * 16u; i += 32) {
+                const uint32_t lrb = i >> 4, r = i & 15u;
+                if (!((W.rm[lrb] >> r) & 1u)) continue;
+                const bool partial = (lrb == 0u && (edge & 1u)) || (lrb == span - 1u && (edge & 2u));
+                float *dst = DOUT ? P.y_dense : P.y_acc;
+                const size_t row = (size_t)(rb0 + lrb) * 16u + r;
+                if (partial) atomicAdd(dst + row, W.y[i]);
+                else dst[row] = W.y[i];
+            }
+            if (!DOUT && lane < (int)span && W.rm[lane]) or16(out_rm, rb0 + lane, W.rm[lane]);
         }
-        if (P.stats) {
-            stat_add(S, 0, c_vis);
-            stat_add(S, 1, c_hit);
-            stat_add(S, 2, c_touch);
-            stat_add(S, 3, c_bytes + (tid == 0 ? 16u + 4u * (span + 1u) : 0u));
-        }
-        td = td_next;
-        __syncthreads();
+        if (P.stats && lane == 0) c_bytes += 8u * nblk + 24u + (stored ? 4u : 0u);
+        __syncwarp();
+    }
+    if (P.stats) {
+        stat_add(S, 0, c_vis);
+        stat_add(S, 1, c_hit);
+        stat_add(S, 2, c_touch);
+        stat_add(S, 3, c_bytes);
     }
 }
 
 // Push (Section 3.3.2): warps take tasks of 32 consecutive CSC positions of
 // one active column block; the active vector block is cached in shared memory
 // (Section 3.3.3) and each block's rows are written back with atomics.
-template <int SR, bool DOUT, bool BFS>
+template <int SR, bool DOUT>
 __device__ void push_tasks(const KParams &P, Smem &S, const uint32_t *xm, const uint32_t *vis,
-                           uint32_t *out_rm, int cslot, int nslot)
+                           uint32_t *out_rm, int cslot)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t nch = ld_cg(&P.ctrl->n_chunk[cslot]);
@@ -661,9 +682,11 @@ __device__ void push_tasks(const KParams &P, Smem &S, const uint32_t *xm, const 
                 if (vm == 0xFFFFu) act = 0;
             }
             if (act) {
-                ref = __ldg(P.csc_ref + q);
                 ++c_hit;
-                c_bytes += 4;
+                if (!meta_inline(meta)) {
+                    ref = __ldg(P.csc_ref + q);
+                    c_bytes += 4;
+                }
             }
         }
         const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + ref);
@@ -671,10 +694,7 @@ __device__ void push_tasks(const KParams &P, Smem &S, const uint32_t *xm, const 
             if (act) {
                 uint32_t f = bool_found(b, meta, act) & ~vm;
                 c_bytes += bool_bytes(meta);
-                if (f) {
-                    uint32_t old = or16(out_rm, rb, f);
-                    if (BFS && old == 0u) append_active(P, nslot, rb);
-                }
+                if (f) or16(out_rm, rb, f);
             }
         } else {
             float *y = DOUT ? P.y_dense : P.y_acc;
@@ -707,16 +727,10 @@ __device__ void push_tasks(const KParams &P, Smem &S, const uint32_t *xm, const 
         }
     }
     if (P.stats) {
-        c_vis = __reduce_add_sync(FULL, (unsigned)c_vis);
-        c_hit = __reduce_add_sync(FULL, (unsigned)c_hit);
-        c_touch = __reduce_add_sync(FULL, (unsigned)c_touch);
-        c_bytes = __reduce_add_sync(FULL, (unsigned)c_bytes);
-        if (lane == 0) {
-            stat_add(S, 0, c_vis);
-            stat_add(S, 1, c_hit);
-            stat_add(S, 2, c_touch);
-            stat_add(S, 3, c_bytes);
-        }
+        stat_add(S, 0, c_vis);
+        stat_add(S, 1, c_hit);
+        stat_add(S, 2, c_touch);
+        stat_add(S, 3, c_bytes);
     }
 }
 
@@ -748,52 +762,89 @@ __device__ __forceinline__ void reset_stats(const KParams &P)
     Ctrl *c = P.ctrl;
     c->x_active = 0; c->visited = 0; c->hits = 0; c->touched = 0; c->bytes = 0;
     c->nzblk = 0; c->y_nnz = 0; c->reached = 0;
+    for (int i = 0; i < 4; ++i) c->t_phase[i] = 0;
 }
 
 // ------------------------------------------------------------- kernels
 
 // One SpMSpV with a sparse x (index list + values) and a sparse output.
-// Phases: metadata | traversal | compaction counts | compaction writes.
+// Phases: metadata | [push list] | traversal | compaction counts | writes.
 template <int SR>
 __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
 {
-    __shared__ Smem S;
+    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
     if (ld_cg(&P.ctrl->err) != 0u) return;
     const int tid = threadIdx.x;
     const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
+    const int slot = P.slot;
     stats_begin(S);
     if (blockIdx.x == 0 && tid == 0 && P.stats) reset_stats(P);
+    stamp(P, 0);
 
-    // Phase 1 (Section 4.1): scatter x, build blk_x_mask, count and list the
-    // nonzero vector blocks (first setter of a block appends it).
-    unsigned act_cnt = 0;
-    for (size_t e = gtid; e < (size_t)P.x_nnz; e += gsz) {
-        const uint32_t j = (uint32_t)__ldg(P.x_idx + e);
-        if (j >= (uint32_t)P.n) {                 // also catches negative indices
-            latch_error(P, DBS_ERR_INVALID_ARG);
-            continue;
+    // Phase 1 (Section 4.1): scatter x and set the blk_x_mask bits.  Lanes
+    // hitting the same mask word merge their bits and one of them issues the
+    // atomic; a block whose half of the word was empty is new and counted.
+    // Counts are added to the global total once per CTA.
+    const int lane = tid & 31;
+    uint32_t first = 0, act_cnt = 0;
+    for (size_t base = (size_t)blockIdx.x * NT + (tid & ~31); base < (size_t)P.x_nnz; base += gsz) {
+        const size_t e = base + lane;
+        uint32_t j = 0;
+        bool active = false;
+        if (e < (size_t)P.x_nnz) {
+            j = (uint32_t)__ldg(P.x_idx + e);
+            if (j >= (uint32_t)P.n) {                 // also catches negative indices
+                latch_error(P, DBS_ERR_INVALID_ARG);
+            } else {
+                const float v = P.x_val ? __ldg(P.x_val + e) : 1.0f;
+                active = v != 0.0f;
+                if (active && SR == 0) P.x_dense[j] = v;
+            }
         }
-        const float v = P.x_val ? __ldg(P.x_val + e) : 1.0f;
-        if (!(v != 0.0f)) continue;
-        ++act_cnt;
-        if (SR == 0) P.x_dense[j] = v;
-        const uint32_t sh = j & 31u;
-        const uint32_t old = atomicOr(P.xm32 + (j >> 5), 1u << sh);
-        if (((old >> (sh & 16u)) & 0xFFFFu) == 0u) append_active(P, P.slot, j >> 4);
+        const uint32_t am = __ballot_sync(FULL, active);
+        if (active) {
+            ++act_cnt;
+            const uint32_t word = j >> 5;
+            const uint32_t peers = __match_any_sync(am, word);
+            const uint32_t bits = __reduce_or_sync(peers, 1u << (j & 31u));
+            if (lane == __ffs(peers) - 1) {
+                const uint32_t old = atomicOr(P.xm32 + word, bits);
+                first += ((bits & 0xFFFFu) && !(old & 0xFFFFu)) + ((bits >> 16) && !(old >> 16));
+            }
+        }
     }
-    if (P.stats) {
-        act_cnt = __reduce_add_sync(FULL, act_cnt);
-        if ((tid & 31) == 0 && act_cnt) atomicAdd(&P.ctrl->x_active, (unsigned long long)act_cnt);
-    }
+    cta_count(&P.ctrl->n_blk[slot], first);
+    if (P.stats) cta_count(&P.ctrl->x_active, act_cnt);
     if (!grid_sync(P)) return;
+    stamp(P, 1);
 
     // Phase 2 (Section 3.3.1): device-side path choice, then traversal.
-    const uint32_t n_act = ld_cg(&P.ctrl->n_act[P.slot]);
-    const bool push = choose_push(P, n_act);
-    if (push) push_tasks<SR, false, false>(P, S, P.xm32, P.uvis32, P.yrm32, P.slot, 0);
-    else pull_tiles<SR, false, false>(P, S, P.xm32, P.uvis32, P.yrm32, 0);
+    const uint32_t n_nz = ld_cg(&P.ctrl->n_blk[slot]);
+    const bool push = choose_push(P, n_nz);
+    if (push) {
+        // push list: each nonzero vector block is appended by the x entry
+        // holding its lowest set mask bit (indices are unique)
+        for (size_t base = (size_t)blockIdx.x * NT; base < (size_t)P.x_nnz; base += gsz) {
+            const size_t e = base + tid;
+            bool want = false;
+            uint32_t j = 0;
+            if (e < (size_t)P.x_nnz) {
+                j = (uint32_t)__ldg(P.x_idx + e);
+                if (j < (uint32_t)P.n) {
+                    const uint32_t mb = mask16(P.xm32, j >> 4);
+                    want = (mb & (0u - mb)) == (1u << (j & 15u));
+                }
+            }
+            cta_append(P, S.L, slot, want, j >> 4);
+        }
+        if (!grid_sync(P)) return;
+        push_tasks<SR, false>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
+    } else {
+        pull_tiles<SR, false, true>(P, S, P.xm32, P.uvis32, P.yrm32);
+    }
     stats_flush(P, S);
     if (!grid_sync(P)) return;
+    stamp(P, 2);
 
     // Phase 3: clear x, count output rows per compaction tile, reset counters.
     for (size_t e = gtid; e < (size_t)P.x_nnz; e += gsz) {
@@ -802,67 +853,51 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
         if (SR == 0) P.x_dense[j] = 0.0f;
         P.xm32[j >> 5] = 0u;
     }
-    const uint16_t *yrm16 = reinterpret_cast<const uint16_t *>(P.yrm32);
     for (uint32_t ct = blockIdx.x; ct < P.n_ctiles; ct += gridDim.x) {
-        const uint4 *w4 = reinterpret_cast<const uint4 *>(yrm16 + (size_t)ct * CTILE + tid * 16u);
-        uint4 a = __ldcg(w4), b = __ldcg(w4 + 1);
-        uint32_t cnt = __popc(a.x) + __popc(a.y) + __popc(a.z) + __popc(a.w) + __popc(b.x) + __popc(b.y) +
-                       __popc(b.z) + __popc(b.w);
+        const uint32_t wd = __ldcg(P.yrm32 + (size_t)ct * NT + tid);
         uint32_t tot;
-        block_excl_scan(cnt, &tot);
+        block_excl_scan(__popc(wd), &tot);
         if (tid == 0) P.ctile_cnt[ct] = tot;
     }
     if (blockIdx.x == 0 && tid == 0) {
         Ctrl *c = P.ctrl;
         c->path = push ? 1u : 2u;
-        if (P.stats) c->nzblk = n_act;
+        if (P.stats) c->nzblk = n_nz;
         // counters of both slots are clean for the next call, whichever slot it uses
-        c->n_act[0] = 0u; c->n_act[1] = 0u;
-        c->n_chunk[0] = 0u; c->n_chunk[1] = 0u;
+        for (int k = 0; k < 2; ++k) { c->n_blk[k] = 0u; c->n_act[k] = 0u; c->n_chunk[k] = 0u; }
     }
     if (!grid_sync(P)) return;
 
     // Phase 4: ascending output (Section 2.1 "then compaction"); clear the
     // accumulator and the row masks for the next call.
-    uint32_t *yrm_w = P.yrm32;
     for (uint32_t ct = blockIdx.x; ct < P.n_ctiles; ct += gridDim.x) {
-        uint32_t base = 0;
-        for (uint32_t k = tid; k < ct; k += NT) base += __ldcg(P.ctile_cnt + k);
-        uint32_t tmp;
-        base = block_excl_scan(base, &tmp);
-        base = tmp;   // sum over all threads = prefix of this tile
-        uint4 *w4 = reinterpret_cast<uint4 *>(yrm_w) + ((size_t)ct * CTILE + tid * 16u) / 8u;
-        uint4 a = __ldcg(w4), b = __ldcg(w4 + 1);
-        uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        uint32_t cnt = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) cnt += __popc(w[i]);
+        uint32_t part = 0;
+        for (uint32_t k = tid; k < ct; k += NT) part += __ldcg(P.ctile_cnt + k);
+        uint32_t base;
+        block_excl_scan(part, &base);            // total over the CTA = rows before this tile
+        const size_t wi = (size_t)ct * NT + tid;
+        uint32_t bits = __ldcg(P.yrm32 + wi);
         uint32_t tile_tot;
-        uint32_t o = base + block_excl_scan(cnt, &tile_tot);
-        const uint32_t rb_base = ct * CTILE + tid * 16u;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t bits = w[i];
-            while (bits) {
-                uint32_t k = __ffs(bits) - 1u;
-                bits &= bits - 1u;
-                const uint32_t row = (rb_base + 2u * i + (k >> 4)) * 16u + (k & 15u);
-                P.y_idx[o] = (int32_t)row;
-                if (SR == 0) {
-                    P.y_val[o] = __ldcg(P.y_acc + row);
-                    P.y_acc[row] = 0.0f;
-                }
-                ++o;
+        uint32_t o = base + block_excl_scan(__popc(bits), &tile_tot);
+        if (bits) P.yrm32[wi] = 0u;
+        while (bits) {
+            const uint32_t k = __ffs(bits) - 1u;
+            bits &= bits - 1u;
+            const uint32_t row = (uint32_t)(2u * wi + (k >> 4)) * 16u + (k & 15u);
+            P.y_idx[o] = (int32_t)row;
+            if (SR == 0) {
+                P.y_val[o] = __ldcg(P.y_acc + row);
+                P.y_acc[row] = 0.0f;
             }
+            ++o;
         }
-        if (a.x | a.y | a.z | a.w) w4[0] = make_uint4(0, 0, 0, 0);
-        if (b.x | b.y | b.z | b.w) w4[1] = make_uint4(0, 0, 0, 0);
         if (ct == P.n_ctiles - 1 && tid == 0) {
             *P.y_nnz = (long long)(base + tile_tot);
             if (P.stats) P.ctrl->y_nnz = base + tile_tot;
         }
     }
     if (P.n_ctiles == 0 && blockIdx.x == 0 && tid == 0) *P.y_nnz = 0;
+    stamp(P, 3);
 }
 
 // One SpMSpV with a dense x and a dense y (Section 4.3, DB-Decoding): the
@@ -870,83 +905,72 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
 // used by this call; the other slot is reset for the next call.
 __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
 {
-    __shared__ Smem S;
-    __shared__ uint32_t s_cnt[NW];
-    __shared__ uint32_t s_base;
+    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
     if (ld_cg(&P.ctrl->err) != 0u) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
+    const int slot = P.slot;
     stats_begin(S);
     if (blockIdx.x == 0 && tid == 0 && P.stats) reset_stats(P);
+    stamp(P, 0);
     for (size_t i = gtid; i < (size_t)P.m; i += gsz) P.y_dense[i] = 0.0f;
 
     // Phase 1: each warp reads 32 x values, ballots their nonzero pattern and
     // splits it into the two 16-bit block masks; nonzero blocks are counted
     // per warp, per CTA, and added to the global count once per CTA.
     const uint32_t nwords = (uint32_t)((P.n + 31) / 32);
-    const uint32_t wstep = gridDim.x * NW;
-    unsigned act_cnt = 0;
-    for (uint32_t w0 = blockIdx.x * NW; w0 < nwords; w0 += wstep) {
-        const uint32_t w = w0 + warp;
-        uint32_t bal = 0, nb = 0;
-        if (w < nwords) {
-            const size_t j = (size_t)w * 32u + lane;
-            const float v = j < (size_t)P.n ? __ldg(P.x_in + j) : 0.0f;
-            bal = __ballot_sync(FULL, v != 0.0f);
-            if (lane == 0) P.dxm32[w] = bal;
-            nb = ((bal & 0xFFFFu) != 0u) + ((bal >> 16) != 0u);
+    uint32_t nb = 0, act_cnt = 0;
+    for (uint32_t w = blockIdx.x * NW + warp; w < nwords; w += gridDim.x * NW) {
+        const size_t j = (size_t)w * 32u + lane;
+        const float v = j < (size_t)P.n ? __ldg(P.x_in + j) : 0.0f;
+        const uint32_t bal = __ballot_sync(FULL, v != 0.0f);
+        if (lane == 0) {
+            P.dxm32[w] = bal;
+            nb += ((bal & 0xFFFFu) != 0u) + ((bal >> 16) != 0u);
             act_cnt += __popc(bal);
         }
-        if (lane == 0) s_cnt[warp] = nb;
-        __syncthreads();
-        if (tid == 0) {
-            uint32_t tot = 0;
-            for (int k = 0; k < NW; ++k) { uint32_t c = s_cnt[k]; s_cnt[k] = tot; tot += c; }
-            s_base = tot ? atomicAdd(&P.ctrl->n_act[P.slot], tot) : 0u;
-        }
-        __syncthreads();
-        if (w < nwords && lane == 0 && nb) {
-            uint32_t pos = s_base + s_cnt[warp];
-            for (uint32_t h = 0; h < 2; ++h) {
-                if (!((bal >> (16 * h)) & 0xFFFFu)) continue;
-                const uint32_t cb = 2u * w + h;
-                P.act[P.slot][pos++] = cb;
-                const uint32_t s = __ldg(P.cb_ptr + cb), e = __ldg(P.cb_ptr + cb + 1);
-                if (e > s) {
-                    const uint32_t nch = (e - s + PUSH_CHUNK - 1) / PUSH_CHUNK;
-                    const uint32_t base = atomicAdd(&P.ctrl->n_chunk[P.slot], nch);
-                    for (uint32_t k = 0; k < nch; ++k)
-                        P.chunks[P.slot][base + k] = make_uint2(s + k * PUSH_CHUNK, cb);
-                }
-            }
-        }
-        __syncthreads();
     }
-    if (P.stats && lane == 0 && act_cnt) atomicAdd(&P.ctrl->x_active, (unsigned long long)act_cnt);
+    cta_count(&P.ctrl->n_blk[slot], nb);
+    if (P.stats) cta_count(&P.ctrl->x_active, act_cnt);
     if (!grid_sync(P)) return;
+    stamp(P, 1);
 
-    const uint32_t n_act = ld_cg(&P.ctrl->n_act[P.slot]);
-    const bool push = choose_push(P, n_act);
-    if (push) push_tasks<0, true, false>(P, S, P.dxm32, nullptr, nullptr, P.slot, 0);
-    else pull_tiles<0, true, false>(P, S, P.dxm32, nullptr, nullptr, 0);
+    const uint32_t n_nz = ld_cg(&P.ctrl->n_blk[slot]);
+    const bool push = choose_push(P, n_nz);
+    if (push) {
+        for (uint32_t base = blockIdx.x * NT; base < nwords; base += gridDim.x * NT) {
+            const uint32_t w = base + tid;
+            const uint32_t bal = w < nwords ? __ldcg(P.dxm32 + w) : 0u;
+            cta_append(P, S.L, slot, (bal & 0xFFFFu) != 0u, 2u * w);
+            cta_append(P, S.L, slot, (bal >> 16) != 0u, 2u * w + 1u);
+        }
+        if (!grid_sync(P)) return;
+        push_tasks<0, true>(P, S, P.dxm32, nullptr, nullptr, slot);
+    } else {
+        pull_tiles<0, true, false>(P, S, P.dxm32, nullptr, nullptr);
+    }
     stats_flush(P, S);
     if (blockIdx.x == 0 && tid == 0) {
         Ctrl *c = P.ctrl;
-        const int o = P.slot ^ 1;
+        const int o = slot ^ 1;
+        c->n_blk[o] = 0u;
         c->n_act[o] = 0u;
         c->n_chunk[o] = 0u;
         c->path = push ? 1u : 2u;
-        if (P.stats) c->nzblk = n_act;
+        if (P.stats) c->nzblk = n_nz;
     }
+    stamp(P, 3);
 }
 
 // DB-BFS (Section 4.2): the frontier is the vector-block mask; each level is
 // next = (A or.and frontier) and not visited, on the path chosen from the
-// frontier's nonzero-block ratio.  Lists and counters rotate over three
-// slots so each level needs two grid barriers.
+// frontier's nonzero-block ratio.  After a level's traversal one scan over
+// the next-frontier words updates visited and levels, clears the old
+// frontier, counts the new one's nonzero blocks and builds its push list.
+// Counters rotate over three slots so each level needs two grid barriers.
 __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
 {
-    __shared__ Smem S;
+    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
     if (ld_cg(&P.ctrl->err) != 0u) return;
     const int tid = threadIdx.x;
     const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
@@ -968,78 +992,87 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
     }
     if (blockIdx.x == 0 && tid == 0) {
         Ctrl *c = P.ctrl;
-        for (int s = 0; s < 3; ++s) { c->n_act[s] = 0u; c->n_chunk[s] = 0u; }
+        for (int k = 0; k < 3; ++k) { c->n_blk[k] = 0u; c->n_act[k] = 0u; c->n_chunk[k] = 0u; }
         reset_stats(P);
         c->bfs_levels = 0u;
         c->bfs_push_levels = 0u;
     }
+    stamp(P, 0);
     if (!grid_sync(P)) return;
-    if (blockIdx.x == 0 && tid == 0) {
+    {   // level 0: the source; its push list has one block
         const uint32_t s = (uint32_t)P.bfs_src;
-        P.levels[s] = 0;
-        or16(P.fm32[0], s >> 4, 1u << (s & 15u));
-        or16(P.bvis32, s >> 4, 1u << (s & 15u));
-        append_active(P, 0, s >> 4);
+        if (blockIdx.x == 0 && tid == 0) {
+            P.levels[s] = 0;
+            or16(P.fm32[0], s >> 4, 1u << (s & 15u));
+            or16(P.bvis32, s >> 4, 1u << (s & 15u));
+            P.ctrl->n_blk[0] = 1u;
+        }
+        if (blockIdx.x == 0) cta_append(P, S.L, 0, tid == 0, s >> 4);
     }
     if (!grid_sync(P)) return;
+    stamp(P, 1);
 
-    unsigned long long reached = 1, nz_sum = 0;
+    unsigned long long nz_sum = 0;
     uint32_t push_levels = 0, L = 1;
     for (;; ++L) {
         const int cur = (int)((L - 1) % 3), nxt = (int)(L % 3), old = (int)((L + 1) % 3);
         uint32_t *fcur = P.fm32[(L - 1) & 1], *fnext = P.fm32[L & 1];
-        const uint32_t n_act = ld_cg(&P.ctrl->n_act[cur]);
-        if (n_act == 0u) break;
-        nz_sum += n_act;
-        const bool push = choose_push(P, n_act);
+        const uint32_t n_nz = ld_cg(&P.ctrl->n_blk[cur]);
+        if (n_nz == 0u) break;
+        nz_sum += n_nz;
+        const bool push = choose_push(P, n_nz);
         push_levels += push;
-        if (push) push_tasks<1, false, true>(P, S, fcur, P.bvis32, fnext, cur, nxt);
-        else pull_tiles<1, false, true>(P, S, fcur, P.bvis32, fnext, nxt);
+        if (push) push_tasks<1, false>(P, S, fcur, P.bvis32, fnext, cur);
+        else pull_tiles<1, false, false>(P, S, fcur, P.bvis32, fnext);
         if (!grid_sync(P)) return;
 
-        // level update: visited |= next, levels of the new vertices, clear
-        // the old frontier, reset the slot two levels back.
-        const uint32_t n_next = ld_cg(&P.ctrl->n_act[nxt]);
-        for (size_t i = gtid; i < n_next; i += gsz) {
-            const uint32_t rb = __ldcg(P.act[nxt] + i);
-            const uint32_t f = mask16(fnext, rb);
-            or16(P.bvis32, rb, f);
-            uint32_t bits = f;
-            while (bits) {
-                const uint32_t r = __ffs(bits) - 1u;
-                bits &= bits - 1u;
-                P.levels[rb * 16u + r] = (int32_t)L;
+        // level update over all frontier words (one thread per word)
+        uint32_t nb = 0, reached = 0;
+        for (uint32_t base = blockIdx.x * NT; base < nwords; base += gridDim.x * NT) {
+            const uint32_t w = base + tid;
+            uint32_t nm = 0;
+            if (w < nwords) {
+                nm = __ldcg(fnext + w);
+                if (__ldcg(fcur + w)) fcur[w] = 0u;
+                if (nm) {
+                    P.bvis32[w] = __ldcg(P.bvis32 + w) | nm;
+                    reached += __popc(nm);
+                    nb += ((nm & 0xFFFFu) != 0u) + ((nm >> 16) != 0u);
+                    uint32_t bits = nm;
+                    while (bits) {
+                        const uint32_t k = __ffs(bits) - 1u;
+                        bits &= bits - 1u;
+                        P.levels[(2u * w + (k >> 4)) * 16u + (k & 15u)] = (int32_t)L;
+                    }
+                }
             }
+            cta_append(P, S.L, nxt, (nm & 0xFFFFu) != 0u, 2u * w);
+            cta_append(P, S.L, nxt, (nm >> 16) != 0u, 2u * w + 1u);
         }
-        if (P.stats) {
-            unsigned long long cnt = 0;
-            for (size_t i = gtid; i < n_next; i += gsz) cnt += __popc(mask16(fnext, __ldcg(P.act[nxt] + i)));
-            cnt = __reduce_add_sync(FULL, (unsigned)cnt);
-            if ((tid & 31) == 0 && cnt) atomicAdd(&P.ctrl->reached, cnt);
-        }
-        for (size_t i = gtid; i < n_act; i += gsz) {
-            const uint32_t rb = __ldcg(P.act[cur] + i);
-            atomicAnd(fcur + (rb >> 1), ~(0xFFFFu << ((rb & 1u) << 4)));
-        }
+        cta_count(&P.ctrl->n_blk[nxt], nb);
+        if (P.stats) cta_count(&P.ctrl->reached, reached);
         if (blockIdx.x == 0 && tid == 0) {
             Ctrl *c = P.ctrl;
+            c->n_blk[old] = 0u;
             c->n_act[old] = 0u;
             c->n_chunk[old] = 0u;
         }
         if (!grid_sync(P)) return;
     }
+    stamp(P, 2);
     stats_flush(P, S);
     if (blockIdx.x == 0 && tid == 0) {
         Ctrl *c = P.ctrl;
-        // Every block has passed the last barrier and reads only n_act[cur],
+        // Every block has passed the last barrier and reads only n_blk[cur],
         // which is already 0: all slots can be cleared for the next call.
-        for (int s = 0; s < 3; ++s) { c->n_act[s] = 0u; c->n_chunk[s] = 0u; }
+        for (int k = 0; k < 3; ++k) { c->n_blk[k] = 0u; c->n_act[k] = 0u; c->n_chunk[k] = 0u; }
         c->bfs_levels = L - 1u;   // the loop stops when frontier L-1 is empty
         c->bfs_push_levels = push_levels;
         c->path = 0u;
         c->nzblk = nz_sum;
-        if (P.stats) c->reached += reached;
+        if (P.stats) c->reached += 1;   // the source
     }
+    stamp(P, 3);
 }
 
 // Withholds block 0 from the barrier so every other block's wait expires.
@@ -1108,6 +1141,7 @@ KParams make_params(const dbs_matrix *A, dbs_workspace *w)
     P.csc_ref = A->d_csc_ref;
     P.payload = reinterpret_cast<const uint4 *>(A->d_payload);
     P.tiles = reinterpret_cast<const uint4 *>(A->d_tiles);
+    P.tile_ref = A->d_tile_ref;
     P.x_dense = w->x_dense; P.xm32 = w->xm32; P.dxm32 = w->dxm32;
     for (int s = 0; s < 3; ++s) { P.act[s] = w->act[s]; P.chunks[s] = w->chunks[s]; }
     P.y_acc = w->y_acc; P.yrm32 = w->yrm32; P.ctile_cnt = w->ctile_cnt; P.n_ctiles = w->n_ctiles;
@@ -1120,18 +1154,23 @@ KParams make_params(const dbs_matrix *A, dbs_workspace *w)
     return P;
 }
 
-dbs_status launch(const void *fn, int grid, KParams &P, cudaStream_t s)
+dbs_status launch(const void *fn, int grid, KParams &P, cudaStream_t s, size_t smem = sizeof(Smem))
 {
     void *args[] = {&P};
-    cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NT), args, 0, s);
+    cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NT), args, smem, s);
     if (e != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
     return DBS_OK;
 }
 
-int coop_grid(const void *fn, int sms)
+int coop_grid(const void *fn, int sms, size_t smem = sizeof(Smem))
 {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, NT, 0) != cudaSuccess) { cudaGetLastError(); return 0; }
+    if (smem > 48u * 1024u &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, NT, smem) != cudaSuccess) { cudaGetLastError(); return 0; }
     return nb * sms;
 }
 
@@ -1336,6 +1375,8 @@ dbs_status dbs_last_stats(dbs_workspace *w, void *stream, dbs_stats *out)
     out->y_nnz = w->last_was_bfs ? (int64_t)c.reached : (int64_t)c.y_nnz;
     out->bfs_levels = (int32_t)c.bfs_levels;
     out->bfs_push_levels = (int32_t)c.bfs_push_levels;
+    for (int i = 0; i < 3; ++i)
+        out->phase_ns[i] = c.t_phase[i + 1] >= c.t_phase[i] ? (int64_t)(c.t_phase[i + 1] - c.t_phase[i]) : 0;
     return DBS_OK;
 }
 
@@ -1343,9 +1384,9 @@ dbs_status dbs_selftest_wait_timeout(dbs_workspace *w, void *stream)
 {
     if (!w) return DBS_ERR_INVALID_ARG;
     KParams P = make_params(w->A, w);
-    int grid = std::min(w->grid_bfs, 2 * w->sms);
+    int grid = std::min(coop_grid((const void *)k_selftest_wait, w->sms, 0), 2 * w->sms);
     if (grid < 2) return DBS_ERR_UNSUPPORTED;
-    return launch((const void *)k_selftest_wait, grid, P, (cudaStream_t)stream);
+    return launch((const void *)k_selftest_wait, grid, P, (cudaStream_t)stream, 0);
 }
 
 }  // extern "C"

@@ -153,6 +153,16 @@ void convert_chunk(Chunk &ch, int64_t m, int64_t n, const int64_t *rp, const int
             }
             int maxr = *std::max_element(rc, rc + 16), maxc = *std::max_element(cc, cc + 16);
             uint32_t fmt = o.force_format >= 0 ? (uint32_t)o.force_format : classify(nnz, maxr, maxc, o);
+            if (fmt == FMT_COO && !valued && (uint32_t)nnz <= INLINE_MAX_NNZ) {
+                // pattern-only COO block small enough to live in its meta word
+                uint8_t coords[3];
+                for (int k = 0; k < nnz; ++k) coords[k] = (uint8_t)((lr[k] << 4) | lc[k]);
+                ch.desc.push_back(U2{(uint32_t)cb, meta_pack_inline(coords, (uint32_t)nnz)});
+                ch.units.push_back(0);
+                ch.rb_count[(size_t)(rb - ch.rb0)]++;
+                s = e;
+                continue;
+            }
             uint32_t units = payload_units(fmt, (uint32_t)nnz, valued);
             size_t base = ch.payload.size();
             ch.payload.resize(base + units, U4{0, 0, 0, 0});
@@ -219,6 +229,8 @@ void free_device(dbs_matrix *A)
 {
     cudaFree(A->d_rb_ptr); cudaFree(A->d_blk_desc); cudaFree(A->d_blk_ref); cudaFree(A->d_cb_ptr);
     cudaFree(A->d_csc_desc); cudaFree(A->d_csc_ref); cudaFree(A->d_payload); cudaFree(A->d_tiles);
+    cudaFree(A->d_tile_ref);
+    A->d_tile_ref = nullptr;
     A->d_rb_ptr = nullptr; A->d_blk_desc = nullptr; A->d_blk_ref = nullptr; A->d_cb_ptr = nullptr;
     A->d_csc_desc = nullptr; A->d_csc_ref = nullptr; A->d_payload = nullptr; A->d_tiles = nullptr;
 }
@@ -243,7 +255,8 @@ dbs_status host_view(const dbs_matrix *A, HostFormat &tmp, const HostFormat **ou
               copy_from_device(tmp.csc_desc, A->d_csc_desc, (size_t)A->B) &&
               copy_from_device(tmp.csc_ref, A->d_csc_ref, (size_t)A->B) &&
               copy_from_device(tmp.payload, A->d_payload, (size_t)A->P) &&
-              copy_from_device(tmp.tiles, A->d_tiles, (size_t)A->T);
+              copy_from_device(tmp.tiles, A->d_tiles, (size_t)A->T) &&
+              copy_from_device(tmp.tile_ref, A->d_tile_ref, (size_t)A->T);
     if (!ok) { cudaGetLastError(); return DBS_ERR_CUDA; }
     *out = &tmp;
     return DBS_OK;
@@ -419,13 +432,29 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         for (int64_t p = 0; p < B; ++p) total_w += fmt_weight(meta_fmt(H.blk_desc[(size_t)p].y));
         uint32_t W = (uint32_t)o.tile_weight;
         if (W == 0) {
-            uint64_t target = (uint64_t)num_sms_or_default() * 8u;
-            W = (uint32_t)std::min<uint64_t>(2048, std::max<uint64_t>(16, (total_w + target - 1) / target));
+            // about 64 tiles per SM (two per resident warp), within [16, 256]
+            uint64_t target = (uint64_t)num_sms_or_default() * 64u;
+            W = (uint32_t)std::min<uint64_t>(TILE_MAX_BLOCKS, std::max<uint64_t>(16, (total_w + target - 1) / target));
         }
         W = std::min<uint32_t>(W, TILE_MAX_BLOCKS);
         uint32_t R = o.tile_max_row_blocks > 0 ? (uint32_t)o.tile_max_row_blocks : TILE_MAX_SPAN;
         build_tiles(H.rb_ptr, H.blk_desc, nbr, W, R, H.tiles);
         A->T = (int64_t)H.tiles.size();
+        H.tile_ref.resize(H.tiles.size());
+        for (size_t i = 0; i < H.tiles.size(); ++i) {
+            U4 &tl = H.tiles[i];
+            H.tile_ref[i] = H.blk_ref[tl.x];
+            // local row block of each block into blk_desc.x bits 27-31; flag
+            // tiles that hold payload-carrying blocks
+            uint32_t rb = tl.z;
+            bool stored = false;
+            for (uint32_t p = tl.x; p < tl.y; ++p) {
+                while (H.rb_ptr[rb + 1] <= p) ++rb;
+                H.blk_desc[p].x |= (rb - tl.z) << DESC_LRB_SHIFT;
+                stored |= !meta_inline(H.blk_desc[p].y);
+            }
+            if (stored) tl.w |= TILE_HAS_STORED;
+        }
     } catch (const std::bad_alloc &) {
         return fail(DBS_ERR_OOM);
     }
@@ -440,7 +469,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
     }
     I.ntiles = A->T;
     I.payload_bytes = A->P * 16;
-    I.view_bytes = (nbr + 1) * 4 + A->B * 8 + A->B * 4 + (nbc + 1) * 4 + A->B * 8 + A->B * 4 + A->T * 16;
+    I.view_bytes = (nbr + 1) * 4 + A->B * 8 + A->B * 4 + (nbc + 1) * 4 + A->B * 8 + A->B * 4 + A->T * 20;
     I.total_bytes = I.payload_bytes + I.view_bytes;
     I.csr_bytes = (m + 1) * 4 + nnz * 4 + (valued ? nnz * 4 : 0);
     I.csr_csc_bytes = I.csr_bytes + (n + 1) * 4 + nnz * 4 + (valued ? nnz * 4 : 0);
@@ -459,6 +488,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         if ((st = upload(H.csc_ref, &A->d_csc_ref, (size_t)A->B + 8, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.payload, &A->d_payload, 1, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.tiles, &A->d_tiles, 1, s)) != DBS_OK) return fail(st);
+        if ((st = upload(H.tile_ref, &A->d_tile_ref, 1, s)) != DBS_OK) return fail(st);
         if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return fail(DBS_ERR_CUDA); }
         A->on_device = true;
     }
@@ -498,19 +528,25 @@ dbs_status dbs_matrix_export_views(const dbs_matrix *A, int64_t *blk_row_ptr, in
         if (blk_row_ptr) for (int64_t i = 0; i <= A->nbr; ++i) blk_row_ptr[i] = H->rb_ptr[(size_t)i];
         if (blk_col_ptr) for (int64_t i = 0; i <= A->nbc; ++i) blk_col_ptr[i] = H->cb_ptr[(size_t)i];
         for (int64_t p = 0; p < A->B; ++p) {
-            if (blk_col_idx) blk_col_idx[p] = H->blk_desc[(size_t)p].x;
+            if (blk_col_idx) blk_col_idx[p] = H->blk_desc[(size_t)p].x & DESC_COL_MASK;
             if (blk_nnz) blk_nnz[p] = (int32_t)meta_nnz(H->blk_desc[(size_t)p].y);
             if (blk_format) blk_format[p] = (int32_t)meta_fmt(H->blk_desc[(size_t)p].y);
             if (blk_row_idx) blk_row_idx[p] = H->csc_desc[(size_t)p].x;
         }
         if (blk_csc2csr) {
-            // csc_ref points at the shared payload; blk_ref is increasing in the
-            // primary id, so the primary id is found by binary search.
-            for (int64_t q = 0; q < A->B; ++q) {
-                auto it = std::lower_bound(H->blk_ref.begin(), H->blk_ref.end(), H->csc_ref[(size_t)q]);
-                if (it == H->blk_ref.end() || *it != H->csc_ref[(size_t)q]) return DBS_ERR_INTERNAL;
-                blk_csc2csr[q] = (int64_t)(it - H->blk_ref.begin());
-            }
+            // The CSC position q of column block c holding row block r maps to
+            // the primary block (r, c): search row block r's column indices.
+            for (int64_t c = 0; c < A->nbc; ++c)
+                for (uint32_t q = H->cb_ptr[(size_t)c]; q < H->cb_ptr[(size_t)c + 1]; ++q) {
+                    const uint32_t r = H->csc_desc[q].x;
+                    auto b0 = H->blk_desc.begin() + H->rb_ptr[r], b1 = H->blk_desc.begin() + H->rb_ptr[r + 1];
+                    auto it = std::lower_bound(b0, b1, (uint32_t)c,
+                                               [](const U2 &d, uint32_t v) { return (d.x & DESC_COL_MASK) < v; });
+                    if (it == b1 || (it->x & DESC_COL_MASK) != (uint32_t)c) return DBS_ERR_INTERNAL;
+                    const size_t p = (size_t)(it - H->blk_desc.begin());
+                    if (H->csc_ref[q] != H->blk_ref[p] || H->csc_desc[q].y != it->y) return DBS_ERR_INTERNAL;
+                    blk_csc2csr[q] = (int64_t)p;
+                }
         }
     } catch (const std::bad_alloc &) {
         return DBS_ERR_OOM;
@@ -534,11 +570,13 @@ dbs_status dbs_matrix_export_csr(const dbs_matrix *A, int64_t *row_ptr, int32_t 
             for (int64_t rb = 0; rb < A->nbr; ++rb)
                 for (uint32_t p = H->rb_ptr[(size_t)rb]; p < H->rb_ptr[(size_t)rb + 1]; ++p) {
                     const uint32_t meta = H->blk_desc[p].y, fmt = meta_fmt(meta), nnz = meta_nnz(meta);
-                    const uint32_t cb = H->blk_desc[p].x;
-                    const uint8_t *b = pay + (size_t)H->blk_ref[p] * 16;
+                    const uint32_t cb = H->blk_desc[p].x & DESC_COL_MASK;
+                    uint8_t inl[4] = {(uint8_t)(meta & 0xFF), (uint8_t)((meta >> 8) & 0xFF),
+                                      (uint8_t)((meta >> 16) & 0xFF), 0};
+                    const uint8_t *b = meta_inline(meta) ? inl : pay + (size_t)H->blk_ref[p] * 16;
                     const float *v = reinterpret_cast<const float *>(b + val_offset(fmt, nnz));
-                    uint16_t mask[16];
-                    std::memcpy(mask, b + (fmt == FMT_DENSE ? 0 : OFF_MASK), 32);
+                    uint16_t mask[16] = {0};
+                    if (fmt != FMT_COO) std::memcpy(mask, b + (fmt == FMT_DENSE ? 0 : OFF_MASK), 32);
                     uint32_t found = 0;
                     for (int r = 0; r < 16; ++r) {
                         for (int c = 0; c < 16; ++c) {

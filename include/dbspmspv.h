@@ -82,10 +82,11 @@ typedef struct {
     double th2;                /* skew ratio above which a block is ForceCSR/ForceCSC (paper: 2.0) */
     int32_t force_format;      /* DBS_FMT_AUTO, or one dbs_format for every block (ablation) */
     int32_t tile_weight;       /* pull tile weight cap; block weights Dense 4, ForceCSR /
-                                  ForceCSC / patched CSR 2, COO 1 (Section 3.3.2).
+                                  ForceCSC / patched CSR 2, COO 1 (Section 3.3.2).  A tile
+                                  is one warp's task and holds at most 256 blocks.
                                   0 = sized from the matrix and the GPU's SM count. */
-    int32_t tile_max_row_blocks; /* row blocks one pull tile may span (1..64); 1 with
-                                  tile_weight 16 reproduces the paper's segments. 0 = 64 */
+    int32_t tile_max_row_blocks; /* row blocks one pull tile may span (1..32); 1 with
+                                  tile_weight 16 reproduces the paper's segments. 0 = 32 */
     int32_t keep_host;         /* keep a host copy of the blocked format (export) */
     int32_t host_only;         /* build the format on the host only; no device memory
                                   is touched (the matrix can be inspected and exported
@@ -244,6 +245,8 @@ typedef struct {
     int64_t y_nnz;              /* output entries (BFS: vertices reached) */
     int32_t bfs_levels;         /* BFS: number of levels */
     int32_t bfs_push_levels;    /* BFS: levels run on the push path */
+    int64_t phase_ns[3];        /* device time seen by block 0 (collect_stats only):
+                                   metadata, traversal (BFS: all levels), output */
 } dbs_stats;
 
 dbs_status dbs_last_stats(dbs_workspace *ws, void *stream, dbs_stats *out);

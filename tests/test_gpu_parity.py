@@ -400,7 +400,7 @@ def test_ragged_tiny_shapes():
     assert gi.size == 0
 
 
-@pytest.mark.parametrize("W,R", [(16, 1), (40, 3), (2048, 64)])
+@pytest.mark.parametrize("W,R", [(16, 1), (40, 3), (256, 32)])
 def test_tile_shapes_do_not_change_results(W, R):
     A = synth.config("llm", "small")
     O = oracle.Oracle(A)
