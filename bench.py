@@ -269,7 +269,7 @@ def main():
             bytes_x[d].append(st["bytes_alg"])
             path_x[d].append(st["path"])
             phase_x[d].append(st["phase_ns"])
-    touched_bfs, bytes_bfs, edges_bfs, nlev_bfs, push_lev, phase_bfs = [], [], [], [], [], []
+    touched_bfs, bytes_bfs, edges_bfs, nlev_bfs, push_lev, phase_bfs, level_bfs = [], [], [], [], [], [], []
     deg = np.diff(A.row_ptr)
     for src in sources:
         _, nl = dbs.bfs(M, int(src), levels=levels, ws=ws)
@@ -281,6 +281,8 @@ def main():
         nlev_bfs.append(nl)
         push_lev.append(st["bfs_push_levels"])
         phase_bfs.append(st["phase_ns"])
+        if len(level_bfs) < 3:
+            level_bfs.append(ws.bfs_levels())
     assert ws.check() == 0
     ws.set_opts(dbs.exec_opts(collect_stats=0))
 
@@ -378,7 +380,8 @@ def main():
                 "push_levels_mean": float(np.mean(push_lev)),
                 "gbs": bytes_b / (t_bfs * 1e-3) / 1e9,
                 "device_phase_us_with_stats": [round(float(np.mean([p[i] for p in phase_bfs])) / 1e3, 2)
-                                               for i in range(3)]}
+                                               for i in range(3)],
+                "levels_first_sources": level_bfs}
     # harmonic mean of per-source GTEPS from per-call times
     per_src_t = {}
     for kind, d, i, e0, e1 in rec:

@@ -15,13 +15,11 @@
 //                         This is the paper's csc2csr mapping resolved to the
 //                         shared payload, so push reaches a block in one load.
 //   payload  uint4[P]     the low-level blocks, 16-byte aligned
-//   tiles    uint4[T]     pull work units {p0, p1, rb0, span | flags << 16} (Section 3.3.2)
-//   tile_ref u32[T]       payload offset of each tile's first block
+//   tiles    uint4[T]     pull work units {p0, p1, rb0, span} (Section 3.3.2)
 //
 // blk_desc.x holds the column block in bits 0-26 and, in bits 27-31, the
 // block's row block relative to the first row block of its pull tile, so a
-// pull task needs no row-block search.  Tile flag bit 0: the tile holds at
-// least one block with a payload (not inline).
+// pull task needs no row-block search.
 //
 // meta word (the same word in both views):
 //   stored block:  bits 0-15 column-occupancy mask (bit c = local column c
@@ -68,7 +66,6 @@ constexpr uint32_t PUSH_CHUNK = 32;
 
 constexpr uint32_t DESC_COL_MASK = 0x07FFFFFFu;   // column block bits of blk_desc.x
 constexpr uint32_t DESC_LRB_SHIFT = 27;            // local row block bits of blk_desc.x
-constexpr uint32_t TILE_HAS_STORED = 1u << 16;     // flag in tiles[].w
 
 constexpr uint32_t META_INLINE = 0x80000000u;
 constexpr uint32_t INLINE_MAX_NNZ = 3;

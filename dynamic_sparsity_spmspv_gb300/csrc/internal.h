@@ -23,7 +23,6 @@ struct HostFormat {
     std::vector<uint32_t> csc2csr;    // B (host only)
     std::vector<U4> payload;          // P
     std::vector<U4> tiles;            // T: {p0, p1, rb0, span}
-    std::vector<uint32_t> tile_ref;   // T: payload offset of each tile's first block
 };
 
 }  // namespace dbs
@@ -43,7 +42,6 @@ struct dbs_matrix {
     uint32_t *d_csc_ref = nullptr;
     dbs::U4 *d_payload = nullptr;
     dbs::U4 *d_tiles = nullptr;
-    uint32_t *d_tile_ref = nullptr;
     dbs::HostFormat *host = nullptr;
     dbs_matrix_info info{};
 };

@@ -37,6 +37,7 @@ constexpr int NT = 256;              // threads per CTA
 constexpr int NW = NT / 32;          // warps per CTA
 constexpr uint32_t FULL = 0xFFFFFFFFu;
 constexpr uint32_t CTILE = 2 * NT;   // row blocks per compaction tile (one mask word per thread)
+constexpr int BFS_LEVEL_LOG = 64;    // BFS levels whose frontier, path and time are recorded
 
 struct Ctrl {
     unsigned int bar_count;
@@ -58,6 +59,9 @@ struct Ctrl {
     unsigned long long y_nnz;
     unsigned long long reached;
     unsigned long long t_phase[4];   // device timestamps: start, metadata done, traversal done, end
+    unsigned long long lv_t[BFS_LEVEL_LOG + 1];   // BFS: start time of each level (and of the exit)
+    unsigned int lv_nz[BFS_LEVEL_LOG];            // BFS: nonzero frontier blocks per level
+    unsigned int lv_path[BFS_LEVEL_LOG];          // BFS: 1 push, 2 pull per level
 };
 
 struct KParams {
@@ -73,7 +77,6 @@ struct KParams {
     const uint32_t *__restrict__ csc_ref;
     const uint4 *__restrict__ payload;
     const uint4 *__restrict__ tiles;
-    const uint32_t *__restrict__ tile_ref;
     // call
     int path_force;
     const int32_t *x_idx;
@@ -166,7 +169,7 @@ __device__ bool grid_sync(const KParams &P)
                     break;
                 }
                 __nanosleep(ns);
-                if (ns < 1024) ns <<= 1;
+                if (ns < 256) ns <<= 1;
             }
         }
         if (ok && ld_cg(&c->err) != 0u) ok = 0;
@@ -420,14 +423,20 @@ __device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint
                                             const float *xb, bool valued, Add add)
 {
     const float *vals = reinterpret_cast<const float *>(b + val_offset(FMT_COO, nnz));
+    const uint4 *c4 = reinterpret_cast<const uint4 *>(b);
     uint32_t rows = 0;
-    for (uint32_t k = 0; k < nnz; ++k) {
-        uint32_t e = __ldg(b + k);
-        uint32_t c = e & 15u;
-        if ((act >> c) & 1u) {
-            uint32_t r = e >> 4;
-            rows |= 1u << r;
-            if (valued) add(r, __ldg(vals + k) * xval(xb, c));
+    for (uint32_t base = 0; base < nnz; base += 16u) {
+        const uint4 v = __ldg(c4 + (base >> 4));
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (uint32_t j = 0; j < 16u; ++j) {
+            const uint32_t e = (wv[j >> 2] >> (8u * (j & 3u))) & 0xFFu;
+            const uint32_t c = e & 15u;
+            if (base + j < nnz && ((act >> c) & 1u)) {
+                const uint32_t r = e >> 4;
+                rows |= 1u << r;
+                if (valued) add(r, __ldg(vals + base + j) * xval(xb, c));
+            }
         }
     }
     return rows;
@@ -441,9 +450,16 @@ __device__ __forceinline__ uint32_t bool_found(const uint8_t *__restrict__ b, ui
     const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
     uint32_t f = 0;
     if (fmt == FMT_COO) {
-        for (uint32_t k = 0; k < nnz; ++k) {
-            uint32_t e = __ldg(b + k);
-            if ((act >> (e & 15u)) & 1u) f |= 1u << (e >> 4);
+        // 16 coordinates per 16-byte load (the payload is 16-byte aligned)
+        const uint4 *c4 = reinterpret_cast<const uint4 *>(b);
+        for (uint32_t base = 0; base < nnz; base += 16u) {
+            const uint4 v = __ldg(c4 + (base >> 4));
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (uint32_t j = 0; j < 16u; ++j) {
+                const uint32_t e = (wv[j >> 2] >> (8u * (j & 3u))) & 0xFFu;
+                if (base + j < nnz && ((act >> (e & 15u)) & 1u)) f |= 1u << (e >> 4);
+            }
         }
     } else {
         const uint4 *m4 = reinterpret_cast<const uint4 *>(b + (fmt == FMT_DENSE ? 0u : OFF_MASK));
@@ -475,7 +491,7 @@ struct WarpPull {
     uint32_t rm[TILE_MAX_SPAN];       // touched (Boolean: found) rows per row block
     uint32_t vis[TILE_MAX_SPAN];      // visited rows per row block (Boolean)
     float y[TILE_MAX_SPAN * 16];      // partial row sums (plus-times)
-    uint4 q[TILE_MAX_BLOCKS];         // hit blocks with a payload: {ref, meta, col, lrb | act << 16}
+    uint32_t q[TILE_MAX_BLOCKS];      // hits with a payload: local index | row block << 8 | act << 16
     uint32_t nq;
 };
 
@@ -502,14 +518,16 @@ __device__ __forceinline__ void stat_add(Smem &S, int i, unsigned long long v)
 // through them without block-wide synchronisation.  Each lane issues the
 // descriptor loads of its 8 blocks together and then their 8 vector-mask
 // lookups, so many independent requests are in flight per warp.  Inline
-// blocks finish right there; hits with a payload are queued (payload offsets
-// from a warp prefix sum of the block sizes) and drained by the lanes, or by
-// the whole warp for the Dense / Force / patched-CSR microkernels.  Row
-// results gather in the warp's shared-memory accumulators and are written
-// back once per row block (Section 3.3.3).
-// SR 0 = plus-times, 1 = Boolean.  DOUT: dense output y.  L1M: the vector
-// masks may be cached in L1 (they do not change during the launch).
-template <int SR, bool DOUT, bool L1M>
+// blocks finish right there; hits with a payload are queued and drained by
+// the lanes, or by the whole warp for the Dense / Force / patched-CSR
+// microkernels.  Row results gather in the warp's shared-memory accumulators
+// and are written back once per row block (Section 3.3.3).
+// SR 0 = plus-times, 1 = Boolean.  DOUT: dense output y.
+// Mask lookups go through L1: the masks are read-only between two grid
+// barriers, and every barrier ends with an acquire at GPU scope, after which
+// plain loads observe all writes made before the barrier (the same guarantee
+// that cooperative grid synchronisation gives).
+template <int SR, bool DOUT>
 __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const uint32_t *vis,
                            uint32_t *out_rm)
 {
@@ -517,13 +535,17 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     WarpPull &W = S.wp[warp];
     const float *xv = P.xv;
-    const bool valued = P.valued != 0;
     const uint32_t nwarps = gridDim.x * NW;
     unsigned long long c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
     for (uint32_t t = blockIdx.x * NW + warp; t < P.T; t += nwarps) {
         const uint4 td = __ldg(P.tiles + t);
-        const uint32_t p0 = td.x, p1 = td.y, rb0 = td.z, span = td.w & 0xFFFFu, nblk = p1 - p0;
-        const bool stored = (td.w & TILE_HAS_STORED) != 0u;
+        const uint32_t p0 = td.x, p1 = td.y, rb0 = td.z, span = td.w, nblk = p1 - p0;
+        uint32_t vrow = 0;
+        if (SR == 1 && vis) {
+            // every row of the task's row blocks already visited: nothing to find
+            vrow = lane < (int)span ? mask16(vis, rb0 + lane) : 0xFFFFu;
+            if (__all_sync(FULL, vrow == 0xFFFFu)) continue;
+        }
         uint2 d[WK];
 #pragma unroll
         for (int k = 0; k < WK; ++k) {
@@ -537,37 +559,33 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
         edge = __reduce_or_sync(FULL, edge);
         if (lane < (int)span) {
             W.rm[lane] = 0u;
-            if (SR == 1) W.vis[lane] = vis ? mask16(vis, rb0 + lane) : 0u;
+            if (SR == 1) W.vis[lane] = vrow;
         }
         if (SR == 0)
             for (uint32_t i = lane; i < span * 16u; i += 32) W.y[i] = 0.0f;
         if (lane == 0) W.nq = 0u;
         __syncwarp();
 
-        uint32_t carry = stored ? __ldg(P.tile_ref + t) : 0u;
 #pragma unroll
         for (int k = 0; k < WK; ++k) {
             const uint32_t li = (uint32_t)(k * 32 + lane);
             const uint32_t meta = d[k].y, col = d[k].x & DESC_COL_MASK, lrb = d[k].x >> DESC_LRB_SHIFT;
-            uint32_t ref = 0;
-            if (stored) {                                     // warp-uniform
-                const uint32_t sz = li < nblk ? meta_units(meta, valued) : 0u;
-                const uint32_t inc = warp_incl_scan(sz, lane);
-                ref = carry + inc - sz;
-                carry += __shfl_sync(FULL, inc, 31);
-            }
             const bool skip = li >= nblk || (SR == 1 && vis && W.vis[lrb] == 0xFFFFu);
-            const uint32_t w = skip ? 0u : (L1M ? __ldca(xm + (col >> 1)) : __ldcg(xm + (col >> 1)));
-            const uint32_t m = (w >> ((col & 1u) << 4)) & 0xFFFFu;
+            const uint32_t m = skip ? 0u : (uint32_t)__ldca(reinterpret_cast<const unsigned short *>(xm) + col);
             if (P.stats && m) { ++c_vis; c_touch += meta_nnz(meta); }
+            if (SR == 1 && meta_inline(meta)) {
+                // inline block: its rows met by active columns, straight from x's mask
+                const uint32_t f = meta_inline_found(meta, m);
+                if (f) {
+                    atomicOr(&W.rm[lrb], f);
+                    if (P.stats) ++c_hit;
+                }
+                continue;
+            }
             const uint32_t a = m & meta_cmask(meta);
             if (a) {
-                if (SR == 1 && meta_inline(meta)) {
-                    atomicOr(&W.rm[lrb], meta_inline_found(meta, a));
-                } else {
-                    const uint32_t slot = atomicAdd(&W.nq, 1u);
-                    W.q[slot] = make_uint4(ref, meta, col, lrb | (a << 16));
-                }
+                const uint32_t slot = atomicAdd(&W.nq, 1u);
+                W.q[slot] = li | (lrb << 8) | (a << 16);
                 if (P.stats) ++c_hit;
             }
         }
@@ -577,36 +595,39 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
         // other formats by the whole warp
         const uint32_t nq = W.nq;
         for (uint32_t i = lane; i < nq; i += 32) {
-            const uint4 e = W.q[i];
-            const uint32_t meta = e.y, lrb = e.w & 0xFFFFu, a = e.w >> 16;
-            const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + e.x);
+            const uint32_t e = W.q[i];
+            const uint32_t p = p0 + (e & 0xFFu), lrb = (e >> 8) & 0xFFu, a = e >> 16;
+            const uint32_t meta = __ldg(&P.blk_desc[p].y);
+            if (SR == 0 && meta_fmt(meta) != FMT_COO) continue;
+            const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.blk_ref + p));
             uint32_t rows = 0;
             if (SR == 1) {
                 rows = bool_found(b, meta, a);
-                if (P.stats) c_bytes += bool_bytes(meta);
-            } else if (meta_fmt(meta) == FMT_COO) {
-                const uint32_t nnz = meta_nnz(meta);
+                if (P.stats) c_bytes += 4u + bool_bytes(meta);
+            } else {
+                const uint32_t nnz = meta_nnz(meta), col = __ldg(&P.blk_desc[p].x) & DESC_COL_MASK;
                 float *sy = &W.y[lrb * 16u];
-                rows = coo_lane(b, nnz, a, xv + (size_t)e.z * 16u, true,
+                rows = coo_lane(b, nnz, a, xv + (size_t)col * 16u, true,
                                 [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
-                if (P.stats) c_bytes += val_offset(FMT_COO, nnz) + 4u * nnz;
+                if (P.stats) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
             }
             if (rows) atomicOr(&W.rm[lrb], rows);
         }
         if (SR == 0) {
             __syncwarp();
             for (uint32_t i = 0; i < nq; ++i) {
-                const uint4 e = W.q[i];
-                if (meta_fmt(e.y) == FMT_COO) continue;           // warp-uniform
-                const uint32_t lrb = e.w & 0xFFFFu, a = e.w >> 16;
+                const uint32_t e = W.q[i];
+                const uint32_t p = p0 + (e & 0xFFu), lrb = (e >> 8) & 0xFFu, a = e >> 16;
+                const uint2 dd = __ldg(P.blk_desc + p);
+                if (meta_fmt(dd.y) == FMT_COO) continue;            // warp-uniform
                 uint32_t by = 0;
-                RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + e.x), e.y, a,
-                                    xv + (size_t)e.z * 16u, lane, S.wacc[warp], &by);
+                RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.blk_ref + p)), dd.y, a,
+                                    xv + (size_t)(dd.x & DESC_COL_MASK) * 16u, lane, S.wacc[warp], &by);
                 if (lane < 16 && o.touched) W.y[lrb * 16u + lane] += o.sum;
                 const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
                 if (lane == 0) {
                     if (bits) W.rm[lrb] |= bits;
-                    if (P.stats) c_bytes += by;
+                    if (P.stats) c_bytes += 4u + by;
                 }
                 __syncwarp();
             }
@@ -632,7 +653,7 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
             }
             if (!DOUT && lane < (int)span && W.rm[lane]) or16(out_rm, rb0 + lane, W.rm[lane]);
         }
-        if (P.stats && lane == 0) c_bytes += 8u * nblk + 24u + (stored ? 4u : 0u);
+        if (P.stats && lane == 0) c_bytes += 8u * nblk + 24u;
         __syncwarp();
     }
     if (P.stats) {
@@ -770,7 +791,7 @@ __device__ __forceinline__ void reset_stats(const KParams &P)
 // One SpMSpV with a sparse x (index list + values) and a sparse output.
 // Phases: metadata | [push list] | traversal | compaction counts | writes.
 template <int SR>
-__global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
+__global__ void __launch_bounds__(NT, 5) k_spmspv_sparse(KParams P)
 {
     Smem &S = *reinterpret_cast<Smem *>(smem_raw);
     if (ld_cg(&P.ctrl->err) != 0u) return;
@@ -840,7 +861,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
         if (!grid_sync(P)) return;
         push_tasks<SR, false>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
     } else {
-        pull_tiles<SR, false, true>(P, S, P.xm32, P.uvis32, P.yrm32);
+        pull_tiles<SR, false>(P, S, P.xm32, P.uvis32, P.yrm32);
     }
     stats_flush(P, S);
     if (!grid_sync(P)) return;
@@ -903,7 +924,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
 // One SpMSpV with a dense x and a dense y (Section 4.3, DB-Decoding): the
 // vector masks come from warp ballots (Section 4.1).  Counter slot P.slot is
 // used by this call; the other slot is reset for the next call.
-__global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
+__global__ void __launch_bounds__(NT, 5) k_spmspv_dense(KParams P)
 {
     Smem &S = *reinterpret_cast<Smem *>(smem_raw);
     if (ld_cg(&P.ctrl->err) != 0u) return;
@@ -947,7 +968,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
         if (!grid_sync(P)) return;
         push_tasks<0, true>(P, S, P.dxm32, nullptr, nullptr, slot);
     } else {
-        pull_tiles<0, true, false>(P, S, P.dxm32, nullptr, nullptr);
+        pull_tiles<0, true>(P, S, P.dxm32, nullptr, nullptr);
     }
     stats_flush(P, S);
     if (blockIdx.x == 0 && tid == 0) {
@@ -966,9 +987,10 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
 // next = (A or.and frontier) and not visited, on the path chosen from the
 // frontier's nonzero-block ratio.  After a level's traversal one scan over
 // the next-frontier words updates visited and levels, clears the old
-// frontier, counts the new one's nonzero blocks and builds its push list.
-// Counters rotate over three slots so each level needs two grid barriers.
-__global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
+// frontier and counts the new one's nonzero blocks; a level that takes the
+// push path first builds its task list from the frontier words.  Counters
+// rotate over three slots: two grid barriers per pull level, three per push.
+__global__ void __launch_bounds__(NT, 5) k_bfs(KParams P)
 {
     Smem &S = *reinterpret_cast<Smem *>(smem_raw);
     if (ld_cg(&P.ctrl->err) != 0u) return;
@@ -1018,36 +1040,48 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
         const int cur = (int)((L - 1) % 3), nxt = (int)(L % 3), old = (int)((L + 1) % 3);
         uint32_t *fcur = P.fm32[(L - 1) & 1], *fnext = P.fm32[L & 1];
         const uint32_t n_nz = ld_cg(&P.ctrl->n_blk[cur]);
+        if (blockIdx.x == 0 && tid == 0 && L - 1u < (uint32_t)BFS_LEVEL_LOG) P.ctrl->lv_t[L - 1u] = globaltimer();
         if (n_nz == 0u) break;
         nz_sum += n_nz;
         const bool push = choose_push(P, n_nz);
         push_levels += push;
-        if (push) push_tasks<1, false>(P, S, fcur, P.bvis32, fnext, cur);
-        else pull_tiles<1, false, false>(P, S, fcur, P.bvis32, fnext);
+        if (blockIdx.x == 0 && tid == 0 && L - 1u < (uint32_t)BFS_LEVEL_LOG) {
+            P.ctrl->lv_nz[L - 1u] = n_nz;
+            P.ctrl->lv_path[L - 1u] = push ? 1u : 2u;
+        }
+        if (push) {
+            // push list of the frontier, built only for push levels (few blocks)
+            if (L > 1u) {
+                for (uint32_t base = blockIdx.x * NT; base < nwords; base += gridDim.x * NT) {
+                    const uint32_t w = base + tid;
+                    const uint32_t fm = w < nwords ? __ldcg(fcur + w) : 0u;
+                    cta_append(P, S.L, cur, (fm & 0xFFFFu) != 0u, 2u * w);
+                    cta_append(P, S.L, cur, (fm >> 16) != 0u, 2u * w + 1u);
+                }
+                if (!grid_sync(P)) return;
+            }
+            push_tasks<1, false>(P, S, fcur, P.bvis32, fnext, cur);
+        } else {
+            pull_tiles<1, false>(P, S, fcur, P.bvis32, fnext);
+        }
         if (!grid_sync(P)) return;
 
         // level update over all frontier words (one thread per word)
         uint32_t nb = 0, reached = 0;
-        for (uint32_t base = blockIdx.x * NT; base < nwords; base += gridDim.x * NT) {
-            const uint32_t w = base + tid;
-            uint32_t nm = 0;
-            if (w < nwords) {
-                nm = __ldcg(fnext + w);
-                if (__ldcg(fcur + w)) fcur[w] = 0u;
-                if (nm) {
-                    P.bvis32[w] = __ldcg(P.bvis32 + w) | nm;
-                    reached += __popc(nm);
-                    nb += ((nm & 0xFFFFu) != 0u) + ((nm >> 16) != 0u);
-                    uint32_t bits = nm;
-                    while (bits) {
-                        const uint32_t k = __ffs(bits) - 1u;
-                        bits &= bits - 1u;
-                        P.levels[(2u * w + (k >> 4)) * 16u + (k & 15u)] = (int32_t)L;
-                    }
+        for (uint32_t w = blockIdx.x * NT + tid; w < nwords; w += gridDim.x * NT) {
+            const uint32_t nm = __ldcg(fnext + w);
+            if (__ldcg(fcur + w)) fcur[w] = 0u;
+            if (nm) {
+                P.bvis32[w] = __ldcg(P.bvis32 + w) | nm;
+                reached += __popc(nm);
+                nb += ((nm & 0xFFFFu) != 0u) + ((nm >> 16) != 0u);
+                uint32_t bits = nm;
+                while (bits) {
+                    const uint32_t k = __ffs(bits) - 1u;
+                    bits &= bits - 1u;
+                    P.levels[(2u * w + (k >> 4)) * 16u + (k & 15u)] = (int32_t)L;
                 }
             }
-            cta_append(P, S.L, nxt, (nm & 0xFFFFu) != 0u, 2u * w);
-            cta_append(P, S.L, nxt, (nm >> 16) != 0u, 2u * w + 1u);
         }
         cta_count(&P.ctrl->n_blk[nxt], nb);
         if (P.stats) cta_count(&P.ctrl->reached, reached);
@@ -1076,7 +1110,7 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
 }
 
 // Withholds block 0 from the barrier so every other block's wait expires.
-__global__ void __launch_bounds__(NT, 4) k_selftest_wait(KParams P)
+__global__ void __launch_bounds__(NT, 5) k_selftest_wait(KParams P)
 {
     if (blockIdx.x == 0) return;
     grid_sync(P);
@@ -1141,7 +1175,6 @@ KParams make_params(const dbs_matrix *A, dbs_workspace *w)
     P.csc_ref = A->d_csc_ref;
     P.payload = reinterpret_cast<const uint4 *>(A->d_payload);
     P.tiles = reinterpret_cast<const uint4 *>(A->d_tiles);
-    P.tile_ref = A->d_tile_ref;
     P.x_dense = w->x_dense; P.xm32 = w->xm32; P.dxm32 = w->dxm32;
     for (int s = 0; s < 3; ++s) { P.act[s] = w->act[s]; P.chunks[s] = w->chunks[s]; }
     P.y_acc = w->y_acc; P.yrm32 = w->yrm32; P.ctile_cnt = w->ctile_cnt; P.n_ctiles = w->n_ctiles;
@@ -1377,6 +1410,26 @@ dbs_status dbs_last_stats(dbs_workspace *w, void *stream, dbs_stats *out)
     out->bfs_push_levels = (int32_t)c.bfs_push_levels;
     for (int i = 0; i < 3; ++i)
         out->phase_ns[i] = c.t_phase[i + 1] >= c.t_phase[i] ? (int64_t)(c.t_phase[i + 1] - c.t_phase[i]) : 0;
+    return DBS_OK;
+}
+
+dbs_status dbs_bfs_level_stats(dbs_workspace *w, void *stream, int32_t max_levels, int64_t *frontier_blocks,
+                               int32_t *path, int64_t *level_ns)
+{
+    if (!w || max_levels < 0) return DBS_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+    Ctrl c;
+    if (cudaMemcpy(&c, w->ctrl, sizeof(Ctrl), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return DBS_ERR_CUDA;
+    }
+    if (!w->last_was_bfs) return DBS_ERR_INVALID_ARG;
+    const int n = std::min<int>(std::min<int>(max_levels, BFS_LEVEL_LOG), (int)c.bfs_levels);
+    for (int l = 0; l < n; ++l) {
+        if (frontier_blocks) frontier_blocks[l] = c.lv_nz[l];
+        if (path) path[l] = (int32_t)c.lv_path[l];
+        if (level_ns) level_ns[l] = c.lv_t[l + 1] >= c.lv_t[l] ? (int64_t)(c.lv_t[l + 1] - c.lv_t[l]) : 0;
+    }
     return DBS_OK;
 }
 

@@ -229,8 +229,6 @@ void free_device(dbs_matrix *A)
 {
     cudaFree(A->d_rb_ptr); cudaFree(A->d_blk_desc); cudaFree(A->d_blk_ref); cudaFree(A->d_cb_ptr);
     cudaFree(A->d_csc_desc); cudaFree(A->d_csc_ref); cudaFree(A->d_payload); cudaFree(A->d_tiles);
-    cudaFree(A->d_tile_ref);
-    A->d_tile_ref = nullptr;
     A->d_rb_ptr = nullptr; A->d_blk_desc = nullptr; A->d_blk_ref = nullptr; A->d_cb_ptr = nullptr;
     A->d_csc_desc = nullptr; A->d_csc_ref = nullptr; A->d_payload = nullptr; A->d_tiles = nullptr;
 }
@@ -255,8 +253,7 @@ dbs_status host_view(const dbs_matrix *A, HostFormat &tmp, const HostFormat **ou
               copy_from_device(tmp.csc_desc, A->d_csc_desc, (size_t)A->B) &&
               copy_from_device(tmp.csc_ref, A->d_csc_ref, (size_t)A->B) &&
               copy_from_device(tmp.payload, A->d_payload, (size_t)A->P) &&
-              copy_from_device(tmp.tiles, A->d_tiles, (size_t)A->T) &&
-              copy_from_device(tmp.tile_ref, A->d_tile_ref, (size_t)A->T);
+              copy_from_device(tmp.tiles, A->d_tiles, (size_t)A->T);
     if (!ok) { cudaGetLastError(); return DBS_ERR_CUDA; }
     *out = &tmp;
     return DBS_OK;
@@ -440,20 +437,14 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         uint32_t R = o.tile_max_row_blocks > 0 ? (uint32_t)o.tile_max_row_blocks : TILE_MAX_SPAN;
         build_tiles(H.rb_ptr, H.blk_desc, nbr, W, R, H.tiles);
         A->T = (int64_t)H.tiles.size();
-        H.tile_ref.resize(H.tiles.size());
         for (size_t i = 0; i < H.tiles.size(); ++i) {
-            U4 &tl = H.tiles[i];
-            H.tile_ref[i] = H.blk_ref[tl.x];
-            // local row block of each block into blk_desc.x bits 27-31; flag
-            // tiles that hold payload-carrying blocks
+            // local row block of each block into blk_desc.x bits 27-31
+            const U4 &tl = H.tiles[i];
             uint32_t rb = tl.z;
-            bool stored = false;
             for (uint32_t p = tl.x; p < tl.y; ++p) {
                 while (H.rb_ptr[rb + 1] <= p) ++rb;
                 H.blk_desc[p].x |= (rb - tl.z) << DESC_LRB_SHIFT;
-                stored |= !meta_inline(H.blk_desc[p].y);
             }
-            if (stored) tl.w |= TILE_HAS_STORED;
         }
     } catch (const std::bad_alloc &) {
         return fail(DBS_ERR_OOM);
@@ -469,7 +460,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
     }
     I.ntiles = A->T;
     I.payload_bytes = A->P * 16;
-    I.view_bytes = (nbr + 1) * 4 + A->B * 8 + A->B * 4 + (nbc + 1) * 4 + A->B * 8 + A->B * 4 + A->T * 20;
+    I.view_bytes = (nbr + 1) * 4 + A->B * 8 + A->B * 4 + (nbc + 1) * 4 + A->B * 8 + A->B * 4 + A->T * 16;
     I.total_bytes = I.payload_bytes + I.view_bytes;
     I.csr_bytes = (m + 1) * 4 + nnz * 4 + (valued ? nnz * 4 : 0);
     I.csr_csc_bytes = I.csr_bytes + (n + 1) * 4 + nnz * 4 + (valued ? nnz * 4 : 0);
@@ -488,7 +479,6 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         if ((st = upload(H.csc_ref, &A->d_csc_ref, (size_t)A->B + 8, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.payload, &A->d_payload, 1, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.tiles, &A->d_tiles, 1, s)) != DBS_OK) return fail(st);
-        if ((st = upload(H.tile_ref, &A->d_tile_ref, 1, s)) != DBS_OK) return fail(st);
         if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return fail(DBS_ERR_CUDA); }
         A->on_device = true;
     }

@@ -306,6 +306,19 @@ def test_bfs_small(small, name, path):
         assert nl == int(ref.max()) + 1
 
 
+def test_bfs_level_stats_match_frontiers(small):
+    A, O, M = small["rmat"]
+    ws = dbs.Workspace(M)
+    src = int(synth.bfs_sources(A, 1, [9, 9])[0])
+    lev, nl = dbs.bfs(M, src, ws=ws)
+    st = ws.bfs_levels()
+    ref = O.bfs_queue(src)
+    assert len(st["frontier_blocks"]) == nl
+    for l in range(nl):
+        assert st["frontier_blocks"][l] == len(np.unique(np.nonzero(ref == l)[0] // 16))
+        assert st["path"][l] in ("push", "pull")
+
+
 def test_bfs_grid_closed_form():
     side = 61
     r, c = np.meshgrid(np.arange(side), np.arange(side - 1), indexing="ij")
