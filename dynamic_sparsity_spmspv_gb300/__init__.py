@@ -246,6 +246,16 @@ def dbs_spmspv_dense(A: DBMatrix, x, *, y=None, path="auto", ws: Workspace, stre
     return y
 
 
+def dbs_spmspv_dense_noalloc(A: DBMatrix, x, *, y, stream=None):
+    """dbs_spmspv_dense_noalloc: like dbs_spmspv_dense on the pull path, but
+    with the scratch in a fixed device array of the library, for callers that
+    may not allocate GPU memory after start-up.  `y` must be given
+    (float32[m] on the device); nothing is allocated by the call."""
+    st = _lib.load().dbs_spmspv_dense_noalloc(A.handle, _ptr(x), _ptr(y), _stream_handle(stream))
+    _lib.check("dbs_spmspv_dense_noalloc", st)
+    return y
+
+
 def dbs_bfs(A: DBMatrix, src: int, *, levels=None, path="auto", ws: Workspace, stream=None, sync: bool = True):
     """dbs_bfs: levels (int32 CUDA tensor, -1 unreached) and, with sync, the
     number of levels."""

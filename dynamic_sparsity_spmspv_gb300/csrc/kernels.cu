@@ -1443,3 +1443,102 @@ dbs_status dbs_selftest_wait_timeout(dbs_workspace *w, void *stream)
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- allocation-free entry
+//
+// dbs_spmspv_dense_noalloc runs the dense-x SpMSpV kernel on the pull path
+// with its scratch (the control block with the grid-barrier state and
+// counters, and the vector-block mask words) in the fixed device array
+// below instead of a workspace.  It is meant for callers that must not
+// allocate GPU memory after start-up: cudaMalloc can synchronise the device
+// and its failures surface at arbitrary times, which real-time serving loops
+// and callers running under a fixed, pre-reserved memory budget cannot
+// accept.  The array lives as long as the library is loaded on every device
+// that loads it.
+
+namespace {
+
+constexpr int64_t NOALLOC_MAX_N = int64_t(1) << 22;                  // columns of A
+constexpr size_t NOALLOC_MASK_WORDS = (size_t)NOALLOC_MAX_N / 32 + 8;  // 2 block masks per word
+constexpr size_t NOALLOC_CTRL_BYTES = (sizeof(Ctrl) + 255) / 256 * 256;
+constexpr size_t NOALLOC_BYTES = NOALLOC_CTRL_BYTES + NOALLOC_MASK_WORDS * sizeof(uint32_t);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
+
+struct NoAllocDevice {
+    bool ready = false;
+    unsigned char *scratch = nullptr;   // device address of g_noalloc_scratch
+    int grid = 0;
+};
+constexpr int NOALLOC_MAX_DEVICES = 64;
+NoAllocDevice g_noalloc_dev[NOALLOC_MAX_DEVICES];
+
+// Once per device, with that device current: resolve the array's device
+// address (in host code its name is only a stand-in) and the cooperative
+// grid size.  No memory is allocated.
+dbs_status noalloc_setup(int dev)
+{
+    NoAllocDevice &d = g_noalloc_dev[dev];
+    if (d.ready) return DBS_OK;
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return DBS_ERR_CUDA;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return DBS_ERR_CUDA;
+    }
+    const int grid = coop_grid((const void *)k_spmspv_dense, sms);
+    if (grid <= 0) return DBS_ERR_CUDA;
+    d.scratch = static_cast<unsigned char *>(ptr);
+    d.grid = grid;
+    d.ready = true;
+    return DBS_OK;
+}
+
+}  // namespace
+
+extern "C" dbs_status dbs_spmspv_dense_noalloc(const dbs_matrix *A, const float *x, float *y, void *stream)
+{
+    if (!A || !A->on_device || !A->valued) return A && !A->valued ? DBS_ERR_UNSUPPORTED : DBS_ERR_INVALID_ARG;
+    if ((A->n > 0 && !x) || (A->m > 0 && !y)) return DBS_ERR_INVALID_ARG;
+    if (A->n > NOALLOC_MAX_N) return DBS_ERR_INVALID_ARG;      // beyond the fixed scratch
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+    if (dev != A->device || dev < 0 || dev >= NOALLOC_MAX_DEVICES) return DBS_ERR_INVALID_ARG;
+    dbs_status st = noalloc_setup(dev);
+    if (st != DBS_OK) return st;
+    NoAllocDevice &d = g_noalloc_dev[dev];
+    cudaStream_t s = (cudaStream_t)stream;
+    // barrier state and counters must start at zero; the mask words are
+    // fully rewritten by the kernel
+    if (cudaMemsetAsync(d.scratch, 0, sizeof(Ctrl), s) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+
+    KParams P{};
+    P.m = (int32_t)A->m; P.n = (int32_t)A->n; P.nbr = (int32_t)A->nbr; P.nbc = (int32_t)A->nbc;
+    P.B = (uint32_t)A->B; P.T = (uint32_t)A->T; P.valued = A->valued;
+    P.rb_ptr = A->d_rb_ptr;
+    P.blk_desc = reinterpret_cast<const uint2 *>(A->d_blk_desc);
+    P.blk_ref = A->d_blk_ref;
+    P.cb_ptr = A->d_cb_ptr;
+    P.csc_desc = reinterpret_cast<const uint2 *>(A->d_csc_desc);
+    P.csc_ref = A->d_csc_ref;
+    P.payload = reinterpret_cast<const uint4 *>(A->d_payload);
+    P.tiles = reinterpret_cast<const uint4 *>(A->d_tiles);
+    P.ctrl = reinterpret_cast<Ctrl *>(d.scratch);
+    P.dxm32 = reinterpret_cast<uint32_t *>(d.scratch + NOALLOC_CTRL_BYTES);
+    P.path_force = DBS_PATH_PULL;          // the pull path needs no task lists
+    P.x_in = x;
+    P.xv = x;
+    P.y_dense = y;
+    P.slot = 0;
+    dbs_exec_opts o;
+    dbs_exec_opts_default(&o);
+    P.th3 = o.th3;
+    P.local_pull_min = o.local_pull_min;
+    P.stats = 0;
+    P.timeout_ns = o.wait_timeout_ns;
+    return launch((const void *)k_spmspv_dense, d.grid, P, s);
+}

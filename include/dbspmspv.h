@@ -266,6 +266,28 @@ dbs_status dbs_bfs_level_stats(dbs_workspace *ws, void *stream, int32_t max_leve
  * dbs_workspace_check() then reports it.  No GPU fault is involved. */
 dbs_status dbs_selftest_wait_timeout(dbs_workspace *ws, void *stream);
 
+/* Allocation-free variant of dbs_spmspv_dense (the paper has no counterpart:
+ * it is an interface for callers that may not allocate GPU memory after
+ * start-up, such as real-time serving loops, where cudaMalloc's implicit
+ * device synchronisation and late failures are not acceptable, or hosts that
+ * reserve a fixed memory budget up front).  Same inputs and outputs as
+ * dbs_spmspv_dense (x: device float32[n], y: device float32[m]), always on
+ * the pull path, plus-times only.  Its scratch -- grid-barrier state,
+ * counters and the vector-block masks, about 513 KiB -- is a fixed device
+ * array inside the library that every GPU loading the library holds until
+ * the process exits; the call itself allocates nothing.
+ *   Limits: n <= 2^22 (4,194,304) columns, else DBS_ERR_INVALID_ARG; the
+ *   matrix must be valued (else DBS_ERR_UNSUPPORTED) and on the current
+ *   device.
+ *   The first call on a device resolves the array's device address and the
+ *   launch grid for that device (make it before any stream capture).
+ *   All calls share the one array: calls that may overlap on the GPU (on
+ *   different streams, or from different threads) race and must be
+ *   serialised by the caller.  Each call clears the state it needs.
+ *   Device-side wait timeouts are not reported (y is then undefined).
+ * ASYNC. */
+dbs_status dbs_spmspv_dense_noalloc(const dbs_matrix *A, const float *x, float *y, void *stream);
+
 /* Human-readable name of a status. */
 const char *dbs_status_string(dbs_status s);
 
