@@ -51,6 +51,28 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("kernels.cu", "format.h"):
+        with open(os.path.join(ROOT, "dynamic_sparsity_spmspv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the kernel sources changed since it was captured."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic_rmat_s20.json")) as f:
+            d = json.load(f)
+        if d.get("kernel_source_sha256") != _kernel_source_hash():
+            return None
+        return d["traffic_bytes_per_launch"][kernel]["mean"]
+    except Exception:
+        return None
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -399,7 +421,7 @@ def main():
         dom, dom_bytes, dom_t, dom_n = "k_bfs", bytes_b, t_bfs, args.steps
     achieved = dom_bytes / dom_n / (dom_t / dom_n * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                "frac": achieved / peak, "peak_kind": peak_kind, "traffic": _traffic(dom),
                 "bytes_alg_per_launch": dom_bytes / dom_n, "us_per_launch": 1e3 * dom_t / dom_n,
                 "share_of_step": dom_t / t_total_ms}
 
