@@ -245,6 +245,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--path-sweep", type=int, default=8,
+                    help="calls per density and forced path for the push/pull crossover table (0 = off)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -436,6 +438,27 @@ def main():
            "gpu_launches": calls_per_step * args.steps,
            "roofline": roofline, "per_density": per_density, "bfs": bfs_info, "clocks": clocks,
            "wall_s_timed_region": wall}
+
+    # push/pull crossover on this GPU: forced paths, same inputs, same timing
+    if args.path_sweep > 0:
+        sweep = []
+        for d in DENSITIES:
+            row = {"density": d}
+            for path in ("push", "pull"):
+                ts = []
+                for i in range(args.path_sweep):
+                    flush(i)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    dbs.spmspv(M, x_dev[d][i % POOL], None, semiring="or_and", path=path, ws=ws,
+                               y_idx=y_idx, y_nnz=y_nnz)
+                    e1.record(stream)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+                row[f"{path}_us"] = round(1e3 * float(np.median(ts)), 2)
+            sweep.append(row)
+        out["path_sweep"] = sweep
+        assert ws.check() == 0
 
     # end to end through the public API with host buffers
     if not args.no_e2e:

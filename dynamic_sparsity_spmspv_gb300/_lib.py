@@ -26,7 +26,7 @@ class dbs_build_opts(ctypes.Structure):
 
 class dbs_exec_opts(ctypes.Structure):
     _fields_ = [("th3", F64), ("local_pull_min", I32), ("collect_stats", I32),
-                ("wait_timeout_ns", I64)]
+                ("wait_timeout_ns", I64), ("push_work_frac", F64)]
 
 
 class dbs_matrix_info(ctypes.Structure):

@@ -15,7 +15,7 @@
 //                         This is the paper's csc2csr mapping resolved to the
 //                         shared payload, so push reaches a block in one load.
 //   payload  uint4[P]     the low-level blocks, 16-byte aligned
-//   tiles    uint4[T]     pull work units {p0, p1, rb0, span} (Section 3.3.2)
+//   tiles    uint4[T]     pull work units {p0, p1, rb0, span | shared-edge flags} (Section 3.3.2)
 //
 // blk_desc.x holds the column block in bits 0-26 and, in bits 27-31, the
 // block's row block relative to the first row block of its pull tile, so a
@@ -57,10 +57,14 @@ namespace dbs {
 constexpr int BS = 16;
 constexpr uint32_t FMT_COO = 0, FMT_DENSE = 1, FMT_FCSR = 2, FMT_FCSC = 3, FMT_PCSR = 4;
 
-// Pull tiles (one warp task each): at most this many blocks (32 lanes x 8) and
-// this many row blocks (the warp's shared-memory row accumulators).
+// Pull tiles (one warp task each): at most this many blocks (32 lanes x 8)
+// and this many row blocks (the warp's shared-memory row accumulators).
 constexpr uint32_t TILE_MAX_BLOCKS = 256;
 constexpr uint32_t TILE_MAX_SPAN = 32;
+// tiles[].w: span in bits 0-15, bit 16: the first row block continues in the
+// previous tile, bit 17: the last row block continues in the next tile.
+constexpr uint32_t TILE_FIRST_SHARED = 1u << 16;
+constexpr uint32_t TILE_LAST_SHARED = 1u << 17;
 // Push tasks: CSC positions per work item (one warp, one position per lane).
 constexpr uint32_t PUSH_CHUNK = 32;
 

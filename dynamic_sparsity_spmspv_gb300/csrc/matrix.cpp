@@ -429,7 +429,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         for (int64_t p = 0; p < B; ++p) total_w += fmt_weight(meta_fmt(H.blk_desc[(size_t)p].y));
         uint32_t W = (uint32_t)o.tile_weight;
         if (W == 0) {
-            // about 64 tiles per SM (two per resident warp), within [16, 256]
+            // about 64 tiles per SM, within [16, TILE_MAX_BLOCKS]
             uint64_t target = (uint64_t)num_sms_or_default() * 64u;
             W = (uint32_t)std::min<uint64_t>(TILE_MAX_BLOCKS, std::max<uint64_t>(16, (total_w + target - 1) / target));
         }
@@ -438,13 +438,16 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         build_tiles(H.rb_ptr, H.blk_desc, nbr, W, R, H.tiles);
         A->T = (int64_t)H.tiles.size();
         for (size_t i = 0; i < H.tiles.size(); ++i) {
-            // local row block of each block into blk_desc.x bits 27-31
-            const U4 &tl = H.tiles[i];
+            // local row block of each block into blk_desc.x bits 27-31; flags
+            // for row blocks shared with the neighbouring tiles
+            U4 &tl = H.tiles[i];
             uint32_t rb = tl.z;
             for (uint32_t p = tl.x; p < tl.y; ++p) {
                 while (H.rb_ptr[rb + 1] <= p) ++rb;
                 H.blk_desc[p].x |= (rb - tl.z) << DESC_LRB_SHIFT;
             }
+            if (H.rb_ptr[tl.z] < tl.x) tl.w |= TILE_FIRST_SHARED;
+            if (H.rb_ptr[tl.z + (tl.w & 0xFFFFu)] > tl.y) tl.w |= TILE_LAST_SHARED;
         }
     } catch (const std::bad_alloc &) {
         return fail(DBS_ERR_OOM);

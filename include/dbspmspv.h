@@ -98,7 +98,8 @@ void dbs_build_opts_default(dbs_build_opts *opts);
 
 /* Execution options of a workspace.  dbs_exec_opts_default() fills them. */
 typedef struct {
-    double th3;                /* push iff N_nzblk < th3 * N_blk (paper: 0.01) */
+    double th3;                /* push iff N_nzblk < th3 * N_blk (paper: 0.01); used when
+                                  push_work_frac is 0 */
     int32_t local_pull_min;    /* patched-CSR blocks use the row-wise (pull) microkernel
                                   when popc(active block columns) >= this; else the
                                   column-wise (push) one.  Unstated in the paper; 8. */
@@ -107,6 +108,10 @@ typedef struct {
     int64_t wait_timeout_ns;   /* bound on every device-side wait (grid barriers);
                                   default 2 s.  On expiry the kernel latches
                                   DBS_ERR_TIMEOUT and returns. */
+    double push_work_frac;     /* > 0: push iff the matrix blocks of the active column
+                                  blocks (push's work) number fewer than push_work_frac * B
+                                  (pull's scan); default 0.1, the crossover measured on
+                                  GB300.  0: the paper's th3 rule. */
 } dbs_exec_opts;
 
 void dbs_exec_opts_default(dbs_exec_opts *opts);

@@ -43,12 +43,12 @@ def test_status_strings_and_version():
 def test_struct_layouts_match_header_sizes():
     # sizes implied by the C declarations on LP64
     assert ctypes.sizeof(_lib.dbs_build_opts) == 40
-    assert ctypes.sizeof(_lib.dbs_exec_opts) == 24
+    assert ctypes.sizeof(_lib.dbs_exec_opts) == 32
     assert ctypes.sizeof(_lib.dbs_stats) == 104
     o = dbs.build_opts()
     assert (o.th0, o.th1, o.th2, o.force_format) == (32, 128, 2.0, -1)
     e = dbs.exec_opts()
-    assert (e.th3, e.local_pull_min) == (0.01, 8)
+    assert (e.th3, e.local_pull_min, e.push_work_frac) == (0.01, 8, 0.1)
 
 
 def _host(A, **kw):

@@ -205,20 +205,39 @@ def test_permutation_and_identity():
         np.testing.assert_array_equal(gv, (vals[j] * xd[j]).astype(np.float32))
 
 
-def test_selector_boundary():
-    # nbc = 6400 column blocks: th3 = 0.01 puts the switch at 64 nonzero blocks
+@pytest.mark.parametrize("th3,switch", [(0.01, 64), (0.1, 640)])
+def test_selector_boundary(th3, switch):
+    # nbc = 6400 column blocks: push iff N_nzblk / 6400 < th3 (the paper's 0.01
+    # switches at 64 nonzero blocks, the GB300 default 0.1 at 640)
     n = 6400 * 16
     A = synth.random_csr(64, n, 0.002, 3)
     M = dbs.DBMatrix.from_csr(A)
-    ws = dbs.Workspace(M, collect_stats=1)
+    ws = dbs.Workspace(M, collect_stats=1, th3=th3, push_work_frac=0.0)     # the paper's rule
     O = oracle.Oracle(A)
-    for nzb, expect in ((63, 1), (64, 2), (65, 2), (1, 1)):
-        blocks = np.arange(nzb) * 97                   # all < 6400 column blocks
-        assert blocks.max() * 16 + 3 < n
+    for nzb, expect in ((switch - 1, 1), (switch, 2), (switch + 1, 2), (1, 1)):
+        blocks = np.arange(nzb) * (6400 // (switch + 2))           # all < 6400 column blocks
+        assert len(np.unique(blocks)) == nzb and blocks.max() * 16 + 3 < n
         x = synth.SparseVec(n, (blocks * 16 + 3).astype(np.int32), np.ones(nzb, np.float32))
         assert_parity(A, O, M, ws, x)
         st = ws.stats()
         assert st["n_nzblk"] == nzb and st["path"] == expect, (nzb, st)
+
+
+def test_work_based_selector():
+    # push iff the blocks of the active column blocks < push_work_frac * B
+    A = synth.config("fem", "small")
+    M = dbs.DBMatrix.from_csr(A)
+    O = oracle.Oracle(A)
+    V = oracle.block_views(A)
+    deg = np.diff(V["blk_col_ptr"])
+    B = V["B"]
+    ws = dbs.Workspace(M, collect_stats=1, push_work_frac=0.1)
+    for k in (1, 3, 10, 40, 200, 1000):
+        x = synth.x_uniform(A.n, k, [k, 5])
+        act = np.unique(x.idx // 16)
+        expect = 1 if deg[act].sum() < 0.1 * B else 2
+        assert_parity(A, O, M, ws, x)
+        assert ws.stats()["path"] == expect, (k, deg[act].sum(), B)
 
 
 def test_stats_count_touched_nnz(small):
