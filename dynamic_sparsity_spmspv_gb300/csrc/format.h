@@ -15,7 +15,7 @@
 //                         This is the paper's csc2csr mapping resolved to the
 //                         shared payload, so push reaches a block in one load.
 //   payload  uint4[P]     the low-level blocks, 16-byte aligned
-//   tiles    uint4[T]     pull work units {p0, p1, rb0, span | shared-edge flags} (Section 3.3.2)
+//   tiles    uint4[T]     pull work units {p0, payload offset, rb0, span | flags | count} (Section 3.3.2)
 //
 // blk_desc.x holds the column block in bits 0-26 and, in bits 27-31, the
 // block's row block relative to the first row block of its pull tile, so a
@@ -61,10 +61,15 @@ constexpr uint32_t FMT_COO = 0, FMT_DENSE = 1, FMT_FCSR = 2, FMT_FCSC = 3, FMT_P
 // and this many row blocks (the warp's shared-memory row accumulators).
 constexpr uint32_t TILE_MAX_BLOCKS = 256;
 constexpr uint32_t TILE_MAX_SPAN = 32;
-// tiles[].w: span in bits 0-15, bit 16: the first row block continues in the
-// previous tile, bit 17: the last row block continues in the next tile.
+// tiles[] = {p0, payload offset of block p0, first row block rb0, w}.
+// w: span in bits 0-15, bit 16: the first row block continues in the
+// previous tile, bit 17: the last row block continues in the next tile,
+// bits 20-28: block count.  A tile's descriptors, copied in 16-byte units
+// from the even index at or below p0, fit 256 slots: (p0 & 1) + count <= 256.
+constexpr uint32_t TILE_SPAN_MASK = 0xFFFFu;
 constexpr uint32_t TILE_FIRST_SHARED = 1u << 16;
 constexpr uint32_t TILE_LAST_SHARED = 1u << 17;
+constexpr uint32_t TILE_NBLK_SHIFT = 20;
 // Push tasks: CSC positions per work item (one warp, one position per lane).
 constexpr uint32_t PUSH_CHUNK = 32;
 

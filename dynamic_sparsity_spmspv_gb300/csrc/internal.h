@@ -22,7 +22,7 @@ struct HostFormat {
     std::vector<uint32_t> csc_ref;    // B
     std::vector<uint32_t> csc2csr;    // B (host only)
     std::vector<U4> payload;          // P
-    std::vector<U4> tiles;            // T: {p0, p1, rb0, span}
+    std::vector<U4> tiles;            // T: {p0, payload offset, rb0, span | flags | count}
 };
 
 }  // namespace dbs

@@ -39,12 +39,10 @@ constexpr uint32_t FULL = 0xFFFFFFFFu;
 constexpr uint32_t CTILE = 2 * NT;   // row blocks per compaction tile (one mask word per thread)
 constexpr int BFS_LEVEL_LOG = 64;    // BFS levels whose frontier, path and time are recorded
 
-constexpr int BAR_GROUPS = 64;       // first-level barrier counters (32 blocks each)
+constexpr int MAX_GRID = 4096;       // cooperative grid size cap
 
 struct Ctrl {
-    unsigned int bar_sub[BAR_GROUPS][32];   // one 128-byte line per group counter
-    unsigned int bar_count;             // second level: groups arrived
-    unsigned int bar_gen;
+    unsigned long long bar[2][16];      // grid-barrier arrival counters, one 128-byte line each
     unsigned int err;
     unsigned int path;
     unsigned int n_blk[3];      // nonzero vector blocks (N_nzblk) of the slot's vector
@@ -110,6 +108,7 @@ struct KParams {
     uint32_t *fm32[2];
     Ctrl *ctrl;
     int slot;                 // counter slot of this call (dense mode alternates 0/1)
+    int bslot;                // grid-barrier counter of this launch (launch parity)
     double th3;
     double push_frac;
     int local_pull_min;
@@ -149,45 +148,52 @@ __device__ __forceinline__ uint32_t or16(uint32_t *w, uint32_t b, uint32_t bits)
 }
 
 // Bounded grid barrier.  Returns false (and every caller must return) when
-// the wait timed out or another block latched an error.  Arrival is a
-// two-level tree: blocks arrive on their group's counter (32 blocks per
-// group, one cache line each) and the last of a group arrives on the root,
-// so no single counter takes more than a few dozen atomics.  Every arrival
-// is preceded by a fence (release); the wait is an acquire at GPU scope.
+// the wait timed out or another block latched an error.  Every launch owns
+// one of two 64-bit arrival counters (by launch parity) and clears the other
+// one for the launch after it.  Block b's k-th barrier adds 1 to the counter
+// with a release (the block's writes, ordered before it by the block-wide
+// barrier, become visible first) and waits, with acquire loads, until the
+// counter reaches k * gridDim.x.  Arrival is fire-and-forget, so the last
+// block to arrive releases everyone after one trip to L2.
+__device__ __forceinline__ void red_release_add(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__shared__ unsigned s_bar_epoch;
+
+// Start of every kernel that uses grid_sync.
+__device__ __forceinline__ void grid_sync_init(const KParams &P)
+{
+    if (threadIdx.x == 0) {
+        s_bar_epoch = 0u;
+        if (blockIdx.x == 0) P.ctrl->bar[P.bslot ^ 1][0] = 0ull;
+    }
+}
 __device__ bool grid_sync(const KParams &P)
 {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         Ctrl *c = P.ctrl;
+        unsigned long long *cnt = &c->bar[P.bslot][0];
+        const unsigned long long target = (unsigned long long)(++s_bar_epoch) * gridDim.x;
         int ok = 1;
-        const unsigned gen = ld_acquire(&c->bar_gen);
-        const unsigned g = blockIdx.x >> 5, ngroups = (gridDim.x + 31u) >> 5;
-        const unsigned gsize = min(32u, gridDim.x - (g << 5));
-        __threadfence();
-        bool released = false;
-        if (atomicAdd(&c->bar_sub[g][0], 1u) == gsize - 1u) {
-            atomicExch(&c->bar_sub[g][0], 0u);
-            __threadfence();
-            if (atomicAdd(&c->bar_count, 1u) == ngroups - 1u) {
-                atomicExch(&c->bar_count, 0u);
-                __threadfence();
-                st_release(&c->bar_gen, gen + 1);
-                released = true;
-            }
-        }
-        if (!released) {
-            unsigned long long t0 = globaltimer();
-            unsigned ns = 32;
-            while (ld_acquire(&c->bar_gen) == gen) {
+        red_release_add(cnt, 1ull);
+        if (ld_acquire64(cnt) < target) {
+            const unsigned long long t0 = globaltimer();
+            while (ld_acquire64(cnt) < target) {
                 if (ld_cg(&c->err) != 0u) { ok = 0; break; }
                 if ((long long)(globaltimer() - t0) > P.timeout_ns) {
                     atomicCAS(&c->err, 0u, (unsigned)DBS_ERR_TIMEOUT);
                     ok = 0;
                     break;
                 }
-                __nanosleep(ns);
-                if (ns < 256) ns <<= 1;
             }
         }
         if (ok && ld_cg(&c->err) != 0u) ok = 0;
@@ -504,164 +510,249 @@ __device__ __forceinline__ uint32_t bool_bytes(uint32_t meta)
 
 // ------------------------------------------------------------- traversal
 
-// Per-warp state of a pull task.
+// Per-warp state of a pull task.  Plus-times keeps per-row partial sums;
+// the Boolean variant does not.
+template <int SR>
 struct WarpPull {
+    uint32_t qe[TILE_MAX_BLOCKS];     // queued hits with a payload: li | lrb << 8 | act << 16
+    uint32_t qm[TILE_MAX_BLOCKS];     // their meta words
     uint32_t rm[TILE_MAX_SPAN];       // touched (Boolean: found) rows per row block
-    uint32_t vis[TILE_MAX_SPAN];      // visited rows per row block (Boolean)
-    float y[TILE_MAX_SPAN * 16];      // partial row sums (plus-times)
-    uint32_t q[TILE_MAX_BLOCKS];      // hits with a payload: local index | row block << 10 | act << 16
-    uint32_t nq;
+    uint32_t nq;                      // queued hits
+    float y[SR == 0 ? TILE_MAX_SPAN * 16 : 1];   // partial row sums (plus-times)
 };
 
-struct Smem {
-    WarpPull wp[NW];
+struct SmemBase {
     float wacc[NW][16];
     float wx[NW][16];
     unsigned long long st[4];   // visited, hits, touched, bytes
     ListStage L;
 };
 
+template <int SR>
+struct SmemT : SmemBase {
+    WarpPull<SR> wp[NW];
+};
+
 extern __shared__ __align__(128) unsigned char smem_raw[];
 
 // Statistics: a warp sums its lanes' counts and one lane adds them to the
 // CTA's shared counter (all lanes of the warp must call it).
-__device__ __forceinline__ void stat_add(Smem &S, int i, unsigned long long v)
+__device__ __forceinline__ void stat_add(SmemBase &S, int i, unsigned long long v)
 {
     const unsigned long long w = __reduce_add_sync(FULL, (unsigned)v);
     if ((threadIdx.x & 31) == 0 && w) atomicAdd(&S.st[i], w);
 }
 
+// Bit operations on a 16-bit column mask m held twice, mm = m | m << 16: a
+// right funnel shift of (mm:mm) by a coordinate byte (row << 4 | col) wraps
+// at 32 and so brings bit col of m to bit 0 whatever the row's low bit is.
+__device__ __forceinline__ uint32_t dup16(uint32_t m) { return m | (m << 16); }
+__device__ __forceinline__ uint32_t coord_found(uint32_t mm, uint32_t s)
+{
+    return (__funnelshift_r(mm, mm, s) & 1u) << ((s >> 4) & 15u);
+}
+
+// Rows of an inline block (its coordinate bytes in bits 0-23 of the meta
+// word) reached from the active columns.
+__device__ __forceinline__ uint32_t inline_found(uint32_t meta, uint32_t mm)
+{
+    return coord_found(mm, meta) | coord_found(mm, meta >> 8) | coord_found(mm, meta >> 16);
+}
+
+// Rows of a COO block reached from its active columns: 16 coordinates per
+// 16-byte unit, the first `cnt` of them valid.
+__device__ __forceinline__ uint32_t coo_found16(uint4 v, uint32_t mm, uint32_t cnt)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t f = 0;
+#pragma unroll
+    for (uint32_t j = 0; j < 16u; ++j) {
+        const uint32_t b = coord_found(mm, w[j >> 2] >> (8u * (j & 3u)));
+        f |= j < cnt ? b : 0u;
+    }
+    return f;
+}
+// Rows of a stored block reached from its active columns `act` (Algorithm 5
+// semantics), given the first two 16-byte units that hold its pattern (see
+// bool_load); longer COO blocks read the rest.
+__device__ __forceinline__ uint32_t bool_found_units(uint32_t fmt, uint32_t nnz, uint32_t act, uint4 u0, uint4 u1,
+                                                     const uint4 *b4)
+{
+    uint32_t f = 0;
+    if (fmt == FMT_COO) {
+        const uint32_t mm = dup16(act);
+        f = coo_found16(u0, mm, nnz);
+        if (nnz > 16u) f |= coo_found16(u1, mm, nnz - 16u);
+        for (uint32_t base = 32; base < nnz; base += 16u) f |= coo_found16(__ldg(b4 + (base >> 4)), mm, nnz - base);
+    } else {
+        const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        if (fmt == FMT_DENSE || fmt == FMT_FCSC) {          // column masks: OR the active columns
+#pragma unroll
+            for (uint32_t c = 0; c < 16; ++c)
+                f |= ((act >> c) & 1u) ? (w[c >> 1] >> ((c & 1u) << 4)) & 0xFFFFu : 0u;
+        } else {                                            // row masks: rows meeting an active column
+#pragma unroll
+            for (uint32_t r = 0; r < 16; ++r)
+                f |= ((w[r >> 1] >> ((r & 1u) << 4)) & act) ? 1u << r : 0u;
+        }
+    }
+    return f;
+}
+// The two units bool_found_units starts from: COO coordinates 0-31, the
+// Dense column masks (bytes 0-31), or the Force / patched masks (bytes 16-47).
+__device__ __forceinline__ void bool_load(const uint4 *b4, uint32_t fmt, uint32_t nnz, uint4 &u0, uint4 &u1)
+{
+    const uint32_t s = (fmt == FMT_COO || fmt == FMT_DENSE) ? 0u : 1u;
+    u0 = __ldg(b4 + s);
+    u1 = (fmt != FMT_COO || nnz > 16u) ? __ldg(b4 + s + 1) : make_uint4(0u, 0u, 0u, 0u);
+}
+
 // Pull (Section 3.3.2): every warp takes tiles of consecutive primary blocks
 // (load-weighted segments of at most 256 blocks and 32 row blocks) and works
-// through them without block-wide synchronisation.  Each lane issues the
-// descriptor loads of its 8 blocks together and then their 8 vector-mask
-// lookups, so many independent requests are in flight per warp.  Inline
-// blocks finish right there; hits with a payload are queued and drained by
-// the lanes, or by the whole warp for the Dense / Force / patched-CSR
-// microkernels.  Row results gather in the warp's shared-memory accumulators
-// and are written back once per row block (Section 3.3.3).
-// SR 0 = plus-times, 1 = Boolean.  DOUT: dense output y.
+// through them without block-wide synchronisation.
+//   * Each lane loads the descriptors of its eight blocks (li = k*32 + lane,
+//     so every load instruction of the warp reads 256 contiguous bytes), then
+//     issues all eight vector-mask lookups before using any of them.
+//   * Inline blocks are resolved in registers and OR-ed into the row
+//     accumulators; stored blocks that meet an active column are queued with
+//     their meta word.
+//   * Queued hits are drained one per lane (Boolean, COO) or by the whole
+//     warp (Dense / Force / patched-CSR microkernels); the payload offset of
+//     a hit comes from blk_ref.
+// Row results gather in the warp's shared-memory accumulators and are written
+// back once per row block (Section 3.3.3).
+// SR 0 = plus-times, 1 = Boolean.  DOUT: dense output y.  With a visited
+// mask, tiles whose rows are all visited are skipped.
 // Mask lookups go through L1: the masks are read-only between two grid
 // barriers, and every barrier ends with an acquire at GPU scope, after which
 // plain loads observe all writes made before the barrier (the same guarantee
 // that cooperative grid synchronisation gives).
 template <int SR, bool DOUT>
-__device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const uint32_t *vis,
+__device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, const uint32_t *vis,
                            uint32_t *out_rm, int tslot)
 {
-    constexpr int WK = 8;                       // blocks per lane per pass
+    constexpr int WK = 8;                       // blocks per lane per tile
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    WarpPull &W = S.wp[warp];
+    WarpPull<SR> &W = S.wp[warp];
+    const unsigned short *xm16 = reinterpret_cast<const unsigned short *>(xm);
     const float *xv = P.xv;
     const uint32_t nwarps = gridDim.x * NW;
-    unsigned long long c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
-    // Tiles [0, T0) are taken in a static strided order; the tail [T0, T) is
-    // handed out one tile at a time, the next index being requested while
-    // the current tile is processed, so warps that drew cheap tiles help
-    // finish the expensive ones.
+    // Tiles [0, T0) are taken in a static strided order; the last six
+    // rounds [T0, T) are handed out one tile at a time, so warps that drew
+    // cheap tiles help finish the expensive ones.
     const uint32_t rounds = P.T / nwarps;
-    const uint32_t T0 = rounds > 2u ? (rounds - 2u) * nwarps : 0u;
+    const uint32_t T0 = rounds > 6u ? (rounds - 6u) * nwarps : 0u;
     unsigned *ctr = &P.ctrl->tile_next[tslot];
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+    auto next_tile = [&](uint32_t t) -> uint32_t {
+        if (t + nwarps < T0) return t + nwarps;
+        const uint32_t v = lane == 0 ? T0 + atomicAdd(ctr, 1u) : 0u;
+        return __shfl_sync(FULL, v, 0);
+    };
+
     uint32_t t = blockIdx.x * NW + warp;
-    uint32_t t_next = 0;
-    if (t >= T0) {
-        t = T0 + (lane == 0 ? atomicAdd(ctr, 1u) : 0u);
-        t = __shfl_sync(FULL, t, 0);
+    if (t >= T0) {                                   // straight to the dynamic tail
+        const uint32_t v = lane == 0 ? T0 + atomicAdd(ctr, 1u) : 0u;
+        t = __shfl_sync(FULL, v, 0);
     }
-    for (; t < P.T; t = t_next) {
-        if (t + nwarps < T0) {
-            t_next = t + nwarps;
-        } else {
-            t_next = lane == 0 ? T0 + atomicAdd(ctr, 1u) : 0u;   // consumed after this tile
-        }
-        const uint4 td = __ldg(P.tiles + t);
-        const uint32_t p0 = td.x, p1 = td.y, rb0 = td.z, span = td.w & 0xFFFFu, nblk = p1 - p0;
-        const uint32_t edge = td.w >> 16;   // bit 0: first row block shared, bit 1: last
+    uint4 td = t < P.T ? __ldg(P.tiles + t) : z4;
+    while (t < P.T) {
+        uint32_t c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;   // statistics of this tile
+        // the next tile's descriptor is fetched while this one is processed
+        const uint32_t t_n = next_tile(t);
+        const uint4 td_n = t_n < P.T ? __ldg(P.tiles + t_n) : z4;
+        const uint32_t p0 = td.x, rb0 = td.z, span = td.w & TILE_SPAN_MASK, nblk = td.w >> TILE_NBLK_SHIFT;
+        const uint32_t edge = td.w;   // TILE_FIRST_SHARED / TILE_LAST_SHARED
         uint32_t vrow = 0;
         if (SR == 1 && vis) {
             // every row of the task's row blocks already visited: nothing to find
             vrow = lane < (int)span ? mask16(vis, rb0 + lane) : 0xFFFFu;
             if (__all_sync(FULL, vrow == 0xFFFFu)) {
-                t_next = __shfl_sync(FULL, t_next, 0);
+                t = t_n;
+                td = td_n;
                 continue;
             }
         }
-        if (lane < (int)span) {
-            W.rm[lane] = 0u;
-            if (SR == 1) W.vis[lane] = vrow;
+        uint2 d[WK];
+#pragma unroll
+        for (int k = 0; k < WK; ++k) {
+            const uint32_t li = (uint32_t)(k * 32 + lane);
+            d[k] = li < nblk ? __ldcs(P.blk_desc + p0 + li) : make_uint2(0u, 0u);
         }
+        if (lane < (int)span) W.rm[lane] = 0u;
         if (SR == 0)
             for (uint32_t i = lane; i < span * 16u; i += 32) W.y[i] = 0.0f;
         if (lane == 0) W.nq = 0u;
+        uint32_t mm[WK / 2];   // the eight column-block masks, two per register
+#pragma unroll
+        for (int j = 0; j < WK / 2; ++j) {
+            const uint32_t l0 = (uint32_t)(2 * j * 32 + lane), l1 = l0 + 32u;
+            const uint32_t a = l0 < nblk ? (uint32_t)__ldca(xm16 + (d[2 * j].x & DESC_COL_MASK)) : 0u;
+            const uint32_t b = l1 < nblk ? (uint32_t)__ldca(xm16 + (d[2 * j + 1].x & DESC_COL_MASK)) : 0u;
+            mm[j] = a | (b << 16);
+        }
         __syncwarp();
-
-        // 8 blocks per lane: descriptor loads together, then the mask lookups
-        {
-            const uint32_t pb = 0;
-            uint2 d[WK];
 #pragma unroll
-            for (int k = 0; k < WK; ++k) {
-                const uint32_t li = pb + (uint32_t)(k * 32 + lane);
-                d[k] = li < nblk ? __ldcs(P.blk_desc + p0 + li) : make_uint2(0u, 0u);
-            }
-#pragma unroll
-            for (int k = 0; k < WK; ++k) {
-                const uint32_t li = pb + (uint32_t)(k * 32 + lane);
-                const uint32_t meta = d[k].y, col = d[k].x & DESC_COL_MASK, lrb = d[k].x >> DESC_LRB_SHIFT;
-                const bool skip = li >= nblk || (SR == 1 && vis && W.vis[lrb] == 0xFFFFu);
-                const uint32_t m = skip ? 0u : (uint32_t)__ldca(reinterpret_cast<const unsigned short *>(xm) + col);
-                if (P.stats && m) { ++c_vis; c_touch += meta_nnz(meta); }
-                if (SR == 1 && meta_inline(meta)) {
-                    // inline block: its rows met by active columns, straight from x's mask
-                    const uint32_t f = meta_inline_found(meta, m);
-                    if (f) {
-                        atomicOr(&W.rm[lrb], f);
-                        if (P.stats) ++c_hit;
-                    }
-                    continue;
+        for (int k = 0; k < WK; ++k) {
+            const uint32_t li = (uint32_t)(k * 32 + lane);
+            const uint32_t m = (mm[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu;   // 0 past the tile's end
+            const uint32_t meta = d[k].y, lrb = d[k].x >> DESC_LRB_SHIFT;
+            if (P.stats && m) { ++c_vis; c_touch += meta_nnz(meta); }
+            if (SR == 1 && meta_inline(meta)) {
+                const uint32_t f = inline_found(meta, dup16(m));
+                if (f) {
+                    atomicOr(&W.rm[lrb], f);
+                    if (P.stats) ++c_hit;
                 }
-                const uint32_t a = m & meta_cmask(meta);
+            } else {
+                const uint32_t a = m & meta & 0xFFFFu;
                 if (a) {
                     const uint32_t slot = atomicAdd(&W.nq, 1u);
-                    W.q[slot] = li | (lrb << 10) | (a << 16);
+                    W.qe[slot] = li | (lrb << 8) | (a << 16);
+                    W.qm[slot] = meta;
                     if (P.stats) ++c_hit;
                 }
             }
         }
         __syncwarp();
 
-        // payload-carrying hits: COO and Boolean blocks one per lane, the
-        // other formats by the whole warp
+        // payload-carrying hits
         const uint32_t nq = W.nq;
-        for (uint32_t i = lane; i < nq; i += 32) {
-            const uint32_t e = W.q[i];
-            const uint32_t p = p0 + (e & 0x3FFu), lrb = (e >> 10) & 0x3Fu, a = e >> 16;
-            const uint32_t meta = __ldg(&P.blk_desc[p].y);
-            if (SR == 0 && meta_fmt(meta) != FMT_COO) continue;
-            const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.blk_ref + p));
-            uint32_t rows = 0;
-            if (SR == 1) {
-                rows = bool_found(b, meta, a);
-                if (P.stats) c_bytes += 4u + bool_bytes(meta);
-            } else {
-                const uint32_t nnz = meta_nnz(meta), col = __ldg(&P.blk_desc[p].x) & DESC_COL_MASK;
+        if (SR == 1) {
+            for (uint32_t i = lane; i < nq; i += 32) {
+                const uint32_t e = W.qe[i], meta = W.qm[i];
+                const uint4 *b = P.payload + __ldg(P.blk_ref + p0 + (e & 0xFFu));
+                const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
+                uint4 u0, u1;
+                bool_load(b, fmt, nnz, u0, u1);
+                const uint32_t r = bool_found_units(fmt, nnz, e >> 16, u0, u1, b);
+                if (r) atomicOr(&W.rm[(e >> 8) & 0xFFu], r);
+                if (P.stats) c_bytes += 4u + (fmt == FMT_COO ? nnz : 32u);
+            }
+        } else {
+            // COO hits one per lane
+            for (uint32_t i = lane; i < nq; i += 32) {
+                const uint32_t e = W.qe[i], meta = W.qm[i];
+                if (meta_fmt(meta) != FMT_COO) continue;
+                const uint32_t p = p0 + (e & 0xFFu), lrb = (e >> 8) & 0xFFu, nnz = meta_nnz(meta);
+                const uint32_t col = __ldg(&P.blk_desc[p].x) & DESC_COL_MASK;
                 float *sy = &W.y[lrb * 16u];
-                rows = coo_lane(b, nnz, a, xv + (size_t)col * 16u, true,
-                                [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
+                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.blk_ref + p));
+                const uint32_t rows = coo_lane(b, nnz, e >> 16, xv + (size_t)col * 16u, true,
+                                               [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
+                if (rows) atomicOr(&W.rm[lrb], rows);
                 if (P.stats) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
             }
-            if (rows) atomicOr(&W.rm[lrb], rows);
-        }
-        if (SR == 0) {
             __syncwarp();
+            // the other formats by the whole warp
             for (uint32_t i = 0; i < nq; ++i) {
-                const uint32_t e = W.q[i];
-                const uint32_t p = p0 + (e & 0x3FFu), lrb = (e >> 10) & 0x3Fu, a = e >> 16;
-                const uint2 dd = __ldg(P.blk_desc + p);
-                if (meta_fmt(dd.y) == FMT_COO) continue;            // warp-uniform
+                const uint32_t e = W.qe[i], meta = W.qm[i];
+                if (meta_fmt(meta) == FMT_COO) continue;            // warp-uniform
+                const uint32_t p = p0 + (e & 0xFFu), lrb = (e >> 8) & 0xFFu;
+                const uint32_t col = __ldg(&P.blk_desc[p].x) & DESC_COL_MASK;
                 uint32_t by = 0;
-                RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.blk_ref + p)), dd.y, a,
-                                    xv + (size_t)(dd.x & DESC_COL_MASK) * 16u, lane, S.wacc[warp], &by);
+                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.blk_ref + p));
+                RowOut o = mk_heavy(P, b, meta, e >> 16, xv + (size_t)col * 16u, lane, S.wacc[warp], &by);
                 if (lane < 16 && o.touched) W.y[lrb * 16u + lane] += o.sum;
                 const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
                 if (lane == 0) {
@@ -677,14 +768,15 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
         // task is stored, one shared with a neighbouring task is added
         if (SR == 1) {
             if (lane < (int)span) {
-                const uint32_t f = W.rm[lane] & ~W.vis[lane];
+                const uint32_t f = W.rm[lane] & ~vrow;
                 if (f) or16(out_rm, rb0 + lane, f);
             }
         } else {
             for (uint32_t i = lane; i < span * 16u; i += 32) {
                 const uint32_t lrb = i >> 4, r = i & 15u;
                 if (!((W.rm[lrb] >> r) & 1u)) continue;
-                const bool partial = (lrb == 0u && (edge & 1u)) || (lrb == span - 1u && (edge & 2u));
+                const bool partial = (lrb == 0u && (edge & TILE_FIRST_SHARED)) ||
+                                     (lrb == span - 1u && (edge & TILE_LAST_SHARED));
                 float *dst = DOUT ? P.y_dense : P.y_acc;
                 const size_t row = (size_t)(rb0 + lrb) * 16u + r;
                 if (partial) atomicAdd(dst + row, W.y[i]);
@@ -692,15 +784,16 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
             }
             if (!DOUT && lane < (int)span && W.rm[lane]) or16(out_rm, rb0 + lane, W.rm[lane]);
         }
-        if (P.stats && lane == 0) c_bytes += 8u * nblk + 24u;
+        if (P.stats) {
+            if (lane == 0) c_bytes += 8u * nblk + 16u;
+            stat_add(S, 0, c_vis);
+            stat_add(S, 1, c_hit);
+            stat_add(S, 2, c_touch);
+            stat_add(S, 3, c_bytes);
+        }
         __syncwarp();
-        t_next = __shfl_sync(FULL, t_next, 0);
-    }
-    if (P.stats) {
-        stat_add(S, 0, c_vis);
-        stat_add(S, 1, c_hit);
-        stat_add(S, 2, c_touch);
-        stat_add(S, 3, c_bytes);
+        t = t_n;
+        td = td_n;
     }
 }
 
@@ -708,7 +801,7 @@ __device__ void pull_tiles(const KParams &P, Smem &S, const uint32_t *xm, const 
 // one active column block; the active vector block is cached in shared memory
 // (Section 3.3.3) and each block's rows are written back with atomics.
 template <int SR, bool DOUT>
-__device__ void push_tasks(const KParams &P, Smem &S, const uint32_t *xm, const uint32_t *vis,
+__device__ void push_tasks(const KParams &P, SmemBase &S, const uint32_t *xm, const uint32_t *vis,
                            uint32_t *out_rm, int cslot)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -814,11 +907,11 @@ __device__ __forceinline__ uint32_t cb_len(const KParams &P, uint32_t cb)
     return __ldg(P.cb_ptr + cb + 1) - __ldg(P.cb_ptr + cb);
 }
 
-__device__ __forceinline__ void stats_begin(Smem &S)
+__device__ __forceinline__ void stats_begin(SmemBase &S)
 {
     if (threadIdx.x < 4) S.st[threadIdx.x] = 0ull;
 }
-__device__ __forceinline__ void stats_flush(const KParams &P, Smem &S)
+__device__ __forceinline__ void stats_flush(const KParams &P, SmemBase &S)
 {
     __syncthreads();
     if (P.stats && threadIdx.x == 0) {
@@ -844,7 +937,8 @@ __device__ __forceinline__ void reset_stats(const KParams &P)
 template <int SR>
 __global__ void __launch_bounds__(NT, 5) k_spmspv_sparse(KParams P)
 {
-    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
+    SmemT<SR> &S = *reinterpret_cast<SmemT<SR> *>(smem_raw);
+    grid_sync_init(P);
     if (ld_cg(&P.ctrl->err) != 0u) return;
     const int tid = threadIdx.x;
     const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
@@ -981,7 +1075,8 @@ __global__ void __launch_bounds__(NT, 5) k_spmspv_sparse(KParams P)
 // used by this call; the other slot is reset for the next call.
 __global__ void __launch_bounds__(NT, 5) k_spmspv_dense(KParams P)
 {
-    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
+    SmemT<0> &S = *reinterpret_cast<SmemT<0> *>(smem_raw);
+    grid_sync_init(P);
     if (ld_cg(&P.ctrl->err) != 0u) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
@@ -1051,7 +1146,8 @@ __global__ void __launch_bounds__(NT, 5) k_spmspv_dense(KParams P)
 // rotate over three slots: two grid barriers per pull level, three per push.
 __global__ void __launch_bounds__(NT, 5) k_bfs(KParams P)
 {
-    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
+    SmemT<1> &S = *reinterpret_cast<SmemT<1> *>(smem_raw);
+    grid_sync_init(P);
     if (ld_cg(&P.ctrl->err) != 0u) return;
     const int tid = threadIdx.x;
     const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
@@ -1180,6 +1276,7 @@ __global__ void __launch_bounds__(NT, 5) k_bfs(KParams P)
 // Withholds block 0 from the barrier so every other block's wait expires.
 __global__ void __launch_bounds__(NT, 5) k_selftest_wait(KParams P)
 {
+    grid_sync_init(P);
     if (blockIdx.x == 0) return;
     grid_sync(P);
 }
@@ -1195,6 +1292,7 @@ struct dbs_workspace {
     int grid_sparse[2] = {0, 0};
     int grid_dense = 0, grid_bfs = 0;
     int call_count = 0;
+    unsigned launches = 0;      // launches made; its parity picks the grid-barrier counter
     dbs_exec_opts opts{};
     float *x_dense = nullptr;
     uint32_t *xm32 = nullptr;
@@ -1256,7 +1354,9 @@ KParams make_params(const dbs_matrix *A, dbs_workspace *w)
     return P;
 }
 
-dbs_status launch(const void *fn, int grid, KParams &P, cudaStream_t s, size_t smem = sizeof(Smem))
+constexpr size_t SMEM0 = sizeof(SmemT<0>), SMEM1 = sizeof(SmemT<1>);   // dynamic shared memory per CTA
+
+dbs_status launch(const void *fn, int grid, KParams &P, cudaStream_t s, size_t smem)
 {
     void *args[] = {&P};
     cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NT), args, smem, s);
@@ -1264,7 +1364,17 @@ dbs_status launch(const void *fn, int grid, KParams &P, cudaStream_t s, size_t s
     return DBS_OK;
 }
 
-int coop_grid(const void *fn, int sms, size_t smem = sizeof(Smem))
+// A workspace launch: launches alternate the grid-barrier counter, and the
+// parity advances only when the kernel was actually queued.
+dbs_status launch_ws(dbs_workspace *w, const void *fn, int grid, KParams &P, cudaStream_t s, size_t smem)
+{
+    P.bslot = (int)(w->launches & 1u);
+    const dbs_status st = launch(fn, grid, P, s, smem);
+    if (st == DBS_OK) w->launches++;
+    return st;
+}
+
+int coop_grid(const void *fn, int sms, size_t smem)
 {
     int nb = 0;
     if (smem > 48u * 1024u &&
@@ -1273,7 +1383,7 @@ int coop_grid(const void *fn, int sms, size_t smem = sizeof(Smem))
         return 0;
     }
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, NT, smem) != cudaSuccess) { cudaGetLastError(); return 0; }
-    return std::min(nb * sms, BAR_GROUPS * 32);     // the grid barrier's capacity
+    return std::min(nb * sms, MAX_GRID);
 }
 
 dbs_status check_ready(const dbs_matrix *A, dbs_workspace *w)
@@ -1326,10 +1436,10 @@ dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
               dalloc(&w->fm32[0], nbc / 2 + 8) && dalloc(&w->fm32[1], nbc / 2 + 8) && dalloc(&w->ctrl, 1);
     for (int s = 0; s < 3 && ok; ++s) ok = dalloc(&w->act[s], nbc + 1) && dalloc(&w->chunks[s], chunk_cap);
     if (!ok) { ws_free(w); delete w; return DBS_ERR_OOM; }
-    w->grid_sparse[0] = coop_grid((const void *)k_spmspv_sparse<0>, w->sms);
-    w->grid_sparse[1] = coop_grid((const void *)k_spmspv_sparse<1>, w->sms);
-    w->grid_dense = coop_grid((const void *)k_spmspv_dense, w->sms);
-    w->grid_bfs = coop_grid((const void *)k_bfs, w->sms);
+    w->grid_sparse[0] = coop_grid((const void *)k_spmspv_sparse<0>, w->sms, SMEM0);
+    w->grid_sparse[1] = coop_grid((const void *)k_spmspv_sparse<1>, w->sms, SMEM1);
+    w->grid_dense = coop_grid((const void *)k_spmspv_dense, w->sms, SMEM0);
+    w->grid_bfs = coop_grid((const void *)k_bfs, w->sms, SMEM1);
     if (!w->grid_sparse[0] || !w->grid_sparse[1] || !w->grid_dense || !w->grid_bfs) {
         ws_free(w);
         delete w;
@@ -1408,7 +1518,8 @@ dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx
     P.slot = w->call_count & 1;
     w->call_count++;
     w->last_was_bfs = false;
-    return launch(fn, w->grid_sparse[sr == DBS_PLUS_TIMES_F32 ? 0 : 1], P, (cudaStream_t)stream);
+    return launch_ws(w, fn, w->grid_sparse[sr == DBS_PLUS_TIMES_F32 ? 0 : 1], P, (cudaStream_t)stream,
+                     sr == DBS_PLUS_TIMES_F32 ? SMEM0 : SMEM1);
 }
 
 dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_path path, dbs_workspace *w,
@@ -1427,7 +1538,7 @@ dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_p
     P.slot = w->call_count & 1;
     w->call_count++;
     w->last_was_bfs = false;
-    return launch((const void *)k_spmspv_dense, w->grid_dense, P, (cudaStream_t)stream);
+    return launch_ws(w, (const void *)k_spmspv_dense, w->grid_dense, P, (cudaStream_t)stream, SMEM0);
 }
 
 dbs_status dbs_bfs(const dbs_matrix *A, int64_t src, int32_t *levels, int32_t *nlevels_host, dbs_path path,
@@ -1447,7 +1558,7 @@ dbs_status dbs_bfs(const dbs_matrix *A, int64_t src, int32_t *levels, int32_t *n
     // slot clear.
     w->call_count = 0;
     w->last_was_bfs = true;
-    st = launch((const void *)k_bfs, w->grid_bfs, P, s);
+    st = launch_ws(w, (const void *)k_bfs, w->grid_bfs, P, s, SMEM1);
     if (st != DBS_OK || !nlevels_host) return st;
     Ctrl c;
     if (cudaMemcpyAsync(&c, w->ctrl, sizeof(Ctrl), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
@@ -1513,7 +1624,7 @@ dbs_status dbs_selftest_wait_timeout(dbs_workspace *w, void *stream)
     KParams P = make_params(w->A, w);
     int grid = std::min(coop_grid((const void *)k_selftest_wait, w->sms, 0), 2 * w->sms);
     if (grid < 2) return DBS_ERR_UNSUPPORTED;
-    return launch((const void *)k_selftest_wait, grid, P, (cudaStream_t)stream, 0);
+    return launch_ws(w, (const void *)k_selftest_wait, grid, P, (cudaStream_t)stream, 0);
 }
 
 }  // extern "C"
@@ -1564,7 +1675,7 @@ dbs_status noalloc_setup(int dev)
         cudaGetLastError();
         return DBS_ERR_CUDA;
     }
-    const int grid = coop_grid((const void *)k_spmspv_dense, sms);
+    const int grid = coop_grid((const void *)k_spmspv_dense, sms, SMEM0);
     if (grid <= 0) return DBS_ERR_CUDA;
     d.scratch = static_cast<unsigned char *>(ptr);
     d.grid = grid;
@@ -1615,5 +1726,5 @@ extern "C" dbs_status dbs_spmspv_dense_noalloc(const dbs_matrix *A, const float 
     P.local_pull_min = o.local_pull_min;
     P.stats = 0;
     P.timeout_ns = o.wait_timeout_ns;
-    return launch((const void *)k_spmspv_dense, d.grid, P, s);
+    return launch((const void *)k_spmspv_dense, d.grid, P, s, SMEM0);
 }

@@ -207,7 +207,7 @@ void build_tiles(const std::vector<uint32_t> &rb_ptr, const std::vector<U2> &des
             w += fmt_weight(meta_fmt(desc[p].y));
             ++count;
             last_rb = (uint32_t)rb;
-            if (w >= W || count >= TILE_MAX_BLOCKS) close(p + 1, last_rb);
+            if (w >= W || count + (p0 & 1u) >= TILE_MAX_BLOCKS) close(p + 1, last_rb);
         }
     }
     if (count > 0) close(rb_ptr[(size_t)nbr], last_rb);
@@ -447,7 +447,23 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
                 H.blk_desc[p].x |= (rb - tl.z) << DESC_LRB_SHIFT;
             }
             if (H.rb_ptr[tl.z] < tl.x) tl.w |= TILE_FIRST_SHARED;
-            if (H.rb_ptr[tl.z + (tl.w & 0xFFFFu)] > tl.y) tl.w |= TILE_LAST_SHARED;
+            if (H.rb_ptr[tl.z + (tl.w & TILE_SPAN_MASK)] > tl.y) tl.w |= TILE_LAST_SHARED;
+            // kernel form: the block count joins w, the payload offset of
+            // the first block replaces the end index
+            tl.w |= (tl.y - tl.x) << TILE_NBLK_SHIFT;
+            tl.y = tl.x < (uint32_t)B ? H.blk_ref[tl.x] : 0u;
+        }
+        // the pull kernel's copy and queue bounds rely on these
+        {
+            uint64_t next = 0;
+            for (const U4 &tl : H.tiles) {
+                const uint32_t nb = tl.w >> TILE_NBLK_SHIFT, span = tl.w & TILE_SPAN_MASK;
+                if (tl.x != next || nb == 0 || (tl.x & 1u) + nb > TILE_MAX_BLOCKS || span == 0 ||
+                    span > TILE_MAX_SPAN || (int64_t)tl.z + span > nbr)
+                    return fail(DBS_ERR_INTERNAL);
+                next += nb;
+            }
+            if (next != (uint64_t)B) return fail(DBS_ERR_INTERNAL);
         }
     } catch (const std::bad_alloc &) {
         return fail(DBS_ERR_OOM);
