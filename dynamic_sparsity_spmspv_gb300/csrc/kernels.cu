@@ -650,35 +650,42 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
         return __shfl_sync(FULL, v, 0);
     };
 
+    // visited rows of a tile's row blocks (lane i: row block rb0 + i); a tile
+    // whose rows are all visited is skipped before its descriptors are read
+    auto settle = [&](uint32_t &tt, uint4 &tdd, uint32_t &vr) {
+        while (tt < P.T) {
+            vr = lane < (int)(tdd.w & TILE_SPAN_MASK) ? mask16(vis, tdd.z + lane) : 0xFFFFu;
+            if (!__all_sync(FULL, vr == 0xFFFFu)) return;
+            tt = next_tile(tt);
+            tdd = tt < P.T ? __ldg(P.tiles + tt) : z4;
+        }
+    };
+    auto load_desc = [&](const uint4 &tdd, uint2 (&dd)[WK]) {
+#pragma unroll
+        for (int k = 0; k < WK; ++k) {
+            const uint32_t li = (uint32_t)(k * 32 + lane);
+            dd[k] = li < (tdd.w >> TILE_NBLK_SHIFT) ? __ldcs(P.blk_desc + tdd.x + li) : make_uint2(0u, 0u);
+        }
+    };
+
+    // Software pipeline over a warp's tiles: the descriptors of the next tile
+    // are loaded while the current one is looked up and processed.
     uint32_t t = blockIdx.x * NW + warp;
     if (t >= T0) {                                   // straight to the dynamic tail
         const uint32_t v = lane == 0 ? T0 + atomicAdd(ctr, 1u) : 0u;
         t = __shfl_sync(FULL, v, 0);
     }
     uint4 td = t < P.T ? __ldg(P.tiles + t) : z4;
+    uint32_t vrow = 0;
+    if (SR == 1 && vis) settle(t, td, vrow);
+    uint2 d[WK];
+    load_desc(td, d);
     while (t < P.T) {
         uint32_t c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;   // statistics of this tile
-        // the next tile's descriptor is fetched while this one is processed
-        const uint32_t t_n = next_tile(t);
-        const uint4 td_n = t_n < P.T ? __ldg(P.tiles + t_n) : z4;
-        const uint32_t p0 = td.x, rb0 = td.z, span = td.w & TILE_SPAN_MASK, nblk = td.w >> TILE_NBLK_SHIFT;
-        const uint32_t edge = td.w;   // TILE_FIRST_SHARED / TILE_LAST_SHARED
-        uint32_t vrow = 0;
-        if (SR == 1 && vis) {
-            // every row of the task's row blocks already visited: nothing to find
-            vrow = lane < (int)span ? mask16(vis, rb0 + lane) : 0xFFFFu;
-            if (__all_sync(FULL, vrow == 0xFFFFu)) {
-                t = t_n;
-                td = td_n;
-                continue;
-            }
-        }
-        uint2 d[WK];
-#pragma unroll
-        for (int k = 0; k < WK; ++k) {
-            const uint32_t li = (uint32_t)(k * 32 + lane);
-            d[k] = li < nblk ? __ldcs(P.blk_desc + p0 + li) : make_uint2(0u, 0u);
-        }
+        uint32_t t_n = next_tile(t);
+        uint4 td_n = t_n < P.T ? __ldg(P.tiles + t_n) : z4;
+        const uint32_t rb0 = td.z, span = td.w & TILE_SPAN_MASK, nblk = td.w >> TILE_NBLK_SHIFT;
+        const uint32_t p0 = td.x, edge = td.w;   // TILE_FIRST_SHARED / TILE_LAST_SHARED
         if (lane < (int)span) W.rm[lane] = 0u;
         if (SR == 0)
             for (uint32_t i = lane; i < span * 16u; i += 32) W.y[i] = 0.0f;
@@ -691,6 +698,10 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             const uint32_t b = l1 < nblk ? (uint32_t)__ldca(xm16 + (d[2 * j + 1].x & DESC_COL_MASK)) : 0u;
             mm[j] = a | (b << 16);
         }
+        uint32_t vrow_n = 0;
+        if (SR == 1 && vis) settle(t_n, td_n, vrow_n);
+        uint2 d_n[WK];
+        load_desc(td_n, d_n);
         __syncwarp();
 #pragma unroll
         for (int k = 0; k < WK; ++k) {
@@ -794,6 +805,9 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
         __syncwarp();
         t = t_n;
         td = td_n;
+        vrow = vrow_n;
+#pragma unroll
+        for (int k = 0; k < WK; ++k) d[k] = d_n[k];
     }
 }
 
@@ -935,7 +949,7 @@ __device__ __forceinline__ void reset_stats(const KParams &P)
 // One SpMSpV with a sparse x (index list + values) and a sparse output.
 // Phases: metadata | [push list] | traversal | compaction counts | writes.
 template <int SR>
-__global__ void __launch_bounds__(NT, 5) k_spmspv_sparse(KParams P)
+__global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
 {
     SmemT<SR> &S = *reinterpret_cast<SmemT<SR> *>(smem_raw);
     grid_sync_init(P);
@@ -1073,7 +1087,7 @@ __global__ void __launch_bounds__(NT, 5) k_spmspv_sparse(KParams P)
 // One SpMSpV with a dense x and a dense y (Section 4.3, DB-Decoding): the
 // vector masks come from warp ballots (Section 4.1).  Counter slot P.slot is
 // used by this call; the other slot is reset for the next call.
-__global__ void __launch_bounds__(NT, 5) k_spmspv_dense(KParams P)
+__global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
 {
     SmemT<0> &S = *reinterpret_cast<SmemT<0> *>(smem_raw);
     grid_sync_init(P);
@@ -1144,7 +1158,7 @@ __global__ void __launch_bounds__(NT, 5) k_spmspv_dense(KParams P)
 // frontier and counts the new one's nonzero blocks; a level that takes the
 // push path first builds its task list from the frontier words.  Counters
 // rotate over three slots: two grid barriers per pull level, three per push.
-__global__ void __launch_bounds__(NT, 5) k_bfs(KParams P)
+__global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
 {
     SmemT<1> &S = *reinterpret_cast<SmemT<1> *>(smem_raw);
     grid_sync_init(P);
