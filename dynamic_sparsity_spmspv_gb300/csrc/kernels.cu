@@ -141,6 +141,12 @@ __device__ __forceinline__ uint32_t mask16(const uint32_t *w, uint32_t b)
 {
     return (__ldcg(w + (b >> 1)) >> ((b & 1u) << 4)) & 0xFFFFu;
 }
+// Visited rows of row block b: a 16-bit load, so a caller's mask of exactly
+// ceil(m / 16) half-words is never read past its end.
+__device__ __forceinline__ uint32_t vis16(const uint32_t *v, uint32_t b)
+{
+    return __ldcg(reinterpret_cast<const unsigned short *>(v) + b);
+}
 __device__ __forceinline__ uint32_t or16(uint32_t *w, uint32_t b, uint32_t bits)
 {
     uint32_t sh = (b & 1u) << 4;
@@ -516,6 +522,7 @@ template <int SR>
 struct WarpPull {
     uint32_t qe[TILE_MAX_BLOCKS];     // queued hits with a payload: li | lrb << 8 | act << 16
     uint32_t qm[TILE_MAX_BLOCKS];     // their meta words
+    uint32_t qr[TILE_MAX_BLOCKS];     // push: their row blocks
     uint32_t rm[TILE_MAX_SPAN];       // touched (Boolean: found) rows per row block
     uint32_t nq;                      // queued hits
     float y[SR == 0 ? TILE_MAX_SPAN * 16 : 1];   // partial row sums (plus-times)
@@ -654,7 +661,7 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
     // whose rows are all visited is skipped before its descriptors are read
     auto settle = [&](uint32_t &tt, uint4 &tdd, uint32_t &vr) {
         while (tt < P.T) {
-            vr = lane < (int)(tdd.w & TILE_SPAN_MASK) ? mask16(vis, tdd.z + lane) : 0xFFFFu;
+            vr = lane < (int)(tdd.w & TILE_SPAN_MASK) ? vis16(vis, tdd.z + lane) : 0xFFFFu;
             if (!__all_sync(FULL, vr == 0xFFFFu)) return;
             tt = next_tile(tt);
             tdd = tt < P.T ? __ldg(P.tiles + tt) : z4;
@@ -811,88 +818,112 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
     }
 }
 
-// Push (Section 3.3.2): warps take tasks of 32 consecutive CSC positions of
-// one active column block; the active vector block is cached in shared memory
-// (Section 3.3.3) and each block's rows are written back with atomics.
+// Push (Section 3.3.2): warps take tasks of up to 256 consecutive CSC
+// positions of one active column block; the active vector block is cached
+// in shared memory (Section 3.3.3).  Each lane loads the descriptors of its
+// eight positions together.  Inline blocks are resolved at once and their
+// found rows OR-ed into the output mask; stored blocks meeting an active
+// column are queued and drained one per lane (Boolean, COO) or by the whole
+// warp (Dense / Force / patched CSR), their payload reached through csc_ref.
+// Rows are written back with atomics.  Boolean found rows are not masked by
+// the visited rows here: the caller masks them once afterwards (a stored
+// block whose rows are all visited is skipped in the drain).
 template <int SR, bool DOUT>
-__device__ void push_tasks(const KParams &P, SmemBase &S, const uint32_t *xm, const uint32_t *vis,
+__device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, const uint32_t *vis,
                            uint32_t *out_rm, int cslot)
 {
+    constexpr int WK = PUSH_CHUNK / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    WarpPull<SR> &W = S.wp[warp];
     const uint32_t nch = ld_cg(&P.ctrl->n_chunk[cslot]);
     const uint32_t gw = blockIdx.x * NW + warp, nwarps = gridDim.x * NW;
     float *wx = S.wx[warp];
-    unsigned long long c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
+    float *y = DOUT ? P.y_dense : P.y_acc;
+    uint32_t c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
     for (uint32_t ci = gw; ci < nch; ci += nwarps) {
         const uint2 ch = __ldcg(P.chunks[cslot] + ci);
         const uint32_t q0 = ch.x, c = ch.y;
         const uint32_t q1 = min(q0 + PUSH_CHUNK, __ldg(P.cb_ptr + c + 1));
-        const uint32_t xmb = mask16(xm, c);
-        if (SR == 0) {
-            if (lane < 16) {
-                const size_t j = (size_t)c * 16u + lane;
-                wx[lane] = j < (size_t)P.n ? __ldcg(P.xv + j) : 0.0f;
-            }
-            __syncwarp();
+        uint2 d[WK];
+#pragma unroll
+        for (int k = 0; k < WK; ++k) {
+            const uint32_t q = q0 + (uint32_t)(k * 32 + lane);
+            d[k] = q < q1 ? __ldg(P.csc_desc + q) : make_uint2(0u, 0u);
         }
-        const uint32_t q = q0 + lane;
-        uint32_t rb = 0, meta = 0, act = 0, vm = 0, ref = 0;
-        if (q < q1) {
-            const uint2 d = __ldg(P.csc_desc + q);
-            rb = d.x;
-            meta = d.y;
-            act = meta_cmask(meta) & xmb;
-            ++c_vis;
-            c_touch += meta_nnz(meta);
-            c_bytes += 8;
-            if (SR == 1 && vis && act) {
-                vm = mask16(vis, rb);
-                if (vm == 0xFFFFu) act = 0;
-            }
-            if (act) {
-                ++c_hit;
-                if (!meta_inline(meta)) {
-                    ref = __ldg(P.csc_ref + q);
-                    c_bytes += 4;
+        const uint32_t xmb = mask16(xm, c), mm = dup16(xmb);
+        if (SR == 0 && lane < 16) {
+            const size_t j = (size_t)c * 16u + lane;
+            wx[lane] = j < (size_t)P.n ? __ldcg(P.xv + j) : 0.0f;
+        }
+        if (lane == 0) W.nq = 0u;
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < WK; ++k) {
+            const uint32_t ql = (uint32_t)(k * 32 + lane);
+            if (q0 + ql >= q1) continue;
+            const uint32_t rb = d[k].x, meta = d[k].y;
+            if (P.stats) { ++c_vis; c_touch += meta_nnz(meta); c_bytes += 8u; }
+            if (SR == 1 && meta_inline(meta)) {
+                const uint32_t f = inline_found(meta, mm);
+                if (f) {
+                    or16(out_rm, rb, f);
+                    if (P.stats) ++c_hit;
+                }
+            } else {
+                const uint32_t a = meta & xmb & 0xFFFFu;
+                if (a) {
+                    const uint32_t slot = atomicAdd(&W.nq, 1u);
+                    W.qe[slot] = ql | (a << 16);
+                    W.qm[slot] = meta;
+                    W.qr[slot] = rb;
+                    if (P.stats) ++c_hit;
                 }
             }
         }
-        const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + ref);
+        __syncwarp();
+        const uint32_t nq = W.nq;
         if (SR == 1) {
-            if (act) {
-                uint32_t f = bool_found(b, meta, act) & ~vm;
-                c_bytes += bool_bytes(meta);
+            for (uint32_t i = lane; i < nq; i += 32) {
+                const uint32_t e = W.qe[i], meta = W.qm[i], rb = W.qr[i];
+                const uint32_t ref = __ldg(P.csc_ref + q0 + (e & 0xFFFFu));
+                const uint32_t vm = vis ? vis16(vis, rb) : 0u;
+                if (vm == 0xFFFFu) continue;
+                const uint4 *pb = P.payload + ref;
+                const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
+                uint4 u0, u1;
+                bool_load(pb, fmt, nnz, u0, u1);
+                const uint32_t f = bool_found_units(fmt, nnz, e >> 16, u0, u1, pb) & ~vm;
                 if (f) or16(out_rm, rb, f);
+                if (P.stats) c_bytes += 4u + (fmt == FMT_COO ? nnz : 32u);
             }
         } else {
-            float *y = DOUT ? P.y_dense : P.y_acc;
-            if (act && meta_fmt(meta) == FMT_COO) {
+            for (uint32_t i = lane; i < nq; i += 32) {
+                const uint32_t e = W.qe[i], meta = W.qm[i], rb = W.qr[i];
+                if (meta_fmt(meta) != FMT_COO) continue;
                 const uint32_t nnz = meta_nnz(meta);
+                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.csc_ref + q0 + (e & 0xFFFFu)));
                 float *yr = y + (size_t)rb * 16u;
-                uint32_t rows = coo_lane(b, nnz, act, wx, true, [&](uint32_t r, float v) { atomicAdd(yr + r, v); });
+                const uint32_t rows = coo_lane(b, nnz, e >> 16, wx, true, [&](uint32_t r, float v) { atomicAdd(yr + r, v); });
                 if (!DOUT && rows) or16(out_rm, rb, rows);
-                c_bytes += val_offset(FMT_COO, nnz) + 4u * nnz;
-            }
-            uint32_t heavy = __ballot_sync(FULL, act && meta_fmt(meta) != FMT_COO);
-            while (heavy) {
-                const int L = __ffs(heavy) - 1;
-                heavy &= heavy - 1u;
-                const uint32_t h_ref = __shfl_sync(FULL, ref, L);
-                const uint32_t h_meta = __shfl_sync(FULL, meta, L);
-                const uint32_t h_rb = __shfl_sync(FULL, rb, L);
-                const uint32_t h_act = __shfl_sync(FULL, act, L);
-                uint32_t by = 0;
-                RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + h_ref), h_meta, h_act, wx,
-                                    lane, S.wacc[warp], &by);
-                if (lane < 16 && o.touched) atomicAdd(y + (size_t)h_rb * 16u + lane, o.sum);
-                uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
-                if (lane == 0) {
-                    if (!DOUT && bits) or16(out_rm, h_rb, bits);
-                    c_bytes += by;
-                }
+                if (P.stats) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
             }
             __syncwarp();
+            for (uint32_t i = 0; i < nq; ++i) {
+                const uint32_t e = W.qe[i], meta = W.qm[i], rb = W.qr[i];
+                if (meta_fmt(meta) == FMT_COO) continue;            // warp-uniform
+                uint32_t by = 0;
+                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.csc_ref + q0 + (e & 0xFFFFu)));
+                RowOut o = mk_heavy(P, b, meta, e >> 16, wx, lane, S.wacc[warp], &by);
+                if (lane < 16 && o.touched) atomicAdd(y + (size_t)rb * 16u + lane, o.sum);
+                const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
+                if (lane == 0) {
+                    if (!DOUT && bits) or16(out_rm, rb, bits);
+                    if (P.stats) c_bytes += 4u + by;
+                }
+                __syncwarp();
+            }
         }
+        __syncwarp();
     }
     if (P.stats) {
         stat_add(S, 0, c_vis);
@@ -1035,8 +1066,18 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
         if (SR == 0) P.x_dense[j] = 0.0f;
         P.xm32[j >> 5] = 0u;
     }
+    // Rows found by push may include visited ones: the caller's mask is
+    // applied here, per word of two row blocks.
+    auto unvisited = [&](size_t w) -> uint32_t {
+        if (SR != 1 || !P.uvis32) return FULL;
+        const uint32_t lo = 2u * w < (size_t)P.nbr ? vis16(P.uvis32, (uint32_t)(2u * w)) : 0u;
+        const uint32_t hi = 2u * w + 1u < (size_t)P.nbr ? vis16(P.uvis32, (uint32_t)(2u * w + 1u)) : 0u;
+        return ~(lo | (hi << 16));
+    };
     for (uint32_t ct = blockIdx.x; ct < P.n_ctiles; ct += gridDim.x) {
-        const uint32_t wd = __ldcg(P.yrm32 + (size_t)ct * NT + tid);
+        const size_t wi = (size_t)ct * NT + tid;
+        uint32_t wd = __ldcg(P.yrm32 + wi);
+        if (wd) wd &= unvisited(wi);
         uint32_t tot;
         block_excl_scan(__popc(wd), &tot);
         if (tid == 0) P.ctile_cnt[ct] = tot;
@@ -1060,10 +1101,11 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
         uint32_t base;
         block_excl_scan(part, &base);            // total over the CTA = rows before this tile
         const size_t wi = (size_t)ct * NT + tid;
-        uint32_t bits = __ldcg(P.yrm32 + wi);
+        const uint32_t raw = __ldcg(P.yrm32 + wi);
+        uint32_t bits = raw ? raw & unvisited(wi) : 0u;
         uint32_t tile_tot;
         uint32_t o = base + block_excl_scan(__popc(bits), &tile_tot);
-        if (bits) P.yrm32[wi] = 0u;
+        if (raw) P.yrm32[wi] = 0u;
         while (bits) {
             const uint32_t k = __ffs(bits) - 1u;
             bits &= bits - 1u;
@@ -1241,10 +1283,14 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
         // level update over all frontier words (one thread per word)
         uint32_t nb = 0, reached = 0, work = 0;
         for (uint32_t w = blockIdx.x * NT + tid; w < nwords; w += gridDim.x * NT) {
-            const uint32_t nm = __ldcg(fnext + w);
+            const uint32_t raw = __ldcg(fnext + w);
             if (__ldcg(fcur + w)) fcur[w] = 0u;
+            // push leaves visited rows among the found ones: keep the new rows
+            const uint32_t vw = raw ? __ldcg(P.bvis32 + w) : 0u;
+            const uint32_t nm = raw & ~vw;
+            if (nm != raw) fnext[w] = nm;
             if (nm) {
-                P.bvis32[w] = __ldcg(P.bvis32 + w) | nm;
+                P.bvis32[w] = vw | nm;
                 reached += __popc(nm);
                 if (nm & 0xFFFFu) { ++nb; work += cb_len(P, 2u * w); }
                 if (nm >> 16) { ++nb; work += cb_len(P, 2u * w + 1u); }
