@@ -456,8 +456,24 @@ def main():
                     e1.synchronize()
                     ts.append(e0.elapsed_time(e1))
                 row[f"{path}_us"] = round(1e3 * float(np.median(ts)), 2)
+            # blocks push visits, as a share of the B blocks pull scans
+            ws.set_opts(dbs.exec_opts(collect_stats=1))
+            dbs.spmspv(M, x_dev[d][0], None, semiring="or_and", ws=ws, y_idx=y_idx, y_nnz=y_nnz)
+            row["push_work_frac"] = round(ws.stats()["visited_blocks"] / info["nblocks"], 4)
+            ws.set_opts(dbs.exec_opts(collect_stats=0))
             sweep.append(row)
+        # BFS levels with every level forced to one path
+        bfs_sweep = []
+        for src in sources[:3]:
+            lv = {}
+            for path in ("push", "pull"):
+                flush(0)
+                dbs.bfs(M, int(src), levels=levels, path=path, ws=ws)
+                lv[path] = ws.bfs_levels()
+            bfs_sweep.append({"push_work_frac": [round(w / info["nblocks"], 4) for w in lv["pull"]["push_work"]],
+                              "push_us": lv["push"]["level_us"], "pull_us": lv["pull"]["level_us"]})
         out["path_sweep"] = sweep
+        out["bfs_path_sweep"] = bfs_sweep
         assert ws.check() == 0
 
     # end to end through the public API with host buffers

@@ -188,14 +188,17 @@ class Workspace:
         return d
 
     def bfs_levels(self, max_levels: int = 64, stream=None) -> dict:
-        """dbs_bfs_level_stats: per-level frontier blocks, path and device ns."""
+        """dbs_bfs_level_stats: per-level frontier blocks, push work (matrix
+        blocks in the frontier's column blocks), path and device time."""
         fb = np.zeros(max_levels, np.int64)
+        pw = np.zeros(max_levels, np.int64)
         pa = np.zeros(max_levels, np.int32)
         ns = np.zeros(max_levels, np.int64)
         _lib.check("dbs_bfs_level_stats", _lib.load().dbs_bfs_level_stats(
-            self._h, _stream_handle(stream), max_levels, _ptr(fb), _ptr(pa), _ptr(ns)))
+            self._h, _stream_handle(stream), max_levels, _ptr(fb), _ptr(pw), _ptr(pa), _ptr(ns)))
         n = int((pa > 0).sum())
-        return {"frontier_blocks": fb[:n].tolist(), "path": ["push" if p == 1 else "pull" for p in pa[:n]],
+        return {"frontier_blocks": fb[:n].tolist(), "push_work": pw[:n].tolist(),
+                "path": ["push" if p == 1 else "pull" for p in pa[:n]],
                 "level_us": (ns[:n] / 1e3).round(2).tolist()}
 
     def selftest_wait_timeout(self, stream=None):

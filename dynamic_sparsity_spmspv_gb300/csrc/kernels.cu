@@ -64,6 +64,7 @@ struct Ctrl {
     unsigned long long t_phase[4];   // device timestamps: start, metadata done, traversal done, end
     unsigned long long lv_t[BFS_LEVEL_LOG + 1];   // BFS: start time of each level (and of the exit)
     unsigned int lv_nz[BFS_LEVEL_LOG];            // BFS: nonzero frontier blocks per level
+    unsigned int lv_nv[BFS_LEVEL_LOG];            // BFS: matrix blocks in the frontier's column blocks
     unsigned int lv_path[BFS_LEVEL_LOG];          // BFS: 1 push, 2 pull per level
 };
 
@@ -1261,6 +1262,7 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
         push_levels += push;
         if (blockIdx.x == 0 && tid == 0 && L - 1u < (uint32_t)BFS_LEVEL_LOG) {
             P.ctrl->lv_nz[L - 1u] = n_nz;
+            P.ctrl->lv_nv[L - 1u] = ld_cg(&P.ctrl->n_vis[cur]);
             P.ctrl->lv_path[L - 1u] = push ? 1u : 2u;
         }
         if (push) {
@@ -1463,10 +1465,11 @@ void dbs_exec_opts_default(dbs_exec_opts *o)
 {
     if (!o) return;
     o->th3 = 0.01;
-    // GB300 default: decide on the implied work.  The forced-path sweep on
-    // R-MAT scale 20 puts the crossover near n_vis / B = 0.14 (push 1.7x
-    // faster at 0.015, equal at 0.144); 0 selects the paper's th3 rule.
-    o->push_work_frac = 0.1;
+    // GB300 default: decide on the implied work.  Forced-path sweeps on
+    // R-MAT scale 20 (SpMSpV and BFS levels) put the crossover near
+    // n_vis / B = 0.45 (push 1.6x faster at 0.14 and 1.1x at 0.25, pull
+    // 1.06x faster at 0.61 and 1.35x at 0.81); 0 selects the paper's th3 rule.
+    o->push_work_frac = 0.45;
     o->local_pull_min = 8;
     o->collect_stats = 0;
     o->wait_timeout_ns = 2000000000LL;
@@ -1659,7 +1662,7 @@ dbs_status dbs_last_stats(dbs_workspace *w, void *stream, dbs_stats *out)
 }
 
 dbs_status dbs_bfs_level_stats(dbs_workspace *w, void *stream, int32_t max_levels, int64_t *frontier_blocks,
-                               int32_t *path, int64_t *level_ns)
+                               int64_t *push_work, int32_t *path, int64_t *level_ns)
 {
     if (!w || max_levels < 0) return DBS_ERR_INVALID_ARG;
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
@@ -1672,6 +1675,7 @@ dbs_status dbs_bfs_level_stats(dbs_workspace *w, void *stream, int32_t max_level
     const int n = std::min<int>(std::min<int>(max_levels, BFS_LEVEL_LOG), (int)c.bfs_levels);
     for (int l = 0; l < n; ++l) {
         if (frontier_blocks) frontier_blocks[l] = c.lv_nz[l];
+        if (push_work) push_work[l] = c.lv_nv[l];
         if (path) path[l] = (int32_t)c.lv_path[l];
         if (level_ns) level_ns[l] = c.lv_t[l + 1] >= c.lv_t[l] ? (int64_t)(c.lv_t[l + 1] - c.lv_t[l]) : 0;
     }

@@ -110,7 +110,7 @@ typedef struct {
                                   DBS_ERR_TIMEOUT and returns. */
     double push_work_frac;     /* > 0: push iff the matrix blocks of the active column
                                   blocks (push's work) number fewer than push_work_frac * B
-                                  (pull's scan); default 0.1, the crossover measured on
+                                  (pull's scan); default 0.45, the crossover measured on
                                   GB300.  0: the paper's th3 rule. */
 } dbs_exec_opts;
 
@@ -259,11 +259,12 @@ dbs_status dbs_last_stats(dbs_workspace *ws, void *stream, dbs_stats *out);
 /* Section 4.2 / Figure 7 diagnostics of the last dbs_bfs on this workspace
  * (the frontier evolution the paper profiles in Figure 3): for each level
  * l < min(max_levels, 64, number of levels), the frontier's nonzero vector
- * blocks, the path taken (1 push, 2 pull) and the level's device time in ns
+ * blocks, the matrix blocks in those column blocks (the blocks push visits),
+ * the path taken (1 push, 2 pull) and the level's device time in ns
  * (traversal + update, as seen by block 0).  HOST arrays, any may be NULL.
  * Synchronizes the stream.  DBS_ERR_INVALID_ARG if the last call was not a BFS. */
 dbs_status dbs_bfs_level_stats(dbs_workspace *ws, void *stream, int32_t max_levels, int64_t *frontier_blocks,
-                               int32_t *path, int64_t *level_ns);
+                               int64_t *push_work, int32_t *path, int64_t *level_ns);
 
 /* Self-test of the bounded device wait: launches the grid barrier with one
  * block withheld, so every other block's wait expires after

@@ -45,7 +45,7 @@ def test_er_full(full):
 def test_rmat_full_sweep_and_bfs(full):
     A, O, M = full("rmat")
     ws = dbs.Workspace(M, collect_stats=1)
-    expected_path = {1e-4: 1, 1e-3: 1, 1e-2: 2, 1e-1: 2, 5e-1: 2}   # default work rule, 0.1
+    expected_path = {1e-4: 1, 1e-3: 1, 1e-2: 1, 1e-1: 2, 5e-1: 2}   # default work rule, 0.45
     for d, p_exp in expected_path.items():
         x = synth.x_uniform(A.n, int(round(d * A.n)), [44, 0, int(d * 1e6), 0], valued=False)
         for path in PATHS:

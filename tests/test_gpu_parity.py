@@ -333,8 +333,11 @@ def test_bfs_level_stats_match_frontiers(small):
     st = ws.bfs_levels()
     ref = O.bfs_queue(src)
     assert len(st["frontier_blocks"]) == nl
+    deg = np.diff(oracle.block_views(A)["blk_col_ptr"])      # blocks per column block
     for l in range(nl):
-        assert st["frontier_blocks"][l] == len(np.unique(np.nonzero(ref == l)[0] // 16))
+        cbs = np.unique(np.nonzero(ref == l)[0] // 16)
+        assert st["frontier_blocks"][l] == len(cbs)
+        assert st["push_work"][l] == int(deg[cbs].sum())
         assert st["path"][l] in ("push", "pull")
 
 
