@@ -119,16 +119,6 @@ struct KParams {
 
 // ---------------------------------------------------------------- helpers
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release(unsigned *p, unsigned v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ unsigned long long globaltimer()
 {
     unsigned long long t;
@@ -471,48 +461,6 @@ __device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint
         }
     }
     return rows;
-}
-
-// Boolean microkernel, one lane (Algorithm 5 semantics): the rows of the
-// block reached from its active columns.
-__device__ __forceinline__ uint32_t bool_found(const uint8_t *__restrict__ b, uint32_t meta, uint32_t act)
-{
-    if (meta_inline(meta)) return meta_inline_found(meta, act);   // no payload to read
-    const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
-    uint32_t f = 0;
-    if (fmt == FMT_COO) {
-        // 16 coordinates per 16-byte load (the payload is 16-byte aligned)
-        const uint4 *c4 = reinterpret_cast<const uint4 *>(b);
-        for (uint32_t base = 0; base < nnz; base += 16u) {
-            const uint4 v = __ldg(c4 + (base >> 4));
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (uint32_t j = 0; j < 16u; ++j) {
-                const uint32_t e = (wv[j >> 2] >> (8u * (j & 3u))) & 0xFFu;
-                if (base + j < nnz && ((act >> (e & 15u)) & 1u)) f |= 1u << (e >> 4);
-            }
-        }
-    } else {
-        const uint4 *m4 = reinterpret_cast<const uint4 *>(b + (fmt == FMT_DENSE ? 0u : OFF_MASK));
-        const uint4 lo = __ldg(m4), hi = __ldg(m4 + 1);
-        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        if (fmt == FMT_DENSE || fmt == FMT_FCSC) {          // column masks: OR the active columns
-#pragma unroll
-            for (uint32_t c = 0; c < 16; ++c)
-                if ((act >> c) & 1u) f |= (w[c >> 1] >> ((c & 1u) << 4)) & 0xFFFFu;
-        } else {                                            // row masks: rows meeting an active column
-#pragma unroll
-            for (uint32_t r = 0; r < 16; ++r)
-                if ((w[r >> 1] >> ((r & 1u) << 4)) & act) f |= 1u << r;
-        }
-    }
-    return f;
-}
-
-__device__ __forceinline__ uint32_t bool_bytes(uint32_t meta)
-{
-    if (meta_inline(meta)) return 0u;
-    return meta_fmt(meta) == FMT_COO ? meta_nnz(meta) : 32u;
 }
 
 // ------------------------------------------------------------- traversal
