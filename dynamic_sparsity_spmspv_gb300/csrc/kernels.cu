@@ -583,7 +583,7 @@ __device__ __forceinline__ void bool_load(const uint4 *b4, uint32_t fmt, uint32_
 // barriers, and every barrier ends with an acquire at GPU scope, after which
 // plain loads observe all writes made before the barrier (the same guarantee
 // that cooperative grid synchronisation gives).
-template <int SR, bool DOUT>
+template <int SR, bool DOUT, bool ST>
 __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, const uint32_t *vis,
                            uint32_t *out_rm, int tslot)
 {
@@ -664,21 +664,22 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             const uint32_t li = (uint32_t)(k * 32 + lane);
             const uint32_t m = (mm[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu;   // 0 past the tile's end
             const uint32_t meta = d[k].y, lrb = d[k].x >> DESC_LRB_SHIFT;
-            if (P.stats && m) { ++c_vis; c_touch += meta_nnz(meta); }
-            if (SR == 1 && meta_inline(meta)) {
-                const uint32_t f = inline_found(meta, dup16(m));
+            if (ST && m) { ++c_vis; c_touch += meta_nnz(meta); }
+            // both outcomes computed, one kept: no divergent branch per block
+            const bool inl = SR == 1 && meta_inline(meta);
+            if (SR == 1) {
+                const uint32_t f = inl ? inline_found(meta, dup16(m)) : 0u;
                 if (f) {
                     atomicOr(&W.rm[lrb], f);
-                    if (P.stats) ++c_hit;
+                    if (ST) ++c_hit;
                 }
-            } else {
-                const uint32_t a = m & meta & 0xFFFFu;
-                if (a) {
-                    const uint32_t slot = atomicAdd(&W.nq, 1u);
-                    W.qe[slot] = li | (lrb << 8) | (a << 16);
-                    W.qm[slot] = meta;
-                    if (P.stats) ++c_hit;
-                }
+            }
+            const uint32_t a = inl ? 0u : m & meta & 0xFFFFu;
+            if (a) {
+                const uint32_t slot = atomicAdd(&W.nq, 1u);
+                W.qe[slot] = li | (lrb << 8) | (a << 16);
+                W.qm[slot] = meta;
+                if (ST) ++c_hit;
             }
         }
         __syncwarp();
@@ -694,7 +695,7 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 bool_load(b, fmt, nnz, u0, u1);
                 const uint32_t r = bool_found_units(fmt, nnz, e >> 16, u0, u1, b);
                 if (r) atomicOr(&W.rm[(e >> 8) & 0xFFu], r);
-                if (P.stats) c_bytes += 4u + (fmt == FMT_COO ? nnz : 32u);
+                if (ST) c_bytes += 4u + (fmt == FMT_COO ? nnz : 32u);
             }
         } else {
             // COO hits one per lane
@@ -708,7 +709,7 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 const uint32_t rows = coo_lane(b, nnz, e >> 16, xv + (size_t)col * 16u, true,
                                                [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
                 if (rows) atomicOr(&W.rm[lrb], rows);
-                if (P.stats) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
+                if (ST) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
             }
             __syncwarp();
             // the other formats by the whole warp
@@ -724,7 +725,7 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
                 if (lane == 0) {
                     if (bits) W.rm[lrb] |= bits;
-                    if (P.stats) c_bytes += 4u + by;
+                    if (ST) c_bytes += 4u + by;
                 }
                 __syncwarp();
             }
@@ -751,7 +752,7 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             }
             if (!DOUT && lane < (int)span && W.rm[lane]) or16(out_rm, rb0 + lane, W.rm[lane]);
         }
-        if (P.stats) {
+        if (ST) {
             if (lane == 0) c_bytes += 8u * nblk + 16u;
             stat_add(S, 0, c_vis);
             stat_add(S, 1, c_hit);
@@ -777,7 +778,7 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
 // Rows are written back with atomics.  Boolean found rows are not masked by
 // the visited rows here: the caller masks them once afterwards (a stored
 // block whose rows are all visited is skipped in the drain).
-template <int SR, bool DOUT>
+template <int SR, bool DOUT, bool ST>
 __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, const uint32_t *vis,
                            uint32_t *out_rm, int cslot)
 {
@@ -811,12 +812,12 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             const uint32_t ql = (uint32_t)(k * 32 + lane);
             if (q0 + ql >= q1) continue;
             const uint32_t rb = d[k].x, meta = d[k].y;
-            if (P.stats) { ++c_vis; c_touch += meta_nnz(meta); c_bytes += 8u; }
+            if (ST) { ++c_vis; c_touch += meta_nnz(meta); c_bytes += 8u; }
             if (SR == 1 && meta_inline(meta)) {
                 const uint32_t f = inline_found(meta, mm);
                 if (f) {
                     or16(out_rm, rb, f);
-                    if (P.stats) ++c_hit;
+                    if (ST) ++c_hit;
                 }
             } else {
                 const uint32_t a = meta & xmb & 0xFFFFu;
@@ -825,7 +826,7 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                     W.qe[slot] = ql | (a << 16);
                     W.qm[slot] = meta;
                     W.qr[slot] = rb;
-                    if (P.stats) ++c_hit;
+                    if (ST) ++c_hit;
                 }
             }
         }
@@ -843,7 +844,7 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 bool_load(pb, fmt, nnz, u0, u1);
                 const uint32_t f = bool_found_units(fmt, nnz, e >> 16, u0, u1, pb) & ~vm;
                 if (f) or16(out_rm, rb, f);
-                if (P.stats) c_bytes += 4u + (fmt == FMT_COO ? nnz : 32u);
+                if (ST) c_bytes += 4u + (fmt == FMT_COO ? nnz : 32u);
             }
         } else {
             for (uint32_t i = lane; i < nq; i += 32) {
@@ -854,7 +855,7 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 float *yr = y + (size_t)rb * 16u;
                 const uint32_t rows = coo_lane(b, nnz, e >> 16, wx, true, [&](uint32_t r, float v) { atomicAdd(yr + r, v); });
                 if (!DOUT && rows) or16(out_rm, rb, rows);
-                if (P.stats) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
+                if (ST) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
             }
             __syncwarp();
             for (uint32_t i = 0; i < nq; ++i) {
@@ -867,14 +868,14 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
                 if (lane == 0) {
                     if (!DOUT && bits) or16(out_rm, rb, bits);
-                    if (P.stats) c_bytes += 4u + by;
+                    if (ST) c_bytes += 4u + by;
                 }
                 __syncwarp();
             }
         }
         __syncwarp();
     }
-    if (P.stats) {
+    if (ST) {
         stat_add(S, 0, c_vis);
         stat_add(S, 1, c_hit);
         stat_add(S, 2, c_touch);
@@ -928,7 +929,7 @@ __device__ __forceinline__ void reset_stats(const KParams &P)
 
 // One SpMSpV with a sparse x (index list + values) and a sparse output.
 // Phases: metadata | [push list] | traversal | compaction counts | writes.
-template <int SR>
+template <int SR, bool ST>
 __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
 {
     SmemT<SR> &S = *reinterpret_cast<SmemT<SR> *>(smem_raw);
@@ -938,7 +939,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
     const int slot = P.slot;
     stats_begin(S);
-    if (blockIdx.x == 0 && tid == 0 && P.stats) reset_stats(P);
+    if (blockIdx.x == 0 && tid == 0 && ST) reset_stats(P);
     stamp(P, 0);
 
     // Phase 1 (Section 4.1): scatter x and set the blk_x_mask bits.  Lanes
@@ -976,7 +977,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     }
     cta_count(&P.ctrl->n_blk[slot], first);
     cta_count(&P.ctrl->n_vis[slot], work);
-    if (P.stats) cta_count(&P.ctrl->x_active, act_cnt);
+    if (ST) cta_count(&P.ctrl->x_active, act_cnt);
     if (!grid_sync(P)) return;
     stamp(P, 1);
 
@@ -1000,9 +1001,9 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
             cta_append(P, S.L, slot, want, j >> 4);
         }
         if (!grid_sync(P)) return;
-        push_tasks<SR, false>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
+        push_tasks<SR, false, ST>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
     } else {
-        pull_tiles<SR, false>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
+        pull_tiles<SR, false, ST>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
     }
     stats_flush(P, S);
     if (!grid_sync(P)) return;
@@ -1034,7 +1035,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     if (blockIdx.x == 0 && tid == 0) {
         Ctrl *c = P.ctrl;
         c->path = push ? 1u : 2u;
-        if (P.stats) c->nzblk = n_nz;
+        if (ST) c->nzblk = n_nz;
         // counters of both slots are clean for the next call, whichever slot it uses
         for (int k = 0; k < 2; ++k) {
             c->n_blk[k] = 0u; c->n_vis[k] = 0u; c->n_act[k] = 0u; c->n_chunk[k] = 0u; c->tile_next[k] = 0u;
@@ -1068,7 +1069,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
         }
         if (ct == P.n_ctiles - 1 && tid == 0) {
             *P.y_nnz = (long long)(base + tile_tot);
-            if (P.stats) P.ctrl->y_nnz = base + tile_tot;
+            if (ST) P.ctrl->y_nnz = base + tile_tot;
         }
     }
     if (P.n_ctiles == 0 && blockIdx.x == 0 && tid == 0) *P.y_nnz = 0;
@@ -1078,6 +1079,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
 // One SpMSpV with a dense x and a dense y (Section 4.3, DB-Decoding): the
 // vector masks come from warp ballots (Section 4.1).  Counter slot P.slot is
 // used by this call; the other slot is reset for the next call.
+template <bool ST>
 __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
 {
     SmemT<0> &S = *reinterpret_cast<SmemT<0> *>(smem_raw);
@@ -1087,7 +1089,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
     const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
     const int slot = P.slot;
     stats_begin(S);
-    if (blockIdx.x == 0 && tid == 0 && P.stats) reset_stats(P);
+    if (blockIdx.x == 0 && tid == 0 && ST) reset_stats(P);
     stamp(P, 0);
     for (size_t i = gtid; i < (size_t)P.m; i += gsz) P.y_dense[i] = 0.0f;
 
@@ -1109,7 +1111,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
     }
     cta_count(&P.ctrl->n_blk[slot], nb);
     cta_count(&P.ctrl->n_vis[slot], work);
-    if (P.stats) cta_count(&P.ctrl->x_active, act_cnt);
+    if (ST) cta_count(&P.ctrl->x_active, act_cnt);
     if (!grid_sync(P)) return;
     stamp(P, 1);
 
@@ -1123,9 +1125,9 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
             cta_append(P, S.L, slot, (bal >> 16) != 0u, 2u * w + 1u);
         }
         if (!grid_sync(P)) return;
-        push_tasks<0, true>(P, S, P.dxm32, nullptr, nullptr, slot);
+        push_tasks<0, true, ST>(P, S, P.dxm32, nullptr, nullptr, slot);
     } else {
-        pull_tiles<0, true>(P, S, P.dxm32, nullptr, nullptr, slot);
+        pull_tiles<0, true, ST>(P, S, P.dxm32, nullptr, nullptr, slot);
     }
     stats_flush(P, S);
     if (blockIdx.x == 0 && tid == 0) {
@@ -1137,7 +1139,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
         c->n_chunk[o] = 0u;
         c->tile_next[o] = 0u;
         c->path = push ? 1u : 2u;
-        if (P.stats) c->nzblk = n_nz;
+        if (ST) c->nzblk = n_nz;
     }
     stamp(P, 3);
 }
@@ -1149,6 +1151,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
 // frontier and counts the new one's nonzero blocks; a level that takes the
 // push path first builds its task list from the frontier words.  Counters
 // rotate over three slots: two grid barriers per pull level, three per push.
+template <bool ST>
 __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
 {
     SmemT<1> &S = *reinterpret_cast<SmemT<1> *>(smem_raw);
@@ -1224,9 +1227,9 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
                 }
                 if (!grid_sync(P)) return;
             }
-            push_tasks<1, false>(P, S, fcur, P.bvis32, fnext, cur);
+            push_tasks<1, false, ST>(P, S, fcur, P.bvis32, fnext, cur);
         } else {
-            pull_tiles<1, false>(P, S, fcur, P.bvis32, fnext, cur);
+            pull_tiles<1, false, ST>(P, S, fcur, P.bvis32, fnext, cur);
         }
         if (!grid_sync(P)) return;
 
@@ -1254,7 +1257,7 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
         }
         cta_count(&P.ctrl->n_blk[nxt], nb);
         cta_count(&P.ctrl->n_vis[nxt], work);
-        if (P.stats) cta_count(&P.ctrl->reached, reached);
+        if (ST) cta_count(&P.ctrl->reached, reached);
         if (blockIdx.x == 0 && tid == 0) {
             Ctrl *c = P.ctrl;
             c->n_blk[old] = 0u;
@@ -1278,7 +1281,7 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
         c->bfs_push_levels = push_levels;
         c->path = 0u;
         c->nzblk = nz_sum;
-        if (P.stats) c->reached += 1;   // the source
+        if (ST) c->reached += 1;   // the source
     }
     stamp(P, 3);
 }
@@ -1299,8 +1302,8 @@ struct dbs_workspace {
     const dbs_matrix *A = nullptr;
     int device = -1;
     int sms = 0;
-    int grid_sparse[2] = {0, 0};
-    int grid_dense = 0, grid_bfs = 0;
+    int grid_sparse[2][2] = {{0, 0}, {0, 0}};   // [semiring][statistics]
+    int grid_dense[2] = {0, 0}, grid_bfs[2] = {0, 0};
     int call_count = 0;
     unsigned launches = 0;      // launches made; its parity picks the grid-barrier counter
     dbs_exec_opts opts{};
@@ -1447,11 +1450,18 @@ dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
               dalloc(&w->fm32[0], nbc / 2 + 8) && dalloc(&w->fm32[1], nbc / 2 + 8) && dalloc(&w->ctrl, 1);
     for (int s = 0; s < 3 && ok; ++s) ok = dalloc(&w->act[s], nbc + 1) && dalloc(&w->chunks[s], chunk_cap);
     if (!ok) { ws_free(w); delete w; return DBS_ERR_OOM; }
-    w->grid_sparse[0] = coop_grid((const void *)k_spmspv_sparse<0>, w->sms, SMEM0);
-    w->grid_sparse[1] = coop_grid((const void *)k_spmspv_sparse<1>, w->sms, SMEM1);
-    w->grid_dense = coop_grid((const void *)k_spmspv_dense, w->sms, SMEM0);
-    w->grid_bfs = coop_grid((const void *)k_bfs, w->sms, SMEM1);
-    if (!w->grid_sparse[0] || !w->grid_sparse[1] || !w->grid_dense || !w->grid_bfs) {
+    w->grid_sparse[0][0] = coop_grid((const void *)k_spmspv_sparse<0, false>, w->sms, SMEM0);
+    w->grid_sparse[0][1] = coop_grid((const void *)k_spmspv_sparse<0, true>, w->sms, SMEM0);
+    w->grid_sparse[1][0] = coop_grid((const void *)k_spmspv_sparse<1, false>, w->sms, SMEM1);
+    w->grid_sparse[1][1] = coop_grid((const void *)k_spmspv_sparse<1, true>, w->sms, SMEM1);
+    w->grid_dense[0] = coop_grid((const void *)k_spmspv_dense<false>, w->sms, SMEM0);
+    w->grid_dense[1] = coop_grid((const void *)k_spmspv_dense<true>, w->sms, SMEM0);
+    w->grid_bfs[0] = coop_grid((const void *)k_bfs<false>, w->sms, SMEM1);
+    w->grid_bfs[1] = coop_grid((const void *)k_bfs<true>, w->sms, SMEM1);
+    bool grids_ok = true;
+    for (int a = 0; a < 2; ++a)
+        grids_ok = grids_ok && w->grid_sparse[0][a] && w->grid_sparse[1][a] && w->grid_dense[a] && w->grid_bfs[a];
+    if (!grids_ok) {
         ws_free(w);
         delete w;
         return DBS_ERR_CUDA;
@@ -1525,11 +1535,14 @@ dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx
     P.y_idx = y_idx;
     P.y_val = y_val;
     P.y_nnz = reinterpret_cast<long long *>(y_nnz);
-    const void *fn = sr == DBS_PLUS_TIMES_F32 ? (const void *)k_spmspv_sparse<0> : (const void *)k_spmspv_sparse<1>;
+    const int st_on = P.stats ? 1 : 0, sri = sr == DBS_PLUS_TIMES_F32 ? 0 : 1;
+    const void *fns[2][2] = {{(const void *)k_spmspv_sparse<0, false>, (const void *)k_spmspv_sparse<0, true>},
+                             {(const void *)k_spmspv_sparse<1, false>, (const void *)k_spmspv_sparse<1, true>}};
+    const void *fn = fns[sri][st_on];
     P.slot = w->call_count & 1;
     w->call_count++;
     w->last_was_bfs = false;
-    return launch_ws(w, fn, w->grid_sparse[sr == DBS_PLUS_TIMES_F32 ? 0 : 1], P, (cudaStream_t)stream,
+    return launch_ws(w, fn, w->grid_sparse[sri][st_on], P, (cudaStream_t)stream,
                      sr == DBS_PLUS_TIMES_F32 ? SMEM0 : SMEM1);
 }
 
@@ -1549,7 +1562,8 @@ dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_p
     P.slot = w->call_count & 1;
     w->call_count++;
     w->last_was_bfs = false;
-    return launch_ws(w, (const void *)k_spmspv_dense, w->grid_dense, P, (cudaStream_t)stream, SMEM0);
+    return P.stats ? launch_ws(w, (const void *)k_spmspv_dense<true>, w->grid_dense[1], P, (cudaStream_t)stream, SMEM0)
+                   : launch_ws(w, (const void *)k_spmspv_dense<false>, w->grid_dense[0], P, (cudaStream_t)stream, SMEM0);
 }
 
 dbs_status dbs_bfs(const dbs_matrix *A, int64_t src, int32_t *levels, int32_t *nlevels_host, dbs_path path,
@@ -1569,7 +1583,8 @@ dbs_status dbs_bfs(const dbs_matrix *A, int64_t src, int32_t *levels, int32_t *n
     // slot clear.
     w->call_count = 0;
     w->last_was_bfs = true;
-    st = launch_ws(w, (const void *)k_bfs, w->grid_bfs, P, s, SMEM1);
+    st = P.stats ? launch_ws(w, (const void *)k_bfs<true>, w->grid_bfs[1], P, s, SMEM1)
+                 : launch_ws(w, (const void *)k_bfs<false>, w->grid_bfs[0], P, s, SMEM1);
     if (st != DBS_OK || !nlevels_host) return st;
     Ctrl c;
     if (cudaMemcpyAsync(&c, w->ctrl, sizeof(Ctrl), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
@@ -1687,7 +1702,7 @@ dbs_status noalloc_setup(int dev)
         cudaGetLastError();
         return DBS_ERR_CUDA;
     }
-    const int grid = coop_grid((const void *)k_spmspv_dense, sms, SMEM0);
+    const int grid = coop_grid((const void *)k_spmspv_dense<false>, sms, SMEM0);
     if (grid <= 0) return DBS_ERR_CUDA;
     d.scratch = static_cast<unsigned char *>(ptr);
     d.grid = grid;
@@ -1738,5 +1753,5 @@ extern "C" dbs_status dbs_spmspv_dense_noalloc(const dbs_matrix *A, const float 
     P.local_pull_min = o.local_pull_min;
     P.stats = 0;
     P.timeout_ns = o.wait_timeout_ns;
-    return launch((const void *)k_spmspv_dense, d.grid, P, s, SMEM0);
+    return launch((const void *)k_spmspv_dense<false>, d.grid, P, s, SMEM0);
 }
