@@ -42,7 +42,7 @@ constexpr int BFS_LEVEL_LOG = 64;    // BFS levels whose frontier, path and time
 constexpr int MAX_GRID = 4096;       // cooperative grid size cap
 
 struct Ctrl {
-    unsigned long long bar[2][16];      // grid-barrier arrival counters, one 128-byte line each
+    unsigned long long bar[2][16];      // grid-barrier arrival counters by launch parity, one 128-byte line each
     unsigned int err;
     unsigned int path;
     unsigned int n_blk[3];      // nonzero vector blocks (N_nzblk) of the slot's vector
@@ -103,13 +103,14 @@ struct KParams {
     uint2 *chunks[3];
     float *y_acc;
     uint32_t *yrm32;
-    uint32_t *ctile_cnt;
+    unsigned long long *ctile_flag;   // per compaction tile: epoch << 34 | state << 32 | count or prefix
     uint32_t n_ctiles;
     uint32_t *bvis32;
     uint32_t *fm32[2];
     Ctrl *ctrl;
     int slot;                 // counter slot of this call (dense mode alternates 0/1)
     int bslot;                // grid-barrier counter of this launch (launch parity)
+    uint32_t epoch;           // launch number (30 bits), tags the compaction flags
     double th3;
     double push_frac;
     int local_pull_min;
@@ -156,6 +157,10 @@ __device__ __forceinline__ void red_release_add(unsigned long long *p, unsigned 
 {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ void st_release64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long *p)
 {
     unsigned long long v;
@@ -169,7 +174,9 @@ __device__ __forceinline__ void grid_sync_init(const KParams &P)
 {
     if (threadIdx.x == 0) {
         s_bar_epoch = 0u;
-        if (blockIdx.x == 0) P.ctrl->bar[P.bslot ^ 1][0] = 0ull;
+        if (blockIdx.x == 0) {
+            P.ctrl->bar[P.bslot ^ 1][0] = 0ull;
+        }
     }
 }
 __device__ bool grid_sync(const KParams &P)
@@ -1009,7 +1016,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     if (!grid_sync(P)) return;
     stamp(P, 2);
 
-    // Phase 3: clear x, count output rows per compaction tile, reset counters.
+    // Phase 3: clear x, reset counters, compact the output.
     for (size_t e = gtid; e < (size_t)P.x_nnz; e += gsz) {
         const uint32_t j = (uint32_t)__ldg(P.x_idx + e);
         if (j >= (uint32_t)P.n) continue;
@@ -1024,14 +1031,6 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
         const uint32_t hi = 2u * w + 1u < (size_t)P.nbr ? vis16(P.uvis32, (uint32_t)(2u * w + 1u)) : 0u;
         return ~(lo | (hi << 16));
     };
-    for (uint32_t ct = blockIdx.x; ct < P.n_ctiles; ct += gridDim.x) {
-        const size_t wi = (size_t)ct * NT + tid;
-        uint32_t wd = __ldcg(P.yrm32 + wi);
-        if (wd) wd &= unvisited(wi);
-        uint32_t tot;
-        block_excl_scan(__popc(wd), &tot);
-        if (tid == 0) P.ctile_cnt[ct] = tot;
-    }
     if (blockIdx.x == 0 && tid == 0) {
         Ctrl *c = P.ctrl;
         c->path = push ? 1u : 2u;
@@ -1041,21 +1040,57 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
             c->n_blk[k] = 0u; c->n_vis[k] = 0u; c->n_act[k] = 0u; c->n_chunk[k] = 0u; c->tile_next[k] = 0u;
         }
     }
-    if (!grid_sync(P)) return;
 
-    // Phase 4: ascending output (Section 2.1 "then compaction"); clear the
-    // accumulator and the row masks for the next call.
+    // Ascending output (Section 2.1 "then compaction") in one pass: block b
+    // takes compaction tiles b, b + gridDim.x, ... in order; a tile publishes
+    // its row count, adds up its predecessors' published counts back to the
+    // first published prefix (waits bounded), publishes its own prefix and
+    // writes its rows.  A tile waits only on lower tiles, which belong to
+    // earlier rounds or to lower blocks of the same round, and every block
+    // of the cooperative launch is resident, so the waits end.  The
+    // accumulator and the row masks are cleared for the next call on the way.
+    __shared__ uint32_t s_base;
     for (uint32_t ct = blockIdx.x; ct < P.n_ctiles; ct += gridDim.x) {
-        uint32_t part = 0;
-        for (uint32_t k = tid; k < ct; k += NT) part += __ldcg(P.ctile_cnt + k);
-        uint32_t base;
-        block_excl_scan(part, &base);            // total over the CTA = rows before this tile
         const size_t wi = (size_t)ct * NT + tid;
         const uint32_t raw = __ldcg(P.yrm32 + wi);
         uint32_t bits = raw ? raw & unvisited(wi) : 0u;
         uint32_t tile_tot;
-        uint32_t o = base + block_excl_scan(__popc(bits), &tile_tot);
+        const uint32_t off = block_excl_scan(__popc(bits), &tile_tot);
+        if (tid < 32) {
+            // warp 0 looks back over windows of 32 predecessors (lane l reads
+            // tile j - l) until one has published its prefix
+            const int lane = tid;
+            const unsigned long long tag = (unsigned long long)P.epoch << 34;
+            if (lane == 0) st_release64(P.ctile_flag + ct, tag | (1ull << 32) | tile_tot);   // count published
+            uint32_t base = 0;
+            bool ok = true;
+            const unsigned long long t0 = globaltimer();
+            for (int j = (int)ct - 1; j >= 0 && ok; j -= 32) {
+                const int idx = j - lane;
+                unsigned long long f = 0;
+                if (idx >= 0) {
+                    while (((f = ld_acquire64(P.ctile_flag + idx)) >> 34) != (unsigned long long)P.epoch) {
+                        if ((long long)(globaltimer() - t0) > P.timeout_ns) { ok = false; break; }
+                    }
+                }
+                ok = __all_sync(FULL, ok);
+                if (!ok) break;
+                const uint32_t pm = __ballot_sync(FULL, idx >= 0 && ((f >> 32) & 2ull));   // prefixes
+                const int stop = pm ? __ffs(pm) - 1 : 31;
+                base += __reduce_add_sync(FULL, (lane <= stop && idx >= 0) ? (uint32_t)f : 0u);
+                if (pm) break;
+            }
+            if (!ok && lane == 0) atomicCAS(&P.ctrl->err, 0u, (unsigned)DBS_ERR_TIMEOUT);
+            if (lane == 0) {
+                st_release64(P.ctile_flag + ct, tag | (2ull << 32) | (base + tile_tot));      // prefix published
+                s_base = ok ? base : 0xFFFFFFFFu;
+            }
+        }
+        __syncthreads();
+        const uint32_t base = s_base;
+        if (base == 0xFFFFFFFFu) return;
         if (raw) P.yrm32[wi] = 0u;
+        uint32_t o = base + off;
         while (bits) {
             const uint32_t k = __ffs(bits) - 1u;
             bits &= bits - 1u;
@@ -1071,6 +1106,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
             *P.y_nnz = (long long)(base + tile_tot);
             if (ST) P.ctrl->y_nnz = base + tile_tot;
         }
+        __syncthreads();
     }
     if (P.n_ctiles == 0 && blockIdx.x == 0 && tid == 0) *P.y_nnz = 0;
     stamp(P, 3);
@@ -1314,7 +1350,7 @@ struct dbs_workspace {
     uint2 *chunks[3] = {nullptr, nullptr, nullptr};
     float *y_acc = nullptr;
     uint32_t *yrm32 = nullptr;
-    uint32_t *ctile_cnt = nullptr;
+    unsigned long long *ctile_flag = nullptr;
     uint32_t n_ctiles = 0;
     uint32_t *bvis32 = nullptr;
     uint32_t *fm32[2] = {nullptr, nullptr};
@@ -1327,7 +1363,7 @@ namespace {
 void ws_free(dbs_workspace *w)
 {
     cudaFree(w->x_dense); cudaFree(w->xm32); cudaFree(w->dxm32); cudaFree(w->y_acc); cudaFree(w->yrm32);
-    cudaFree(w->ctile_cnt); cudaFree(w->bvis32); cudaFree(w->fm32[0]); cudaFree(w->fm32[1]);
+    cudaFree(w->ctile_flag); cudaFree(w->bvis32); cudaFree(w->fm32[0]); cudaFree(w->fm32[1]);
     cudaFree(w->ctrl);
     for (int s = 0; s < 3; ++s) { cudaFree(w->act[s]); cudaFree(w->chunks[s]); }
 }
@@ -1356,7 +1392,7 @@ KParams make_params(const dbs_matrix *A, dbs_workspace *w)
     P.tiles = reinterpret_cast<const uint4 *>(A->d_tiles);
     P.x_dense = w->x_dense; P.xm32 = w->xm32; P.dxm32 = w->dxm32;
     for (int s = 0; s < 3; ++s) { P.act[s] = w->act[s]; P.chunks[s] = w->chunks[s]; }
-    P.y_acc = w->y_acc; P.yrm32 = w->yrm32; P.ctile_cnt = w->ctile_cnt; P.n_ctiles = w->n_ctiles;
+    P.y_acc = w->y_acc; P.yrm32 = w->yrm32; P.ctile_flag = w->ctile_flag; P.n_ctiles = w->n_ctiles;
     P.bvis32 = w->bvis32; P.fm32[0] = w->fm32[0]; P.fm32[1] = w->fm32[1];
     P.ctrl = w->ctrl;
     P.th3 = w->opts.th3;
@@ -1382,6 +1418,7 @@ dbs_status launch(const void *fn, int grid, KParams &P, cudaStream_t s, size_t s
 dbs_status launch_ws(dbs_workspace *w, const void *fn, int grid, KParams &P, cudaStream_t s, size_t smem)
 {
     P.bslot = (int)(w->launches & 1u);
+    P.epoch = w->launches % 0x3FFFFFFFu + 1u;      // 1 .. 2^30 - 1; zeroed flags never match
     const dbs_status st = launch(fn, grid, P, s, smem);
     if (st == DBS_OK) w->launches++;
     return st;
@@ -1446,7 +1483,7 @@ dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
     bool ok = dalloc(&w->x_dense, nbc * 16 + 16) && dalloc(&w->xm32, nbc / 2 + 8) &&
               dalloc(&w->dxm32, nbc / 2 + 8) &&
               dalloc(&w->y_acc, nbr * 16 + 16) && dalloc(&w->yrm32, yrm_words) &&
-              dalloc(&w->ctile_cnt, (size_t)w->n_ctiles + 1) && dalloc(&w->bvis32, nbr / 2 + 8) &&
+              dalloc(&w->ctile_flag, (size_t)w->n_ctiles + 1) && dalloc(&w->bvis32, nbr / 2 + 8) &&
               dalloc(&w->fm32[0], nbc / 2 + 8) && dalloc(&w->fm32[1], nbc / 2 + 8) && dalloc(&w->ctrl, 1);
     for (int s = 0; s < 3 && ok; ++s) ok = dalloc(&w->act[s], nbc + 1) && dalloc(&w->chunks[s], chunk_cap);
     if (!ok) { ws_free(w); delete w; return DBS_ERR_OOM; }
