@@ -952,12 +952,18 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     // Phase 1 (Section 4.1): scatter x and set the blk_x_mask bits.  Lanes
     // hitting the same mask word merge their bits and one of them issues the
     // atomic; a block whose half of the word was empty is new and counted.
-    // Counts are added to the global total once per CTA.
+    // Counts are added to the global total once per CTA.  When push is
+    // likely (x has at most nbc / 4 entries, or push is forced) the new
+    // blocks also form the push list right here, which saves a pass and a
+    // grid barrier; pull ignores the list.
     const int lane = tid & 31;
+    const bool early_list = P.path_force == DBS_PATH_PUSH ||
+                            (P.path_force == DBS_PATH_AUTO && (unsigned long long)P.x_nnz * 4ull <= (unsigned long long)P.nbc);
     uint32_t first = 0, act_cnt = 0, work = 0;
-    for (size_t base = (size_t)blockIdx.x * NT + (tid & ~31); base < (size_t)P.x_nnz; base += gsz) {
-        const size_t e = base + lane;
+    for (size_t base = (size_t)blockIdx.x * NT; base < (size_t)P.x_nnz; base += gsz) {
+        const size_t e = base + tid;
         uint32_t j = 0;
+        bool new_lo = false, new_hi = false;
         bool active = false;
         if (e < (size_t)P.x_nnz) {
             j = (uint32_t)__ldg(P.x_idx + e);
@@ -977,9 +983,15 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
             const uint32_t bits = __reduce_or_sync(peers, 1u << (j & 31u));
             if (lane == __ffs(peers) - 1) {
                 const uint32_t old = atomicOr(P.xm32 + word, bits);
-                if ((bits & 0xFFFFu) && !(old & 0xFFFFu)) { ++first; work += cb_len(P, 2u * word); }
-                if ((bits >> 16) && !(old >> 16)) { ++first; work += cb_len(P, 2u * word + 1u); }
+                new_lo = (bits & 0xFFFFu) && !(old & 0xFFFFu);
+                new_hi = (bits >> 16) && !(old >> 16);
+                if (new_lo) { ++first; work += cb_len(P, 2u * word); }
+                if (new_hi) { ++first; work += cb_len(P, 2u * word + 1u); }
             }
+        }
+        if (early_list) {
+            cta_append(P, S.L, slot, new_lo, 2u * (j >> 5));
+            cta_append(P, S.L, slot, new_hi, 2u * (j >> 5) + 1u);
         }
     }
     cta_count(&P.ctrl->n_blk[slot], first);
@@ -992,22 +1004,24 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     const uint32_t n_nz = ld_cg(&P.ctrl->n_blk[slot]);
     const bool push = choose_push(P, n_nz, ld_cg(&P.ctrl->n_vis[slot]));
     if (push) {
-        // push list: each nonzero vector block is appended by the x entry
-        // holding its lowest set mask bit (indices are unique)
-        for (size_t base = (size_t)blockIdx.x * NT; base < (size_t)P.x_nnz; base += gsz) {
-            const size_t e = base + tid;
-            bool want = false;
-            uint32_t j = 0;
-            if (e < (size_t)P.x_nnz) {
-                j = (uint32_t)__ldg(P.x_idx + e);
-                if (j < (uint32_t)P.n) {
-                    const uint32_t mb = mask16(P.xm32, j >> 4);
-                    want = (mb & (0u - mb)) == (1u << (j & 15u));
+        if (!early_list) {
+            // push list: each nonzero vector block is appended by the x entry
+            // holding its lowest set mask bit (indices are unique)
+            for (size_t base = (size_t)blockIdx.x * NT; base < (size_t)P.x_nnz; base += gsz) {
+                const size_t e = base + tid;
+                bool want = false;
+                uint32_t j = 0;
+                if (e < (size_t)P.x_nnz) {
+                    j = (uint32_t)__ldg(P.x_idx + e);
+                    if (j < (uint32_t)P.n) {
+                        const uint32_t mb = mask16(P.xm32, j >> 4);
+                        want = (mb & (0u - mb)) == (1u << (j & 15u));
+                    }
                 }
+                cta_append(P, S.L, slot, want, j >> 4);
             }
-            cta_append(P, S.L, slot, want, j >> 4);
+            if (!grid_sync(P)) return;
         }
-        if (!grid_sync(P)) return;
         push_tasks<SR, false, ST>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
     } else {
         pull_tiles<SR, false, ST>(P, S, P.xm32, P.uvis32, P.yrm32, slot);

@@ -59,7 +59,7 @@ typedef enum {
 } dbs_semiring;
 
 typedef enum {
-    DBS_PATH_AUTO = 0,         /* push iff N_nzblk / N_blk < th3 (Section 3.3.1) */
+    DBS_PATH_AUTO = 0,         /* device-side choice (Section 3.3.1; see dbs_exec_opts) */
     DBS_PATH_PUSH = 1,         /* column-driven over the block-CSC view */
     DBS_PATH_PULL = 2          /* row-driven over the block-CSR view */
 } dbs_path;
