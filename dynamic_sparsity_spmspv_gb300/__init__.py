@@ -194,12 +194,13 @@ class Workspace:
         pw = np.zeros(max_levels, np.int64)
         pa = np.zeros(max_levels, np.int32)
         ns = np.zeros(max_levels, np.int64)
+        tr = np.zeros(max_levels, np.int64)
         _lib.check("dbs_bfs_level_stats", _lib.load().dbs_bfs_level_stats(
-            self._h, _stream_handle(stream), max_levels, _ptr(fb), _ptr(pw), _ptr(pa), _ptr(ns)))
+            self._h, _stream_handle(stream), max_levels, _ptr(fb), _ptr(pw), _ptr(pa), _ptr(ns), _ptr(tr)))
         n = int((pa > 0).sum())
         return {"frontier_blocks": fb[:n].tolist(), "push_work": pw[:n].tolist(),
                 "path": ["push" if p == 1 else "pull" for p in pa[:n]],
-                "level_us": (ns[:n] / 1e3).round(2).tolist()}
+                "level_us": (ns[:n] / 1e3).round(2).tolist(), "traversal_us": (tr[:n] / 1e3).round(2).tolist()}
 
     def selftest_wait_timeout(self, stream=None):
         _lib.check("dbs_selftest_wait_timeout",

@@ -64,7 +64,7 @@ PROTOTYPES = {
     "dbs_bfs": (I32, [P, I64, P, P, ctypes.c_int, P, P]),
     "dbs_last_stats": (I32, [P, P, P]),
     "dbs_selftest_wait_timeout": (I32, [P, P]),
-    "dbs_bfs_level_stats": (I32, [P, P, I32, P, P, P, P]),
+    "dbs_bfs_level_stats": (I32, [P, P, I32, P, P, P, P, P]),
     "dbs_status_string": (ctypes.c_char_p, [I32]),
     "dbs_version": (ctypes.c_char_p, []),
 }

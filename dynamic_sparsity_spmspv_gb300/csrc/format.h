@@ -70,8 +70,10 @@ constexpr uint32_t TILE_SPAN_MASK = 0xFFFFu;
 constexpr uint32_t TILE_FIRST_SHARED = 1u << 16;
 constexpr uint32_t TILE_LAST_SHARED = 1u << 17;
 constexpr uint32_t TILE_NBLK_SHIFT = 20;
-// Push tasks: CSC positions per work item (one warp, eight positions per lane).
+// Push tasks: CSC positions per work item (one warp, up to eight positions
+// per lane); the size is chosen per call from the push work.
 constexpr uint32_t PUSH_CHUNK = 256;
+constexpr uint32_t PUSH_CHUNK_MIN = 32;
 
 constexpr uint32_t DESC_COL_MASK = 0x07FFFFFFu;   // column block bits of blk_desc.x
 constexpr uint32_t DESC_LRB_SHIFT = 27;            // local row block bits of blk_desc.x

@@ -63,6 +63,7 @@ struct Ctrl {
     unsigned long long reached;
     unsigned long long t_phase[4];   // device timestamps: start, metadata done, traversal done, end
     unsigned long long lv_t[BFS_LEVEL_LOG + 1];   // BFS: start time of each level (and of the exit)
+    unsigned long long lv_u[BFS_LEVEL_LOG];       // BFS: end of each level's traversal
     unsigned int lv_nz[BFS_LEVEL_LOG];            // BFS: nonzero frontier blocks per level
     unsigned int lv_nv[BFS_LEVEL_LOG];            // BFS: matrix blocks in the frontier's column blocks
     unsigned int lv_path[BFS_LEVEL_LOG];          // BFS: 1 push, 2 pull per level
@@ -245,6 +246,18 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t *total)
     return r;
 }
 
+// Push task size: CSC positions per warp task, a power of two in
+// [PUSH_CHUNK_MIN, PUSH_CHUNK] giving about one task per warp for `work`
+// matrix blocks, so a small push still spreads over the grid and a large one
+// amortises each task's fixed cost.
+__device__ __forceinline__ uint32_t push_chunk(unsigned long long work)
+{
+    const unsigned long long target = work / ((unsigned long long)gridDim.x * NW);
+    uint32_t ch = PUSH_CHUNK_MIN;
+    while (ch < PUSH_CHUNK && 2ull * ch <= target) ch <<= 1;
+    return ch;
+}
+
 // Push list construction (Section 3.3.2: matrix-block tasks flattened over
 // the active column blocks).  Every thread of the CTA calls this together;
 // thread t appends column block cb if `want`.  The CTA reserves its list
@@ -258,7 +271,7 @@ struct ListStage {
     uint32_t base_a, base_c;
 };
 
-__device__ void cta_append(const KParams &P, ListStage &L, int slot, bool want, uint32_t cb)
+__device__ void cta_append(const KParams &P, ListStage &L, int slot, bool want, uint32_t cb, uint32_t ch)
 {
     const int tid = threadIdx.x;
     uint32_t s = 0, e = 0;
@@ -266,7 +279,7 @@ __device__ void cta_append(const KParams &P, ListStage &L, int slot, bool want, 
         s = __ldg(P.cb_ptr + cb);
         e = __ldg(P.cb_ptr + cb + 1);
     }
-    const uint32_t nch = want ? (e - s + PUSH_CHUNK - 1) / PUSH_CHUNK : 0u;
+    const uint32_t nch = want ? (e - s + ch - 1) / ch : 0u;
     uint32_t tot_a, tot_c;
     const uint32_t oa = block_excl_scan(want ? 1u : 0u, &tot_a);
     const uint32_t oc = block_excl_scan(nch, &tot_c);
@@ -289,7 +302,7 @@ __device__ void cta_append(const KParams &P, ListStage &L, int slot, bool want, 
             const uint32_t mid = (lo + hi + 1u) >> 1;
             if (L.cstart[mid] <= t) lo = mid; else hi = mid - 1u;
         }
-        P.chunks[slot][L.base_c + t] = make_uint2(L.q0[lo] + (t - L.cstart[lo]) * PUSH_CHUNK, L.cb[lo]);
+        P.chunks[slot][L.base_c + t] = make_uint2(L.q0[lo] + (t - L.cstart[lo]) * ch, L.cb[lo]);
     }
     __syncthreads();
 }
@@ -787,7 +800,7 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
 // block whose rows are all visited is skipped in the drain).
 template <int SR, bool DOUT, bool ST>
 __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, const uint32_t *vis,
-                           uint32_t *out_rm, int cslot)
+                           uint32_t *out_rm, int cslot, uint32_t ch)
 {
     constexpr int WK = PUSH_CHUNK / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -798,9 +811,9 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
     float *y = DOUT ? P.y_dense : P.y_acc;
     uint32_t c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
     for (uint32_t ci = gw; ci < nch; ci += nwarps) {
-        const uint2 ch = __ldcg(P.chunks[cslot] + ci);
-        const uint32_t q0 = ch.x, c = ch.y;
-        const uint32_t q1 = min(q0 + PUSH_CHUNK, __ldg(P.cb_ptr + c + 1));
+        const uint2 task = __ldcg(P.chunks[cslot] + ci);
+        const uint32_t q0 = task.x, c = task.y;
+        const uint32_t q1 = min(q0 + ch, __ldg(P.cb_ptr + c + 1));
         uint2 d[WK];
 #pragma unroll
         for (int k = 0; k < WK; ++k) {
@@ -959,6 +972,9 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     const int lane = tid & 31;
     const bool early_list = P.path_force == DBS_PATH_PUSH ||
                             (P.path_force == DBS_PATH_AUTO && (unsigned long long)P.x_nnz * 4ull <= (unsigned long long)P.nbc);
+    // task size of an early list, from the expected work (entries x mean blocks per column block)
+    const uint32_t ch_early = push_chunk((unsigned long long)min((long long)P.x_nnz, (long long)P.nbc) *
+                                         (P.nbc ? ((unsigned long long)P.B + P.nbc - 1) / P.nbc : 1ull));
     uint32_t first = 0, act_cnt = 0, work = 0;
     for (size_t base = (size_t)blockIdx.x * NT; base < (size_t)P.x_nnz; base += gsz) {
         const size_t e = base + tid;
@@ -990,8 +1006,8 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
             }
         }
         if (early_list) {
-            cta_append(P, S.L, slot, new_lo, 2u * (j >> 5));
-            cta_append(P, S.L, slot, new_hi, 2u * (j >> 5) + 1u);
+            cta_append(P, S.L, slot, new_lo, 2u * (j >> 5), ch_early);
+            cta_append(P, S.L, slot, new_hi, 2u * (j >> 5) + 1u, ch_early);
         }
     }
     cta_count(&P.ctrl->n_blk[slot], first);
@@ -1004,6 +1020,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     const uint32_t n_nz = ld_cg(&P.ctrl->n_blk[slot]);
     const bool push = choose_push(P, n_nz, ld_cg(&P.ctrl->n_vis[slot]));
     if (push) {
+        const uint32_t ch = early_list ? ch_early : push_chunk(ld_cg(&P.ctrl->n_vis[slot]));
         if (!early_list) {
             // push list: each nonzero vector block is appended by the x entry
             // holding its lowest set mask bit (indices are unique)
@@ -1018,11 +1035,11 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
                         want = (mb & (0u - mb)) == (1u << (j & 15u));
                     }
                 }
-                cta_append(P, S.L, slot, want, j >> 4);
+                cta_append(P, S.L, slot, want, j >> 4, ch);
             }
             if (!grid_sync(P)) return;
         }
-        push_tasks<SR, false, ST>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
+        push_tasks<SR, false, ST>(P, S, P.xm32, P.uvis32, P.yrm32, slot, ch);
     } else {
         pull_tiles<SR, false, ST>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
     }
@@ -1168,14 +1185,15 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
     const uint32_t n_nz = ld_cg(&P.ctrl->n_blk[slot]);
     const bool push = choose_push(P, n_nz, ld_cg(&P.ctrl->n_vis[slot]));
     if (push) {
+        const uint32_t ch = push_chunk(ld_cg(&P.ctrl->n_vis[slot]));
         for (uint32_t base = blockIdx.x * NT; base < nwords; base += gridDim.x * NT) {
             const uint32_t w = base + tid;
             const uint32_t bal = w < nwords ? __ldcg(P.dxm32 + w) : 0u;
-            cta_append(P, S.L, slot, (bal & 0xFFFFu) != 0u, 2u * w);
-            cta_append(P, S.L, slot, (bal >> 16) != 0u, 2u * w + 1u);
+            cta_append(P, S.L, slot, (bal & 0xFFFFu) != 0u, 2u * w, ch);
+            cta_append(P, S.L, slot, (bal >> 16) != 0u, 2u * w + 1u, ch);
         }
         if (!grid_sync(P)) return;
-        push_tasks<0, true, ST>(P, S, P.dxm32, nullptr, nullptr, slot);
+        push_tasks<0, true, ST>(P, S, P.dxm32, nullptr, nullptr, slot, ch);
     } else {
         pull_tiles<0, true, ST>(P, S, P.dxm32, nullptr, nullptr, slot);
     }
@@ -1245,7 +1263,7 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
             P.ctrl->n_blk[0] = 1u;
             P.ctrl->n_vis[0] = cb_len(P, s >> 4);
         }
-        if (blockIdx.x == 0) cta_append(P, S.L, 0, tid == 0, s >> 4);
+        if (blockIdx.x == 0) cta_append(P, S.L, 0, tid == 0, s >> 4, push_chunk(cb_len(P, s >> 4)));
     }
     if (!grid_sync(P)) return;
     stamp(P, 1);
@@ -1267,21 +1285,24 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
             P.ctrl->lv_path[L - 1u] = push ? 1u : 2u;
         }
         if (push) {
-            // push list of the frontier, built only for push levels (few blocks)
+            // push list of the frontier, built only for push levels (few
+            // blocks; level 1's was built with the source)
+            const uint32_t ch = push_chunk(ld_cg(&P.ctrl->n_vis[cur]));
             if (L > 1u) {
                 for (uint32_t base = blockIdx.x * NT; base < nwords; base += gridDim.x * NT) {
                     const uint32_t w = base + tid;
                     const uint32_t fm = w < nwords ? __ldcg(fcur + w) : 0u;
-                    cta_append(P, S.L, cur, (fm & 0xFFFFu) != 0u, 2u * w);
-                    cta_append(P, S.L, cur, (fm >> 16) != 0u, 2u * w + 1u);
+                    cta_append(P, S.L, cur, (fm & 0xFFFFu) != 0u, 2u * w, ch);
+                    cta_append(P, S.L, cur, (fm >> 16) != 0u, 2u * w + 1u, ch);
                 }
                 if (!grid_sync(P)) return;
             }
-            push_tasks<1, false, ST>(P, S, fcur, P.bvis32, fnext, cur);
+            push_tasks<1, false, ST>(P, S, fcur, P.bvis32, fnext, cur, ch);
         } else {
             pull_tiles<1, false, ST>(P, S, fcur, P.bvis32, fnext, cur);
         }
         if (!grid_sync(P)) return;
+        if (blockIdx.x == 0 && tid == 0 && L - 1u < (uint32_t)BFS_LEVEL_LOG) P.ctrl->lv_u[L - 1u] = globaltimer();
 
         // level update over all frontier words (one thread per word)
         uint32_t nb = 0, reached = 0, work = 0;
@@ -1491,7 +1512,7 @@ dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
         return DBS_ERR_CUDA;
     }
     const size_t nbc = (size_t)A->nbc, nbr = (size_t)A->nbr;
-    const size_t chunk_cap = (size_t)A->B / PUSH_CHUNK + nbc + 1;
+    const size_t chunk_cap = (size_t)A->B / PUSH_CHUNK_MIN + nbc + 1;   // tasks of the smallest size
     w->n_ctiles = (uint32_t)((nbr + CTILE - 1) / CTILE);
     const size_t yrm_words = std::max<size_t>(1, (size_t)w->n_ctiles) * CTILE / 2 + 8;
     bool ok = dalloc(&w->x_dense, nbc * 16 + 16) && dalloc(&w->xm32, nbc / 2 + 8) &&
@@ -1676,7 +1697,7 @@ dbs_status dbs_last_stats(dbs_workspace *w, void *stream, dbs_stats *out)
 }
 
 dbs_status dbs_bfs_level_stats(dbs_workspace *w, void *stream, int32_t max_levels, int64_t *frontier_blocks,
-                               int64_t *push_work, int32_t *path, int64_t *level_ns)
+                               int64_t *push_work, int32_t *path, int64_t *level_ns, int64_t *traversal_ns)
 {
     if (!w || max_levels < 0) return DBS_ERR_INVALID_ARG;
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
@@ -1692,6 +1713,7 @@ dbs_status dbs_bfs_level_stats(dbs_workspace *w, void *stream, int32_t max_level
         if (push_work) push_work[l] = c.lv_nv[l];
         if (path) path[l] = (int32_t)c.lv_path[l];
         if (level_ns) level_ns[l] = c.lv_t[l + 1] >= c.lv_t[l] ? (int64_t)(c.lv_t[l + 1] - c.lv_t[l]) : 0;
+        if (traversal_ns) traversal_ns[l] = c.lv_u[l] >= c.lv_t[l] ? (int64_t)(c.lv_u[l] - c.lv_t[l]) : 0;
     }
     return DBS_OK;
 }

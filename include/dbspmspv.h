@@ -260,11 +260,12 @@ dbs_status dbs_last_stats(dbs_workspace *ws, void *stream, dbs_stats *out);
  * (the frontier evolution the paper profiles in Figure 3): for each level
  * l < min(max_levels, 64, number of levels), the frontier's nonzero vector
  * blocks, the matrix blocks in those column blocks (the blocks push visits),
- * the path taken (1 push, 2 pull) and the level's device time in ns
- * (traversal + update, as seen by block 0).  HOST arrays, any may be NULL.
- * Synchronizes the stream.  DBS_ERR_INVALID_ARG if the last call was not a BFS. */
+ * the path taken (1 push, 2 pull), the level's device time in ns (traversal
+ * + update, as seen by block 0) and the part of it up to the end of the
+ * traversal.  HOST arrays, any may be NULL.  Synchronizes the stream.
+ * DBS_ERR_INVALID_ARG if the last call was not a BFS. */
 dbs_status dbs_bfs_level_stats(dbs_workspace *ws, void *stream, int32_t max_levels, int64_t *frontier_blocks,
-                               int64_t *push_work, int32_t *path, int64_t *level_ns);
+                               int64_t *push_work, int32_t *path, int64_t *level_ns, int64_t *traversal_ns);
 
 /* Self-test of the bounded device wait: launches the grid barrier with one
  * block withheld, so every other block's wait expires after

@@ -339,6 +339,7 @@ def test_bfs_level_stats_match_frontiers(small):
         assert st["frontier_blocks"][l] == len(cbs)
         assert st["push_work"][l] == int(deg[cbs].sum())
         assert st["path"][l] in ("push", "pull")
+        assert 0 <= st["traversal_us"][l] <= st["level_us"][l]
 
 
 def test_bfs_grid_closed_form():
