@@ -493,7 +493,8 @@ struct WarpPull {
     uint32_t qm[TILE_MAX_BLOCKS];     // their meta words
     uint32_t qr[TILE_MAX_BLOCKS];     // push: their row blocks
     uint32_t rm[TILE_MAX_SPAN];       // touched (Boolean: found) rows per row block
-    uint32_t nq;                      // queued hits
+    uint32_t nq;                      // queued hits (Boolean: COO hits, from the front)
+    uint32_t nq2;                     // Boolean: other hits, from the back
     float y[SR == 0 ? TILE_MAX_SPAN * 16 : 1];   // partial row sums (plus-times)
 };
 
@@ -665,7 +666,7 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
         if (lane < (int)span) W.rm[lane] = 0u;
         if (SR == 0)
             for (uint32_t i = lane; i < span * 16u; i += 32) W.y[i] = 0.0f;
-        if (lane == 0) W.nq = 0u;
+        if (lane == 0) { W.nq = 0u; W.nq2 = 0u; }
         uint32_t mm[WK / 2];   // the eight column-block masks, two per register
 #pragma unroll
         for (int j = 0; j < WK / 2; ++j) {
@@ -696,7 +697,10 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             }
             const uint32_t a = inl ? 0u : m & meta & 0xFFFFu;
             if (a) {
-                const uint32_t slot = atomicAdd(&W.nq, 1u);
+                // Boolean: COO hits from the front of the queue, the others
+                // from the back, so drain rounds run one decoder each
+                const bool back = SR == 1 && meta_fmt(meta) != FMT_COO;
+                const uint32_t slot = back ? TILE_MAX_BLOCKS - 1u - atomicAdd(&W.nq2, 1u) : atomicAdd(&W.nq, 1u);
                 W.qe[slot] = li | (lrb << 8) | (a << 16);
                 W.qm[slot] = meta;
                 if (ST) ++c_hit;
@@ -707,15 +711,27 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
         // payload-carrying hits
         const uint32_t nq = W.nq;
         if (SR == 1) {
+            // COO hits (front of the queue), then the mask formats (back)
             for (uint32_t i = lane; i < nq; i += 32) {
-                const uint32_t e = W.qe[i], meta = W.qm[i];
+                const uint32_t e = W.qe[i], nnz = meta_nnz(W.qm[i]);
+                const uint4 *b = P.payload + __ldg(P.blk_ref + p0 + (e & 0xFFu));
+                const uint4 u0 = __ldg(b);
+                const uint4 u1 = nnz > 16u ? __ldg(b + 1) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t r = bool_found_units(FMT_COO, nnz, e >> 16, u0, u1, b);
+                if (r) atomicOr(&W.rm[(e >> 8) & 0xFFu], r);
+                if (ST) c_bytes += 4u + nnz;
+            }
+            const uint32_t nq2 = W.nq2;
+            for (uint32_t i = lane; i < nq2; i += 32) {
+                const uint32_t k = TILE_MAX_BLOCKS - 1u - i;
+                const uint32_t e = W.qe[k], meta = W.qm[k];
                 const uint4 *b = P.payload + __ldg(P.blk_ref + p0 + (e & 0xFFu));
                 const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
                 uint4 u0, u1;
                 bool_load(b, fmt, nnz, u0, u1);
                 const uint32_t r = bool_found_units(fmt, nnz, e >> 16, u0, u1, b);
                 if (r) atomicOr(&W.rm[(e >> 8) & 0xFFu], r);
-                if (ST) c_bytes += 4u + (fmt == FMT_COO ? nnz : 32u);
+                if (ST) c_bytes += 4u + 32u;
             }
         } else {
             // COO hits one per lane
