@@ -23,6 +23,7 @@ struct HostFormat {
     std::vector<uint32_t> csc2csr;    // B (host only)
     std::vector<U4> payload;          // P
     std::vector<U4> tiles;            // T: {p0, payload offset, rb0, span | flags | count}
+    std::vector<uint16_t> rb_rows;    // nbr: rows of each row block that hold an entry (bit r = row r)
 };
 
 }  // namespace dbs
@@ -42,6 +43,7 @@ struct dbs_matrix {
     uint32_t *d_csc_ref = nullptr;
     dbs::U4 *d_payload = nullptr;
     dbs::U4 *d_tiles = nullptr;
+    uint16_t *d_rb_rows = nullptr;
     dbs::HostFormat *host = nullptr;
     dbs_matrix_info info{};
 };

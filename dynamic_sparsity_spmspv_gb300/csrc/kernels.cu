@@ -82,6 +82,7 @@ struct KParams {
     const uint32_t *__restrict__ csc_ref;
     const uint4 *__restrict__ payload;
     const uint4 *__restrict__ tiles;
+    const unsigned short *__restrict__ rb_rows;   // rows holding an entry, per row block
     // call
     int path_force;
     const int32_t *x_idx;
@@ -1247,15 +1248,12 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
     const uint32_t nwords = (uint32_t)((P.nbc + 1) / 2);
     for (size_t v = gtid; v < (size_t)P.n; v += gsz) P.levels[v] = -1;
     for (size_t w = gtid; w < nwords; w += gsz) {
-        uint32_t vis = 0;
-        // rows beyond m in the last row block count as visited
-        for (uint32_t h = 0; h < 2; ++h) {
-            const uint32_t rb = 2u * (uint32_t)w + h;
-            if (rb >= (uint32_t)P.nbr) { vis |= 0xFFFFu << (16 * h); continue; }
-            const int64_t r0 = (int64_t)rb * 16;
-            if (r0 + 16 > P.m) vis |= ((0xFFFFu << (uint32_t)(P.m - r0)) & 0xFFFFu) << (16 * h);
-        }
-        P.bvis32[w] = vis;
+        // rows that hold no entry can never be reached (nor can rows beyond
+        // m): they start out visited, so tiles of reached and unreachable
+        // rows are skipped as soon as the reachable ones are all visited
+        const uint32_t lo = 2u * w < (size_t)P.nbr ? (uint32_t)__ldg(P.rb_rows + 2u * w) : 0u;
+        const uint32_t hi = 2u * w + 1u < (size_t)P.nbr ? (uint32_t)__ldg(P.rb_rows + 2u * w + 1u) : 0u;
+        P.bvis32[w] = ~(lo | (hi << 16));
         P.fm32[0][w] = 0u;
         P.fm32[1][w] = 0u;
     }
@@ -1441,6 +1439,7 @@ KParams make_params(const dbs_matrix *A, dbs_workspace *w)
     P.csc_ref = A->d_csc_ref;
     P.payload = reinterpret_cast<const uint4 *>(A->d_payload);
     P.tiles = reinterpret_cast<const uint4 *>(A->d_tiles);
+    P.rb_rows = A->d_rb_rows;
     P.x_dense = w->x_dense; P.xm32 = w->xm32; P.dxm32 = w->dxm32;
     for (int s = 0; s < 3; ++s) { P.act[s] = w->act[s]; P.chunks[s] = w->chunks[s]; }
     P.y_acc = w->y_acc; P.yrm32 = w->yrm32; P.ctile_flag = w->ctile_flag; P.n_ctiles = w->n_ctiles;
@@ -1828,6 +1827,7 @@ extern "C" dbs_status dbs_spmspv_dense_noalloc(const dbs_matrix *A, const float 
     P.csc_ref = A->d_csc_ref;
     P.payload = reinterpret_cast<const uint4 *>(A->d_payload);
     P.tiles = reinterpret_cast<const uint4 *>(A->d_tiles);
+    P.rb_rows = A->d_rb_rows;
     P.ctrl = reinterpret_cast<Ctrl *>(d.scratch);
     P.dxm32 = reinterpret_cast<uint32_t *>(d.scratch + NOALLOC_CTRL_BYTES);
     P.path_force = DBS_PATH_PULL;          // the pull path needs no task lists

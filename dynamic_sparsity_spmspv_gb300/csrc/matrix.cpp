@@ -229,8 +229,10 @@ void free_device(dbs_matrix *A)
 {
     cudaFree(A->d_rb_ptr); cudaFree(A->d_blk_desc); cudaFree(A->d_blk_ref); cudaFree(A->d_cb_ptr);
     cudaFree(A->d_csc_desc); cudaFree(A->d_csc_ref); cudaFree(A->d_payload); cudaFree(A->d_tiles);
+    cudaFree(A->d_rb_rows);
     A->d_rb_ptr = nullptr; A->d_blk_desc = nullptr; A->d_blk_ref = nullptr; A->d_cb_ptr = nullptr;
     A->d_csc_desc = nullptr; A->d_csc_ref = nullptr; A->d_payload = nullptr; A->d_tiles = nullptr;
+    A->d_rb_rows = nullptr;
 }
 
 template <class T>
@@ -424,6 +426,12 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
                 }
         }
 
+        // Rows that hold an entry, per row block (a row without one can
+        // never be reached or touched).
+        H.rb_rows.assign((size_t)nbr, 0);
+        for (int64_t i = 0; i < m; ++i)
+            if (rp[i + 1] > rp[i]) H.rb_rows[(size_t)(i / BS)] |= (uint16_t)(1u << (i % BS));
+
         // 4. Pull tiles.
         uint64_t total_w = 0;
         for (int64_t p = 0; p < B; ++p) total_w += fmt_weight(meta_fmt(H.blk_desc[(size_t)p].y));
@@ -498,6 +506,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         if ((st = upload(H.csc_ref, &A->d_csc_ref, (size_t)A->B + 8, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.payload, &A->d_payload, 1, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.tiles, &A->d_tiles, 1, s)) != DBS_OK) return fail(st);
+        if ((st = upload(H.rb_rows, &A->d_rb_rows, (size_t)nbr + 2, s)) != DBS_OK) return fail(st);
         if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return fail(DBS_ERR_CUDA); }
         A->on_device = true;
     }
