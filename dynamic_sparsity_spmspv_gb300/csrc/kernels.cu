@@ -511,6 +511,11 @@ struct SmemT : SmemBase {
     WarpPull<SR> wp[NW];
 };
 
+// Output rows staged per round by the compaction, in the warps' pull state
+// (index, and for plus-times the value, per row).
+template <int SR>
+constexpr uint32_t STAGE_ROWS = (uint32_t)(sizeof(WarpPull<SR>) * NW / (SR == 0 ? 8u : 4u)) & ~31u;
+
 extern __shared__ __align__(128) unsigned char smem_raw[];
 
 // Statistics: a warp sums its lanes' counts and one lane adds them to the
@@ -1098,6 +1103,8 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     // of the cooperative launch is resident, so the waits end.  The
     // accumulator and the row masks are cleared for the next call on the way.
     __shared__ uint32_t s_base;
+    uint32_t *stage_idx = reinterpret_cast<uint32_t *>(&S.wp[0]);
+    float *stage_val = reinterpret_cast<float *>(stage_idx + STAGE_ROWS<SR>);
     for (uint32_t ct = blockIdx.x; ct < P.n_ctiles; ct += gridDim.x) {
         const size_t wi = (size_t)ct * NT + tid;
         const uint32_t raw = __ldcg(P.yrm32 + wi);
@@ -1138,17 +1145,33 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
         const uint32_t base = s_base;
         if (base == 0xFFFFFFFFu) return;
         if (raw) P.yrm32[wi] = 0u;
-        uint32_t o = base + off;
-        while (bits) {
-            const uint32_t k = __ffs(bits) - 1u;
-            bits &= bits - 1u;
-            const uint32_t row = (uint32_t)(2u * wi + (k >> 4)) * 16u + (k & 15u);
-            P.y_idx[o] = (int32_t)row;
-            if (SR == 0) {
-                P.y_val[o] = __ldcg(P.y_acc + row);
-                P.y_acc[row] = 0.0f;
+        // The tile's rows go to shared memory first (the warps' pull state
+        // is free by now), in rounds of R, and out to y with coalesced
+        // stores.
+        for (uint32_t r0 = 0; r0 < tile_tot; r0 += STAGE_ROWS<SR>) {
+            const uint32_t r1 = min(tile_tot, r0 + STAGE_ROWS<SR>);
+            if (off < r1 && off + __popc(bits) > r0) {
+                uint32_t b = bits, o = off;
+                while (b) {
+                    const uint32_t k = __ffs(b) - 1u;
+                    b &= b - 1u;
+                    if (o >= r0 && o < r1) {
+                        const uint32_t row = (uint32_t)(2u * wi + (k >> 4)) * 16u + (k & 15u);
+                        stage_idx[o - r0] = row;
+                        if (SR == 0) {
+                            stage_val[o - r0] = __ldcg(P.y_acc + row);
+                            P.y_acc[row] = 0.0f;
+                        }
+                    }
+                    ++o;
+                }
             }
-            ++o;
+            __syncthreads();
+            for (uint32_t i = tid; i < r1 - r0; i += NT) {
+                P.y_idx[base + r0 + i] = (int32_t)stage_idx[i];
+                if (SR == 0) P.y_val[base + r0 + i] = stage_val[i];
+            }
+            __syncthreads();
         }
         if (ct == P.n_ctiles - 1 && tid == 0) {
             *P.y_nnz = (long long)(base + tile_tot);
