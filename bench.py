@@ -235,6 +235,67 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+ABLATION_FORMATS = (("auto", -1), ("coo", 0), ("force_csr", 2))
+
+
+def run_ablation(dbs, torch, dev, stream, flush, reps: int):
+    """Format ablation (the paper's Fig. 10 setting: pull at x density 0.1,
+    plus push at 0.001): every block forced to COO or to ForceCSR, against
+    the automatic choice, on the R-MAT (Boolean), FEM and LLM (fp32)
+    workloads.  Median kernel time per call, algorithmic bytes, GB/s."""
+    import synth
+    rows = []
+    for name in ("rmat", "fem", "llm"):
+        A = synth.config(name, "full")
+        boolean = A.vals is None
+        sr = "or_and" if boolean else "plus_times"
+        xs = {}
+        for d in (0.1, 0.001):
+            if name == "fem":
+                x = synth.x_clusters(A.n, d, [70, int(d * 1e4)])
+            elif name == "llm":
+                xd = synth.x_relu_topk(A.n, max(1, int(round(d * A.n))), [71, int(d * 1e4)])
+                nz = np.nonzero(xd)[0].astype(np.int32)
+                x = synth.SparseVec(A.n, nz, xd[nz])
+            else:
+                x = synth.x_uniform(A.n, int(round(d * A.n)), [72, int(d * 1e4)], valued=False)
+            xv = None if (boolean or x.val is None) else torch.from_numpy(x.val.astype(np.float32)).to(dev)
+            xs[d] = (torch.from_numpy(x.idx).to(dev), xv)
+        y_idx = torch.empty(A.m, dtype=torch.int32, device=dev)
+        y_val = torch.empty(A.m, dtype=torch.float32, device=dev)
+        y_nnz = torch.empty(1, dtype=torch.int64, device=dev)
+        for fname, ff in ABLATION_FORMATS:
+            M = dbs.DBMatrix.from_csr(A, force_format=ff)
+            info = M.info()
+            ws = dbs.Workspace(M, collect_stats=1)
+            for d, path in ((0.1, "pull"), (0.001, "push")):
+                xi, xv = xs[d]
+                dbs.spmspv(M, xi, xv, semiring=sr, path=path, ws=ws, y_idx=y_idx, y_val=y_val, y_nnz=y_nnz)
+                bytes_alg = ws.stats()["bytes_alg"]
+                ws.set_opts(dbs.exec_opts(collect_stats=0))
+                ts = []
+                for i in range(reps + 2):
+                    flush(i)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    dbs.spmspv(M, xi, xv, semiring=sr, path=path, ws=ws, y_idx=y_idx, y_val=y_val, y_nnz=y_nnz)
+                    e1.record(stream)
+                    e1.synchronize()
+                    if i >= 2:
+                        ts.append(e0.elapsed_time(e1))
+                ws.set_opts(dbs.exec_opts(collect_stats=1))
+                us = 1e3 * float(np.median(ts))
+                rows.append({"workload": name, "format": fname, "density": d, "path": path,
+                             "us": round(us, 2), "bytes_alg": int(bytes_alg),
+                             "gbs": round(bytes_alg / us / 1e3, 1),
+                             "blocks_by_format": list(info["blocks_by_format"]),
+                             "payload_mb": round(info["payload_bytes"] / 1e6, 1)})
+            assert ws.check() == 0
+            ws.close()
+            M.close()
+    return rows
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -247,6 +308,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--path-sweep", type=int, default=8,
                     help="calls per density and forced path for the push/pull crossover table (0 = off)")
+    ap.add_argument("--ablation", type=int, default=0,
+                    help="calls per point of the format ablation (Auto / COO-only / CSR-only on the "
+                         "R-MAT, FEM and LLM workloads) and per-level frontier histograms (0 = off)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -475,6 +539,22 @@ def main():
         out["path_sweep"] = sweep
         out["bfs_path_sweep"] = bfs_sweep
         assert ws.check() == 0
+
+    if args.ablation > 0:
+        out["ablation"] = run_ablation(dbs, torch, dev, stream, flush, args.ablation)
+        # Fig. 3 style frontier diagnostics: per BFS level, how many of the
+        # frontier's nonzero vector blocks hold 1, 2, ..., 16 active entries
+        hist = []
+        for src in sources[:3]:
+            dbs.bfs(M, int(src), levels=levels, ws=ws)
+            lv = levels.cpu().numpy()
+            per = []
+            for l in range(int(lv.max()) + 1):
+                vb = np.nonzero(lv == l)[0] >> 4
+                cnt = np.bincount(np.bincount(vb)[np.unique(vb)], minlength=17)[1:17]
+                per.append(cnt.tolist())
+            hist.append(per)
+        out["frontier_block_histograms"] = hist
 
     # end to end through the public API with host buffers
     if not args.no_e2e:
