@@ -352,12 +352,24 @@ __device__ __forceinline__ RowOut mk_colwise(const uint8_t *__restrict__ b, uint
     while (a) {
         uint32_t c = __ffs(a) - 1u;
         a &= a - 1u;
-        uint32_t cm = __ldg(cmask + c);
-        if ((cm >> r) & 1u) {
-            uint32_t idx = FMT == FMT_DENSE ? c * 16u + r : (uint32_t)__ldg(b + OFF_PTR + c) + __popc(cm & ((1u << r) - 1u));
-            sum = fmaf(__ldg(vals + idx), xval(xb, c), sum);
-            t = 1u;
-            ++cnt;
+        if (FMT == FMT_DENSE) {
+            // column-major with zeros for absent entries: the value's address
+            // does not depend on the mask, so both loads go out together
+            const float v = __ldg(vals + c * 16u + r);
+            const uint32_t cm = __ldg(cmask + c);
+            if ((cm >> r) & 1u) {
+                sum = fmaf(v, xval(xb, c), sum);
+                t = 1u;
+                ++cnt;
+            }
+        } else {
+            uint32_t cm = __ldg(cmask + c);
+            if ((cm >> r) & 1u) {
+                uint32_t idx = (uint32_t)__ldg(b + OFF_PTR + c) + __popc(cm & ((1u << r) - 1u));
+                sum = fmaf(__ldg(vals + idx), xval(xb, c), sum);
+                t = 1u;
+                ++cnt;
+            }
         }
     }
     sum += __shfl_xor_sync(FULL, sum, 16);
@@ -436,6 +448,57 @@ __device__ __forceinline__ RowOut mk_pcsr_col(const uint8_t *__restrict__ b, uin
     return RowOut{s, (rows >> (lane & 15)) & 1u};
 }
 
+// Half-warp forms of the fp32 microkernels: lane l (0..15) of a half-warp
+// computes row l of one block, so a warp works on two blocks at once.  The
+// loads of one step do not depend on each other (Dense: value and column
+// mask together; row-wise: row mask and row pointer together, then the
+// values), which keeps each block to one or two memory round trips.
+// Returns the row's sum and whether the row met an active column; *nread
+// counts the values read.
+__device__ __forceinline__ RowOut hw_heavy(const uint8_t *__restrict__ b, uint32_t meta, uint32_t act,
+                                           const float *xb, uint32_t l, uint32_t *nread)
+{
+    const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
+    const float *vals = reinterpret_cast<const float *>(b + val_offset(fmt, nnz));
+    float sum = 0.0f;
+    uint32_t t = 0, cnt = 0;
+    if (fmt == FMT_DENSE || fmt == FMT_FCSC) {
+        const uint16_t *cmask = reinterpret_cast<const uint16_t *>(b + (fmt == FMT_DENSE ? 0u : OFF_MASK));
+        uint32_t a = act;
+        while (a) {
+            const uint32_t c = __ffs(a) - 1u;
+            a &= a - 1u;
+            const uint32_t cm = __ldg(cmask + c);
+            float v;
+            if (fmt == FMT_DENSE) v = __ldg(vals + c * 16u + l);
+            else v = ((cm >> l) & 1u) ? __ldg(vals + (uint32_t)__ldg(b + OFF_PTR + c) + __popc(cm & ((1u << l) - 1u))) : 0.0f;
+            if ((cm >> l) & 1u) {
+                sum = fmaf(v, xval(xb, c), sum);
+                t = 1u;
+                ++cnt;
+            }
+        }
+    } else {                                               // ForceCSR, patched CSR (row mode)
+        const uint32_t rm = __ldg(reinterpret_cast<const uint16_t *>(b + OFF_MASK) + l);
+        const uint32_t base = __ldg(b + OFF_PTR + l);
+        uint32_t a = rm & act;
+        t = a != 0u;
+        while (a) {
+            const uint32_t c = __ffs(a) - 1u;
+            a &= a - 1u;
+            sum = fmaf(__ldg(vals + base + __popc(rm & ((1u << c) - 1u))), xval(xb, c), sum);
+            ++cnt;
+        }
+    }
+    *nread = cnt;
+    return RowOut{sum, t};
+}
+// Whether a block needs the whole-warp patched-CSR column mode.
+__device__ __forceinline__ bool needs_col_mode(const KParams &P, uint32_t meta, uint32_t act)
+{
+    return meta_fmt(meta) == FMT_PCSR && (int)__popc(act) < P.local_pull_min;
+}
+
 // Dispatch of the fp32 warp microkernel for a non-COO block (Section 3.3.1:
 // by blocks_type and blk_x_mask).
 __device__ __forceinline__ RowOut mk_heavy(const KParams &P, const uint8_t *b, uint32_t meta, uint32_t act,
@@ -459,7 +522,9 @@ __device__ __forceinline__ RowOut mk_heavy(const KParams &P, const uint8_t *b, u
 }
 
 // COO block, one lane: scan the packed coordinates (Section 3.3.3).  Adds the
-// products through `add(row, value)` and returns the touched-row bits.
+// products through `add(row, value)` and returns the touched-row bits.  The
+// entries go in groups of four, whose value and x loads are all issued
+// before any product is formed.
 template <class Add>
 __device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint32_t nnz, uint32_t act,
                                             const float *xb, bool valued, Add add)
@@ -471,13 +536,24 @@ __device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint
         const uint4 v = __ldg(c4 + (base >> 4));
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (uint32_t j = 0; j < 16u; ++j) {
-            const uint32_t e = (wv[j >> 2] >> (8u * (j & 3u))) & 0xFFu;
-            const uint32_t c = e & 15u;
-            if (base + j < nnz && ((act >> c) & 1u)) {
-                const uint32_t r = e >> 4;
+        for (uint32_t g = 0; g < 4u; ++g) {
+            if (base + 4u * g >= nnz) break;
+            float av[4], xx[4];
+            uint32_t hit = 0;
+#pragma unroll
+            for (uint32_t j = 0; j < 4u; ++j) {
+                const uint32_t e = (wv[g] >> (8u * j)) & 0xFFu, idx = base + 4u * g + j;
+                const bool on = idx < nnz && ((act >> (e & 15u)) & 1u);
+                hit |= (on ? 1u : 0u) << j;
+                av[j] = on && valued ? __ldg(vals + idx) : 0.0f;
+                xx[j] = on && valued ? xval(xb, e & 15u) : 0.0f;
+            }
+#pragma unroll
+            for (uint32_t j = 0; j < 4u; ++j) {
+                if (!((hit >> j) & 1u)) continue;
+                const uint32_t r = ((wv[g] >> (8u * j)) >> 4) & 15u;
                 rows |= 1u << r;
-                if (valued) add(r, __ldg(vals + base + j) * xval(xb, c));
+                if (valued) add(r, av[j] * xx[j]);
             }
         }
     }
@@ -494,8 +570,8 @@ struct WarpPull {
     uint32_t qm[TILE_MAX_BLOCKS];     // their meta words
     uint32_t qr[TILE_MAX_BLOCKS];     // push: their row blocks
     uint32_t rm[TILE_MAX_SPAN];       // touched (Boolean: found) rows per row block
-    uint32_t nq;                      // queued hits (Boolean: COO hits, from the front)
-    uint32_t nq2;                     // Boolean: other hits, from the back
+    uint32_t nq;                      // queued COO hits, from the front
+    uint32_t nq2;                     // queued hits of the other formats, from the back
     float y[SR == 0 ? TILE_MAX_SPAN * 16 : 1];   // partial row sums (plus-times)
 };
 
@@ -703,9 +779,9 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             }
             const uint32_t a = inl ? 0u : m & meta & 0xFFFFu;
             if (a) {
-                // Boolean: COO hits from the front of the queue, the others
-                // from the back, so drain rounds run one decoder each
-                const bool back = SR == 1 && meta_fmt(meta) != FMT_COO;
+                // COO hits from the front of the queue, the others from the
+                // back, so drain rounds run one decoder each
+                const bool back = meta_fmt(meta) != FMT_COO;
                 const uint32_t slot = back ? TILE_MAX_BLOCKS - 1u - atomicAdd(&W.nq2, 1u) : atomicAdd(&W.nq, 1u);
                 W.qe[slot] = li | (lrb << 8) | (a << 16);
                 W.qm[slot] = meta;
@@ -740,36 +816,70 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 if (ST) c_bytes += 4u + 32u;
             }
         } else {
+            // payload offsets of all hits first (independent loads), so each
+            // block below waits for its payload only
+            const uint32_t nq2 = W.nq2;
+            for (uint32_t i = lane; i < nq; i += 32) W.qr[i] = __ldg(P.blk_ref + p0 + (W.qe[i] & 0xFFu));
+            for (uint32_t i = lane; i < nq2; i += 32) {
+                const uint32_t k = TILE_MAX_BLOCKS - 1u - i;
+                W.qr[k] = __ldg(P.blk_ref + p0 + (W.qe[k] & 0xFFu));
+            }
+            __syncwarp();
             // COO hits one per lane
             for (uint32_t i = lane; i < nq; i += 32) {
                 const uint32_t e = W.qe[i], meta = W.qm[i];
-                if (meta_fmt(meta) != FMT_COO) continue;
                 const uint32_t p = p0 + (e & 0xFFu), lrb = (e >> 8) & 0xFFu, nnz = meta_nnz(meta);
                 const uint32_t col = __ldg(&P.blk_desc[p].x) & DESC_COL_MASK;
                 float *sy = &W.y[lrb * 16u];
-                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.blk_ref + p));
+                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + W.qr[i]);
                 const uint32_t rows = coo_lane(b, nnz, e >> 16, xv + (size_t)col * 16u, true,
                                                [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
                 if (rows) atomicOr(&W.rm[lrb], rows);
                 if (ST) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
             }
             __syncwarp();
-            // the other formats by the whole warp
-            for (uint32_t i = 0; i < nq; ++i) {
-                const uint32_t e = W.qe[i], meta = W.qm[i];
-                if (meta_fmt(meta) == FMT_COO) continue;            // warp-uniform
+            // the other formats two at a time, one block per half-warp (a
+            // patched-CSR block in column mode takes the whole warp)
+            const uint32_t l = lane & 15u, h = lane >> 4;
+            for (uint32_t i = 0; i < nq2; i += 2) {
+                const bool two = i + 1u < nq2;
+                const uint32_t k = TILE_MAX_BLOCKS - 1u - i - (h & (two ? 1u : 0u));
+                const uint32_t e = W.qe[k], meta = W.qm[k], act = e >> 16;
                 const uint32_t p = p0 + (e & 0xFFu), lrb = (e >> 8) & 0xFFu;
-                const uint32_t col = __ldg(&P.blk_desc[p].x) & DESC_COL_MASK;
-                uint32_t by = 0;
-                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.blk_ref + p));
-                RowOut o = mk_heavy(P, b, meta, e >> 16, xv + (size_t)col * 16u, lane, S.wacc[warp], &by);
-                if (lane < 16 && o.touched) W.y[lrb * 16u + lane] += o.sum;
-                const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
-                if (lane == 0) {
-                    if (bits) W.rm[lrb] |= bits;
-                    if (ST) c_bytes += 4u + by;
+                const float *xb = xv + (size_t)(__ldg(&P.blk_desc[p].x) & DESC_COL_MASK) * 16u;
+                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + W.qr[k]);
+                if (__any_sync(FULL, needs_col_mode(P, meta, act))) {
+                    // one block at a time with the whole warp
+                    for (uint32_t j = 0; j < (two ? 2u : 1u); ++j) {
+                        const uint32_t kj = TILE_MAX_BLOCKS - 1u - i - j;
+                        const uint32_t ej = W.qe[kj], mj = W.qm[kj], lj = (ej >> 8) & 0xFFu;
+                        const float *xj = xv + (size_t)(__ldg(&P.blk_desc[p0 + (ej & 0xFFu)].x) & DESC_COL_MASK) * 16u;
+                        uint32_t by = 0;
+                        RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + W.qr[kj]), mj, ej >> 16,
+                                            xj, lane, S.wacc[warp], &by);
+                        if (lane < 16 && o.touched) W.y[lj * 16u + lane] += o.sum;
+                        const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
+                        if (lane == 0) {
+                            if (bits) W.rm[lj] |= bits;
+                            if (ST) c_bytes += 4u + by;
+                        }
+                        __syncwarp();
+                    }
+                    continue;
                 }
-                __syncwarp();
+                uint32_t nr = 0;
+                const RowOut o = hw_heavy(b, meta, act, xb, l, &nr);
+                // half 0 then half 1 (their row blocks may coincide)
+                const uint32_t bits = __ballot_sync(FULL, o.touched);
+                for (uint32_t hh = 0; hh < (two ? 2u : 1u); ++hh) {
+                    if (h == hh && o.touched) W.y[lrb * 16u + l] += o.sum;
+                    if (lane == 16u * hh && ((bits >> (16u * hh)) & 0xFFFFu)) W.rm[lrb] |= (bits >> (16u * hh)) & 0xFFFFu;
+                    __syncwarp();
+                }
+                if (ST) {
+                    const uint32_t tot = __reduce_add_sync(FULL, (two || h == 0) ? nr : 0u);
+                    if (lane == 0) c_bytes += 8u + 32u + 4u * tot;
+                }
             }
         }
         __syncwarp();
@@ -847,7 +957,7 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             const size_t j = (size_t)c * 16u + lane;
             wx[lane] = j < (size_t)P.n ? __ldcg(P.xv + j) : 0.0f;
         }
-        if (lane == 0) W.nq = 0u;
+        if (lane == 0) { W.nq = 0u; W.nq2 = 0u; }
         __syncwarp();
 #pragma unroll
         for (int k = 0; k < WK; ++k) {
@@ -864,7 +974,9 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             } else {
                 const uint32_t a = meta & xmb & 0xFFFFu;
                 if (a) {
-                    const uint32_t slot = atomicAdd(&W.nq, 1u);
+                    // plus-times: COO hits from the front, the others from the back
+                    const bool back = SR == 0 && meta_fmt(meta) != FMT_COO;
+                    const uint32_t slot = back ? TILE_MAX_BLOCKS - 1u - atomicAdd(&W.nq2, 1u) : atomicAdd(&W.nq, 1u);
                     W.qe[slot] = ql | (a << 16);
                     W.qm[slot] = meta;
                     W.qr[slot] = rb;
@@ -889,9 +1001,10 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 if (ST) c_bytes += 4u + (fmt == FMT_COO ? nnz : 32u);
             }
         } else {
+            const uint32_t nq2 = W.nq2;
+            // COO hits one per lane
             for (uint32_t i = lane; i < nq; i += 32) {
                 const uint32_t e = W.qe[i], meta = W.qm[i], rb = W.qr[i];
-                if (meta_fmt(meta) != FMT_COO) continue;
                 const uint32_t nnz = meta_nnz(meta);
                 const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.csc_ref + q0 + (e & 0xFFFFu)));
                 float *yr = y + (size_t)rb * 16u;
@@ -899,20 +1012,50 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 if (!DOUT && rows) or16(out_rm, rb, rows);
                 if (ST) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
             }
+            // the other hits: payload offsets first (independent loads; the
+            // offset replaces the position and the active columns replace
+            // the meta word's column mask), then two blocks at a time, one
+            // per half-warp (a patched-CSR block in column mode takes the warp)
+            for (uint32_t i = lane; i < nq2; i += 32) {
+                const uint32_t k = TILE_MAX_BLOCKS - 1u - i;
+                const uint32_t e = W.qe[k];
+                W.qe[k] = __ldg(P.csc_ref + q0 + (e & 0xFFFFu));
+                W.qm[k] = (W.qm[k] & ~0xFFFFu) | (e >> 16);
+            }
             __syncwarp();
-            for (uint32_t i = 0; i < nq; ++i) {
-                const uint32_t e = W.qe[i], meta = W.qm[i], rb = W.qr[i];
-                if (meta_fmt(meta) == FMT_COO) continue;            // warp-uniform
-                uint32_t by = 0;
-                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.csc_ref + q0 + (e & 0xFFFFu)));
-                RowOut o = mk_heavy(P, b, meta, e >> 16, wx, lane, S.wacc[warp], &by);
-                if (lane < 16 && o.touched) atomicAdd(y + (size_t)rb * 16u + lane, o.sum);
-                const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
-                if (lane == 0) {
-                    if (!DOUT && bits) or16(out_rm, rb, bits);
-                    if (ST) c_bytes += 4u + by;
+            const uint32_t l = lane & 15u, h = lane >> 4;
+            for (uint32_t i = 0; i < nq2; i += 2) {
+                const bool two = i + 1u < nq2;
+                const uint32_t k = TILE_MAX_BLOCKS - 1u - i - (h & (two ? 1u : 0u));
+                const uint32_t meta = W.qm[k], act = meta & 0xFFFFu, rb = W.qr[k];
+                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + W.qe[k]);
+                if (__any_sync(FULL, needs_col_mode(P, meta, act))) {
+                    for (uint32_t j = 0; j < (two ? 2u : 1u); ++j) {
+                        const uint32_t kj = TILE_MAX_BLOCKS - 1u - i - j;
+                        const uint32_t mj = W.qm[kj], rj = W.qr[kj];
+                        uint32_t by = 0;
+                        RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + W.qe[kj]), mj, mj & 0xFFFFu,
+                                            wx, lane, S.wacc[warp], &by);
+                        if (lane < 16 && o.touched) atomicAdd(y + (size_t)rj * 16u + lane, o.sum);
+                        const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
+                        if (lane == 0) {
+                            if (!DOUT && bits) or16(out_rm, rj, bits);
+                            if (ST) c_bytes += 4u + by;
+                        }
+                        __syncwarp();
+                    }
+                    continue;
                 }
-                __syncwarp();
+                uint32_t nr = 0;
+                const RowOut o = hw_heavy(b, meta, act, wx, l, &nr);
+                const bool mine = two || h == 0u;
+                if (mine && o.touched) atomicAdd(y + (size_t)rb * 16u + l, o.sum);
+                const uint32_t bits = __ballot_sync(FULL, mine && o.touched);
+                if (!DOUT && l == 0 && mine && ((bits >> (16u * h)) & 0xFFFFu)) or16(out_rm, rb, (bits >> (16u * h)) & 0xFFFFu);
+                if (ST) {
+                    const uint32_t tot = __reduce_add_sync(FULL, mine ? nr : 0u);
+                    if (lane == 0) c_bytes += 8u + 32u + 4u * tot;
+                }
             }
         }
         __syncwarp();
@@ -1531,7 +1674,9 @@ void dbs_exec_opts_default(dbs_exec_opts *o)
     // n_vis / B = 0.45 (push 1.6x faster at 0.14 and 1.1x at 0.25, pull
     // 1.06x faster at 0.61 and 1.35x at 0.81); 0 selects the paper's th3 rule.
     o->push_work_frac = 0.45;
-    o->local_pull_min = 8;
+    // patched CSR always in row mode on GB300: its two dependent loads beat
+    // the column mode's four even at ~2 active columns per block (LLM weight)
+    o->local_pull_min = 0;
     o->collect_stats = 0;
     o->wait_timeout_ns = 2000000000LL;
 }

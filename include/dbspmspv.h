@@ -102,7 +102,8 @@ typedef struct {
                                   push_work_frac is 0 */
     int32_t local_pull_min;    /* patched-CSR blocks use the row-wise (pull) microkernel
                                   when popc(active block columns) >= this; else the
-                                  column-wise (push) one.  Unstated in the paper; 8. */
+                                  column-wise (push) one.  Unstated in the paper; default
+                                  0 (always row-wise: measured faster on GB300). */
     int32_t collect_stats;     /* 1: count visited / hit blocks, touched nnz and
                                   algorithmic bytes on the device (a few atomics per CTA) */
     int64_t wait_timeout_ns;   /* bound on every device-side wait (grid barriers);

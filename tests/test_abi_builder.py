@@ -48,7 +48,7 @@ def test_struct_layouts_match_header_sizes():
     o = dbs.build_opts()
     assert (o.th0, o.th1, o.th2, o.force_format) == (32, 128, 2.0, -1)
     e = dbs.exec_opts()
-    assert (e.th3, e.local_pull_min, e.push_work_frac) == (0.01, 8, 0.45)
+    assert (e.th3, e.local_pull_min, e.push_work_frac) == (0.01, 0, 0.45)
 
 
 def _host(A, **kw):
