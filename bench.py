@@ -238,6 +238,117 @@ def run_reference(args):
 ABLATION_FORMATS = (("auto", -1), ("coo", 0), ("force_csr", 2))
 
 
+def run_configs(dbs, torch, dev, stream, flush, reps: int):
+    """The other workloads at full size, default options (auto path): ER and
+    FEM plus-times SpMSpV, the LLM layer with dense and sparse activations,
+    and BFS on the grid with hubs.  Per line: median kernel µs over `reps`
+    calls (L2 flushed before each), touched nnz and algorithmic bytes from
+    one statistics call per input, touched-nnz/s, GB/s, share of HBM."""
+    import synth
+    peak, _ = _peaks()
+    lines = []
+
+    def timed(call, i):
+        flush(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3
+
+    def measure(name, mode, M, ws, calls, extra):
+        touched = bytes_alg = 0
+        paths = set()
+        ws.set_opts(dbs.exec_opts(collect_stats=1))
+        for c in calls:
+            c()
+            st = ws.stats()
+            touched += st["touched_nnz"]
+            bytes_alg += st["bytes_alg"]
+            paths.add({0: "-", 1: "push", 2: "pull"}.get(st["path"], "?"))
+        ws.set_opts(dbs.exec_opts(collect_stats=0))
+        for i in range(2):
+            timed(calls[i % len(calls)], i)
+        ts = [timed(calls[i % len(calls)], i) for i in range(reps)]
+        us = float(np.median(ts))
+        t_nnz, b_alg = touched / len(calls), bytes_alg / len(calls)
+        line = {"workload": name, "mode": mode, "path": "/".join(sorted(paths)), "us": round(us, 2),
+                "touched_nnz_per_s": round(t_nnz / us * 1e6), "gbs": round(b_alg / us / 1e3, 1),
+                "frac_of_measured_hbm": round(b_alg / us / 1e3 / peak, 4)}
+        line.update(extra)
+        lines.append(line)
+
+    # ER, plus-times, 1 % active
+    A = synth.config("er", "full")
+    M = dbs.DBMatrix.from_csr(A)
+    ws = dbs.Workspace(M)
+    y_idx = torch.empty(A.m, dtype=torch.int32, device=dev)
+    y_val = torch.empty(A.m, dtype=torch.float32, device=dev)
+    y_nnz = torch.empty(1, dtype=torch.int64, device=dev)
+    xs = [synth.x_uniform(A.n, 41, [43, i]) for i in range(8)]
+    xt = [(torch.from_numpy(x.idx).to(dev), torch.from_numpy(x.val).to(dev)) for x in xs]
+    measure("er", "spmspv x 1%", M, ws, [lambda xi=xi, xv=xv: dbs.spmspv(M, xi, xv, ws=ws, y_idx=y_idx, y_val=y_val,
+                                                                          y_nnz=y_nnz) for xi, xv in xt], {})
+    ws.close(); M.close()
+
+    # FEM, plus-times, clustered x
+    A = synth.config("fem", "full")
+    M = dbs.DBMatrix.from_csr(A)
+    ws = dbs.Workspace(M)
+    y_idx = torch.empty(A.m, dtype=torch.int32, device=dev)
+    y_val = torch.empty(A.m, dtype=torch.float32, device=dev)
+    for f in (0.001, 0.01, 0.1):
+        xs = [synth.x_clusters(A.n, f, [45, int(f * 1e4), i]) for i in range(4)]
+        xt = [(torch.from_numpy(x.idx).to(dev), torch.from_numpy(x.val).to(dev)) for x in xs]
+        measure("fem", f"spmspv x {f:g}", M, ws,
+                [lambda xi=xi, xv=xv: dbs.spmspv(M, xi, xv, ws=ws, y_idx=y_idx, y_val=y_val, y_nnz=y_nnz)
+                 for xi, xv in xt], {"density": f})
+    ws.close(); M.close()
+
+    # LLM layer: dense activations (decoding form) and the same as a sparse x
+    A = synth.config("llm", "full")
+    M = dbs.DBMatrix.from_csr(A)
+    ws = dbs.Workspace(M)
+    y = torch.empty(A.m, dtype=torch.float32, device=dev)
+    y_idx = torch.empty(A.m, dtype=torch.int32, device=dev)
+    y_val = torch.empty(A.m, dtype=torch.float32, device=dev)
+    xds = [synth.x_relu_topk(A.n, 1101, [46, t]) for t in range(8)]
+    xdt = [torch.from_numpy(xd).to(dev) for xd in xds]
+    measure("llm", "dense x (10% nonzero)", M, ws, [lambda x=x: dbs.spmspv_dense(M, x, y=y, ws=ws) for x in xdt], {})
+    sp = []
+    for xd in xds:
+        nz = np.nonzero(xd)[0].astype(np.int32)
+        sp.append((torch.from_numpy(nz).to(dev), torch.from_numpy(xd[nz]).to(dev)))
+    measure("llm", "sparse x (1,101 entries)", M, ws,
+            [lambda xi=xi, xv=xv: dbs.spmspv(M, xi, xv, ws=ws, y_idx=y_idx, y_val=y_val, y_nnz=y_nnz)
+             for xi, xv in sp], {})
+    ws.close(); M.close()
+
+    # grid with hubs: BFS
+    A = synth.config("grid", "full")
+    M = dbs.DBMatrix.from_csr(A)
+    ws = dbs.Workspace(M)
+    levels = torch.empty(A.n, dtype=torch.int32, device=dev)
+    deg = np.diff(A.row_ptr)
+    srcs = synth.bfs_sources(A, 8, [47, 7])
+    ts, teps, nls = [], [], []
+    for i, src in enumerate(srcs):
+        timed(lambda: dbs.bfs(M, int(src), levels=levels, ws=ws, sync=False), i)   # warm-up
+        t = timed(lambda: dbs.bfs(M, int(src), levels=levels, ws=ws, sync=False), i)
+        lv = levels.cpu().numpy()
+        edges = int(deg[lv >= 0].sum()) // 2
+        ts.append(t)
+        teps.append(edges / t * 1e6 / 1e9)
+        nls.append(int(lv.max()) + 1)
+    lines.append({"workload": "grid", "mode": "bfs (8 sources)", "us": round(float(np.median(ts)), 2),
+                  "gteps_harmonic": round(len(teps) / sum(1.0 / v for v in teps), 3),
+                  "levels_mean": float(np.mean(nls))})
+    assert ws.check() == 0
+    ws.close(); M.close()
+    return lines
+
+
 def run_ablation(dbs, torch, dev, stream, flush, reps: int):
     """Format ablation (the paper's Fig. 10 setting: pull at x density 0.1,
     plus push at 0.001): every block forced to COO or to ForceCSR, against
@@ -308,6 +419,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--path-sweep", type=int, default=8,
                     help="calls per density and forced path for the push/pull crossover table (0 = off)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the secondary lines for the ER, FEM, LLM and grid workloads")
     ap.add_argument("--ablation", type=int, default=0,
                     help="calls per point of the format ablation (Auto / COO-only / CSR-only on the "
                          "R-MAT, FEM and LLM workloads) and per-level frontier histograms (0 = off)")
@@ -539,6 +652,9 @@ def main():
         out["path_sweep"] = sweep
         out["bfs_path_sweep"] = bfs_sweep
         assert ws.check() == 0
+
+    if not args.no_configs:
+        out["other_workloads"] = run_configs(dbs, torch, dev, stream, flush, 10)
 
     if args.ablation > 0:
         out["ablation"] = run_ablation(dbs, torch, dev, stream, flush, args.ablation)

@@ -588,9 +588,9 @@ struct SmemT : SmemBase {
 };
 
 // Output rows staged per round by the compaction, in the warps' pull state
-// (index, and for plus-times the value, per row).
+// (the row index of each output entry).
 template <int SR>
-constexpr uint32_t STAGE_ROWS = (uint32_t)(sizeof(WarpPull<SR>) * NW / (SR == 0 ? 8u : 4u)) & ~31u;
+constexpr uint32_t STAGE_ROWS = (uint32_t)(sizeof(WarpPull<SR>) * NW / 4u) & ~31u;
 
 extern __shared__ __align__(128) unsigned char smem_raw[];
 
@@ -1247,7 +1247,6 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     // accumulator and the row masks are cleared for the next call on the way.
     __shared__ uint32_t s_base;
     uint32_t *stage_idx = reinterpret_cast<uint32_t *>(&S.wp[0]);
-    float *stage_val = reinterpret_cast<float *>(stage_idx + STAGE_ROWS<SR>);
     for (uint32_t ct = blockIdx.x; ct < P.n_ctiles; ct += gridDim.x) {
         const size_t wi = (size_t)ct * NT + tid;
         const uint32_t raw = __ldcg(P.yrm32 + wi);
@@ -1298,21 +1297,20 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
                 while (b) {
                     const uint32_t k = __ffs(b) - 1u;
                     b &= b - 1u;
-                    if (o >= r0 && o < r1) {
-                        const uint32_t row = (uint32_t)(2u * wi + (k >> 4)) * 16u + (k & 15u);
-                        stage_idx[o - r0] = row;
-                        if (SR == 0) {
-                            stage_val[o - r0] = __ldcg(P.y_acc + row);
-                            P.y_acc[row] = 0.0f;
-                        }
-                    }
+                    if (o >= r0 && o < r1) stage_idx[o - r0] = (uint32_t)(2u * wi + (k >> 4)) * 16u + (k & 15u);
                     ++o;
                 }
             }
             __syncthreads();
+            // all threads gather the values (rows ascend within the tile, so
+            // the accumulator reads are nearly contiguous) and store
             for (uint32_t i = tid; i < r1 - r0; i += NT) {
-                P.y_idx[base + r0 + i] = (int32_t)stage_idx[i];
-                if (SR == 0) P.y_val[base + r0 + i] = stage_val[i];
+                const uint32_t row = stage_idx[i];
+                P.y_idx[base + r0 + i] = (int32_t)row;
+                if (SR == 0) {
+                    P.y_val[base + r0 + i] = __ldcg(P.y_acc + row);
+                    P.y_acc[row] = 0.0f;
+                }
             }
             __syncthreads();
         }
