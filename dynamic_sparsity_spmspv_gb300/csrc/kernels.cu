@@ -102,7 +102,7 @@ struct KParams {
     uint32_t *xm32;           // sparse-x masks: zero between calls
     uint32_t *dxm32;          // dense-x masks: fully rewritten by every dense call
     uint32_t *act[3];
-    uint2 *chunks[3];
+    uint4 *chunks[3];         // push tasks {q0, q1, column block, 0}
     float *y_acc;
     uint32_t *yrm32;
     unsigned long long *ctile_flag;   // per compaction tile: epoch << 34 | state << 32 | count or prefix
@@ -268,6 +268,7 @@ __device__ __forceinline__ uint32_t push_chunk(unsigned long long work)
 struct ListStage {
     uint32_t cb[NT];
     uint32_t q0[NT];
+    uint32_t qe[NT];
     uint32_t cstart[NT + 1];
     uint32_t base_a, base_c;
 };
@@ -293,6 +294,7 @@ __device__ void cta_append(const KParams &P, ListStage &L, int slot, bool want, 
     if (want) {
         L.cb[oa] = cb;
         L.q0[oa] = s;
+        L.qe[oa] = e;
         L.cstart[oa] = oc;
     }
     __syncthreads();
@@ -303,7 +305,8 @@ __device__ void cta_append(const KParams &P, ListStage &L, int slot, bool want, 
             const uint32_t mid = (lo + hi + 1u) >> 1;
             if (L.cstart[mid] <= t) lo = mid; else hi = mid - 1u;
         }
-        P.chunks[slot][L.base_c + t] = make_uint2(L.q0[lo] + (t - L.cstart[lo]) * ch, L.cb[lo]);
+        const uint32_t q0 = L.q0[lo] + (t - L.cstart[lo]) * ch;
+        P.chunks[slot][L.base_c + t] = make_uint4(q0, min(q0 + ch, L.qe[lo]), L.cb[lo], 0u);
     }
     __syncthreads();
 }
@@ -942,16 +945,27 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
     float *wx = S.wx[warp];
     float *y = DOUT ? P.y_dense : P.y_acc;
     uint32_t c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
-    for (uint32_t ci = gw; ci < nch; ci += nwarps) {
-        const uint2 task = __ldcg(P.chunks[cslot] + ci);
-        const uint32_t q0 = task.x, c = task.y;
-        const uint32_t q1 = min(q0 + ch, __ldg(P.cb_ptr + c + 1));
-        uint2 d[WK];
+    // Software pipeline over a warp's tasks: the next task's descriptors are
+    // loaded while the current one is processed, and the task after that is
+    // fetched a round earlier still.
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+    auto load_desc = [&](const uint4 &tk, uint2 (&dd)[WK]) {
 #pragma unroll
         for (int k = 0; k < WK; ++k) {
-            const uint32_t q = q0 + (uint32_t)(k * 32 + lane);
-            d[k] = q < q1 ? __ldg(P.csc_desc + q) : make_uint2(0u, 0u);
+            const uint32_t q = tk.x + (uint32_t)(k * 32 + lane);
+            dd[k] = q < tk.y ? __ldg(P.csc_desc + q) : make_uint2(0u, 0u);
         }
+    };
+    uint32_t ci = gw;
+    uint4 tk = ci < nch ? __ldcg(P.chunks[cslot] + ci) : z4;
+    uint4 tk_n = ci + nwarps < nch ? __ldcg(P.chunks[cslot] + ci + nwarps) : z4;
+    uint2 d[WK];
+    load_desc(tk, d);
+    for (; ci < nch; ci += nwarps) {
+        const uint32_t q0 = tk.x, q1 = tk.y, c = tk.z;
+        const uint4 tk_nn = ci + 2u * nwarps < nch ? __ldcg(P.chunks[cslot] + ci + 2u * nwarps) : z4;
+        uint2 d_n[WK];
+        load_desc(tk_n, d_n);
         const uint32_t xmb = mask16(xm, c), mm = dup16(xmb);
         if (SR == 0 && lane < 16) {
             const size_t j = (size_t)c * 16u + lane;
@@ -1059,6 +1073,10 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             }
         }
         __syncwarp();
+        tk = tk_n;
+        tk_n = tk_nn;
+#pragma unroll
+        for (int k = 0; k < WK; ++k) d[k] = d_n[k];
     }
     if (ST) {
         stat_add(S, 0, c_vis);
@@ -1560,7 +1578,7 @@ struct dbs_workspace {
     uint32_t *xm32 = nullptr;
     uint32_t *dxm32 = nullptr;
     uint32_t *act[3] = {nullptr, nullptr, nullptr};
-    uint2 *chunks[3] = {nullptr, nullptr, nullptr};
+    uint4 *chunks[3] = {nullptr, nullptr, nullptr};
     float *y_acc = nullptr;
     uint32_t *yrm32 = nullptr;
     unsigned long long *ctile_flag = nullptr;
