@@ -95,22 +95,6 @@ DBS_HD uint32_t meta_pack_inline(const uint8_t *coords, uint32_t nnz)
 DBS_HD bool meta_inline(uint32_t m) { return (m & META_INLINE) != 0u; }
 DBS_HD uint32_t meta_fmt(uint32_t m) { return meta_inline(m) ? FMT_COO : (m >> 16) & 7u; }
 DBS_HD uint32_t meta_nnz(uint32_t m) { return meta_inline(m) ? ((m >> 24) & 3u) + 1u : ((m >> 19) & 0xFFu) + 1u; }
-DBS_HD uint32_t meta_cmask(uint32_t m)
-{
-    return meta_inline(m) ? (1u << (m & 15u)) | (1u << ((m >> 8) & 15u)) | (1u << ((m >> 16) & 15u))
-                          : m & 0xFFFFu;
-}
-// Rows of an inline block reached from the active columns `act`.
-DBS_HD uint32_t meta_inline_found(uint32_t m, uint32_t act)
-{
-    uint32_t f = 0;
-    for (uint32_t k = 0; k < 3u; ++k) {
-        const uint32_t e = (m >> (8u * k)) & 0xFFu;
-        f |= ((act >> (e & 15u)) & 1u) << (e >> 4);
-    }
-    return f;
-}
-
 // Section 3.3.2: Dense 4, ForceCSR / ForceCSC / (patched) CSR 2, COO 1.
 DBS_HD uint32_t fmt_weight(uint32_t fmt)
 {
