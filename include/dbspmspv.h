@@ -197,6 +197,9 @@ dbs_status dbs_workspace_set_opts(dbs_workspace *ws, const dbs_exec_opts *opts);
 dbs_status dbs_workspace_check(dbs_workspace *ws, void *stream);
 
 /* Sections 3.3.1-3.3.3 and 4.1: one SpMSpV y = A x with a sparse x.  ASYNC.
+ * "device" arrays below may also be pinned host memory mapped into the
+ * device's address space: the kernels then read x and write y there in place
+ * (on GB300, coherently over NVLink-C2C), which saves the staging copies.
  *   sr            DBS_PLUS_TIMES_F32 (matrix must be valued) or DBS_OR_AND_BOOL
  *   x_idx         device int32[x_nnz], unique indices in [0, n)
  *   x_val         device float32[x_nnz]; NULL = every listed index active

@@ -444,3 +444,33 @@ def test_tile_shapes_do_not_change_results(W, R):
     ws = dbs.Workspace(M)
     for x in _xs(A, True, 8)[2:]:
         assert_parity(A, O, M, ws, x, path="pull")
+
+
+@pytest.mark.parametrize("path", ["push", "pull"])
+def test_pinned_host_vectors_in_place(small, path):
+    # x read from and y written to pinned host memory by the kernels
+    A, O, M = small["fem"]
+    ws = dbs.Workspace(M)
+    x = synth.x_clusters(A.n, 0.05, [91, 1])
+    xi = torch.from_numpy(x.idx).pin_memory()
+    xv = torch.from_numpy(x.val).pin_memory()
+    yi = torch.empty(A.m, dtype=torch.int32).pin_memory()
+    yv = torch.empty(A.m, dtype=torch.float32).pin_memory()
+    yn = torch.empty(1, dtype=torch.int64).pin_memory()
+    dbs.spmspv(M, xi, xv, ws=ws, path=path, y_idx=yi, y_val=yv, y_nnz=yn)
+    torch.cuda.synchronize()
+    assert ws.check() == 0
+    k = int(yn.item())
+    ri, rv, rs = O.spmspv(x)
+    np.testing.assert_array_equal(yi[:k].numpy(), ri)
+    assert oracle.tolerance_ok(yv[:k].numpy(), rv, rs).all()
+    Ab, Ob, Mb = small["rmat"]
+    wb = dbs.Workspace(Mb)
+    xb = synth.x_uniform(Ab.n, Ab.n // 20, [91, 2], valued=False)
+    xbi = torch.from_numpy(xb.idx).pin_memory()
+    ybi = torch.empty(Ab.m, dtype=torch.int32).pin_memory()
+    dbs.spmspv(Mb, xbi, None, semiring="or_and", ws=wb, path=path, y_idx=ybi, y_nnz=yn)
+    torch.cuda.synchronize()
+    assert wb.check() == 0
+    ri, _, _ = Ob.spmspv(xb, oracle.OR_AND)
+    np.testing.assert_array_equal(ybi[:int(yn.item())].numpy(), ri)
