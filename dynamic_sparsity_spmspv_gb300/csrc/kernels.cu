@@ -266,39 +266,38 @@ __device__ __forceinline__ uint32_t push_chunk(unsigned long long work)
 // and then writes the tasks with all its threads, so a column block with
 // thousands of tasks does not serialise on one thread.
 struct ListStage {
-    uint32_t cb[NT];
-    uint32_t q0[NT];
-    uint32_t qe[NT];
-    uint32_t cstart[NT + 1];
+    uint32_t cb[2 * NT];
+    uint32_t q0[2 * NT];
+    uint32_t qe[2 * NT];
+    uint32_t cstart[2 * NT + 1];
     uint32_t base_a, base_c;
 };
 
-__device__ void cta_append(const KParams &P, ListStage &L, int slot, bool want, uint32_t cb, uint32_t ch)
+__device__ void cta_append(const KParams &P, ListStage &L, int slot, bool want0, uint32_t cb0, bool want1,
+                           uint32_t cb1, uint32_t ch)
 {
     const int tid = threadIdx.x;
-    uint32_t s = 0, e = 0;
-    if (want) {
-        s = __ldg(P.cb_ptr + cb);
-        e = __ldg(P.cb_ptr + cb + 1);
-    }
-    const uint32_t nch = want ? (e - s + ch - 1) / ch : 0u;
+    uint32_t s0 = 0, e0 = 0, s1 = 0, e1 = 0;
+    if (want0) { s0 = __ldg(P.cb_ptr + cb0); e0 = __ldg(P.cb_ptr + cb0 + 1); }
+    if (want1) { s1 = __ldg(P.cb_ptr + cb1); e1 = __ldg(P.cb_ptr + cb1 + 1); }
+    const uint32_t n0 = want0 ? (e0 - s0 + ch - 1) / ch : 0u, n1 = want1 ? (e1 - s1 + ch - 1) / ch : 0u;
     uint32_t tot_a, tot_c;
-    const uint32_t oa = block_excl_scan(want ? 1u : 0u, &tot_a);
-    const uint32_t oc = block_excl_scan(nch, &tot_c);
+    const uint32_t oa = block_excl_scan((want0 ? 1u : 0u) + (want1 ? 1u : 0u), &tot_a);
+    const uint32_t oc = block_excl_scan(n0 + n1, &tot_c);
     if (tot_a == 0u) return;
     if (tid == 0) {
         L.base_a = atomicAdd(&P.ctrl->n_act[slot], tot_a);
         L.base_c = tot_c ? atomicAdd(&P.ctrl->n_chunk[slot], tot_c) : 0u;
         L.cstart[tot_a] = tot_c;
     }
-    if (want) {
-        L.cb[oa] = cb;
-        L.q0[oa] = s;
-        L.qe[oa] = e;
-        L.cstart[oa] = oc;
+    if (want0) { L.cb[oa] = cb0; L.q0[oa] = s0; L.qe[oa] = e0; L.cstart[oa] = oc; }
+    if (want1) {
+        const uint32_t k = oa + (want0 ? 1u : 0u);
+        L.cb[k] = cb1; L.q0[k] = s1; L.qe[k] = e1; L.cstart[k] = oc + n0;
     }
     __syncthreads();
-    if (want) P.act[slot][L.base_a + oa] = cb;
+    if (want0) P.act[slot][L.base_a + oa] = cb0;
+    if (want1) P.act[slot][L.base_a + oa + (want0 ? 1u : 0u)] = cb1;
     for (uint32_t t = tid; t < tot_c; t += NT) {
         uint32_t lo = 0, hi = tot_a - 1u;       // last entry whose tasks start at or before t
         while (lo < hi) {
@@ -1189,8 +1188,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
             }
         }
         if (early_list) {
-            cta_append(P, S.L, slot, new_lo, 2u * (j >> 5), ch_early);
-            cta_append(P, S.L, slot, new_hi, 2u * (j >> 5) + 1u, ch_early);
+            cta_append(P, S.L, slot, new_lo, 2u * (j >> 5), new_hi, 2u * (j >> 5) + 1u, ch_early);
         }
     }
     cta_count(&P.ctrl->n_blk[slot], first);
@@ -1218,7 +1216,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
                         want = (mb & (0u - mb)) == (1u << (j & 15u));
                     }
                 }
-                cta_append(P, S.L, slot, want, j >> 4, ch);
+                cta_append(P, S.L, slot, want, j >> 4, false, 0u, ch);
             }
             if (!grid_sync(P)) return;
         }
@@ -1388,8 +1386,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
         for (uint32_t base = blockIdx.x * NT; base < nwords; base += gridDim.x * NT) {
             const uint32_t w = base + tid;
             const uint32_t bal = w < nwords ? __ldcg(P.dxm32 + w) : 0u;
-            cta_append(P, S.L, slot, (bal & 0xFFFFu) != 0u, 2u * w, ch);
-            cta_append(P, S.L, slot, (bal >> 16) != 0u, 2u * w + 1u, ch);
+            cta_append(P, S.L, slot, (bal & 0xFFFFu) != 0u, 2u * w, (bal >> 16) != 0u, 2u * w + 1u, ch);
         }
         if (!grid_sync(P)) return;
         push_tasks<0, true, ST>(P, S, P.dxm32, nullptr, nullptr, slot, ch);
@@ -1459,7 +1456,7 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
             P.ctrl->n_blk[0] = 1u;
             P.ctrl->n_vis[0] = cb_len(P, s >> 4);
         }
-        if (blockIdx.x == 0) cta_append(P, S.L, 0, tid == 0, s >> 4, push_chunk(cb_len(P, s >> 4)));
+        if (blockIdx.x == 0) cta_append(P, S.L, 0, tid == 0, s >> 4, false, 0u, push_chunk(cb_len(P, s >> 4)));
     }
     if (!grid_sync(P)) return;
     stamp(P, 1);
@@ -1488,8 +1485,7 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
                 for (uint32_t base = blockIdx.x * NT; base < nwords; base += gridDim.x * NT) {
                     const uint32_t w = base + tid;
                     const uint32_t fm = w < nwords ? __ldcg(fcur + w) : 0u;
-                    cta_append(P, S.L, cur, (fm & 0xFFFFu) != 0u, 2u * w, ch);
-                    cta_append(P, S.L, cur, (fm >> 16) != 0u, 2u * w + 1u, ch);
+                    cta_append(P, S.L, cur, (fm & 0xFFFFu) != 0u, 2u * w, (fm >> 16) != 0u, 2u * w + 1u, ch);
                 }
                 if (!grid_sync(P)) return;
             }
