@@ -260,6 +260,17 @@ def dbs_spmspv_dense_noalloc(A: DBMatrix, x, *, y, stream=None):
     return y
 
 
+def dbs_decode_layer(A: DBMatrix, x, tau: float = 0.0, *, y=None, ws: Workspace, stream=None):
+    """dbs_decode_layer: y = A x' with x' = x where |x| > tau, else 0 (dense
+    CUDA float32 x, 16-byte aligned) -> dense y, pull path, one launch."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(max(A.m, 1), dtype=torch.float32, device=x.device)
+    st = _lib.load().dbs_decode_layer(A.handle, _ptr(x), float(tau), _ptr(y), ws.handle, _stream_handle(stream))
+    _lib.check("dbs_decode_layer", st)
+    return y
+
+
 def dbs_bfs(A: DBMatrix, src: int, *, levels=None, path="auto", ws: Workspace, stream=None, sync: bool = True):
     """dbs_bfs: levels (int32 CUDA tensor, -1 unreached) and, with sync, the
     number of levels."""
@@ -276,6 +287,7 @@ def dbs_bfs(A: DBMatrix, src: int, *, levels=None, path="auto", ws: Workspace, s
 # short names
 spmspv = dbs_spmspv
 spmspv_dense = dbs_spmspv_dense
+decode_layer = dbs_decode_layer
 bfs = dbs_bfs
 
 

@@ -61,6 +61,7 @@ PROTOTYPES = {
     "dbs_spmspv": (I32, [P, ctypes.c_int, P, P, I64, P, P, P, P, ctypes.c_int, P, P]),
     "dbs_spmspv_dense": (I32, [P, P, P, ctypes.c_int, P, P]),
     "dbs_spmspv_dense_noalloc": (I32, [P, P, P, P]),
+    "dbs_decode_layer": (I32, [P, P, ctypes.c_float, P, P, P]),
     "dbs_bfs": (I32, [P, I64, P, P, ctypes.c_int, P, P]),
     "dbs_last_stats": (I32, [P, P, P]),
     "dbs_selftest_wait_timeout": (I32, [P, P]),

@@ -52,7 +52,7 @@ struct Ctrl {
     unsigned int tile_next[3];  // pull tiles handed out dynamically (tail of the static order)
     unsigned int bfs_levels;
     unsigned int bfs_push_levels;
-    unsigned int pad0;
+    unsigned int gen;           // launches on this control block; its parity picks the barrier counter
     unsigned long long x_active;
     unsigned long long visited;
     unsigned long long hits;
@@ -83,12 +83,14 @@ struct KParams {
     const uint4 *__restrict__ payload;
     const uint4 *__restrict__ tiles;
     const unsigned short *__restrict__ rb_rows;   // rows holding an entry, per row block
+    const uint32_t *__restrict__ rb_ntiles;       // pull tiles meeting a row block at an end of their span
     // call
     int path_force;
     const int32_t *x_idx;
     const float *x_val;
     long long x_nnz;
     const float *x_in;        // dense x (dense mode)
+    float tau;                // decoding: activation magnitude threshold
     const float *xv;          // x values read by the microkernels
     const uint32_t *uvis32;   // caller's visited mask (Boolean SpMSpV), or NULL
     int32_t *y_idx;
@@ -106,13 +108,11 @@ struct KParams {
     float *y_acc;
     uint32_t *yrm32;
     unsigned long long *ctile_flag;   // per compaction tile: epoch << 34 | state << 32 | count or prefix
+    uint32_t *rb_cnt;         // decoding: tiles done per shared row block (zero between calls)
     uint32_t n_ctiles;
     uint32_t *bvis32;
     uint32_t *fm32[2];
     Ctrl *ctrl;
-    int slot;                 // counter slot of this call (dense mode alternates 0/1)
-    int bslot;                // grid-barrier counter of this launch (launch parity)
-    uint32_t epoch;           // launch number (30 bits), tags the compaction flags
     double th3;
     double push_frac;
     int local_pull_min;
@@ -149,8 +149,10 @@ __device__ __forceinline__ uint32_t or16(uint32_t *w, uint32_t b, uint32_t bits)
 
 // Bounded grid barrier.  Returns false (and every caller must return) when
 // the wait timed out or another block latched an error.  Every launch owns
-// one of two 64-bit arrival counters (by launch parity) and clears the other
-// one for the launch after it.  Block b's k-th barrier adds 1 to the counter
+// one of two 64-bit arrival counters (by the parity of the launch count kept
+// in the control block) and clears the other one for the launch after it.
+// The count lives on the device, so a launch captured once in a CUDA graph
+// and replayed any number of times stays correct.  Block b's k-th barrier adds 1 to the counter
 // with a release (the block's writes, ordered before it by the block-wide
 // barrier, become visible first) and waits, with acquire loads, until the
 // counter reaches k * gridDim.x.  Arrival is fire-and-forget, so the last
@@ -170,24 +172,32 @@ __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long l
     return v;
 }
 __shared__ unsigned s_bar_epoch;
+__shared__ unsigned s_gen;   // this launch's number (the control block's count at entry)
 
-// Start of every kernel that uses grid_sync.
+// Start of every kernel that uses grid_sync (all threads call it).  Every
+// block reads the launch count before its first barrier arrival, and block 0
+// advances it only after that barrier, so all blocks see the same number.
 __device__ __forceinline__ void grid_sync_init(const KParams &P)
 {
     if (threadIdx.x == 0) {
         s_bar_epoch = 0u;
-        if (blockIdx.x == 0) {
-            P.ctrl->bar[P.bslot ^ 1][0] = 0ull;
-        }
+        s_gen = ld_cg(&P.ctrl->gen);
+        if (blockIdx.x == 0) P.ctrl->bar[(s_gen & 1u) ^ 1u][0] = 0ull;
     }
+    __syncthreads();
 }
+// Counter slot of a sparse-x or dense-x call: launches alternate slots.
+__device__ __forceinline__ int launch_slot() { return (int)(s_gen & 1u); }
+// Tag of this launch for the compaction flags: 1 .. 2^30 - 1, so flags left
+// zero never match.
+__device__ __forceinline__ unsigned long long launch_epoch() { return s_gen % 0x3FFFFFFFu + 1u; }
 __device__ bool grid_sync(const KParams &P)
 {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         Ctrl *c = P.ctrl;
-        unsigned long long *cnt = &c->bar[P.bslot][0];
+        unsigned long long *cnt = &c->bar[s_gen & 1u][0];
         const unsigned long long target = (unsigned long long)(++s_bar_epoch) * gridDim.x;
         int ok = 1;
         red_release_add(cnt, 1ull);
@@ -203,6 +213,7 @@ __device__ bool grid_sync(const KParams &P)
             }
         }
         if (ok && ld_cg(&c->err) != 0u) ok = 0;
+        if (ok && s_bar_epoch == 1u && blockIdx.x == 0) c->gen = s_gen + 1u;
         s_ok = ok;
     }
     __syncthreads();
@@ -272,6 +283,12 @@ struct ListStage {
     uint32_t cstart[2 * NT + 1];
     uint32_t base_a, base_c;
 };
+
+// The plus-times pull and push drains keep their (block, column) pair lists
+// in the list stage's memory, which is idle once the traversal starts: up to
+// 32 queued blocks x 16 columns per warp.
+constexpr uint32_t PAIRS_PER_ROUND = 32 * 16;
+static_assert(sizeof(ListStage) >= NW * PAIRS_PER_ROUND * sizeof(uint16_t), "pair lists must fit the list stage");
 
 __device__ void cta_append(const KParams &P, ListStage &L, int slot, bool want0, uint32_t cb0, bool want1,
                            uint32_t cb1, uint32_t ch)
@@ -523,6 +540,76 @@ __device__ __forceinline__ RowOut mk_heavy(const KParams &P, const uint8_t *b, u
     return o;
 }
 
+// Column-pair microkernel (plus-times; Dense, ForceCSR, ForceCSC and patched
+// CSR in row mode): one lane takes one active column c of one block and
+// forms the products a_rc * x_c of every row r holding an entry in column c
+// (acc[r], 0 for the other rows); returns those rows.  None of a pair's loads
+// depends on another, so a warp has the payload reads of 32 pairs in flight
+// together instead of walking a block's active columns one after another
+// (Algorithms 2-4 restated per (block, column) pair).
+__device__ __forceinline__ uint32_t pair_products(const uint8_t *__restrict__ b, uint32_t fmt, uint32_t nnz, uint32_t c,
+                                                  float xc, float (&acc)[16])
+{
+    const float *vals = reinterpret_cast<const float *>(b + val_offset(fmt, nnz));
+    uint32_t rows = 0;
+    if (fmt == FMT_DENSE) {
+        // column c's 16 values are one 64-byte run (absent entries hold 0 and
+        // are excluded by the column mask, so no 0 * inf can appear)
+        rows = __ldg(reinterpret_cast<const uint16_t *>(b) + c);
+        const float4 *v4 = reinterpret_cast<const float4 *>(vals + c * 16u);
+        float v[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 t = __ldg(v4 + q);
+            v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) acc[r] = ((rows >> r) & 1u) ? v[r] * xc : 0.0f;
+    } else if (fmt == FMT_FCSC) {
+        rows = __ldg(reinterpret_cast<const uint16_t *>(b + OFF_MASK) + c);
+        const uint32_t cp = __ldg(b + OFF_PTR + c);
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            acc[r] = ((rows >> r) & 1u) ? __ldg(vals + cp + __popc(rows & ((1u << r) - 1u))) * xc : 0.0f;
+    } else {
+        // row layouts: row_ptr u8[16] at 0, row_mask u16[16] at 16
+        const uint4 *b4 = reinterpret_cast<const uint4 *>(b);
+        const uint4 rp = __ldg(b4), m0 = __ldg(b4 + 1), m1 = __ldg(b4 + 2);
+        const uint32_t rpw[4] = {rp.x, rp.y, rp.z, rp.w};
+        const uint32_t mw[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        const uint32_t below = (1u << c) - 1u;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const uint32_t rm = (mw[r >> 1] >> ((r & 1) * 16)) & 0xFFFFu;
+            const uint32_t base = (rpw[r >> 2] >> ((r & 3) * 8)) & 0xFFu;
+            const bool has = (rm >> c) & 1u;
+            rows |= (has ? 1u : 0u) << r;
+            acc[r] = has ? __ldg(vals + base + __popc(rm & below)) * xc : 0.0f;
+        }
+    }
+    return rows;
+}
+
+// Sum over the warp of acc[r] from the lanes with `in` set (transpose
+// reduction: each step halves the rows a lane keeps and adds its partner's
+// share).  Returns row (lane >> 1) & 15's total on lanes 2r and 2r + 1.
+__device__ __forceinline__ float warp_rows_sum(const float (&acc)[16], bool in, int lane)
+{
+    const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1;
+    float v8[8], v4[4], v2[2];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float lo = in ? acc[j] : 0.0f, hi = in ? acc[j + 8] : 0.0f;
+        v8[j] = (b4 ? hi : lo) + __shfl_xor_sync(FULL, b4 ? lo : hi, 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v4[j] = (b3 ? v8[j + 4] : v8[j]) + __shfl_xor_sync(FULL, b3 ? v8[j] : v8[j + 4], 8);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) v2[j] = (b2 ? v4[j + 2] : v4[j]) + __shfl_xor_sync(FULL, b2 ? v4[j] : v4[j + 2], 4);
+    float v = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(FULL, b1 ? v2[0] : v2[1], 2);
+    return v + __shfl_xor_sync(FULL, v, 1);
+}
+
 // COO block, one lane: scan the packed coordinates (Section 3.3.3).  Adds the
 // products through `add(row, value)` and returns the touched-row bits.  The
 // entries go in groups of four, whose value and x loads are all issued
@@ -568,9 +655,12 @@ __device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint
 // the Boolean variant does not.
 template <int SR>
 struct WarpPull {
-    uint32_t qe[TILE_MAX_BLOCKS];     // queued hits with a payload: li | lrb << 8 | act << 16
-    uint32_t qm[TILE_MAX_BLOCKS];     // their meta words
-    uint32_t qr[TILE_MAX_BLOCKS];     // push: their row blocks
+    // Queued hits with a payload.  Boolean pull: qe = li | lrb << 8 | act << 16,
+    // qm = meta.  Plus-times pull: qe = act | fmt << 16 | (nnz - 1) << 19 |
+    // lrb << 27, qm = column block, qr = payload offset.  Push: see push_tasks.
+    uint32_t qe[TILE_MAX_BLOCKS];
+    uint32_t qm[TILE_MAX_BLOCKS];
+    uint32_t qr[TILE_MAX_BLOCKS];
     uint32_t rm[TILE_MAX_SPAN];       // touched (Boolean: found) rows per row block
     uint32_t nq;                      // queued COO hits, from the front
     uint32_t nq2;                     // queued hits of the other formats, from the back
@@ -668,6 +758,95 @@ __device__ __forceinline__ void bool_load(const uint4 *b4, uint32_t fmt, uint32_
     u1 = (fmt != FMT_COO || nnz > 16u) ? __ldg(b4 + s + 1) : make_uint4(0u, 0u, 0u, 0u);
 }
 
+// Plus-times drain of a pull tile's queued hits (the queue layout of
+// WarpPull for plus-times): COO hits one per lane, the other formats as
+// (block, active column) pairs, patched-CSR blocks in column mode by the
+// whole warp.  Row sums go to the warp's row accumulators W.y / W.rm.
+template <bool ST>
+__device__ __forceinline__ void pt_drain(const KParams &P, SmemT<0> &S, WarpPull<0> &W, int warp, int lane,
+                                         uint32_t nq, const float *xv, uint32_t &c_bytes)
+{
+    const uint32_t nq2 = W.nq2;
+    auto q_nnz = [](uint32_t e) { return ((e >> 19) & 0xFFu) + 1u; };
+    // COO hits one per lane
+    for (uint32_t i = lane; i < nq; i += 32) {
+        const uint32_t e = W.qe[i], lrb = e >> 27, nnz = q_nnz(e);
+        float *sy = &W.y[lrb * 16u];
+        const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + W.qr[i]);
+        const uint32_t rows = coo_lane(b, nnz, e & 0xFFFFu, xv + (size_t)W.qm[i] * 16u, true,
+                                       [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
+        if (rows) atomicOr(&W.rm[lrb], rows);
+        if (ST) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
+    }
+    __syncwarp();
+    // the other formats: every (block, active column) pair is one
+    // lane's work, in rounds of up to 32 queued blocks; the pairs' row
+    // products are summed per row block by the warp.  Patched-CSR
+    // blocks in column mode take the whole-warp microkernel after.
+    uint16_t *pl = reinterpret_cast<uint16_t *>(&S.L) + warp * PAIRS_PER_ROUND;
+    bool any_col_mode = false;
+    for (uint32_t g0 = 0; g0 < nq2; g0 += 32) {
+        uint32_t act = 0;
+        if (g0 + lane < nq2) {
+            const uint32_t e = W.qe[TILE_MAX_BLOCKS - 1u - g0 - lane], fmt = (e >> 16) & 7u;
+            act = e & 0xFFFFu;
+            if (fmt == FMT_PCSR && (int)__popc(act) < P.local_pull_min) { act = 0; any_col_mode = true; }
+            if (ST && act) c_bytes += 4u + (fmt == FMT_DENSE ? 32u : 48u);
+        }
+        const uint32_t np = __popc(act), incl = warp_incl_scan(np, lane);
+        const uint32_t tot = __shfl_sync(FULL, incl, 31);
+        for (uint32_t o = incl - np; act; act &= act - 1u) pl[o++] = (uint16_t)((lane << 4) | (__ffs(act) - 1u));
+        __syncwarp();
+        for (uint32_t q0 = 0; q0 < tot; q0 += 32) {
+            const bool in = q0 + lane < tot;
+            float acc[16];
+            uint32_t rows = 0, lrb = 0;
+            if (in) {
+                const uint32_t pe = pl[q0 + lane], c = pe & 15u;
+                const uint32_t k = TILE_MAX_BLOCKS - 1u - g0 - (pe >> 4), e = W.qe[k], fmt = (e >> 16) & 7u;
+                lrb = e >> 27;
+                const float xc = xval(xv + (size_t)W.qm[k] * 16u, c);
+                rows = pair_products(reinterpret_cast<const uint8_t *>(P.payload + W.qr[k]), fmt, q_nnz(e), c, xc,
+                                     acc);
+                if (ST) c_bytes += fmt == FMT_DENSE ? 64u : 4u * __popc(rows);
+            } else {
+#pragma unroll
+                for (int r = 0; r < 16; ++r) acc[r] = 0.0f;
+            }
+            // one row block at a time (a tile's pairs mostly share one)
+            for (uint32_t pend = __ballot_sync(FULL, in); pend;) {
+                const uint32_t g = __shfl_sync(FULL, lrb, __ffs(pend) - 1);
+                const bool mine = in && lrb == g;
+                pend &= ~__ballot_sync(FULL, mine);
+                const float sum = warp_rows_sum(acc, mine, lane);
+                const uint32_t bits = __reduce_or_sync(FULL, mine ? rows : 0u), r = (lane >> 1) & 15u;
+                if (!(lane & 1) && ((bits >> r) & 1u)) W.y[g * 16u + r] += sum;
+                if (lane == 0 && bits) W.rm[g] |= bits;
+                __syncwarp();
+            }
+        }
+    }
+    if (__any_sync(FULL, any_col_mode)) {
+        for (uint32_t i = 0; i < nq2; ++i) {
+            const uint32_t k = TILE_MAX_BLOCKS - 1u - i;
+            const uint32_t e = W.qe[k], act = e & 0xFFFFu, lj = e >> 27;
+            const uint32_t meta = meta_pack(act, (e >> 16) & 7u, q_nnz(e));
+            if (!needs_col_mode(P, meta, act)) continue;
+            const float *xj = xv + (size_t)W.qm[k] * 16u;
+            uint32_t by = 0;
+            RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + W.qr[k]), meta, act, xj, lane,
+                                S.wacc[warp], &by);
+            if (lane < 16 && o.touched) W.y[lj * 16u + lane] += o.sum;
+            const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
+            if (lane == 0) {
+                if (bits) W.rm[lj] |= bits;
+                if (ST) c_bytes += 4u + by;
+            }
+            __syncwarp();
+        }
+    }
+}
+
 // Pull (Section 3.3.2): every warp takes tiles of consecutive primary blocks
 // (load-weighted segments of at most 256 blocks and 32 row blocks) and works
 // through them without block-wide synchronisation.
@@ -759,10 +938,21 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             const uint32_t b = l1 < nblk ? (uint32_t)__ldca(xm16 + (d[2 * j + 1].x & DESC_COL_MASK)) : 0u;
             mm[j] = a | (b << 16);
         }
+        // plus-times: every block carries a payload, and pull runs when most
+        // blocks are visited, so the payload offsets go out with the mask
+        // lookups (one memory round trip for both)
+        uint32_t rf[SR == 0 ? WK : 1];
+        if (SR == 0) {
+#pragma unroll
+            for (int k = 0; k < WK; ++k) {
+                const uint32_t li = (uint32_t)(k * 32 + lane);
+                rf[k] = li < nblk ? __ldg(P.blk_ref + p0 + li) : 0u;
+            }
+        }
         uint32_t vrow_n = 0;
         if (SR == 1 && vis) settle(t_n, td_n, vrow_n);
         uint2 d_n[WK];
-        load_desc(td_n, d_n);
+        if (SR == 1) load_desc(td_n, d_n);   // plus-times: after the queue (fewer live registers)
         __syncwarp();
 #pragma unroll
         for (int k = 0; k < WK; ++k) {
@@ -783,18 +973,26 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             if (a) {
                 // COO hits from the front of the queue, the others from the
                 // back, so drain rounds run one decoder each
-                const bool back = meta_fmt(meta) != FMT_COO;
+                const uint32_t fmt = meta_fmt(meta);
+                const bool back = fmt != FMT_COO;
                 const uint32_t slot = back ? TILE_MAX_BLOCKS - 1u - atomicAdd(&W.nq2, 1u) : atomicAdd(&W.nq, 1u);
-                W.qe[slot] = li | (lrb << 8) | (a << 16);
-                W.qm[slot] = meta;
+                if (SR == 1) {
+                    W.qe[slot] = li | (lrb << 8) | (a << 16);
+                    W.qm[slot] = meta;
+                } else {
+                    W.qe[slot] = a | (fmt << 16) | ((meta_nnz(meta) - 1u) << 19) | (lrb << 27);
+                    W.qm[slot] = d[k].x & DESC_COL_MASK;
+                    W.qr[slot] = rf[SR == 0 ? k : 0];
+                }
                 if (ST) ++c_hit;
             }
         }
+        if (SR == 0) load_desc(td_n, d_n);
         __syncwarp();
 
         // payload-carrying hits
         const uint32_t nq = W.nq;
-        if (SR == 1) {
+        if constexpr (SR == 1) {
             // COO hits (front of the queue), then the mask formats (back)
             for (uint32_t i = lane; i < nq; i += 32) {
                 const uint32_t e = W.qe[i], nnz = meta_nnz(W.qm[i]);
@@ -818,71 +1016,7 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 if (ST) c_bytes += 4u + 32u;
             }
         } else {
-            // payload offsets of all hits first (independent loads), so each
-            // block below waits for its payload only
-            const uint32_t nq2 = W.nq2;
-            for (uint32_t i = lane; i < nq; i += 32) W.qr[i] = __ldg(P.blk_ref + p0 + (W.qe[i] & 0xFFu));
-            for (uint32_t i = lane; i < nq2; i += 32) {
-                const uint32_t k = TILE_MAX_BLOCKS - 1u - i;
-                W.qr[k] = __ldg(P.blk_ref + p0 + (W.qe[k] & 0xFFu));
-            }
-            __syncwarp();
-            // COO hits one per lane
-            for (uint32_t i = lane; i < nq; i += 32) {
-                const uint32_t e = W.qe[i], meta = W.qm[i];
-                const uint32_t p = p0 + (e & 0xFFu), lrb = (e >> 8) & 0xFFu, nnz = meta_nnz(meta);
-                const uint32_t col = __ldg(&P.blk_desc[p].x) & DESC_COL_MASK;
-                float *sy = &W.y[lrb * 16u];
-                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + W.qr[i]);
-                const uint32_t rows = coo_lane(b, nnz, e >> 16, xv + (size_t)col * 16u, true,
-                                               [&](uint32_t r, float v) { atomicAdd(&sy[r], v); });
-                if (rows) atomicOr(&W.rm[lrb], rows);
-                if (ST) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
-            }
-            __syncwarp();
-            // the other formats two at a time, one block per half-warp (a
-            // patched-CSR block in column mode takes the whole warp)
-            const uint32_t l = lane & 15u, h = lane >> 4;
-            for (uint32_t i = 0; i < nq2; i += 2) {
-                const bool two = i + 1u < nq2;
-                const uint32_t k = TILE_MAX_BLOCKS - 1u - i - (h & (two ? 1u : 0u));
-                const uint32_t e = W.qe[k], meta = W.qm[k], act = e >> 16;
-                const uint32_t p = p0 + (e & 0xFFu), lrb = (e >> 8) & 0xFFu;
-                const float *xb = xv + (size_t)(__ldg(&P.blk_desc[p].x) & DESC_COL_MASK) * 16u;
-                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + W.qr[k]);
-                if (__any_sync(FULL, needs_col_mode(P, meta, act))) {
-                    // one block at a time with the whole warp
-                    for (uint32_t j = 0; j < (two ? 2u : 1u); ++j) {
-                        const uint32_t kj = TILE_MAX_BLOCKS - 1u - i - j;
-                        const uint32_t ej = W.qe[kj], mj = W.qm[kj], lj = (ej >> 8) & 0xFFu;
-                        const float *xj = xv + (size_t)(__ldg(&P.blk_desc[p0 + (ej & 0xFFu)].x) & DESC_COL_MASK) * 16u;
-                        uint32_t by = 0;
-                        RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + W.qr[kj]), mj, ej >> 16,
-                                            xj, lane, S.wacc[warp], &by);
-                        if (lane < 16 && o.touched) W.y[lj * 16u + lane] += o.sum;
-                        const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
-                        if (lane == 0) {
-                            if (bits) W.rm[lj] |= bits;
-                            if (ST) c_bytes += 4u + by;
-                        }
-                        __syncwarp();
-                    }
-                    continue;
-                }
-                uint32_t nr = 0;
-                const RowOut o = hw_heavy(b, meta, act, xb, l, &nr);
-                // half 0 then half 1 (their row blocks may coincide)
-                const uint32_t bits = __ballot_sync(FULL, o.touched);
-                for (uint32_t hh = 0; hh < (two ? 2u : 1u); ++hh) {
-                    if (h == hh && o.touched) W.y[lrb * 16u + l] += o.sum;
-                    if (lane == 16u * hh && ((bits >> (16u * hh)) & 0xFFFFu)) W.rm[lrb] |= (bits >> (16u * hh)) & 0xFFFFu;
-                    __syncwarp();
-                }
-                if (ST) {
-                    const uint32_t tot = __reduce_add_sync(FULL, (two || h == 0) ? nr : 0u);
-                    if (lane == 0) c_bytes += 8u + 32u + 4u * tot;
-                }
-            }
+            pt_drain<ST>(P, S, W, warp, lane, nq, xv, c_bytes);
         }
         __syncwarp();
 
@@ -1139,7 +1273,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
     if (ld_cg(&P.ctrl->err) != 0u) return;
     const int tid = threadIdx.x;
     const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
-    const int slot = P.slot;
+    const int slot = launch_slot();
     stats_begin(S);
     if (blockIdx.x == 0 && tid == 0 && ST) reset_stats(P);
     stamp(P, 0);
@@ -1273,7 +1407,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
             // warp 0 looks back over windows of 32 predecessors (lane l reads
             // tile j - l) until one has published its prefix
             const int lane = tid;
-            const unsigned long long tag = (unsigned long long)P.epoch << 34;
+            const unsigned long long epoch = launch_epoch(), tag = epoch << 34;
             if (lane == 0) st_release64(P.ctile_flag + ct, tag | (1ull << 32) | tile_tot);   // count published
             uint32_t base = 0;
             bool ok = true;
@@ -1282,7 +1416,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
                 const int idx = j - lane;
                 unsigned long long f = 0;
                 if (idx >= 0) {
-                    while (((f = ld_acquire64(P.ctile_flag + idx)) >> 34) != (unsigned long long)P.epoch) {
+                    while (((f = ld_acquire64(P.ctile_flag + idx)) >> 34) != epoch) {
                         if ((long long)(globaltimer() - t0) > P.timeout_ns) { ok = false; break; }
                     }
                 }
@@ -1351,7 +1485,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
     if (ld_cg(&P.ctrl->err) != 0u) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t gtid = (size_t)blockIdx.x * NT + tid, gsz = (size_t)gridDim.x * NT;
-    const int slot = P.slot;
+    const int slot = launch_slot();
     stats_begin(S);
     if (blockIdx.x == 0 && tid == 0 && ST) reset_stats(P);
     stamp(P, 0);
@@ -1393,6 +1527,7 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_dense(KParams P)
     } else {
         pull_tiles<0, true, ST>(P, S, P.dxm32, nullptr, nullptr, slot);
     }
+    stamp(P, 2);
     stats_flush(P, S);
     if (blockIdx.x == 0 && tid == 0) {
         Ctrl *c = P.ctrl;
@@ -1549,6 +1684,124 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
     stamp(P, 3);
 }
 
+// DB-Decoding layer (Section 4.3; the mask generation of Section 4.1 moved
+// into the traversal): y = A x' with x'_j = x_j where |x_j| > tau (NaN is
+// kept) and 0 elsewhere -- magnitude thresholding of the activation -- on
+// the pull path, in one ordinary launch.  Warp w takes pull tile w; each
+// lane forms the activation masks of its blocks' column blocks directly
+// from x, so neither a metadata pass nor a device-wide barrier precedes the
+// traversal.  A row block inside one tile is stored whole (rows without an
+// active entry get 0); a row block split between tiles collects their
+// partial sums in the workspace accumulator with atomics, and the tile that
+// arrives last (a counter per row block) stores it and clears accumulator
+// and counter for the next call.  Row blocks without entries belong to no
+// tile's work and are zeroed up front.
+__device__ __forceinline__ uint32_t act_mask(const float *__restrict__ x, uint32_t col, int n, float tau)
+{
+    const size_t j0 = (size_t)col * 16u;
+    uint32_t m = 0;
+    if (j0 + 16u <= (size_t)n) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(x + j0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 v = __ldg(x4 + q);
+            m |= (!(fabsf(v.x) <= tau) ? 1u : 0u) << (4 * q);
+            m |= (!(fabsf(v.y) <= tau) ? 1u : 0u) << (4 * q + 1);
+            m |= (!(fabsf(v.z) <= tau) ? 1u : 0u) << (4 * q + 2);
+            m |= (!(fabsf(v.w) <= tau) ? 1u : 0u) << (4 * q + 3);
+        }
+    } else {
+        for (uint32_t c = 0; c < 16u; ++c)
+            if (j0 + c < (size_t)n && !(fabsf(__ldg(x + j0 + c)) <= tau)) m |= 1u << c;
+    }
+    return m;
+}
+
+__global__ void __launch_bounds__(NT, 4) k_decode(KParams P)
+{
+    constexpr int WK = 8;
+    SmemT<0> &S = *reinterpret_cast<SmemT<0> *>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (uint32_t rb = blockIdx.x * NT + tid; rb < (uint32_t)P.nbr; rb += gridDim.x * NT) {
+        if (__ldg(P.rb_rows + rb) != 0u) continue;
+        for (uint32_t r = 0; r < 16u; ++r) {
+            const size_t row = (size_t)rb * 16u + r;
+            if (row < (size_t)P.m) P.y_dense[row] = 0.0f;
+        }
+    }
+    const uint32_t t = blockIdx.x * NW + warp;
+    if (t >= P.T) return;
+    WarpPull<0> &W = S.wp[warp];
+    const uint4 td = __ldg(P.tiles + t);
+    const uint32_t p0 = td.x, rb0 = td.z, span = td.w & TILE_SPAN_MASK, nblk = td.w >> TILE_NBLK_SHIFT;
+    uint2 d[WK];
+    uint32_t rf[WK];
+#pragma unroll
+    for (int k = 0; k < WK; ++k) {
+        const uint32_t li = (uint32_t)(k * 32 + lane);
+        d[k] = li < nblk ? __ldcs(P.blk_desc + p0 + li) : make_uint2(0u, 0u);
+        rf[k] = li < nblk ? __ldg(P.blk_ref + p0 + li) : 0u;
+    }
+    if (lane < (int)span) W.rm[lane] = 0u;
+    for (uint32_t i = lane; i < span * 16u; i += 32) W.y[i] = 0.0f;
+    if (lane == 0) { W.nq = 0u; W.nq2 = 0u; }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < WK; ++k) {
+        const uint32_t li = (uint32_t)(k * 32 + lane);
+        if (li >= nblk) continue;
+        const uint32_t col = d[k].x & DESC_COL_MASK, meta = d[k].y, lrb = d[k].x >> DESC_LRB_SHIFT;
+        const uint32_t a = act_mask(P.x_in, col, P.n, P.tau) & meta & 0xFFFFu;
+        if (a) {
+            const uint32_t fmt = meta_fmt(meta);
+            const uint32_t slot = fmt != FMT_COO ? TILE_MAX_BLOCKS - 1u - atomicAdd(&W.nq2, 1u) : atomicAdd(&W.nq, 1u);
+            W.qe[slot] = a | (fmt << 16) | ((meta_nnz(meta) - 1u) << 19) | (lrb << 27);
+            W.qm[slot] = col;
+            W.qr[slot] = rf[k];
+        }
+    }
+    __syncwarp();
+    uint32_t c_bytes = 0;
+    pt_drain<false>(P, S, W, warp, lane, W.nq, P.x_in, c_bytes);
+    __syncwarp();
+
+    const uint32_t nt0 = __ldg(P.rb_ntiles + rb0), nt1 = span > 1u ? __ldg(P.rb_ntiles + rb0 + span - 1u) : nt0;
+    for (uint32_t i = lane; i < span * 16u; i += 32) {
+        const uint32_t lrb = i >> 4, r = i & 15u;
+        const size_t row = (size_t)(rb0 + lrb) * 16u + r;
+        const uint32_t nt = lrb == 0u ? nt0 : (lrb == span - 1u ? nt1 : 1u);
+        if (nt > 1u) {
+            if ((W.rm[lrb] >> r) & 1u) atomicAdd(P.y_acc + row, W.y[i]);
+        } else if (row < (size_t)P.m) {
+            P.y_dense[row] = W.y[i];
+        }
+    }
+    if (nt0 > 1u || nt1 > 1u) {
+        __threadfence();                 // every lane's partial sums before the counter
+        __syncwarp();
+        bool last = false;
+        if (lane < 2 && (lane == 0 || span > 1u)) {
+            const uint32_t nt = lane == 0 ? nt0 : nt1;
+            if (nt > 1u) last = atomicAdd(P.rb_cnt + rb0 + (lane == 0 ? 0u : span - 1u), 1u) == nt - 1u;
+        }
+        const uint32_t lm = __ballot_sync(FULL, last);
+        if (lm) {
+            __threadfence();
+            for (uint32_t h = 0; h < 2u; ++h) {
+                if (!((lm >> h) & 1u)) continue;
+                const uint32_t rb = rb0 + (h ? span - 1u : 0u);
+                if (lane < 16) {
+                    const size_t row = (size_t)rb * 16u + lane;
+                    const float v = __ldcg(P.y_acc + row);
+                    P.y_acc[row] = 0.0f;
+                    if (row < (size_t)P.m) P.y_dense[row] = v;
+                }
+                if (lane == 0) P.rb_cnt[rb] = 0u;
+            }
+        }
+    }
+}
+
 // Withholds block 0 from the barrier so every other block's wait expires.
 __global__ void __launch_bounds__(NT, 5) k_selftest_wait(KParams P)
 {
@@ -1567,8 +1820,7 @@ struct dbs_workspace {
     int sms = 0;
     int grid_sparse[2][2] = {{0, 0}, {0, 0}};   // [semiring][statistics]
     int grid_dense[2] = {0, 0}, grid_bfs[2] = {0, 0};
-    int call_count = 0;
-    unsigned launches = 0;      // launches made; its parity picks the grid-barrier counter
+    bool decode_ok = false;
     dbs_exec_opts opts{};
     float *x_dense = nullptr;
     uint32_t *xm32 = nullptr;
@@ -1578,6 +1830,7 @@ struct dbs_workspace {
     float *y_acc = nullptr;
     uint32_t *yrm32 = nullptr;
     unsigned long long *ctile_flag = nullptr;
+    uint32_t *rb_cnt = nullptr;
     uint32_t n_ctiles = 0;
     uint32_t *bvis32 = nullptr;
     uint32_t *fm32[2] = {nullptr, nullptr};
@@ -1590,7 +1843,7 @@ namespace {
 void ws_free(dbs_workspace *w)
 {
     cudaFree(w->x_dense); cudaFree(w->xm32); cudaFree(w->dxm32); cudaFree(w->y_acc); cudaFree(w->yrm32);
-    cudaFree(w->ctile_flag); cudaFree(w->bvis32); cudaFree(w->fm32[0]); cudaFree(w->fm32[1]);
+    cudaFree(w->ctile_flag); cudaFree(w->rb_cnt); cudaFree(w->bvis32); cudaFree(w->fm32[0]); cudaFree(w->fm32[1]);
     cudaFree(w->ctrl);
     for (int s = 0; s < 3; ++s) { cudaFree(w->act[s]); cudaFree(w->chunks[s]); }
 }
@@ -1618,9 +1871,11 @@ KParams make_params(const dbs_matrix *A, dbs_workspace *w)
     P.payload = reinterpret_cast<const uint4 *>(A->d_payload);
     P.tiles = reinterpret_cast<const uint4 *>(A->d_tiles);
     P.rb_rows = A->d_rb_rows;
+    P.rb_ntiles = A->d_rb_ntiles;
     P.x_dense = w->x_dense; P.xm32 = w->xm32; P.dxm32 = w->dxm32;
     for (int s = 0; s < 3; ++s) { P.act[s] = w->act[s]; P.chunks[s] = w->chunks[s]; }
     P.y_acc = w->y_acc; P.yrm32 = w->yrm32; P.ctile_flag = w->ctile_flag; P.n_ctiles = w->n_ctiles;
+    P.rb_cnt = w->rb_cnt;
     P.bvis32 = w->bvis32; P.fm32[0] = w->fm32[0]; P.fm32[1] = w->fm32[1];
     P.ctrl = w->ctrl;
     P.th3 = w->opts.th3;
@@ -1641,15 +1896,11 @@ dbs_status launch(const void *fn, int grid, KParams &P, cudaStream_t s, size_t s
     return DBS_OK;
 }
 
-// A workspace launch: launches alternate the grid-barrier counter, and the
-// parity advances only when the kernel was actually queued.
-dbs_status launch_ws(dbs_workspace *w, const void *fn, int grid, KParams &P, cudaStream_t s, size_t smem)
+// A workspace launch (the launch count that picks the barrier counter and
+// the counter slot is kept on the device).
+dbs_status launch_ws(dbs_workspace *, const void *fn, int grid, KParams &P, cudaStream_t s, size_t smem)
 {
-    P.bslot = (int)(w->launches & 1u);
-    P.epoch = w->launches % 0x3FFFFFFFu + 1u;      // 1 .. 2^30 - 1; zeroed flags never match
-    const dbs_status st = launch(fn, grid, P, s, smem);
-    if (st == DBS_OK) w->launches++;
-    return st;
+    return launch(fn, grid, P, s, smem);
 }
 
 int coop_grid(const void *fn, int sms, size_t smem)
@@ -1713,7 +1964,8 @@ dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
     bool ok = dalloc(&w->x_dense, nbc * 16 + 16) && dalloc(&w->xm32, nbc / 2 + 8) &&
               dalloc(&w->dxm32, nbc / 2 + 8) &&
               dalloc(&w->y_acc, nbr * 16 + 16) && dalloc(&w->yrm32, yrm_words) &&
-              dalloc(&w->ctile_flag, (size_t)w->n_ctiles + 1) && dalloc(&w->bvis32, nbr / 2 + 8) &&
+              dalloc(&w->ctile_flag, (size_t)w->n_ctiles + 1) && dalloc(&w->rb_cnt, nbr + 1) &&
+              dalloc(&w->bvis32, nbr / 2 + 8) &&
               dalloc(&w->fm32[0], nbc / 2 + 8) && dalloc(&w->fm32[1], nbc / 2 + 8) && dalloc(&w->ctrl, 1);
     for (int s = 0; s < 3 && ok; ++s) ok = dalloc(&w->act[s], nbc + 1) && dalloc(&w->chunks[s], chunk_cap);
     if (!ok) { ws_free(w); delete w; return DBS_ERR_OOM; }
@@ -1725,9 +1977,11 @@ dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
     w->grid_dense[1] = coop_grid((const void *)k_spmspv_dense<true>, w->sms, SMEM0);
     w->grid_bfs[0] = coop_grid((const void *)k_bfs<false>, w->sms, SMEM1);
     w->grid_bfs[1] = coop_grid((const void *)k_bfs<true>, w->sms, SMEM1);
+    w->decode_ok = coop_grid((const void *)k_decode, w->sms, SMEM0) > 0;   // sets its shared-memory size
     bool grids_ok = true;
     for (int a = 0; a < 2; ++a)
         grids_ok = grids_ok && w->grid_sparse[0][a] && w->grid_sparse[1][a] && w->grid_dense[a] && w->grid_bfs[a];
+    grids_ok = grids_ok && w->decode_ok;
     if (!grids_ok) {
         ws_free(w);
         delete w;
@@ -1773,6 +2027,7 @@ dbs_status dbs_workspace_check(dbs_workspace *w, void *stream)
               cudaMemset(w->xm32, 0, ((size_t)A->nbc / 2 + 8) * 4) == cudaSuccess &&
               cudaMemset(w->y_acc, 0, ((size_t)A->nbr * 16 + 16) * sizeof(float)) == cudaSuccess &&
               cudaMemset(w->yrm32, 0, (std::max<size_t>(1, w->n_ctiles) * CTILE / 2 + 8) * 4) == cudaSuccess &&
+              cudaMemset(w->rb_cnt, 0, ((size_t)A->nbr + 1) * 4) == cudaSuccess &&
               cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) { cudaGetLastError(); return DBS_ERR_CUDA; }
     return (dbs_status)c.err;
@@ -1806,8 +2061,6 @@ dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx
     const void *fns[2][2] = {{(const void *)k_spmspv_sparse<0, false>, (const void *)k_spmspv_sparse<0, true>},
                              {(const void *)k_spmspv_sparse<1, false>, (const void *)k_spmspv_sparse<1, true>}};
     const void *fn = fns[sri][st_on];
-    P.slot = w->call_count & 1;
-    w->call_count++;
     w->last_was_bfs = false;
     return launch_ws(w, fn, w->grid_sparse[sri][st_on], P, (cudaStream_t)stream,
                      sr == DBS_PLUS_TIMES_F32 ? SMEM0 : SMEM1);
@@ -1826,11 +2079,30 @@ dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_p
     P.x_in = x;
     P.xv = x;
     P.y_dense = y;
-    P.slot = w->call_count & 1;
-    w->call_count++;
     w->last_was_bfs = false;
     return P.stats ? launch_ws(w, (const void *)k_spmspv_dense<true>, w->grid_dense[1], P, (cudaStream_t)stream, SMEM0)
                    : launch_ws(w, (const void *)k_spmspv_dense<false>, w->grid_dense[0], P, (cudaStream_t)stream, SMEM0);
+}
+
+dbs_status dbs_decode_layer(const dbs_matrix *A, const float *x, float tau, float *y, dbs_workspace *w, void *stream)
+{
+    dbs_status st = check_ready(A, w);
+    if (st != DBS_OK) return st;
+    if (!A->valued) return DBS_ERR_UNSUPPORTED;
+    if ((A->n > 0 && !x) || (A->m > 0 && !y) || !(tau >= 0.0f) || (reinterpret_cast<uintptr_t>(x) & 15u))
+        return DBS_ERR_INVALID_ARG;
+    if (A->m == 0) return DBS_OK;
+    KParams P = make_params(A, w);
+    P.path_force = DBS_PATH_PULL;
+    P.x_in = x;
+    P.xv = x;
+    P.tau = tau;
+    P.y_dense = y;
+    const int64_t g_tiles = (A->T + NW - 1) / NW, g_rows = (A->nbr + NT - 1) / NT;
+    const int grid = (int)std::max<int64_t>(1, std::max(g_tiles, g_rows));
+    k_decode<<<grid, NT, SMEM0, (cudaStream_t)stream>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return DBS_ERR_CUDA;
+    return DBS_OK;
 }
 
 dbs_status dbs_bfs(const dbs_matrix *A, int64_t src, int32_t *levels, int32_t *nlevels_host, dbs_path path,
@@ -1846,9 +2118,8 @@ dbs_status dbs_bfs(const dbs_matrix *A, int64_t src, int32_t *levels, int32_t *n
     P.levels = levels;
     cudaStream_t s = (cudaStream_t)stream;
     // Counter slots: a dense-x call leaves its own slot dirty and clears the
-    // other, so calls alternate slots; sparse-x and BFS calls leave every
-    // slot clear.
-    w->call_count = 0;
+    // other, which the next launch (the count advanced by one) uses;
+    // sparse-x and BFS calls leave every slot clear.
     w->last_was_bfs = true;
     st = P.stats ? launch_ws(w, (const void *)k_bfs<true>, w->grid_bfs[1], P, s, SMEM1)
                  : launch_ws(w, (const void *)k_bfs<false>, w->grid_bfs[0], P, s, SMEM1);
@@ -2014,7 +2285,6 @@ extern "C" dbs_status dbs_spmspv_dense_noalloc(const dbs_matrix *A, const float 
     P.x_in = x;
     P.xv = x;
     P.y_dense = y;
-    P.slot = 0;
     dbs_exec_opts o;
     dbs_exec_opts_default(&o);
     P.th3 = o.th3;

@@ -230,9 +230,11 @@ void free_device(dbs_matrix *A)
     cudaFree(A->d_rb_ptr); cudaFree(A->d_blk_desc); cudaFree(A->d_blk_ref); cudaFree(A->d_cb_ptr);
     cudaFree(A->d_csc_desc); cudaFree(A->d_csc_ref); cudaFree(A->d_payload); cudaFree(A->d_tiles);
     cudaFree(A->d_rb_rows);
+    cudaFree(A->d_rb_ntiles);
     A->d_rb_ptr = nullptr; A->d_blk_desc = nullptr; A->d_blk_ref = nullptr; A->d_cb_ptr = nullptr;
     A->d_csc_desc = nullptr; A->d_csc_ref = nullptr; A->d_payload = nullptr; A->d_tiles = nullptr;
     A->d_rb_rows = nullptr;
+    A->d_rb_ntiles = nullptr;
 }
 
 template <class T>
@@ -473,6 +475,14 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
             }
             if (next != (uint64_t)B) return fail(DBS_ERR_INTERNAL);
         }
+        // tiles meeting each row block at an end of their span (2 or more:
+        // the row block's partial sums come from several tiles)
+        H.rb_ntiles.assign((size_t)nbr, 0u);
+        for (const U4 &tl : H.tiles) {
+            const uint32_t span = tl.w & TILE_SPAN_MASK;
+            ++H.rb_ntiles[tl.z];
+            if (span > 1u) ++H.rb_ntiles[tl.z + span - 1u];
+        }
     } catch (const std::bad_alloc &) {
         return fail(DBS_ERR_OOM);
     }
@@ -487,7 +497,8 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
     }
     I.ntiles = A->T;
     I.payload_bytes = A->P * 16;
-    I.view_bytes = (nbr + 1) * 4 + A->B * 8 + A->B * 4 + (nbc + 1) * 4 + A->B * 8 + A->B * 4 + A->T * 16;
+    I.view_bytes = (nbr + 1) * 4 + A->B * 8 + A->B * 4 + (nbc + 1) * 4 + A->B * 8 + A->B * 4 + A->T * 16 +
+                   nbr * (2 + 4);   // + per row block: rows holding entries, tiles meeting it
     I.total_bytes = I.payload_bytes + I.view_bytes;
     I.csr_bytes = (m + 1) * 4 + nnz * 4 + (valued ? nnz * 4 : 0);
     I.csr_csc_bytes = I.csr_bytes + (n + 1) * 4 + nnz * 4 + (valued ? nnz * 4 : 0);
@@ -507,6 +518,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         if ((st = upload(H.payload, &A->d_payload, 1, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.tiles, &A->d_tiles, 1, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.rb_rows, &A->d_rb_rows, (size_t)nbr + 2, s)) != DBS_OK) return fail(st);
+        if ((st = upload(H.rb_ntiles, &A->d_rb_ntiles, (size_t)nbr + 1, s)) != DBS_OK) return fail(st);
         if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return fail(DBS_ERR_CUDA); }
         A->on_device = true;
     }

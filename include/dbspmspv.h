@@ -228,6 +228,27 @@ dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx
 dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_path path,
                             dbs_workspace *ws, void *stream);
 
+/* Section 4.3 (DB-Decoding: a single-token linear layer whose activations
+ * are sparsified by magnitude thresholding): y = A x' with
+ *     x'_j = x_j  if |x_j| > tau  (NaN entries count as active),
+ *     x'_j = 0    otherwise,
+ * on the pull path.  The activation mask of each 16-entry vector block is
+ * formed from x inside the traversal (Section 4.1's mask generation fused
+ * into the kernel that consumes it), so the call is one ordinary kernel
+ * launch with no device-wide barrier and no path decision: use it when the
+ * input is known to be dense enough for pull (decoding activations at about
+ * 10 % density); dbs_spmspv_dense is the general form with the selector.
+ *   x    device (or host-mapped) float32[n], 16-byte aligned
+ *   tau  threshold, >= 0 (tau = 0: every nonzero entry is active)
+ *   y    device float32[m]; every row is written (0 where nothing is active)
+ * Summation order within a row is not fixed (row blocks split between
+ * pull tiles combine partial sums with atomics).  Capturable in a CUDA
+ * graph.  Errors: DBS_ERR_INVALID_ARG (null pointers, tau < 0 or NaN,
+ * misaligned x), DBS_ERR_UNSUPPORTED (pattern-only matrix), DBS_ERR_CUDA.
+ * ASYNC. */
+dbs_status dbs_decode_layer(const dbs_matrix *A, const float *x, float tau, float *y, dbs_workspace *ws,
+                            void *stream);
+
 /* Section 4.2 (DB-BFS): level-synchronous BFS from src on a square matrix;
  * each level is next = (A or.and frontier) and not visited, with push/pull
  * re-chosen per level (or forced by path).  The whole level loop runs on the

@@ -60,6 +60,8 @@ def _load(path: Optional[str] = None):
     lib.oracle_bfs_queue.argtypes = [P, I64, P]
     lib.oracle_bfs_spmspv.restype = I64
     lib.oracle_bfs_spmspv.argtypes = [P, I64, P]
+    lib.oracle_activation_mask.restype = I64
+    lib.oracle_activation_mask.argtypes = [I64, P, ctypes.c_float, P]
     lib.oracle_block_views.restype = I64
     lib.oracle_block_views.argtypes = [I64, I64, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_double, P, P, P, P, P, P, P]
@@ -135,6 +137,18 @@ class Oracle:
             return y_idx[:k].copy(), y_val[:k].copy(), y_abs[:k].copy()
         return y_idx[:k].copy(), None, None
 
+    # Section 4.3 (DB-Decoding): y = A x' for x' = x thresholded by magnitude
+    def decode_layer(self, x: np.ndarray, tau: float):
+        """Dense results of one decoding layer: (y float64[m], abs_sum
+        float64[m], touched bool[m]); rows nothing reaches are 0."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        keep = activation_mask(x, tau)
+        ri, rv, rs = self.spmspv(_SparseX(self.A.n, keep, x[keep]))
+        m = self.A.m
+        y, s, t = np.zeros(m), np.zeros(m), np.zeros(m, bool)
+        y[ri], s[ri], t[ri] = rv, rs, True
+        return y, s, t
+
     def bfs_queue(self, src: int) -> np.ndarray:
         lev = np.empty(self.A.n, dtype=np.int32)
         r = _load().oracle_bfs_queue(self._h, int(src), _ptr(lev))
@@ -150,6 +164,20 @@ class Oracle:
         if r < 0:
             raise MemoryError("oracle_bfs_spmspv failed")
         return lev
+
+
+class _SparseX:
+    def __init__(self, n, idx, val):
+        self.n, self.idx, self.val = n, idx, val
+
+
+def activation_mask(x: np.ndarray, tau: float) -> np.ndarray:
+    """Section 4.3 / 5 (DB-Decoding, magnitude thresholding): ascending
+    int32 indices j with |x_j| > tau (NaN entries kept)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(max(x.shape[0], 1), dtype=np.int32)
+    k = _load().oracle_activation_mask(x.shape[0], _ptr(x), float(tau), _ptr(out))
+    return out[:k].copy()
 
 
 def spmspv_pull(A, x, semiring: int = PLUS_TIMES, visited: Optional[np.ndarray] = None):

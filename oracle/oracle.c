@@ -17,6 +17,10 @@
  *                          are unique, so a queue BFS fixes them).
  *   - oracle_bfs_spmspv  : Section 4.2 / Algorithm 5 semantics: each level is
  *                          next = (A or.and frontier) and not visited.
+ *   - oracle_activation_mask : Section 4.3 / Section 5 (DB-Decoding): the
+ *                          activation is sparsified by magnitude thresholding;
+ *                          entry j is kept iff |x_j| > tau (NaN kept).  The
+ *                          kept entries are the x of oracle_spmspv_push.
  *   - oracle_block_views : Section 3.2.1 and Figure 5(b): 16x16 blocking,
  *                          block-CSR view, block-CSC view, csc2csr mapping,
  *                          per-block nnz, and the low-level format class from
@@ -342,4 +346,18 @@ int64_t oracle_block_views(int64_t m, int64_t n, const int64_t *row_ptr,
         }
     free(next);
     return B;
+}
+
+/* ------------------------------------------------------------------------ */
+/* DB-Decoding activation mask (magnitude thresholding): writes the indices */
+/* j with NOT(|x_j| <= tau) -- |x_j| > tau, NaN included -- in ascending     */
+/* order and returns how many there are.                                    */
+int64_t oracle_activation_mask(int64_t n, const float *x, float tau, int32_t *idx_out)
+{
+    int64_t k = 0;
+    for (int64_t j = 0; j < n; ++j) {
+        double a = fabs((double)x[j]);
+        if (!(a <= (double)tau)) idx_out[k++] = (int32_t)j;
+    }
+    return k;
 }

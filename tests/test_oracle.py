@@ -63,6 +63,35 @@ def test_integer_values_are_exact(seed):
     np.testing.assert_array_equal(yv, bv)          # small integers: exact in any order
 
 
+def test_activation_mask_rule():
+    """Magnitude thresholding (DB-Decoding, Sections 4.3 and 5): keep x_j
+    iff |x_j| > tau.  Worked by hand: entries equal to +-tau are dropped,
+    NaN is kept (it is not <= tau), +-0 never survive."""
+    x = np.array([0.0, -0.0, 2.0, -2.0, 0.5, np.nan, np.inf, -1.0, 1.0, 1.0000001], np.float32)
+    np.testing.assert_array_equal(oracle.activation_mask(x, 1.0), [2, 3, 5, 6, 9])
+    np.testing.assert_array_equal(oracle.activation_mask(x, 0.0), [2, 3, 4, 5, 6, 7, 8, 9])
+    np.testing.assert_array_equal(oracle.activation_mask(x, np.inf), [5])
+    assert oracle.activation_mask(np.zeros(0, np.float32), 0.5).shape == (0,)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_decode_layer_matches_dense_brute_force(seed):
+    """y = A x' against a dense fp64 matvec of the thresholded activation,
+    with several entries exactly at +-tau."""
+    rng = np.random.default_rng(seed + 100)
+    m = n = int(rng.integers(1, 60))      # square: a transposed-index mutant stays in bounds
+    A = synth.random_csr(m, n, float(rng.uniform(0.05, 0.6)), seed + 100)
+    tau = 0.5
+    x = rng.standard_normal(n).astype(np.float32)
+    x[rng.random(n) < 0.2] = np.float32(tau) * rng.choice([-1, 1])
+    y, s, t = oracle.Oracle(A).decode_layer(x, tau)
+    xp = np.where(np.abs(x.astype(np.float64)) > tau, x.astype(np.float64), 0.0)
+    D = synth.csr_to_dense(A)
+    np.testing.assert_allclose(y, D @ xp, rtol=0, atol=1e-12 * (1 + np.abs(D) @ np.abs(xp)).max())
+    np.testing.assert_allclose(s, np.abs(D) @ np.abs(xp), rtol=1e-12)
+    np.testing.assert_array_equal(t, (D != 0).astype(np.int64) @ (xp != 0).astype(np.int64) > 0)
+
+
 def test_unit_vector_returns_column():
     A = synth.random_csr(60, 40, 0.3, 3)
     D = synth.csr_to_dense(A)

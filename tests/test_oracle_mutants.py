@@ -24,6 +24,7 @@ MUTANTS = {
     "force_classes_swapped": ("if (skew_r / skew_c > th2) cls = 3;", "if (skew_r / skew_c > th2) cls = 2;"),
     "csc2csr_wrong": ("blk_csc2csr[q] = p;", "blk_csc2csr[q] = q;"),
     "abs_sum_signed": ("sab[i] += fabs(p);", "sab[i] += p;"),
+    "threshold_inclusive": ("if (!(a <= (double)tau)) idx_out[k++]", "if (a >= (double)tau) idx_out[k++]"),
 }
 
 PIN_FUNCS = [
@@ -35,6 +36,8 @@ PIN_FUNCS = [
     lambda: [pins.test_block_views_match_figure5(bs) for bs in (4, 16)],
     pins.test_format_classes_by_density,
     pins.test_format_classes_by_skew,
+    pins.test_activation_mask_rule,
+    lambda: [pins.test_decode_layer_matches_dense_brute_force(s) for s in range(3)],
 ]
 
 
