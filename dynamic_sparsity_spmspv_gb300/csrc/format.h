@@ -34,8 +34,11 @@
 // is local column k, bit k of a column mask is local row k, as in Figure 5's
 // "row_mask 10 = 0b1010 -> columns 1 and 3"):
 //   COO         coord u8[nnz] (row << 4 | col, row-major order), values at align4(nnz)
-//   Dense       col_mask u16[16] at 0, values f32[256] column-major (v[c*16+r]) at 32;
-//               absent entries hold 0 and are excluded through col_mask
+//   Dense       with values: values f32[256] column-major (v[c*16+r]) at 0 and
+//               col_mask u16[16] at 1024, the block starting on a 64-byte
+//               boundary (padding units before it are zero), so each column's
+//               16 values are one aligned 64-byte run; absent entries hold 0
+//               and are excluded through col_mask.  Pattern only: col_mask at 0
 //   ForceCSR    row_ptr u8[16] at 0, row_mask u16[16] at 16, values in row order at 48
 //   ForceCSC    col_ptr u8[16] at 0, col_mask u16[16] at 16, values in column order at 48
 //   PatchedCSR  row_ptr u8[16] at 0, row_mask u16[16] at 16, col_ptr u8[16] at 48,
@@ -105,10 +108,18 @@ DBS_HD uint32_t struct_bytes(uint32_t fmt, uint32_t nnz)
 {
     return fmt == FMT_COO ? nnz : fmt == FMT_DENSE ? 32u : fmt == FMT_PCSR ? 64u + nnz : 48u;
 }
-DBS_HD uint32_t val_offset(uint32_t fmt, uint32_t nnz) { return (struct_bytes(fmt, nnz) + 3u) & ~3u; }
+// Byte offset of a Dense block's column masks.
+DBS_HD uint32_t dense_mask_off(bool valued) { return valued ? 1024u : 0u; }
+// Payload units a valued Dense block is aligned to (64 bytes).
+constexpr uint32_t DENSE_ALIGN_UNITS = 4;
+DBS_HD uint32_t val_offset(uint32_t fmt, uint32_t nnz)
+{
+    return fmt == FMT_DENSE ? 0u : (struct_bytes(fmt, nnz) + 3u) & ~3u;
+}
 DBS_HD uint32_t val_count(uint32_t fmt, uint32_t nnz) { return fmt == FMT_DENSE ? 256u : nnz; }
 DBS_HD uint32_t payload_bytes(uint32_t fmt, uint32_t nnz, bool valued)
 {
+    if (fmt == FMT_DENSE) return valued ? 1024u + 32u : 32u;
     return val_offset(fmt, nnz) + (valued ? 4u * val_count(fmt, nnz) : 0u);
 }
 DBS_HD uint32_t payload_units(uint32_t fmt, uint32_t nnz, bool valued)

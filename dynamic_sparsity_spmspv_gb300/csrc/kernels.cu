@@ -363,7 +363,7 @@ __device__ __forceinline__ RowOut mk_colwise(const uint8_t *__restrict__ b, uint
                                              const float *xb, int lane, uint32_t *nread)
 {
     const uint32_t r = lane & 15, h = lane >> 4;
-    const uint16_t *cmask = reinterpret_cast<const uint16_t *>(b + (FMT == FMT_DENSE ? 0u : OFF_MASK));
+    const uint16_t *cmask = reinterpret_cast<const uint16_t *>(b + (FMT == FMT_DENSE ? dense_mask_off(true) : OFF_MASK));
     const float *vals = reinterpret_cast<const float *>(b + val_offset(FMT, nnz));
     uint32_t a = act & (h ? 0xFF00u : 0x00FFu);
     float sum = 0.0f;
@@ -482,7 +482,7 @@ __device__ __forceinline__ RowOut hw_heavy(const uint8_t *__restrict__ b, uint32
     float sum = 0.0f;
     uint32_t t = 0, cnt = 0;
     if (fmt == FMT_DENSE || fmt == FMT_FCSC) {
-        const uint16_t *cmask = reinterpret_cast<const uint16_t *>(b + (fmt == FMT_DENSE ? 0u : OFF_MASK));
+        const uint16_t *cmask = reinterpret_cast<const uint16_t *>(b + (fmt == FMT_DENSE ? dense_mask_off(true) : OFF_MASK));
         uint32_t a = act;
         while (a) {
             const uint32_t c = __ffs(a) - 1u;
@@ -553,9 +553,9 @@ __device__ __forceinline__ uint32_t pair_products(const uint8_t *__restrict__ b,
     const float *vals = reinterpret_cast<const float *>(b + val_offset(fmt, nnz));
     uint32_t rows = 0;
     if (fmt == FMT_DENSE) {
-        // column c's 16 values are one 64-byte run (absent entries hold 0 and
-        // are excluded by the column mask, so no 0 * inf can appear)
-        rows = __ldg(reinterpret_cast<const uint16_t *>(b) + c);
+        // column c's 16 values are one aligned 64-byte run (absent entries
+        // hold 0 and are excluded by the column mask, so no 0 * inf appears)
+        rows = __ldg(reinterpret_cast<const uint16_t *>(b + dense_mask_off(true)) + c);
         const float4 *v4 = reinterpret_cast<const float4 *>(vals + c * 16u);
         float v[16];
 #pragma unroll
@@ -750,10 +750,12 @@ __device__ __forceinline__ uint32_t bool_found_units(uint32_t fmt, uint32_t nnz,
     return f;
 }
 // The two units bool_found_units starts from: COO coordinates 0-31, the
-// Dense column masks (bytes 0-31), or the Force / patched masks (bytes 16-47).
-__device__ __forceinline__ void bool_load(const uint4 *b4, uint32_t fmt, uint32_t nnz, uint4 &u0, uint4 &u1)
+// Dense column masks (32 bytes at dense_mask_off), or the Force / patched
+// masks (bytes 16-47).
+__device__ __forceinline__ void bool_load(const uint4 *b4, uint32_t fmt, uint32_t nnz, bool valued, uint4 &u0,
+                                          uint4 &u1)
 {
-    const uint32_t s = (fmt == FMT_COO || fmt == FMT_DENSE) ? 0u : 1u;
+    const uint32_t s = fmt == FMT_COO ? 0u : fmt == FMT_DENSE ? dense_mask_off(valued) / 16u : 1u;
     u0 = __ldg(b4 + s);
     u1 = (fmt != FMT_COO || nnz > 16u) ? __ldg(b4 + s + 1) : make_uint4(0u, 0u, 0u, 0u);
 }
@@ -1010,7 +1012,7 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 const uint4 *b = P.payload + __ldg(P.blk_ref + p0 + (e & 0xFFu));
                 const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
                 uint4 u0, u1;
-                bool_load(b, fmt, nnz, u0, u1);
+                bool_load(b, fmt, nnz, P.valued != 0, u0, u1);
                 const uint32_t r = bool_found_units(fmt, nnz, e >> 16, u0, u1, b);
                 if (r) atomicOr(&W.rm[(e >> 8) & 0xFFu], r);
                 if (ST) c_bytes += 4u + 32u;
@@ -1142,7 +1144,7 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 const uint4 *pb = P.payload + ref;
                 const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
                 uint4 u0, u1;
-                bool_load(pb, fmt, nnz, u0, u1);
+                bool_load(pb, fmt, nnz, P.valued != 0, u0, u1);
                 const uint32_t f = bool_found_units(fmt, nnz, e >> 16, u0, u1, pb) & ~vm;
                 if (f) or16(out_rm, rb, f);
                 if (ST) c_bytes += 4u + (fmt == FMT_COO ? nnz : 32u);

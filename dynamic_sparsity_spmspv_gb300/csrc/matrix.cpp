@@ -82,7 +82,7 @@ void encode_block(uint32_t fmt, const uint8_t *lr, const uint8_t *lc, const floa
         }
         break;
     case FMT_DENSE:
-        std::memcpy(out, cmask, 32);
+        std::memcpy(out + dense_mask_off(valued), cmask, 32);
         if (valued)
             for (int k = 0; k < nnz; ++k) vals[lc[k] * 16 + lr[k]] = v[k];
         break;
@@ -385,9 +385,19 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         for (auto &c : chunks)
             if (c.error != DBS_OK) return fail((dbs_status)c.error);
 
-        // 2. Concatenate: primary block order, payload offsets.
+        // 2. Concatenate: primary block order, payload offsets (a valued
+        // Dense block starts on a 64-byte boundary).
+        const bool valued_m = va != nullptr;
+        auto aligned = [&](const U2 &d) { return valued_m && !meta_inline(d.y) && meta_fmt(d.y) == FMT_DENSE; };
+        auto align_up = [](int64_t u) { return (u + DENSE_ALIGN_UNITS - 1) / DENSE_ALIGN_UNITS * DENSE_ALIGN_UNITS; };
         int64_t B = 0, P = 0;
-        for (auto &c : chunks) { B += (int64_t)c.desc.size(); P += (int64_t)c.payload.size(); }
+        for (auto &c : chunks) {
+            B += (int64_t)c.desc.size();
+            for (size_t i = 0; i < c.units.size(); ++i) {
+                if (aligned(c.desc[i])) P = align_up(P);
+                P += c.units[i];
+            }
+        }
         if (B >= (int64_t(1) << 32) || P >= (int64_t(1) << 32)) return fail(DBS_ERR_UNSUPPORTED);
         A->B = B; A->P = P;
         H.rb_ptr.resize((size_t)nbr + 1);
@@ -401,8 +411,14 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
                 for (size_t i = 0; i < c.rb_count.size(); ++i)
                     H.rb_ptr[(size_t)c.rb0 + i + 1] = H.rb_ptr[(size_t)c.rb0 + i] + c.rb_count[i];
                 std::copy(c.desc.begin(), c.desc.end(), H.blk_desc.begin() + pb);
-                std::copy(c.payload.begin(), c.payload.end(), H.payload.begin() + pu);
-                for (size_t i = 0; i < c.units.size(); ++i) { H.blk_ref[pb + i] = pu; pu += c.units[i]; }
+                size_t lo = 0;
+                for (size_t i = 0; i < c.units.size(); ++i) {
+                    if (aligned(c.desc[i])) pu = (uint32_t)align_up(pu);
+                    std::copy(c.payload.begin() + lo, c.payload.begin() + lo + c.units[i], H.payload.begin() + pu);
+                    H.blk_ref[pb + i] = pu;
+                    pu += c.units[i];
+                    lo += c.units[i];
+                }
                 pb += (uint32_t)c.desc.size();
                 std::vector<U2>().swap(c.desc);
                 std::vector<U4>().swap(c.payload);
@@ -606,7 +622,8 @@ dbs_status dbs_matrix_export_csr(const dbs_matrix *A, int64_t *row_ptr, int32_t 
                     const uint8_t *b = meta_inline(meta) ? inl : pay + (size_t)H->blk_ref[p] * 16;
                     const float *v = reinterpret_cast<const float *>(b + val_offset(fmt, nnz));
                     uint16_t mask[16] = {0};
-                    if (fmt != FMT_COO) std::memcpy(mask, b + (fmt == FMT_DENSE ? 0 : OFF_MASK), 32);
+                    if (fmt != FMT_COO)
+                        std::memcpy(mask, b + (fmt == FMT_DENSE ? dense_mask_off(A->valued) : OFF_MASK), 32);
                     uint32_t found = 0;
                     for (int r = 0; r < 16; ++r) {
                         for (int c = 0; c < 16; ++c) {

@@ -17,6 +17,7 @@ from .workloads import (  # noqa: F401
     x_uniform,
     x_clusters,
     x_relu_topk,
+    x_activation,
     bfs_sources,
     random_csr,
     config,

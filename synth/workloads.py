@@ -281,6 +281,13 @@ def x_relu_topk(n: int, keep: int, seed) -> np.ndarray:
     return out
 
 
+def x_activation(n: int, seed) -> np.ndarray:
+    """Dense pre-threshold activation of a decoding layer: N(0, 1) float32
+    (magnitude thresholding at 1.6449 keeps about 10 % of the entries)."""
+    rng = _rng(*np.atleast_1d(seed).tolist(), 5)
+    return rng.standard_normal(n, dtype=np.float32)
+
+
 def bfs_sources(A: CSR, k: int, seed) -> np.ndarray:
     """k distinct uniform sources among vertices with at least one neighbour."""
     rng = _rng(*np.atleast_1d(seed).tolist(), 5)

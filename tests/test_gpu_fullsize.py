@@ -103,3 +103,18 @@ def test_grid_hubs_full_bfs(full):
     x = synth.x_uniform(A.n, A.n // 1000, [47, 1], valued=False)
     for path in PATHS:
         assert_parity(A, O, M, ws, x, "or_and", path=path)
+
+
+def test_llm_full_decode_layer(full):
+    """The DB-Decoding layer at the workload's full size, with the paper's
+    thresholds and with the GB300 decode build (th1 = 31, tile weight 160)."""
+    A, O, M = full("llm")
+    for Mb in (M, dbs.DBMatrix.from_csr(A, th1=31, tile_weight=160)):
+        ws = dbs.Workspace(Mb)
+        for t in range(4):
+            xa = synth.x_activation(A.n, [90, t, 0])
+            y = dbs.decode_layer(Mb, _t(xa), 1.6449, ws=ws).cpu().numpy()
+            assert ws.check() == 0
+            ref, s, touched = O.decode_layer(xa, 1.6449)
+            assert oracle.tolerance_ok(y[touched], ref[touched], s[touched]).all()
+            assert (y[~touched] == 0).all()
