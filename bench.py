@@ -407,6 +407,53 @@ def run_ablation(dbs, torch, dev, stream, flush, reps: int):
     return rows
 
 
+def run_spmv(dbs, torch, dev, flush, reps: int):
+    """Dense-input regime: adaptive CSR SpMV (dbs_spmv, plan built once)
+    against the DB-format pull (dbs_spmspv_dense, auto path) on the same
+    matrix with a dense x (every entry nonzero, N(0,1)).  FEM rows (27
+    entries) run as warp rows, LLM rows (5,504) as block rows, the R-MAT
+    graph with unit weights mixes scalar and warp rows with split hub rows.
+    Median µs over `reps` calls, L2 flushed before each; GB/s from the CSR
+    bytes (8 B per row pointer, 8 B per entry, x and y once)."""
+    import synth
+    peak, _ = _peaks()
+    out = []
+    for name in ("fem", "llm", "rmat"):
+        A = synth.config(name, "full")
+        if A.vals is None:
+            A = synth.CSR(A.m, A.n, A.row_ptr, A.col_idx, np.ones(A.nnz, np.float32))
+        plan = dbs.SpMVPlan.from_csr(A)
+        M = dbs.DBMatrix.from_csr(A)
+        ws = dbs.Workspace(M)
+        x = torch.from_numpy(np.random.default_rng(17).standard_normal(A.n).astype(np.float32)).to(dev)
+        y = torch.empty(A.m, dtype=torch.float32, device=dev)
+
+        def timed(call):
+            ts = []
+            for i in range(reps + 2):
+                flush(i)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                call()
+                e1.record()
+                e1.synchronize()
+                if i >= 2:
+                    ts.append(e0.elapsed_time(e1) * 1e3)
+            return float(np.median(ts))
+
+        us_csr = timed(lambda: plan(x, y=y))
+        us_db = timed(lambda: dbs.spmspv_dense(M, x, y=y, ws=ws))
+        csr_bytes = 8 * (A.m + 1) + 8 * A.nnz + 4 * A.n + 4 * A.m
+        line = {"workload": name, "nnz": int(A.nnz), "buckets": plan.info(),
+                "csr_spmv_us": round(us_csr, 2), "csr_gbs": round(csr_bytes / us_csr / 1e3, 1),
+                "csr_frac_of_measured_hbm": round(csr_bytes / us_csr / 1e3 / peak, 3),
+                "db_pull_us": round(us_db, 2)}
+        out.append(line)
+        assert ws.check() == 0
+        ws.close(); M.close(); plan.close()
+    return out
+
+
 DECODE_TAU = 1.6449      # |N(0,1)| > tau for 10 % of the entries
 
 
@@ -556,6 +603,8 @@ def main():
     ap.add_argument("--decode-layers", type=int, default=32,
                     help="layers of the DB-Decoding token step (distinct 4096x11008 weights; 0 = off)")
     ap.add_argument("--decode-tokens", type=int, default=20, help="tokens timed in the decoding step")
+    ap.add_argument("--spmv", type=int, default=10,
+                    help="calls per point of the dense-input comparison (adaptive CSR SpMV vs DB pull; 0 = off)")
     ap.add_argument("--ablation", type=int, default=0,
                     help="calls per point of the format ablation (Auto / COO-only / CSR-only on the "
                          "R-MAT, FEM and LLM workloads) and per-level frontier histograms (0 = off)")
@@ -790,6 +839,9 @@ def main():
 
     if not args.no_configs:
         out["other_workloads"] = run_configs(dbs, torch, dev, stream, flush, 10)
+
+    if args.spmv > 0:
+        out["dense_input"] = run_spmv(dbs, torch, dev, flush, args.spmv)
 
     if args.decode_layers > 0:
         out["decode"] = run_decode(dbs, torch, dev, stream, args.decode_layers, args.decode_tokens)

@@ -291,6 +291,56 @@ decode_layer = dbs_decode_layer
 bfs = dbs_bfs
 
 
+class SpMVPlan:
+    """dbs_spmv_plan: adaptive CSR SpMV for dense x.  The CSR arrays (CUDA
+    tensors: row_ptr int64[m+1], col_idx int32[nnz], vals float32[nnz]) are
+    kept referenced for the plan's lifetime."""
+
+    def __init__(self, m: int, n: int, row_ptr, col_idx, vals, stream=None):
+        torch = _torch()
+        self._arrays = (row_ptr.to(torch.int64).contiguous(), col_idx.to(torch.int32).contiguous(),
+                        vals.to(torch.float32).contiguous())
+        rp, ci, va = self._arrays
+        self.m, self.n = int(m), int(n)
+        h = ctypes.c_void_p()
+        st = _lib.load().dbs_spmv_plan_create(self.m, self.n, int(ci.numel()), _ptr(rp), _ptr(ci), _ptr(va),
+                                              _stream_handle(stream), ctypes.byref(h))
+        _lib.check("dbs_spmv_plan_create", st)
+        self._h = h
+
+    @classmethod
+    def from_csr(cls, A, device="cuda", **kw) -> "SpMVPlan":
+        torch = _torch()
+        return cls(A.m, A.n, torch.from_numpy(np.asarray(A.row_ptr, np.int64)).to(device),
+                   torch.from_numpy(np.asarray(A.col_idx, np.int32)).to(device),
+                   torch.from_numpy(np.asarray(A.vals, np.float32)).to(device), **kw)
+
+    def info(self) -> dict:
+        rows = (ctypes.c_int64 * 8)()
+        chunks = ctypes.c_int64(0)
+        _lib.check("dbs_spmv_plan_info", _lib.load().dbs_spmv_plan_info(self._h, rows, ctypes.byref(chunks)))
+        return {"lane_group_rows": {str(1 << b): rows[b] for b in range(6)}, "block_rows": rows[6],
+                "split_rows": rows[7], "split_chunks": chunks.value}
+
+    def __call__(self, x, *, y=None, stream=None):
+        torch = _torch()
+        if y is None:
+            y = torch.empty(max(self.m, 1), dtype=torch.float32, device=x.device)
+        _lib.check("dbs_spmv", _lib.load().dbs_spmv(self._h, _ptr(x), _ptr(y), _stream_handle(stream)))
+        return y
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib.load().dbs_spmv_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def library_path() -> str:
     return _lib.lib_path()
 

@@ -62,6 +62,10 @@ PROTOTYPES = {
     "dbs_spmspv_dense": (I32, [P, P, P, ctypes.c_int, P, P]),
     "dbs_spmspv_dense_noalloc": (I32, [P, P, P, P]),
     "dbs_decode_layer": (I32, [P, P, ctypes.c_float, P, P, P]),
+    "dbs_spmv_plan_create": (I32, [I64, I64, I64, P, P, P, P, P]),
+    "dbs_spmv": (I32, [P, P, P, P]),
+    "dbs_spmv_plan_info": (I32, [P, P, P]),
+    "dbs_spmv_plan_destroy": (I32, [P]),
     "dbs_bfs": (I32, [P, I64, P, P, ctypes.c_int, P, P]),
     "dbs_last_stats": (I32, [P, P, P]),
     "dbs_selftest_wait_timeout": (I32, [P, P]),

@@ -249,6 +249,46 @@ dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_p
 dbs_status dbs_decode_layer(const dbs_matrix *A, const float *x, float tau, float *y, dbs_workspace *ws,
                             void *stream);
 
+/* Dense-input regime: adaptive CSR SpMV (the adaptive CSR SpMV execution
+ * page: scalar rows, subgroup rows, workgroup rows and long-row split, one
+ * mapping of work to lanes per row shape), for an x dense enough that
+ * SpMSpV's vector metadata buys nothing -- the DB-SpMSpV paper's
+ * Limitations note that conventional SpMV may be preferable there.
+ *
+ * dbs_spmv_plan_create classifies the rows of a caller-owned device CSR once,
+ * on the GPU and without host readback of the row shapes: rows of up to 4,
+ * 8, 16, 32, 64 and 1024 entries go to groups of 1, 2, 4, 8, 16 and 32 lanes
+ * of a warp (the subgroup family, one thread for the shortest), rows of up
+ * to 16384 to one 256-thread block, longer rows are split into 8192-entry
+ * chunks whose partial sums the last chunk to finish adds up in chunk order.
+ * The row queues hold each row's first entry and length, so the multiply
+ * does not go back to row_ptr.
+ *   m, n, nnz   rows, columns (< 2^31) and entries
+ *   row_ptr     device int64[m+1]; col_idx device int32[nnz]; vals device
+ *               float32[nnz].  Caller-owned; they must stay valid and
+ *               unchanged while the plan lives.  Row pointers are clamped to
+ *               [0, nnz] and column indices outside [0, n) contribute
+ *               nothing, so a malformed CSR cannot cause a stray access.
+ *   stream      the classification runs there; the call synchronizes it.
+ * Errors: DBS_ERR_INVALID_ARG, DBS_ERR_UNSUPPORTED (nnz >= 2^32),
+ * DBS_ERR_OOM, DBS_ERR_CUDA.  SYNCHRONOUS. */
+typedef struct dbs_spmv_plan dbs_spmv_plan;
+dbs_status dbs_spmv_plan_create(int64_t m, int64_t n, int64_t nnz, const int64_t *row_ptr, const int32_t *col_idx,
+                                const float *vals, void *stream, dbs_spmv_plan **out);
+
+/* y = A x: x device float32[n] (every entry used, zeros included), y device
+ * float32[m], every row written (0 for rows without entries).  One ordinary
+ * launch, deterministic summation order, capturable in a CUDA graph.  ASYNC. */
+dbs_status dbs_spmv(dbs_spmv_plan *plan, const float *x, float *y, void *stream);
+
+/* Rows per bucket (HOST int64[8], may be NULL: rows on 1, 2, 4, 8, 16 and
+ * 32 lanes, block rows, split rows) and split chunks (may be NULL) of a plan.
+ * Synchronous. */
+dbs_status dbs_spmv_plan_info(const dbs_spmv_plan *plan, int64_t *bucket_rows, int64_t *split_chunks);
+
+/* Frees the plan's scratch (not the CSR).  NULL is accepted. */
+dbs_status dbs_spmv_plan_destroy(dbs_spmv_plan *plan);
+
 /* Section 4.2 (DB-BFS): level-synchronous BFS from src on a square matrix;
  * each level is next = (A or.and frontier) and not visited, with push/pull
  * re-chosen per level (or forced by path).  The whole level loop runs on the

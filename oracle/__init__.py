@@ -62,6 +62,8 @@ def _load(path: Optional[str] = None):
     lib.oracle_bfs_spmspv.argtypes = [P, I64, P]
     lib.oracle_activation_mask.restype = I64
     lib.oracle_activation_mask.argtypes = [I64, P, ctypes.c_float, P]
+    lib.oracle_spmv_csr.restype = None
+    lib.oracle_spmv_csr.argtypes = [I64, I64, P, P, P, P, P, P]
     lib.oracle_block_views.restype = I64
     lib.oracle_block_views.argtypes = [I64, I64, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_double, P, P, P, P, P, P, P]
@@ -169,6 +171,19 @@ class Oracle:
 class _SparseX:
     def __init__(self, n, idx, val):
         self.n, self.idx, self.val = n, idx, val
+
+
+def spmv_csr(A, x: np.ndarray):
+    """Dense-input regime: y = A x over every stored entry (x used as
+    given).  Returns (y float64[m], abs_sum float64[m])."""
+    if A.vals is None:
+        raise ValueError("spmv_csr needs a valued matrix")
+    rp, ci, va = _csr_arrays(A)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(max(A.m, 1), dtype=np.float64)
+    s = np.empty(max(A.m, 1), dtype=np.float64)
+    _load().oracle_spmv_csr(A.m, A.n, _ptr(rp), _ptr(ci), _ptr(va), _ptr(x), _ptr(y), _ptr(s))
+    return y[:A.m].copy(), s[:A.m].copy()
 
 
 def activation_mask(x: np.ndarray, tau: float) -> np.ndarray:

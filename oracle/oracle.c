@@ -17,6 +17,9 @@
  *                          are unique, so a queue BFS fixes them).
  *   - oracle_bfs_spmspv  : Section 4.2 / Algorithm 5 semantics: each level is
  *                          next = (A or.and frontier) and not visited.
+ *   - oracle_spmv_csr    : the dense-input regime (the adaptive CSR SpMV page's
+ *                          output contract: one product per CSR row over all
+ *                          of its entries, x used as given, zeros included).
  *   - oracle_activation_mask : Section 4.3 / Section 5 (DB-Decoding): the
  *                          activation is sparsified by magnitude thresholding;
  *                          entry j is kept iff |x_j| > tau (NaN kept).  The
@@ -360,4 +363,25 @@ int64_t oracle_activation_mask(int64_t n, const float *x, float tau, int32_t *id
         if (!(a <= (double)tau)) idx_out[k++] = (int32_t)j;
     }
     return k;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Plain CSR SpMV: y_i = sum over the entries k of row i of a_k * x[col_k]   */
+/* (every entry, whatever x holds; columns outside [0, n) skipped), with     */
+/* abs_i = sum of |a_k * x[col_k]| for the tolerance.                       */
+void oracle_spmv_csr(int64_t m, int64_t n, const int64_t *row_ptr, const int32_t *col_idx, const float *vals,
+                     const float *x, double *y, double *abs_out)
+{
+    for (int64_t i = 0; i < m; ++i) {
+        double acc = 0.0, sab = 0.0;
+        for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) {
+            int64_t j = col_idx[k];
+            if (j < 0 || j >= n) continue;
+            double p = (double)vals[k] * (double)x[j];
+            acc += p;
+            sab += fabs(p);
+        }
+        y[i] = acc;
+        abs_out[i] = sab;
+    }
 }

@@ -1,0 +1,149 @@
+"""GPU parity of the dense-input regime (adaptive CSR SpMV, dbs_spmv):
+y = A x over every stored entry, against the oracle's plain CSR SpMV, with
+the fp32 tolerance |y - y_ref| <= 1e-5 * sum |a x| + 1e-30 on every row
+(rows without entries must be exactly 0)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+import __graft_entry__  # noqa: E402
+
+__graft_entry__.build()
+import dynamic_sparsity_spmspv_gb300 as dbs  # noqa: E402
+
+DEV = "cuda"
+
+
+def check(A, x, y):
+    ref, s = oracle.spmv_csr(A, x)
+    y = y.cpu().numpy()[:A.m]
+    assert oracle.tolerance_ok(y, ref, s).all()
+    empty = np.diff(A.row_ptr) == 0
+    assert (y[empty] == 0).all()
+
+
+def valued(A, seed):
+    if A.vals is not None:
+        return A
+    v = np.random.default_rng(seed).uniform(-1, 1, A.nnz).astype(np.float32)
+    return synth.CSR(A.m, A.n, A.row_ptr, A.col_idx, v)
+
+
+@pytest.mark.parametrize("name", synth.CONFIG_NAMES)
+def test_spmv_small_configs(name):
+    A = valued(synth.config(name, "small"), 1)
+    plan = dbs.SpMVPlan.from_csr(A)
+    rng = np.random.default_rng(2)
+    for _ in range(3):
+        x = rng.standard_normal(A.n).astype(np.float32)
+        x[rng.random(A.n) < 0.4] = 0.0
+        check(A, x, plan(torch.from_numpy(x).to(DEV)))
+
+
+def _shaped(lengths, n, seed):
+    """Rows of the given lengths, distinct uniform columns, values U[-1, 1]."""
+    rng = np.random.default_rng(seed)
+    rows, cols = [], []
+    for i, L in enumerate(lengths):
+        rows.append(np.full(L, i))
+        cols.append(rng.choice(n, size=L, replace=False))
+    rows = np.concatenate(rows) if rows else np.zeros(0, np.int64)
+    cols = np.concatenate(cols) if cols else np.zeros(0, np.int64)
+    vals = rng.uniform(-1, 1, rows.shape[0]).astype(np.float32)
+    return synth.csr_from_coo(len(lengths), n, rows, cols, vals)
+
+
+def test_spmv_every_bucket_and_boundary():
+    """Row lengths at every bucket boundary (4 .. 64 / 1024 / 16384) and split
+    rows of several chunks, empty rows between them; the plan's bucket counts
+    follow the lengths."""
+    lengths = [0, 1, 4, 5, 8, 9, 16, 17, 32, 33, 64, 65, 0, 1024, 1025, 16384, 16385, 50000, 3, 0,
+               8192 * 4, 8192 * 4 + 1]
+    A = _shaped(lengths, 60000, 4)
+    plan = dbs.SpMVPlan.from_csr(A)
+    inf = plan.info()
+    L = np.array(lengths)
+    lo = 0
+    for b in range(6):                          # 2^b lanes for rows of up to 4 * 2^b entries (32 lanes: 1024)
+        hi = 4 << b if b < 5 else 1024
+        assert inf["lane_group_rows"][str(1 << b)] == int(((L > lo) & (L <= hi)).sum() + (L == 0).sum() * (b == 0)), b
+        lo = hi
+    assert inf["block_rows"] == int(((L > 1024) & (L <= 16384)).sum())
+    assert inf["split_rows"] == int((L > 16384).sum())
+    assert inf["split_chunks"] == int(sum((l + 8191) // 8192 for l in lengths if l > 16384))
+    rng = np.random.default_rng(5)
+    y = torch.full((A.m,), 3.0, dtype=torch.float32, device=DEV)        # stale values are overwritten
+    for _ in range(4):                                                  # split-row counters reset themselves
+        x = rng.standard_normal(A.n).astype(np.float32)
+        plan(torch.from_numpy(x).to(DEV), y=y)
+        check(A, x, y)
+
+
+def test_spmv_integer_values_bit_exact():
+    A = synth.random_csr(300, 300, 0.1, 9, integer_values=True)
+    x = np.random.default_rng(9).integers(-3, 4, 300).astype(np.float32)
+    y = dbs.SpMVPlan.from_csr(A)(torch.from_numpy(x).to(DEV)).cpu().numpy()
+    ref, _ = oracle.spmv_csr(A, x)
+    np.testing.assert_array_equal(y, ref.astype(np.float32))
+
+
+def test_spmv_out_of_range_columns_and_clamped_rows():
+    """Columns outside [0, n) contribute nothing; row pointers past nnz are
+    clamped (no stray access, rows beyond the entries read as empty)."""
+    A = synth.random_csr(100, 80, 0.1, 11)
+    ci = A.col_idx.copy()
+    ci[::7] = 80 + (np.arange(ci[::7].shape[0]) % 5)
+    ci[3::11] = -1
+    B = synth.CSR(A.m, A.n, A.row_ptr, ci, A.vals)
+    x = np.random.default_rng(12).standard_normal(80).astype(np.float32)
+    check(B, x, dbs.SpMVPlan.from_csr(B)(torch.from_numpy(x).to(DEV)))
+    rp = A.row_ptr.copy()
+    rp[60:] = A.nnz + 1000                               # past the end: clamped to nnz
+    dev_rp = torch.from_numpy(rp).to(DEV)
+    plan = dbs.SpMVPlan(A.m, A.n, dev_rp, torch.from_numpy(A.col_idx).to(DEV), torch.from_numpy(A.vals).to(DEV))
+    y = plan(torch.from_numpy(x).to(DEV)).cpu().numpy()
+    C = synth.CSR(A.m, A.n, np.minimum(rp, A.nnz), A.col_idx, A.vals)
+    ref, s = oracle.spmv_csr(C, x)
+    assert oracle.tolerance_ok(y, ref, s).all()
+
+
+def test_spmv_empty_and_graph_replay():
+    E = synth.CSR(5, 7, np.zeros(6, np.int64), np.zeros(0, np.int32), np.zeros(0, np.float32))
+    y = dbs.SpMVPlan.from_csr(E)(torch.ones(7, dtype=torch.float32, device=DEV)).cpu().numpy()
+    assert (y == 0).all()
+    A = valued(synth.config("rmat", "small"), 13)
+    plan = dbs.SpMVPlan.from_csr(A)
+    x = torch.zeros(A.n, dtype=torch.float32, device=DEV)
+    y = torch.empty(A.m, dtype=torch.float32, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        plan(x, y=y)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan(x, y=y)
+    rng = np.random.default_rng(14)
+    for _ in range(3):
+        h = rng.standard_normal(A.n).astype(np.float32)
+        x.copy_(torch.from_numpy(h))
+        g.replay()
+        torch.cuda.synchronize()
+        check(A, h, y)
+
+
+def test_spmv_full_size_llm_and_rmat():
+    for name in ("llm", "rmat"):
+        A = valued(synth.config(name, "full"), 15)
+        plan = dbs.SpMVPlan.from_csr(A)
+        x = np.random.default_rng(16).standard_normal(A.n).astype(np.float32)
+        check(A, x, plan(torch.from_numpy(x).to(DEV)))
+        if name == "rmat":
+            assert plan.info()["split_rows"] > 0          # hub rows exercise the long-row split

@@ -92,6 +92,34 @@ def test_decode_layer_matches_dense_brute_force(seed):
     np.testing.assert_array_equal(t, (D != 0).astype(np.int64) @ (xp != 0).astype(np.int64) > 0)
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_spmv_csr_matches_dense_brute_force(seed):
+    """Dense-input SpMV: every stored entry times x as given (zeros and
+    negative entries included) against a dense fp64 matvec."""
+    rng = np.random.default_rng(seed + 200)
+    m = n = int(rng.integers(1, 70))         # square: an index mix-up mutant stays in bounds
+    A = synth.random_csr(m, n, float(rng.uniform(0.02, 0.7)), seed + 200)
+    x = rng.standard_normal(n).astype(np.float32)
+    x[rng.random(n) < 0.3] = 0.0
+    y, s = oracle.spmv_csr(A, x)
+    D = synth.csr_to_dense(A)
+    np.testing.assert_allclose(y, D @ x.astype(np.float64), rtol=0, atol=1e-12 * (1 + (np.abs(D) @ np.abs(x)).max()))
+    np.testing.assert_allclose(s, np.abs(D) @ np.abs(x.astype(np.float64)), rtol=1e-12)
+
+
+def test_spmv_csr_equals_spmspv_on_a_full_x():
+    """With no zero in x, SpMV and SpMSpV with every index active agree on
+    every row that holds an entry; rows without entries give 0."""
+    A = synth.random_csr(50, 40, 0.2, 7)
+    x = np.random.default_rng(8).uniform(0.5, 1.5, 40).astype(np.float32)
+    y, _ = oracle.spmv_csr(A, x)
+    ri, rv, _ = oracle.Oracle(A).spmspv(synth.SparseVec(40, np.arange(40, dtype=np.int32), x))
+    np.testing.assert_allclose(y[ri], rv, rtol=1e-12)
+    rest = np.ones(50, bool)
+    rest[ri] = False
+    assert (y[rest] == 0).all()
+
+
 def test_unit_vector_returns_column():
     A = synth.random_csr(60, 40, 0.3, 3)
     D = synth.csr_to_dense(A)

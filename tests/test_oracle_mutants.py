@@ -25,6 +25,8 @@ MUTANTS = {
     "csc2csr_wrong": ("blk_csc2csr[q] = p;", "blk_csc2csr[q] = q;"),
     "abs_sum_signed": ("sab[i] += fabs(p);", "sab[i] += p;"),
     "threshold_inclusive": ("if (!(a <= (double)tau)) idx_out[k++]", "if (a >= (double)tau) idx_out[k++]"),
+    "spmv_row_index_for_column": ("double p = (double)vals[k] * (double)x[j];", "double p = (double)vals[k] * (double)x[i];"),
+    "spmv_abs_signed": ("            sab += fabs(p);\n        }\n        y[i] = acc;", "            sab += p;\n        }\n        y[i] = acc;"),
 }
 
 PIN_FUNCS = [
@@ -38,6 +40,7 @@ PIN_FUNCS = [
     pins.test_format_classes_by_skew,
     pins.test_activation_mask_rule,
     lambda: [pins.test_decode_layer_matches_dense_brute_force(s) for s in range(3)],
+    lambda: [pins.test_spmv_csr_matches_dense_brute_force(s) for s in range(3)],
 ]
 
 
