@@ -139,6 +139,20 @@ class DBMatrix:
         out["B"] = B
         return out
 
+    RAW_ARRAYS = ("rb_ptr", "blk_desc", "blk_ref", "cb_ptr", "csc_desc", "csc_ref", "payload", "tiles",
+                  "rb_rows", "rb_ntiles")
+
+    def export_raw(self, name: str) -> np.ndarray:
+        """dbs_matrix_export_raw: one internal array as raw bytes (uint8)."""
+        which = self.RAW_ARRAYS.index(name)
+        lib = _lib.load()
+        nb = ctypes.c_int64(0)
+        _lib.check("dbs_matrix_export_raw", lib.dbs_matrix_export_raw(self._h, which, None, 0, ctypes.byref(nb)))
+        out = np.zeros(max(nb.value, 1), dtype=np.uint8)
+        _lib.check("dbs_matrix_export_raw",
+                   lib.dbs_matrix_export_raw(self._h, which, out.ctypes.data, out.nbytes, ctypes.byref(nb)))
+        return out[:nb.value]
+
     def export_csr(self):
         rp = np.empty(self.m + 1, np.int64)
         ci = np.empty(max(self.nnz, 1), np.int32)

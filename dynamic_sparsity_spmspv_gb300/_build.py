@@ -19,7 +19,7 @@ CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-SOURCES_CU = ["kernels.cu", "spmv.cu"]
+SOURCES_CU = ["kernels.cu", "spmv.cu", "build_gpu.cu"]
 SOURCES_CPP = ["matrix.cpp"]
 HEADERS = ["format.h", "internal.h"]
 

@@ -21,7 +21,7 @@ NUM_FORMATS = 5
 class dbs_build_opts(ctypes.Structure):
     _fields_ = [("th0", I32), ("th1", I32), ("th2", F64), ("force_format", I32),
                 ("tile_weight", I32), ("tile_max_row_blocks", I32), ("keep_host", I32),
-                ("host_only", I32), ("num_threads", I32)]
+                ("host_only", I32), ("num_threads", I32), ("device_convert", I32)]
 
 
 class dbs_exec_opts(ctypes.Structure):
@@ -62,6 +62,7 @@ PROTOTYPES = {
     "dbs_spmspv_dense": (I32, [P, P, P, ctypes.c_int, P, P]),
     "dbs_spmspv_dense_noalloc": (I32, [P, P, P, P]),
     "dbs_decode_layer": (I32, [P, P, ctypes.c_float, P, P, P]),
+    "dbs_matrix_export_raw": (I32, [P, I32, P, I64, P]),
     "dbs_spmv_plan_create": (I32, [I64, I64, I64, P, P, P, P, P]),
     "dbs_spmv": (I32, [P, P, P, P]),
     "dbs_spmv_plan_info": (I32, [P, P, P]),

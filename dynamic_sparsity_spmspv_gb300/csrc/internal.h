@@ -4,6 +4,8 @@
 
 #include <vector>
 
+#include <cuda_runtime_api.h>
+
 #include "../../include/dbspmspv.h"
 #include "format.h"
 
@@ -26,6 +28,13 @@ struct HostFormat {
     std::vector<uint16_t> rb_rows;    // nbr: rows of each row block that hold an entry (bit r = row r)
     std::vector<uint32_t> rb_ntiles;  // nbr: pull tiles whose first or last row block it is
 };
+
+// Device-side conversion (build_gpu.cu): fills H.rb_ptr, H.blk_desc and
+// H.blk_ref, allocates and encodes the payload on the device.  Sets
+// *fallback (and converts nothing) when a row's columns are not ascending.
+dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp, const int32_t *d_ci,
+                          const float *d_va, const dbs_build_opts &o, cudaStream_t s, HostFormat &H, int64_t *B,
+                          int64_t *P, uint4 **d_payload, bool *fallback);
 
 }  // namespace dbs
 

@@ -279,6 +279,7 @@ void dbs_build_opts_default(dbs_build_opts *o)
     o->keep_host = 0;
     o->host_only = 0;
     o->num_threads = 0;
+    o->device_convert = 0;
 }
 
 const char *dbs_status_string(dbs_status s)
@@ -313,28 +314,24 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
     cudaStream_t s = (cudaStream_t)stream;
     auto t_start = std::chrono::steady_clock::now();
 
-    // Inputs to host memory.
+    // Inputs to host memory (with device conversion, only the row pointers:
+    // the entries stay on the GPU).
     std::vector<int64_t> h_rp;
     std::vector<int32_t> h_ci;
     std::vector<float> h_va;
     const int64_t *rp = row_ptr;
     const int32_t *ci = col_idx;
     const float *va = vals;
+    bool on_gpu = inputs_on_device && o.device_convert && !o.host_only;
     try {
         if (inputs_on_device) {
             if (o.host_only) return DBS_ERR_INVALID_ARG;
             h_rp.resize((size_t)m + 1);
-            h_ci.resize((size_t)nnz);
-            if (vals) h_va.resize((size_t)nnz);
-            if (cudaMemcpy(h_rp.data(), row_ptr, sizeof(int64_t) * ((size_t)m + 1), cudaMemcpyDeviceToHost) != cudaSuccess ||
-                (nnz && cudaMemcpy(h_ci.data(), col_idx, sizeof(int32_t) * (size_t)nnz, cudaMemcpyDeviceToHost) != cudaSuccess) ||
-                (vals && nnz && cudaMemcpy(h_va.data(), vals, sizeof(float) * (size_t)nnz, cudaMemcpyDeviceToHost) != cudaSuccess)) {
+            if (cudaMemcpy(h_rp.data(), row_ptr, sizeof(int64_t) * ((size_t)m + 1), cudaMemcpyDeviceToHost) != cudaSuccess) {
                 cudaGetLastError();
                 return DBS_ERR_CUDA;
             }
             rp = h_rp.data();
-            ci = h_ci.data();
-            va = vals ? h_va.data() : nullptr;
         }
     } catch (const std::bad_alloc &) {
         return DBS_ERR_OOM;
@@ -357,7 +354,44 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
     HostFormat &H = *A->host;
     auto fail = [&](dbs_status st) { free_device(A); delete A->host; delete A; return st; };
 
+    if (on_gpu) {
+        // 1-2 on the device: blocks, formats and payload; the host gets the
+        // block-proportional arrays (Section 3.2.1 conversion without a sort)
+        int64_t B = 0, P = 0;
+        bool fallback = false;
+        uint4 *d_pay = nullptr;
+        dbs_status st;
+        try {
+            st = device_convert(m, n, nnz, row_ptr, col_idx, vals, o, s, H, &B, &P, &d_pay, &fallback);
+        } catch (const std::bad_alloc &) {
+            st = DBS_ERR_OOM;
+        }
+        if (st != DBS_OK) return fail(st);
+        if (fallback) {
+            on_gpu = false;                 // a row's columns are not ascending: host conversion
+        } else {
+            A->B = B; A->P = P;
+            A->d_payload = reinterpret_cast<U4 *>(d_pay);
+        }
+    }
+    if (!on_gpu && inputs_on_device) {
+        try {
+            h_ci.resize((size_t)nnz);
+            if (vals) h_va.resize((size_t)nnz);
+        } catch (const std::bad_alloc &) {
+            return fail(DBS_ERR_OOM);
+        }
+        if ((nnz && cudaMemcpy(h_ci.data(), col_idx, sizeof(int32_t) * (size_t)nnz, cudaMemcpyDeviceToHost) != cudaSuccess) ||
+            (vals && nnz && cudaMemcpy(h_va.data(), vals, sizeof(float) * (size_t)nnz, cudaMemcpyDeviceToHost) != cudaSuccess)) {
+            cudaGetLastError();
+            return fail(DBS_ERR_CUDA);
+        }
+        ci = h_ci.data();
+        va = vals ? h_va.data() : nullptr;
+    }
+
     try {
+      if (!on_gpu) {
         // 1. Row-block chunks converted in parallel.
         int nthreads = o.num_threads > 0 ? o.num_threads : (int)std::max(1u, std::thread::hardware_concurrency());
         const int64_t chunk_rb = std::max<int64_t>(1, std::min<int64_t>(4096, nbr / (int64_t)(8 * nthreads) + 1));
@@ -424,6 +458,8 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
                 std::vector<U4>().swap(c.payload);
             }
         }
+      }
+      const int64_t B = A->B;
 
         // 3. Block-CSC view: counting sort of primary blocks by column block;
         //    row blocks stay ascending within a column block.
@@ -531,7 +567,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         if ((st = upload(H.cb_ptr, &A->d_cb_ptr, 1, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.csc_desc, &A->d_csc_desc, (size_t)A->B + 8, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.csc_ref, &A->d_csc_ref, (size_t)A->B + 8, s)) != DBS_OK) return fail(st);
-        if ((st = upload(H.payload, &A->d_payload, 1, s)) != DBS_OK) return fail(st);
+        if (!on_gpu && (st = upload(H.payload, &A->d_payload, 1, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.tiles, &A->d_tiles, 1, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.rb_rows, &A->d_rb_rows, (size_t)nbr + 2, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.rb_ntiles, &A->d_rb_ntiles, (size_t)nbr + 1, s)) != DBS_OK) return fail(st);
@@ -539,6 +575,18 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         A->on_device = true;
     }
     I.on_device = A->on_device ? 1 : 0;
+    if (on_gpu && o.keep_host) {
+        // the host copy holds the payload too
+        try {
+            H.payload.resize((size_t)A->P);
+        } catch (const std::bad_alloc &) {
+            return fail(DBS_ERR_OOM);
+        }
+        if (A->P && cudaMemcpy(H.payload.data(), A->d_payload, (size_t)A->P * 16, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(DBS_ERR_CUDA);
+        }
+    }
     if (!o.keep_host && !o.host_only) { delete A->host; A->host = nullptr; }
     I.build_seconds = std::chrono::duration<double>(std::chrono::steady_clock::now() - t_start).count();
     *out = A;
@@ -596,6 +644,38 @@ dbs_status dbs_matrix_export_views(const dbs_matrix *A, int64_t *blk_row_ptr, in
         }
     } catch (const std::bad_alloc &) {
         return DBS_ERR_OOM;
+    }
+    return DBS_OK;
+}
+
+dbs_status dbs_matrix_export_raw(const dbs_matrix *A, int32_t which, void *dst, int64_t capacity, int64_t *bytes)
+{
+    if (!A || !bytes || which < 0 || which >= DBS_RAW_COUNT) return DBS_ERR_INVALID_ARG;
+    const size_t B = (size_t)A->B, nbr = (size_t)A->nbr, nbc = (size_t)A->nbc;
+    const HostFormat *H = A->host;
+    const void *dsrc = nullptr, *hsrc = nullptr;
+    size_t size = 0;
+    switch (which) {
+    case DBS_RAW_RB_PTR: size = (nbr + 1) * 4; dsrc = A->d_rb_ptr; hsrc = H ? H->rb_ptr.data() : nullptr; break;
+    case DBS_RAW_BLK_DESC: size = B * 8; dsrc = A->d_blk_desc; hsrc = H ? H->blk_desc.data() : nullptr; break;
+    case DBS_RAW_BLK_REF: size = B * 4; dsrc = A->d_blk_ref; hsrc = H ? H->blk_ref.data() : nullptr; break;
+    case DBS_RAW_CB_PTR: size = (nbc + 1) * 4; dsrc = A->d_cb_ptr; hsrc = H ? H->cb_ptr.data() : nullptr; break;
+    case DBS_RAW_CSC_DESC: size = B * 8; dsrc = A->d_csc_desc; hsrc = H ? H->csc_desc.data() : nullptr; break;
+    case DBS_RAW_CSC_REF: size = B * 4; dsrc = A->d_csc_ref; hsrc = H ? H->csc_ref.data() : nullptr; break;
+    case DBS_RAW_PAYLOAD: size = (size_t)A->P * 16; dsrc = A->d_payload; hsrc = H ? H->payload.data() : nullptr; break;
+    case DBS_RAW_TILES: size = (size_t)A->T * 16; dsrc = A->d_tiles; hsrc = H ? H->tiles.data() : nullptr; break;
+    case DBS_RAW_RB_ROWS: size = nbr * 2; dsrc = A->d_rb_rows; hsrc = H ? H->rb_rows.data() : nullptr; break;
+    default: size = nbr * 4; dsrc = A->d_rb_ntiles; hsrc = H ? H->rb_ntiles.data() : nullptr; break;
+    }
+    *bytes = (int64_t)size;
+    if (!dst) return DBS_OK;
+    if (capacity < (int64_t)size) return DBS_ERR_INVALID_ARG;
+    if (size == 0) return DBS_OK;
+    if (A->on_device) {
+        if (cudaMemcpy(dst, dsrc, size, cudaMemcpyDeviceToHost) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+    } else {
+        if (!hsrc) return DBS_ERR_INVALID_ARG;
+        std::memcpy(dst, hsrc, size);
     }
     return DBS_OK;
 }

@@ -92,6 +92,13 @@ typedef struct {
                                   is touched (the matrix can be inspected and exported
                                   but not multiplied).  For CPU-side checks. */
     int32_t num_threads;       /* host builder threads; 0 = all hardware threads */
+    int32_t device_convert;    /* 1 with inputs_on_device: find, classify and encode the
+                                  blocks on the GPU (no sort; device memory beyond input
+                                  and result: 4 B per row block + 13 B per block); the
+                                  block-proportional steps (offsets, block-CSC view,
+                                  tiles) stay on the host.  Needs the columns of every
+                                  row ascending, else the host converts.  Same result
+                                  byte for byte.  Default 0. */
 } dbs_build_opts;
 
 void dbs_build_opts_default(dbs_build_opts *opts);
@@ -181,6 +188,20 @@ dbs_status dbs_matrix_export_views(const dbs_matrix *A, int64_t *blk_row_ptr, in
  * row.  A round trip returns the input bit for bit.  Synchronous. */
 dbs_status dbs_matrix_export_csr(const dbs_matrix *A, int64_t *row_ptr, int32_t *col_idx,
                                  float *vals);
+
+/* Diagnostic copy of one internal array of the matrix (the device layout of
+ * the blocked format: row-block pointers u32[nbr+1], block descriptors
+ * {u32, u32}[B], payload offsets u32[B], column-block pointers u32[nbc+1],
+ * block-CSC descriptors {u32, u32}[B], block-CSC payload offsets u32[B],
+ * payload 16-byte units [P], pull tiles {u32 x4}[T], rows holding an entry
+ * u16[nbr], tiles per row block u32[nbr]) into HOST memory.  *bytes gets
+ * the array's size; the copy happens when dst is non-NULL and capacity is
+ * large enough (else DBS_ERR_INVALID_ARG).  Synchronous. */
+typedef enum {
+    DBS_RAW_RB_PTR = 0, DBS_RAW_BLK_DESC, DBS_RAW_BLK_REF, DBS_RAW_CB_PTR, DBS_RAW_CSC_DESC,
+    DBS_RAW_CSC_REF, DBS_RAW_PAYLOAD, DBS_RAW_TILES, DBS_RAW_RB_ROWS, DBS_RAW_RB_NTILES, DBS_RAW_COUNT
+} dbs_raw_array;
+dbs_status dbs_matrix_export_raw(const dbs_matrix *A, int32_t which, void *dst, int64_t capacity, int64_t *bytes);
 
 /* Scratch for SpMSpV and BFS on one matrix: a dense copy of x, the vector-block
  * masks, active lists, push task list, the output accumulator, counters and

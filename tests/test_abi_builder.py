@@ -42,7 +42,7 @@ def test_status_strings_and_version():
 
 def test_struct_layouts_match_header_sizes():
     # sizes implied by the C declarations on LP64
-    assert ctypes.sizeof(_lib.dbs_build_opts) == 40
+    assert ctypes.sizeof(_lib.dbs_build_opts) == 48
     assert ctypes.sizeof(_lib.dbs_exec_opts) == 32
     assert ctypes.sizeof(_lib.dbs_stats) == 104
     o = dbs.build_opts()
@@ -167,3 +167,21 @@ def test_empty_and_degenerate_shapes():
         M = dbs.DBMatrix(m, n, rp, np.zeros(0, np.int32), np.zeros(0, np.float32), host_only=1)
         inf = M.info()
         assert inf["nblocks"] == 0 and inf["nbr"] == (m + 15) // 16
+
+
+def test_export_raw_sizes_and_contents():
+    A = synth.config("llm", "small")
+    M = dbs.DBMatrix.from_csr(A, host_only=1, keep_host=1)
+    inf = M.info()
+    B, nbr, nbc = inf["nblocks"], inf["nbr"], inf["nbc"]
+    sizes = {"rb_ptr": 4 * (nbr + 1), "blk_desc": 8 * B, "blk_ref": 4 * B, "cb_ptr": 4 * (nbc + 1),
+             "csc_desc": 8 * B, "csc_ref": 4 * B, "payload": inf["payload_bytes"], "tiles": 16 * inf["ntiles"],
+             "rb_rows": 2 * nbr, "rb_ntiles": 4 * nbr}
+    for name, size in sizes.items():
+        assert M.export_raw(name).nbytes == size, name
+    rbp = M.export_raw("rb_ptr").view(np.uint32)
+    views = M.export_views()
+    np.testing.assert_array_equal(rbp, views["blk_row_ptr"])
+    ref = M.export_raw("blk_ref").view(np.uint32)
+    fmt = views["blk_format"]
+    assert (ref[fmt == 1] % 4 == 0).all()            # valued Dense blocks start on 64-byte boundaries

@@ -1,0 +1,113 @@
+"""Device-side conversion (device_convert = 1): the blocks are found,
+classified and encoded on the GPU, and the matrix must equal the host
+builder's byte for byte -- every internal array -- for every workload,
+forced format, pattern-only and valued inputs, ragged sizes and empty rows.
+Rows whose columns are not ascending fall back to the host conversion;
+out-of-range or repeated columns are rejected like on the host."""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+import __graft_entry__  # noqa: E402
+
+__graft_entry__.build()
+import dynamic_sparsity_spmspv_gb300 as dbs  # noqa: E402
+
+DEV = "cuda"
+
+
+def _dev(A):
+    return (torch.from_numpy(np.asarray(A.row_ptr, np.int64)).to(DEV),
+            torch.from_numpy(np.asarray(A.col_idx, np.int32)).to(DEV),
+            None if A.vals is None else torch.from_numpy(np.asarray(A.vals, np.float32)).to(DEV))
+
+
+def assert_same(A, **kw):
+    host = dbs.DBMatrix.from_csr(A, **kw)
+    rp, ci, va = _dev(A)
+    gpu = dbs.DBMatrix(A.m, A.n, rp, ci, va, device_convert=1, **kw)
+    ih, ig = host.info(), gpu.info()
+    for k in ("nblocks", "ntiles", "payload_bytes", "view_bytes", "blocks_by_format", "nnz_by_format"):
+        assert ih[k] == ig[k], k
+    for name in dbs.DBMatrix.RAW_ARRAYS:
+        np.testing.assert_array_equal(host.export_raw(name), gpu.export_raw(name), err_msg=name)
+    return gpu
+
+
+@pytest.mark.parametrize("name", synth.CONFIG_NAMES)
+def test_device_conversion_matches_host(name):
+    assert_same(synth.config(name, "small"))
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("name", ["llm", "fem", "rmat"])
+def test_device_conversion_forced_formats(name, fmt):
+    assert_same(synth.config(name, "small"), force_format=fmt)
+
+
+def test_device_conversion_thresholds_ragged_and_empty():
+    A = synth.random_csr(1003, 517, 0.3, 21)                     # ragged, mid-class blocks
+    assert_same(A)
+    assert_same(A, th0=8, th1=64, th2=1.5, tile_weight=16, tile_max_row_blocks=1)
+    rows = np.repeat(np.arange(A.m), np.diff(A.row_ptr))
+    keep = (rows // 16) % 3 != 1                                   # whole empty row blocks
+    B = synth.csr_from_coo(A.m, A.n, rows[keep], A.col_idx[keep], A.vals[keep])
+    assert_same(B)
+    P = synth.CSR(B.m, B.n, B.row_ptr, B.col_idx, None)            # pattern only (inline blocks)
+    assert_same(P)
+    E = synth.CSR(40, 30, np.zeros(41, np.int64), np.zeros(0, np.int32), np.zeros(0, np.float32))
+    assert_same(E)
+
+
+def test_device_conversion_then_multiply_and_keep_host():
+    """A device-converted matrix multiplies like the host one, and keep_host
+    holds its payload too (export round trip)."""
+    A = synth.config("llm", "small")
+    rp, ci, va = _dev(A)
+    M = dbs.DBMatrix(A.m, A.n, rp, ci, va, device_convert=1, keep_host=1)
+    r2, c2, v2 = M.export_csr()
+    np.testing.assert_array_equal(r2, A.row_ptr)
+    np.testing.assert_array_equal(c2, A.col_idx)
+    np.testing.assert_array_equal(v2.view(np.uint32), A.vals.view(np.uint32))
+    Mh = dbs.DBMatrix.from_csr(A)
+    x = torch.from_numpy(synth.x_activation(A.n, [3])).to(DEV)
+    y1 = dbs.decode_layer(M, x, 1.0, ws=dbs.Workspace(M)).cpu().numpy()
+    y2 = dbs.decode_layer(Mh, x, 1.0, ws=dbs.Workspace(Mh)).cpu().numpy()
+    np.testing.assert_allclose(y1, y2, rtol=1e-6, atol=1e-6)
+
+
+def test_device_conversion_unsorted_rows_fall_back_and_bad_columns_fail():
+    A = synth.random_csr(200, 150, 0.1, 23)
+    ci = A.col_idx.copy()
+    s, e = int(A.row_ptr[5]), int(A.row_ptr[6])
+    ci[s:e] = ci[s:e][::-1]                                        # one row in descending order
+    U = synth.CSR(A.m, A.n, A.row_ptr, ci, A.vals)
+    host = dbs.DBMatrix.from_csr(U)
+    rp, c, v = _dev(U)
+    gpu = dbs.DBMatrix(U.m, U.n, rp, c, v, device_convert=1)
+    for name in dbs.DBMatrix.RAW_ARRAYS:
+        np.testing.assert_array_equal(host.export_raw(name), gpu.export_raw(name), err_msg=name)
+    for bad in (A.n, -1):
+        ci2 = A.col_idx.copy()
+        ci2[7] = bad
+        rp, c, v = _dev(synth.CSR(A.m, A.n, A.row_ptr, ci2, A.vals))
+        with pytest.raises(dbs.DbsError):
+            dbs.DBMatrix(A.m, A.n, rp, c, v, device_convert=1)
+    ci3 = A.col_idx.copy()
+    k = int(A.row_ptr[9])
+    assert A.row_ptr[10] - A.row_ptr[9] >= 2
+    ci3[k + 1] = ci3[k]                                            # repeated column
+    rp, c, v = _dev(synth.CSR(A.m, A.n, A.row_ptr, ci3, A.vals))
+    with pytest.raises(dbs.DbsError):
+        dbs.DBMatrix(A.m, A.n, rp, c, v, device_convert=1)
+
+
+@pytest.mark.parametrize("name", ["rmat", "llm", "fem"])
+def test_device_conversion_full_size(name):
+    M = assert_same(synth.config(name, "full"))
+    assert M.info()["build_seconds"] > 0
