@@ -2064,8 +2064,14 @@ dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx
                              {(const void *)k_spmspv_sparse<1, false>, (const void *)k_spmspv_sparse<1, true>}};
     const void *fn = fns[sri][st_on];
     w->last_was_bfs = false;
-    return launch_ws(w, fn, w->grid_sparse[sri][st_on], P, (cudaStream_t)stream,
-                     sr == DBS_PLUS_TIMES_F32 ? SMEM0 : SMEM1);
+    // A call whose expected push work (x entries times the mean column-block
+    // length) is below 16 tasks of 256 blocks per SM runs on one block per
+    // SM: its grid barriers and block start-up cost less, and the work fits.
+    int grid = w->grid_sparse[sri][st_on];
+    const long long nbc = A->nbc > 0 ? A->nbc : 1;
+    const long long work = (long long)x_nnz * ((A->B + nbc - 1) / nbc);
+    if (path != DBS_PATH_PULL && work < 16LL * 256LL * w->sms) grid = std::min(grid, w->sms);
+    return launch_ws(w, fn, grid, P, (cudaStream_t)stream, sr == DBS_PLUS_TIMES_F32 ? SMEM0 : SMEM1);
 }
 
 dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_path path, dbs_workspace *w,
