@@ -2065,12 +2065,14 @@ dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx
     const void *fn = fns[sri][st_on];
     w->last_was_bfs = false;
     // A call whose expected push work (x entries times the mean column-block
-    // length) is below 16 tasks of 256 blocks per SM runs on one block per
+    // length) is below two tasks of 256 blocks per SM runs on one block per
     // SM: its grid barriers and block start-up cost less, and the work fits.
+    // (A larger bound made calls that turn out to pull, or push with many
+    // payload hits, slower.)
     int grid = w->grid_sparse[sri][st_on];
     const long long nbc = A->nbc > 0 ? A->nbc : 1;
     const long long work = (long long)x_nnz * ((A->B + nbc - 1) / nbc);
-    if (path != DBS_PATH_PULL && work < 16LL * 256LL * w->sms) grid = std::min(grid, w->sms);
+    if (path != DBS_PATH_PULL && work < 2LL * 256LL * w->sms) grid = std::min(grid, w->sms);
     return launch_ws(w, fn, grid, P, (cudaStream_t)stream, sr == DBS_PLUS_TIMES_F32 ? SMEM0 : SMEM1);
 }
 
