@@ -29,7 +29,7 @@
  *                          per-block nnz, and the low-level format class from
  *                          the th0/th1/th2 density and skew rule.
  *
- * Readings of points the paper leaves open (each also listed in the design doc):
+ * Readings of points the paper leaves open:
  *   - Output pattern is structural: row i is in y iff some stored A(i,j) has
  *     an active x_j, even if the values cancel to zero.
  *   - x_j is active iff x_j != 0 (so -0.0 is inactive and NaN is active);
