@@ -800,6 +800,36 @@ def main():
            "roofline": roofline, "per_density": per_density, "bfs": bfs_info, "clocks": clocks,
            "wall_s_timed_region": wall}
 
+    # Hot-L2 numbers (no flush between calls: what L2 reuse adds) and the
+    # kernel's own floor: one call with an empty x (every phase, no work),
+    # against which the smallest densities' µs are read.
+    def back_to_back(call, n=20):
+        for _ in range(3):
+            call()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            call()
+        e1.record(stream)
+        e1.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / n
+
+    x_empty = torch.empty(0, dtype=torch.int32, device=dev)
+    out["hot_l2_us_per_call"] = {str(d): round(back_to_back(
+        lambda d=d: dbs.spmspv(M, x_dev[d][0], None, semiring="or_and", ws=ws, y_idx=y_idx, y_nnz=y_nnz)), 2)
+        for d in DENSITIES}
+    flush(0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    dbs.spmspv(M, x_empty, None, semiring="or_and", ws=ws, y_idx=y_idx, y_nnz=y_nnz)
+    e1.record(stream)
+    e1.synchronize()
+    out["floor_us"] = {"spmspv_empty_x_l2_flushed": round(1e3 * e0.elapsed_time(e1), 2),
+                       "spmspv_empty_x_back_to_back": round(back_to_back(
+                           lambda: dbs.spmspv(M, x_empty, None, semiring="or_and", ws=ws, y_idx=y_idx,
+                                              y_nnz=y_nnz)), 2)}
+    assert ws.check() == 0
+
     # push/pull crossover on this GPU: forced paths, same inputs, same timing
     if args.path_sweep > 0:
         sweep = []
