@@ -649,6 +649,24 @@ __device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint
     return rows;
 }
 
+// A valued COO block of at most three entries is one 16-byte unit:
+// coordinate bytes 0-2, values from byte 4.  Adds the products of its active
+// entries into yr (row r of the block at yr[r]) and returns their rows.
+__device__ __forceinline__ uint32_t coo_unit(uint4 u, uint32_t nnz, uint32_t act, const float *xb, float *yr)
+{
+    const float v[3] = {__uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
+    uint32_t rows = 0;
+#pragma unroll
+    for (uint32_t j = 0; j < 3u; ++j) {
+        const uint32_t e = (u.x >> (8u * j)) & 0xFFu, c = e & 15u, r = e >> 4;
+        if (j < nnz && ((act >> c) & 1u)) {
+            rows |= 1u << r;
+            atomicAdd(yr + r, v[j] * xval(xb, c));
+        }
+    }
+    return rows;
+}
+
 // ------------------------------------------------------------- traversal
 
 // Per-warp state of a pull task.  Plus-times keeps per-row partial sums;
@@ -1151,15 +1169,35 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             }
         } else {
             const uint32_t nq2 = W.nq2;
-            // COO hits one per lane
+            // COO hits: payload offsets of all of them first (independent
+            // loads, the offset replacing the position and the active
+            // columns the meta word's column mask), then one block per lane,
+            // two per lane at a time with both first payload units loaded
+            // before either is decoded
             for (uint32_t i = lane; i < nq; i += 32) {
-                const uint32_t e = W.qe[i], meta = W.qm[i], rb = W.qr[i];
-                const uint32_t nnz = meta_nnz(meta);
-                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + __ldg(P.csc_ref + q0 + (e & 0xFFFFu)));
-                float *yr = y + (size_t)rb * 16u;
-                const uint32_t rows = coo_lane(b, nnz, e >> 16, wx, true, [&](uint32_t r, float v) { atomicAdd(yr + r, v); });
-                if (!DOUT && rows) or16(out_rm, rb, rows);
-                if (ST) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
+                const uint32_t e = W.qe[i];
+                W.qe[i] = __ldg(P.csc_ref + q0 + (e & 0xFFFFu));
+                W.qm[i] = (W.qm[i] & ~0xFFFFu) | (e >> 16);
+            }
+            __syncwarp();
+            for (uint32_t i = lane; i < nq; i += 64) {
+                const bool two = i + 32u < nq;
+                const uint32_t ref[2] = {W.qe[i], two ? W.qe[i + 32u] : W.qe[i]};
+                const uint32_t mt[2] = {W.qm[i], two ? W.qm[i + 32u] : 0u};
+                const uint32_t rbk[2] = {W.qr[i], two ? W.qr[i + 32u] : 0u};
+                const uint4 u[2] = {__ldg(P.payload + ref[0]), __ldg(P.payload + ref[1])};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && !two) break;
+                    const uint32_t nnz = meta_nnz(mt[h]), act = mt[h] & 0xFFFFu;
+                    float *yr = y + (size_t)rbk[h] * 16u;
+                    const uint32_t rows =
+                        nnz <= 3u ? coo_unit(u[h], nnz, act, wx, yr)
+                                  : coo_lane(reinterpret_cast<const uint8_t *>(P.payload + ref[h]), nnz, act, wx, true,
+                                             [&](uint32_t r, float v) { atomicAdd(yr + r, v); });
+                    if (!DOUT && rows) or16(out_rm, rbk[h], rows);
+                    if (ST) c_bytes += 4u + val_offset(FMT_COO, nnz) + 4u * nnz;
+                }
             }
             // the other hits: payload offsets first (independent loads; the
             // offset replaces the position and the active columns replace
