@@ -185,3 +185,26 @@ def test_export_raw_sizes_and_contents():
     ref = M.export_raw("blk_ref").view(np.uint32)
     fmt = views["blk_format"]
     assert (ref[fmt == 1] % 4 == 0).all()            # valued Dense blocks start on 64-byte boundaries
+
+
+def test_export_raw_rejects_bad_requests():
+    A = synth.config("er", "small")
+    M = dbs.DBMatrix.from_csr(A, host_only=1, keep_host=1)
+    lib = _lib.load()
+    nb = ctypes.c_int64(0)
+    assert lib.dbs_matrix_export_raw(M.handle, 99, None, 0, ctypes.byref(nb)) == 1
+    assert lib.dbs_matrix_export_raw(M.handle, 0, None, 0, None) == 1
+    assert lib.dbs_matrix_export_raw(M.handle, 0, None, 0, ctypes.byref(nb)) == 0 and nb.value > 0
+    small = np.zeros(max(nb.value - 1, 1), np.uint8)
+    assert lib.dbs_matrix_export_raw(M.handle, 0, small.ctypes.data, small.nbytes, ctypes.byref(nb)) == \
+        1
+
+
+def test_device_convert_with_host_inputs_is_the_host_conversion():
+    """device_convert applies to device inputs only; with host arrays the
+    host builder runs and the result is unchanged."""
+    A = synth.config("llm", "small")
+    M1 = dbs.DBMatrix.from_csr(A, host_only=1, keep_host=1)
+    M2 = dbs.DBMatrix.from_csr(A, host_only=1, keep_host=1, device_convert=1)
+    for name in dbs.DBMatrix.RAW_ARRAYS:
+        np.testing.assert_array_equal(M1.export_raw(name), M2.export_raw(name), err_msg=name)
