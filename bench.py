@@ -190,6 +190,19 @@ def cpu_baseline(A, xs, sources, touched_x, touched_bfs, budget_s: float):
                       f"+ {bfs_runs} queue BFS; {t_total:.1f} s of CPU time; units = the same touched nnz"}
 
 
+def reduce_over_ranks(t_ms: float, units: float, device):
+    """Whole-job totals of a replicated run: the slowest rank's timed
+    milliseconds and the units all ranks processed (one all-reduce each,
+    on whatever process group is initialised)."""
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([float(t_ms)], device=device, dtype=torch.float64)
+    uu = torch.tensor([float(units)], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    dist.all_reduce(uu, op=dist.ReduceOp.SUM)
+    return float(tt.item()), float(uu.item())
+
+
 def run_reference(args):
     """--impl reference: the CPU oracle timed on this host's cores."""
     ws_, rank, _ = _dist()
@@ -740,11 +753,7 @@ def main():
     units_total = sum(units_sp.values()) + units_bfs
     t_max = t_total_ms
     if world > 1:
-        tt = torch.tensor([t_total_ms], device=dev)
-        uu = torch.tensor([float(units_total)], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.all_reduce(uu, op=torch.distributed.ReduceOp.SUM)
-        t_max, units_total = float(tt.item()), float(uu.item())
+        t_max, units_total = reduce_over_ranks(t_total_ms, units_total, dev)
     value = units_total / (t_max * 1e-3)
 
     peak, peak_kind = _peaks()
