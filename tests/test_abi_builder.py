@@ -208,3 +208,37 @@ def test_device_convert_with_host_inputs_is_the_host_conversion():
     M2 = dbs.DBMatrix.from_csr(A, host_only=1, keep_host=1, device_convert=1)
     for name in dbs.DBMatrix.RAW_ARRAYS:
         np.testing.assert_array_equal(M1.export_raw(name), M2.export_raw(name), err_msg=name)
+
+
+@pytest.mark.parametrize("name,kw", [("llm", {"tile_weight": 24}), ("rmat", {}), ("fem", {"tile_max_row_blocks": 1})])
+def test_tiles_and_row_block_tile_counts(name, kw):
+    """Pull tiles cover the blocks in order within their caps, and every row
+    block records how many tiles start or end in it (what the decoding
+    layer's last-arriver reduction counts on)."""
+    A = synth.config(name, "small")
+    M = dbs.DBMatrix.from_csr(A, host_only=1, keep_host=1, **kw)
+    inf = M.info()
+    tiles = M.export_raw("tiles").view(np.uint32).reshape(-1, 4)
+    rbp = M.export_raw("rb_ptr").view(np.uint32)
+    ntl = M.export_raw("rb_ntiles").view(np.uint32)
+    span = tiles[:, 3] & 0xFFFF
+    nblk = tiles[:, 3] >> 20
+    assert (tiles[1:, 0] == tiles[:-1, 0] + nblk[:-1]).all() and tiles[0, 0] == 0
+    assert int(nblk.sum()) == inf["nblocks"]
+    assert ((tiles[:, 0] & 1) + nblk <= 256).all() and (span >= 1).all() and (span <= 32).all()
+    ref = np.zeros(inf["nbr"], np.int64)
+    for t in range(tiles.shape[0]):
+        p0, n, rb0, sp = int(tiles[t, 0]), int(nblk[t]), int(tiles[t, 2]), int(span[t])
+        # first and last row blocks of the span hold the tile's first and last blocks
+        assert rbp[rb0] <= p0 < rbp[rb0 + 1]
+        assert rbp[rb0 + sp - 1] <= p0 + n - 1 < rbp[rb0 + sp]
+        ref[rb0] += 1
+        if sp > 1:
+            ref[rb0 + sp - 1] += 1
+    np.testing.assert_array_equal(ntl, ref)
+    rows = M.export_raw("rb_rows").view(np.uint16)
+    nonempty = np.diff(A.row_ptr) > 0
+    want = np.zeros(inf["nbr"], np.uint32)
+    for i in np.nonzero(nonempty)[0]:
+        want[i // 16] |= 1 << (i % 16)
+    np.testing.assert_array_equal(rows, want.astype(np.uint16))
