@@ -299,7 +299,9 @@ dbs_status dbs_spmv_plan_create(int64_t m, int64_t n, int64_t nnz, const int64_t
 
 /* y = A x: x device float32[n] (every entry used, zeros included), y device
  * float32[m], every row written (0 for rows without entries).  One ordinary
- * launch, deterministic summation order, capturable in a CUDA graph.  ASYNC. */
+ * launch, deterministic summation order, capturable in a CUDA graph.  Calls
+ * on one plan must be ordered on one stream (they share the split rows'
+ * partial sums and counters).  ASYNC. */
 dbs_status dbs_spmv(dbs_spmv_plan *plan, const float *x, float *y, void *stream);
 
 /* Rows per bucket (HOST int64[8], may be NULL: rows on 1, 2, 4, 8, 16 and
