@@ -359,6 +359,26 @@ def run_configs(dbs, torch, dev, stream, flush, reps: int):
                   "levels_mean": float(np.mean(nls))})
     assert ws.check() == 0
     ws.close(); M.close()
+
+    # the same grid without hubs: thousands of levels with small frontiers
+    # (the long-diameter regime), four sources
+    A = synth.grid_hubs(4096, 0.10, 0, 0, seed=47)
+    M = dbs.DBMatrix.from_csr(A)
+    ws = dbs.Workspace(M)
+    levels = torch.empty(A.n, dtype=torch.int32, device=dev)
+    deg = np.diff(A.row_ptr)
+    ts, teps, nls = [], [], []
+    for i, src in enumerate(synth.bfs_sources(A, 4, [48, 7])):
+        t = timed(lambda: dbs.bfs(M, int(src), levels=levels, ws=ws, sync=False), i)
+        lv = levels.cpu().numpy()
+        ts.append(t)
+        teps.append(int(deg[lv >= 0].sum()) // 2 / t * 1e6 / 1e9)
+        nls.append(int(lv.max()) + 1)
+    lines.append({"workload": "grid (no hubs)", "mode": "bfs (4 sources)", "us": round(float(np.median(ts)), 2),
+                  "gteps_harmonic": round(len(teps) / sum(1.0 / v for v in teps), 3),
+                  "levels_mean": float(np.mean(nls)), "us_per_level": round(float(np.median(ts)) / float(np.mean(nls)), 2)})
+    assert ws.check() == 0
+    ws.close(); M.close()
     return lines
 
 
