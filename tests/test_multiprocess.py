@@ -60,3 +60,27 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_touched_nnz_counter_matches_brute_force():
+    """The bench's unit (touched nnz: nnz of the blocks in column blocks that
+    hold an active x entry, summed over BFS levels) against a direct count
+    over the CSR entries."""
+    import numpy as np
+    import oracle
+    import synth
+    A = synth.config("rmat", "small")
+    counter = bench.TouchedCounter(oracle.block_views(A))
+    col_cb = A.col_idx.astype(np.int64) // 16
+    for k in (0, 1, 7, 100, 2000):
+        x = synth.x_uniform(A.n, k, [5, k], valued=False)
+        act = np.zeros((A.n + 15) // 16, bool)
+        act[x.idx // 16] = True
+        assert counter.spmspv(x.idx) == int(act[col_cb].sum())
+    lv = oracle.Oracle(A).bfs_queue(int(synth.bfs_sources(A, 1, [5, 9])[0]))
+    want = 0
+    for L in range(int(lv.max()) + 1):
+        act = np.zeros((A.n + 15) // 16, bool)
+        act[np.nonzero(lv == L)[0] // 16] = True
+        want += int(act[col_cb].sum())
+    assert counter.bfs(lv) == want
