@@ -163,6 +163,14 @@ class TouchedCounter:
         return int(self.per_cb[key % self.nbc].sum())
 
 
+def _host_cores() -> int:
+    """Cores this process may run on (the oracle itself uses one)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(A, xs, sources, touched_x, touched_bfs, budget_s: float):
     """The oracle as it stands, single-threaded, on a bounded sample of the
     same step (densities cycled, then BFS sources)."""
@@ -185,7 +193,7 @@ def cpu_baseline(A, xs, sources, touched_x, touched_bfs, budget_s: float):
         units += touched_bfs[i % len(sources)]
         bfs_runs += 1
         i += 1
-    return {"value": units / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": units / t_total, "unit": UNIT, "cores": 1, "host_cores_available": _host_cores(), "kind": "oracle",
             "sample": f"{i} steps: {calls} oracle SpMSpV calls (push scatter, fp64 C, 1 thread) at the 5 densities "
                       f"+ {bfs_runs} queue BFS; {t_total:.1f} s of CPU time; units = the same touched nnz"}
 
@@ -241,7 +249,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bool", "data": "synthetic",
             "config": {"workload": WORKLOAD, "densities": list(DENSITIES), "bfs_sources": N_SOURCES},
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "host_cores_available": _host_cores(),
+                             "kind": "oracle",
                              "sample": f"{args.steps} steps, each one oracle SpMSpV at one of the 5 densities "
                                        "(cycling) plus a queue BFS every 5th step; fp64 C, 1 thread"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
