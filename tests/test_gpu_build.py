@@ -111,3 +111,50 @@ def test_device_conversion_unsorted_rows_fall_back_and_bad_columns_fail():
 def test_device_conversion_full_size(name):
     M = assert_same(synth.config(name, "full"))
     assert M.info()["build_seconds"] > 0
+
+
+@pytest.mark.parametrize("name", ["rmat", "llm"])
+def test_device_conversion_full_size_against_oracle(name):
+    """A device-converted matrix against the oracle directly, not only
+    against the host builder: its block views (DB-SpMSpV Section 3.2.1,
+    Figure 5(b)) equal the oracle's, and its products pass the parity bar --
+    Boolean SpMSpV at three densities on every path and BFS levels for the
+    R-MAT graph, plus-times SpMSpV and the DB-Decoding layer (Section 4.3)
+    for the LLM layer."""
+    import oracle
+    from test_gpu_parity import assert_parity, _t
+
+    A = synth.config(name, "full")
+    rp, ci, va = _dev(A)
+    M = dbs.DBMatrix(A.m, A.n, rp, ci, va, device_convert=1)
+    del rp, ci, va
+    V, W = M.export_views(), oracle.block_views(A)
+    assert V["B"] == W["B"]
+    for k in ("blk_row_ptr", "blk_col_idx", "blk_col_ptr", "blk_row_idx", "blk_csc2csr", "blk_nnz"):
+        np.testing.assert_array_equal(V[k], W[k], err_msg=k)
+    np.testing.assert_array_equal(V["blk_format"], W["blk_class"])
+    del V, W
+    O = oracle.Oracle(A)
+    ws = dbs.Workspace(M)
+    if name == "rmat":
+        for d in (1e-3, 1e-2, 1e-1):
+            x = synth.x_uniform(A.n, int(round(d * A.n)), [60, int(d * 1e4)], valued=False)
+            for path in ("auto", "push", "pull"):
+                assert_parity(A, O, M, ws, x, "or_and", path=path)
+        for src in synth.bfs_sources(A, 2, [60, 7]):
+            lev, nl = dbs.bfs(M, int(src), ws=ws)
+            ref = O.bfs_queue(int(src))
+            np.testing.assert_array_equal(lev.cpu().numpy(), ref)
+            assert nl == int(ref.max()) + 1
+    else:
+        for t in range(2):
+            xd = synth.x_relu_topk(A.n, 1101, [61, t])
+            nz = np.nonzero(xd)[0].astype(np.int32)
+            for path in ("auto", "push", "pull"):
+                assert_parity(A, O, M, ws, synth.SparseVec(A.n, nz, xd[nz]), path=path)
+            xa = synth.x_activation(A.n, [62, t])
+            y = dbs.decode_layer(M, _t(xa), 1.6449, ws=ws).cpu().numpy()
+            assert ws.check() == 0
+            ref, s, touched = O.decode_layer(xa, 1.6449)
+            assert oracle.tolerance_ok(y[touched], ref[touched], s[touched]).all()
+            assert (y[~touched] == 0).all()

@@ -118,3 +118,25 @@ def test_llm_full_decode_layer(full):
             ref, s, touched = O.decode_layer(xa, 1.6449)
             assert oracle.tolerance_ok(y[touched], ref[touched], s[touched]).all()
             assert (y[~touched] == 0).all()
+
+
+def test_grid_without_hubs_full_bfs():
+    """DB-SpMSpV Section 4.2 (DB-BFS) in the long-diameter regime: the
+    4096 x 4096 grid with 10 % of its edges deleted and no hubs, whose BFS
+    runs thousands of levels over frontiers of a few thousand vertices.
+    Levels are bit-exact against the queue BFS for the benchmark's four
+    sources on the auto path and for the first source with every level
+    forced to push and to pull; the level count is checked far beyond the
+    first 64 levels, whose per-level statistics the device records."""
+    A = synth.grid_hubs(4096, 0.10, 0, 0, seed=47)
+    O = oracle.Oracle(A)
+    M = dbs.DBMatrix.from_csr(A)
+    ws = dbs.Workspace(M)
+    for i, src in enumerate(synth.bfs_sources(A, 4, [48, 7])):
+        ref = O.bfs_queue(int(src))
+        assert int(ref.max()) + 1 > 1000
+        for path in (PATHS if i == 0 else ("auto",)):
+            lev, nl = dbs.bfs(M, int(src), ws=ws, path=path)
+            assert ws.check() == 0
+            np.testing.assert_array_equal(lev.cpu().numpy(), ref, err_msg=f"source {src}, {path}")
+            assert nl == int(ref.max()) + 1
