@@ -274,6 +274,12 @@ def dbs_spmspv_dense_noalloc(A: DBMatrix, x, *, y, stream=None):
     return y
 
 
+def dbs_spmspv_dense_noalloc_check(stream=None) -> int:
+    """dbs_spmspv_dense_noalloc_check: synchronizes the stream and returns the
+    status the last allocation-free call latched on the device (0 = OK)."""
+    return int(_lib.load().dbs_spmspv_dense_noalloc_check(_stream_handle(stream)))
+
+
 def dbs_decode_layer(A: DBMatrix, x, tau: float = 0.0, *, y=None, ws: Workspace, stream=None):
     """dbs_decode_layer: y = A x' with x' = x where |x| > tau, else 0 (dense
     CUDA float32 x, 16-byte aligned) -> dense y, pull path, one launch."""

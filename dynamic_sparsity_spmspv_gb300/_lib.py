@@ -61,6 +61,8 @@ PROTOTYPES = {
     "dbs_spmspv": (I32, [P, ctypes.c_int, P, P, I64, P, P, P, P, ctypes.c_int, P, P]),
     "dbs_spmspv_dense": (I32, [P, P, P, ctypes.c_int, P, P]),
     "dbs_spmspv_dense_noalloc": (I32, [P, P, P, P]),
+    "dbs_spmspv_dense_noalloc_check": (I32, [P]),
+    "dbs_debug_fail_alloc": (I32, [I64, P]),
     "dbs_decode_layer": (I32, [P, P, ctypes.c_float, P, P, P]),
     "dbs_matrix_export_raw": (I32, [P, I32, P, I64, P]),
     "dbs_spmv_plan_create": (I32, [I64, I64, I64, P, P, P, P, P]),

@@ -291,9 +291,31 @@ namespace dbs {
 // a device allocation holding the encoded payload (P units).  `fallback`
 // is set when a row's columns are not ascending (the host builder handles
 // any order).  Validation failures return DBS_ERR_INVALID_ARG.
+static dbs_status device_convert_impl(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp, const int32_t *d_ci,
+                                      const float *d_va, const dbs_build_opts &o, cudaStream_t s, HostFormat &H,
+                                      int64_t *B, int64_t *P, uint4 **d_payload, bool *fallback,
+                                      void *(&scratch)[6]);
+
 dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp, const int32_t *d_ci,
                           const float *d_va, const dbs_build_opts &o, cudaStream_t s, HostFormat &H, int64_t *B,
                           int64_t *P, uint4 **d_payload, bool *fallback)
+{
+    // the device scratch of a conversion that a host allocation failure
+    // interrupts is released here
+    void *scratch[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    try {
+        return device_convert_impl(m, n, nnz, d_rp, d_ci, d_va, o, s, H, B, P, d_payload, fallback, scratch);
+    } catch (const std::bad_alloc &) {
+        for (void *q : scratch) cudaFree(q);
+        *d_payload = nullptr;
+        return DBS_ERR_OOM;
+    }
+}
+
+static dbs_status device_convert_impl(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp, const int32_t *d_ci,
+                                      const float *d_va, const dbs_build_opts &o, cudaStream_t s, HostFormat &H,
+                                      int64_t *B, int64_t *P, uint4 **d_payload, bool *fallback,
+                                      void *(&scratch)[6])
 {
     *fallback = false;
     *d_payload = nullptr;
@@ -308,16 +330,24 @@ dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp
     uint8_t *d_units = nullptr;
     auto cleanup = [&]() {
         cudaFree(d_count); cudaFree(d_rb_ptr); cudaFree(d_ref); cudaFree(d_err); cudaFree(d_desc); cudaFree(d_units);
+        for (void *&q : scratch) q = nullptr;
+    };
+    // what the caller frees if a host allocation throws
+    auto track = [&]() {
+        scratch[0] = d_count; scratch[1] = d_rb_ptr; scratch[2] = d_ref; scratch[3] = d_err; scratch[4] = d_desc;
+        scratch[5] = d_units;
     };
     auto cuda_fail = [&]() { cudaGetLastError(); cleanup(); return DBS_ERR_CUDA; };
     const unsigned grid = (unsigned)((nbr + CT / 32 - 1) / (CT / 32));
-    if (cudaMalloc(&d_count, sizeof(uint32_t) * (size_t)(nbr + 1)) != cudaSuccess ||
-        cudaMalloc(&d_err, sizeof(unsigned)) != cudaSuccess) { cudaGetLastError(); cleanup(); return DBS_ERR_OOM; }
+    if (dev_malloc(&d_count, sizeof(uint32_t) * (size_t)(nbr + 1)) != cudaSuccess ||
+        dev_malloc(&d_err, sizeof(unsigned)) != cudaSuccess) { cudaGetLastError(); cleanup(); return DBS_ERR_OOM; }
     if (cudaMemsetAsync(d_err, 0, sizeof(unsigned), s) != cudaSuccess ||
         cudaMemsetAsync(d_count, 0, sizeof(uint32_t) * (size_t)(nbr + 1), s) != cudaSuccess) return cuda_fail();
+    track();
     C.rb_count = d_count;
     C.err = d_err;
     if (grid) k_conv_count<<<grid, CT, 0, s>>>(C);
+    host_alloc_point();
     std::vector<uint32_t> cnt((size_t)nbr);
     unsigned err = 0;
     if (cudaGetLastError() != cudaSuccess ||
@@ -337,16 +367,18 @@ dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp
     }
     *B = (int64_t)tot;
     const size_t nB = (size_t)tot;
-    if (cudaMalloc(&d_rb_ptr, sizeof(uint32_t) * (size_t)(nbr + 1)) != cudaSuccess ||
-        cudaMalloc(&d_desc, sizeof(uint2) * (nB + 1)) != cudaSuccess ||
-        cudaMalloc(&d_units, nB + 16) != cudaSuccess ||
-        cudaMalloc(&d_ref, sizeof(uint32_t) * (nB + 1)) != cudaSuccess) { cudaGetLastError(); cleanup(); return DBS_ERR_OOM; }
+    if (dev_malloc(&d_rb_ptr, sizeof(uint32_t) * (size_t)(nbr + 1)) != cudaSuccess ||
+        dev_malloc(&d_desc, sizeof(uint2) * (nB + 1)) != cudaSuccess ||
+        dev_malloc(&d_units, nB + 16) != cudaSuccess ||
+        dev_malloc(&d_ref, sizeof(uint32_t) * (nB + 1)) != cudaSuccess) { cudaGetLastError(); cleanup(); return DBS_ERR_OOM; }
+    track();
     if (cudaMemcpyAsync(d_rb_ptr, H.rb_ptr.data(), sizeof(uint32_t) * (size_t)(nbr + 1), cudaMemcpyHostToDevice, s) != cudaSuccess)
         return cuda_fail();
     C.rb_ptr = d_rb_ptr;
     C.desc = d_desc;
     C.units = d_units;
     if (grid) k_conv_desc<<<grid, CT, 0, s>>>(C);
+    host_alloc_point();
     std::vector<uint8_t> units(nB);
     H.blk_desc.resize(nB);
     if (cudaGetLastError() != cudaSuccess ||
@@ -369,7 +401,7 @@ dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp
     *P = (int64_t)pu;
     uint4 *d_pay = nullptr;
     const size_t pay_bytes = std::max<size_t>((size_t)pu * 16, 16);
-    if (cudaMalloc(&d_pay, pay_bytes) != cudaSuccess) { cudaGetLastError(); cleanup(); return DBS_ERR_OOM; }
+    if (dev_malloc(&d_pay, pay_bytes) != cudaSuccess) { cudaGetLastError(); cleanup(); return DBS_ERR_OOM; }
     if (cudaMemsetAsync(d_pay, 0, pay_bytes, s) != cudaSuccess ||
         (nB && cudaMemcpyAsync(d_ref, H.blk_ref.data(), sizeof(uint32_t) * nB, cudaMemcpyHostToDevice, s) != cudaSuccess)) {
         cudaFree(d_pay);

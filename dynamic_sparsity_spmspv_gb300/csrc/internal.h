@@ -29,6 +29,20 @@ struct HostFormat {
     std::vector<uint32_t> rb_ntiles;  // nbr: pull tiles whose first or last row block it is
 };
 
+// Allocation-failure injection for tests (dbs_debug_fail_alloc): true when
+// this allocation attempt is the one chosen to fail.
+bool alloc_fault();
+// cudaMalloc behind the injection hook.
+template <class T>
+inline cudaError_t dev_malloc(T **p, size_t bytes)
+{
+    if (alloc_fault()) { *p = nullptr; return cudaErrorMemoryAllocation; }
+    return cudaMalloc((void **)p, bytes);
+}
+// A host allocation of the builder, workspace or plan: throws
+// std::bad_alloc when the injection hook chooses it.
+void host_alloc_point();
+
 // Device-side conversion (build_gpu.cu): fills H.rb_ptr, H.blk_desc and
 // H.blk_ref, allocates and encodes the payload on the device.  Sets
 // *fallback (and converts nothing) when a row's columns are not ascending.

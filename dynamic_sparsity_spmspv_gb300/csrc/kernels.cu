@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <new>
 
 #include "internal.h"
@@ -1076,6 +1077,175 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
     }
 }
 
+// Boolean pull (Sections 3.3.2 and 3.3.3, Algorithm 5 semantics), the
+// path of Boolean SpMSpV and of DB-BFS pull levels.  Tiles as in
+// pull_tiles, but each lane handles its eight blocks with as little work per
+// block as the format allows: the descriptors arrive two per 16-byte load
+// (lane l takes units u0 + 32j + l of the tile, u0 the unit holding p0), all
+// eight vector-mask lookups go out together, an inline block's found rows
+// come from its coordinate bytes in registers, and a lane ORs them into one
+// register while its blocks stay in one row block (blocks are in row-block
+// order), so shared memory sees one OR per row-block change instead of one
+// per found block.  Stored blocks that meet an active column are queued and
+// decoded from their payload after the scan.
+template <bool ST>
+__device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, const uint32_t *vis,
+                          uint32_t *out_rm, int tslot)
+{
+    constexpr int WU = 4;                       // 16-byte descriptor units per lane per tile
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    WarpPull<1> &W = S.wp[warp];
+    const unsigned short *xm16 = reinterpret_cast<const unsigned short *>(xm);
+    const uint4 *desc4 = reinterpret_cast<const uint4 *>(P.blk_desc);
+    const uint32_t nwarps = gridDim.x * NW;
+    const uint32_t rounds = P.T / nwarps;
+    const uint32_t T0 = rounds > 6u ? (rounds - 6u) * nwarps : 0u;
+    unsigned *ctr = &P.ctrl->tile_next[tslot];
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+    auto next_tile = [&](uint32_t t) -> uint32_t {
+        if (t + nwarps < T0) return t + nwarps;
+        const uint32_t v = lane == 0 ? T0 + atomicAdd(ctr, 1u) : 0u;
+        return __shfl_sync(FULL, v, 0);
+    };
+    // visited rows of a tile's row blocks; tiles whose rows are all visited
+    // are skipped before their descriptors are read
+    auto settle = [&](uint32_t &tt, uint4 &tdd, uint32_t &vr) {
+        while (tt < P.T) {
+            vr = lane < (int)(tdd.w & TILE_SPAN_MASK) ? vis16(vis, tdd.z + lane) : 0xFFFFu;
+            if (!__all_sync(FULL, vr == 0xFFFFu)) return;
+            tt = next_tile(tt);
+            tdd = tt < P.T ? __ldg(P.tiles + tt) : z4;
+        }
+    };
+    // units holding at least one block of the tile (block 2u < p0 + count);
+    // the descriptor array has padding past B, so a unit's second block may
+    // lie one past the last block
+    auto load_desc = [&](const uint4 &tdd, uint4 (&dd)[WU]) {
+        const uint32_t u0 = tdd.x >> 1, end = tdd.x + (tdd.w >> TILE_NBLK_SHIFT);
+#pragma unroll
+        for (int j = 0; j < WU; ++j) {
+            const uint32_t u = u0 + (uint32_t)(j * 32 + lane);
+            dd[j] = 2u * u < end ? __ldcs(desc4 + u) : z4;
+        }
+    };
+
+    uint32_t t = blockIdx.x * NW + warp;
+    if (t >= T0) {
+        const uint32_t v = lane == 0 ? T0 + atomicAdd(ctr, 1u) : 0u;
+        t = __shfl_sync(FULL, v, 0);
+    }
+    uint4 td = t < P.T ? __ldg(P.tiles + t) : z4;
+    uint32_t vrow = 0;
+    if (vis) settle(t, td, vrow);
+    uint4 d[WU];
+    load_desc(td, d);
+    while (t < P.T) {
+        uint32_t c_vis = 0, c_hit = 0, c_touch = 0, c_bytes = 0;
+        uint32_t t_n = next_tile(t);
+        uint4 td_n = t_n < P.T ? __ldg(P.tiles + t_n) : z4;
+        const uint32_t p0 = td.x, rb0 = td.z, span = td.w & TILE_SPAN_MASK, nblk = td.w >> TILE_NBLK_SHIFT;
+        // block k of this lane (k = 2j + h) is tile block li = 2 (32 j + lane) + h - (p0 & 1)
+        const int lbase = 2 * lane - (int)(p0 & 1u);
+        if (lane < (int)span) W.rm[lane] = 0u;
+        if (lane == 0) { W.nq = 0u; W.nq2 = 0u; }
+        uint32_t mp[WU];   // the eight column-block masks, two per register
+#pragma unroll
+        for (int j = 0; j < WU; ++j) {
+            const int li = lbase + 64 * j;
+            const uint32_t a = li >= 0 && li < (int)nblk ? (uint32_t)__ldca(xm16 + (d[j].x & DESC_COL_MASK)) : 0u;
+            const uint32_t b = li + 1 < (int)nblk ? (uint32_t)__ldca(xm16 + (d[j].z & DESC_COL_MASK)) : 0u;
+            mp[j] = a | (b << 16);
+        }
+        uint32_t vrow_n = 0;
+        if (vis) settle(t_n, td_n, vrow_n);
+        uint4 d_n[WU];
+        load_desc(td_n, d_n);
+        __syncwarp();
+
+        uint32_t acc = 0, cur = 0;
+#pragma unroll
+        for (int k = 0; k < 2 * WU; ++k) {
+            const int li = lbase + 64 * (k >> 1) + (k & 1);
+            const bool valid = li >= 0 && li < (int)nblk;
+            const uint32_t dx = (k & 1) ? d[k >> 1].z : d[k >> 1].x;
+            const uint32_t meta = (k & 1) ? d[k >> 1].w : d[k >> 1].y;
+            const uint32_t mk = (mp[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu, lrb = dx >> DESC_LRB_SHIFT;
+            const bool inl = meta_inline(meta);
+            const uint32_t f = inl ? inline_found(meta, dup16(mk)) : 0u;
+            if (valid && lrb != cur) {
+                if (acc) atomicOr(&W.rm[cur], acc);
+                acc = 0u;
+                cur = lrb;
+            }
+            acc |= f;
+            const uint32_t a = inl ? 0u : mk & meta & 0xFFFFu;
+            if (a) {
+                const bool coo = meta_fmt(meta) == FMT_COO;
+                const uint32_t slot = coo ? atomicAdd(&W.nq, 1u) : TILE_MAX_BLOCKS - 1u - atomicAdd(&W.nq2, 1u);
+                W.qe[slot] = (uint32_t)li | (lrb << 8) | (a << 16);
+                W.qm[slot] = meta;
+            }
+            if (ST) {
+                if (mk) { ++c_vis; c_touch += meta_nnz(meta); }
+                if (f || a) ++c_hit;
+            }
+        }
+        // the lanes' last runs: one OR for the warp when they share a row block
+        const uint32_t c0 = __shfl_sync(FULL, cur, 0);
+        if (__all_sync(FULL, cur == c0 || acc == 0u)) {
+            const uint32_t r = __reduce_or_sync(FULL, acc);
+            if (lane == 0 && r) atomicOr(&W.rm[c0], r);
+        } else if (acc) {
+            atomicOr(&W.rm[cur], acc);
+        }
+        __syncwarp();
+
+        // stored blocks meeting an active column: COO (front of the queue),
+        // then the mask formats (back)
+        const uint32_t nq = W.nq, nq2 = W.nq2;
+        if (nq | nq2) {
+            for (uint32_t i = lane; i < nq; i += 32) {
+                const uint32_t e = W.qe[i], nnz = meta_nnz(W.qm[i]);
+                const uint4 *b = P.payload + __ldg(P.blk_ref + p0 + (e & 0xFFu));
+                const uint4 u0 = __ldg(b);
+                const uint4 u1 = nnz > 16u ? __ldg(b + 1) : z4;
+                const uint32_t r = bool_found_units(FMT_COO, nnz, e >> 16, u0, u1, b);
+                if (r) atomicOr(&W.rm[(e >> 8) & 0xFFu], r);
+                if (ST) c_bytes += 4u + nnz;
+            }
+            for (uint32_t i = lane; i < nq2; i += 32) {
+                const uint32_t k = TILE_MAX_BLOCKS - 1u - i;
+                const uint32_t e = W.qe[k], meta = W.qm[k];
+                const uint4 *b = P.payload + __ldg(P.blk_ref + p0 + (e & 0xFFu));
+                const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
+                uint4 u0, u1;
+                bool_load(b, fmt, nnz, P.valued != 0, u0, u1);
+                const uint32_t r = bool_found_units(fmt, nnz, e >> 16, u0, u1, b);
+                if (r) atomicOr(&W.rm[(e >> 8) & 0xFFu], r);
+                if (ST) c_bytes += 4u + 32u;
+            }
+            __syncwarp();
+        }
+        if (lane < (int)span) {
+            const uint32_t f = W.rm[lane] & ~vrow;
+            if (f) or16(out_rm, rb0 + lane, f);
+        }
+        if (ST) {
+            if (lane == 0) c_bytes += 8u * nblk + 16u;
+            stat_add(S, 0, c_vis);
+            stat_add(S, 1, c_hit);
+            stat_add(S, 2, c_touch);
+            stat_add(S, 3, c_bytes);
+        }
+        __syncwarp();
+        t = t_n;
+        td = td_n;
+        vrow = vrow_n;
+#pragma unroll
+        for (int j = 0; j < WU; ++j) d[j] = d_n[j];
+    }
+}
+
 // Push (Section 3.3.2): warps take tasks of up to 256 consecutive CSC
 // positions of one active column block; the active vector block is cached
 // in shared memory (Section 3.3.3).  Each lane loads the descriptors of its
@@ -1396,7 +1566,8 @@ __global__ void __launch_bounds__(NT, 4) k_spmspv_sparse(KParams P)
         }
         push_tasks<SR, false, ST>(P, S, P.xm32, P.uvis32, P.yrm32, slot, ch);
     } else {
-        pull_tiles<SR, false, ST>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
+        if constexpr (SR == 1) pull_bool<ST>(P, S, P.xm32, P.uvis32, P.yrm32, slot);
+        else pull_tiles<0, false, ST>(P, S, P.xm32, nullptr, P.yrm32, slot);
     }
     stats_flush(P, S);
     if (!grid_sync(P)) return;
@@ -1666,7 +1837,7 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
             }
             push_tasks<1, false, ST>(P, S, fcur, P.bvis32, fnext, cur, ch);
         } else {
-            pull_tiles<1, false, ST>(P, S, fcur, P.bvis32, fnext, cur);
+            pull_bool<ST>(P, S, fcur, P.bvis32, fnext, cur);
         }
         if (!grid_sync(P)) return;
         if (blockIdx.x == 0 && tid == 0 && L - 1u < (uint32_t)BFS_LEVEL_LOG) P.ctrl->lv_u[L - 1u] = globaltimer();
@@ -1892,7 +2063,7 @@ template <class T>
 bool dalloc(T **p, size_t count)
 {
     size_t bytes = std::max<size_t>(count * sizeof(T), 16);
-    if (cudaMalloc((void **)p, bytes) != cudaSuccess) { cudaGetLastError(); *p = nullptr; return false; }
+    if (dev_malloc(p, bytes) != cudaSuccess) { cudaGetLastError(); *p = nullptr; return false; }
     if (cudaMemset(*p, 0, bytes) != cudaSuccess) { cudaGetLastError(); return false; }
     return true;
 }
@@ -1987,7 +2158,7 @@ void dbs_exec_opts_default(dbs_exec_opts *o)
 dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
 {
     if (!A || !out || !A->on_device) return DBS_ERR_INVALID_ARG;
-    dbs_workspace *w = new (std::nothrow) dbs_workspace();
+    dbs_workspace *w = alloc_fault() ? nullptr : new (std::nothrow) dbs_workspace();
     if (!w) return DBS_ERR_OOM;
     w->A = A;
     dbs_exec_opts_default(&w->opts);
@@ -2298,6 +2469,21 @@ dbs_status noalloc_setup(int dev)
 }
 
 }  // namespace
+
+extern "C" dbs_status dbs_spmspv_dense_noalloc_check(void *stream)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES || !g_noalloc_dev[dev].ready) return DBS_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+    unsigned err = 0;
+    if (cudaMemcpyFromSymbol(&err, g_noalloc_scratch, sizeof(unsigned), offsetof(Ctrl, err), cudaMemcpyDeviceToHost) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return DBS_ERR_CUDA;
+    }
+    return (dbs_status)err;
+}
 
 extern "C" dbs_status dbs_spmspv_dense_noalloc(const dbs_matrix *A, const float *x, float *y, void *stream)
 {

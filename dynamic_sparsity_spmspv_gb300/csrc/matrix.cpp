@@ -175,6 +175,10 @@ void convert_chunk(Chunk &ch, int64_t m, int64_t n, const int64_t *rp, const int
     }
 }
 
+// Allocation-failure injection (dbs_debug_fail_alloc): the countdown to the
+// allocation attempt that fails; -1 when off.
+std::atomic<int64_t> g_fail_countdown{-1};
+
 int num_sms_or_default()
 {
     int dev = 0, sms = 0;
@@ -218,7 +222,7 @@ dbs_status upload(const std::vector<T> &h, T **d, size_t min_elems, cudaStream_t
 {
     size_t cnt = std::max(h.size(), min_elems);
     size_t bytes = std::max<size_t>(cnt * sizeof(T), 16);
-    if (cudaMalloc((void **)d, bytes) != cudaSuccess) { cudaGetLastError(); *d = nullptr; return DBS_ERR_OOM; }
+    if (dev_malloc(d, bytes) != cudaSuccess) { cudaGetLastError(); *d = nullptr; return DBS_ERR_OOM; }
     if (cudaMemsetAsync(*d, 0, bytes, s) != cudaSuccess) return DBS_ERR_CUDA;
     if (!h.empty() && cudaMemcpyAsync(*d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice, s) != cudaSuccess)
         return DBS_ERR_CUDA;
@@ -265,7 +269,27 @@ dbs_status host_view(const dbs_matrix *A, HostFormat &tmp, const HostFormat **ou
 
 }  // namespace
 
+bool dbs::alloc_fault()
+{
+    int64_t v = g_fail_countdown.load(std::memory_order_relaxed);
+    while (v >= 0)
+        if (g_fail_countdown.compare_exchange_weak(v, v - 1)) return v == 0;
+    return false;
+}
+
+void dbs::host_alloc_point()
+{
+    if (alloc_fault()) throw std::bad_alloc();
+}
+
 extern "C" {
+
+dbs_status dbs_debug_fail_alloc(int64_t k, int64_t *previous)
+{
+    const int64_t prev = g_fail_countdown.exchange(k < 0 ? -1 : k);
+    if (previous) *previous = prev;
+    return DBS_OK;
+}
 
 void dbs_build_opts_default(dbs_build_opts *o)
 {
@@ -344,6 +368,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
     const bool valued = va != nullptr;
     dbs_matrix *A = nullptr;
     try {
+        host_alloc_point();
         A = new dbs_matrix();
         A->host = new HostFormat();
     } catch (const std::bad_alloc &) {
@@ -405,6 +430,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         auto worker = [&]() {
             std::vector<Entry> ents;
             try {
+                host_alloc_point();
                 for (size_t c; (c = next.fetch_add(1)) < chunks.size();)
                     convert_chunk(chunks[c], m, n, rp, ci, va, o, ents);
             } catch (const std::bad_alloc &) {
@@ -434,6 +460,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         }
         if (B >= (int64_t(1) << 32) || P >= (int64_t(1) << 32)) return fail(DBS_ERR_UNSUPPORTED);
         A->B = B; A->P = P;
+        host_alloc_point();
         H.rb_ptr.resize((size_t)nbr + 1);
         H.blk_desc.resize((size_t)B);
         H.blk_ref.resize((size_t)B);
@@ -463,6 +490,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
 
         // 3. Block-CSC view: counting sort of primary blocks by column block;
         //    row blocks stay ascending within a column block.
+        host_alloc_point();
         H.cb_ptr.assign((size_t)nbc + 1, 0);
         for (int64_t p = 0; p < B; ++p) H.cb_ptr[H.blk_desc[(size_t)p].x + 1]++;
         for (int64_t c = 0; c < nbc; ++c) H.cb_ptr[(size_t)c + 1] += H.cb_ptr[(size_t)c];
@@ -497,6 +525,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         }
         W = std::min<uint32_t>(W, TILE_MAX_BLOCKS);
         uint32_t R = o.tile_max_row_blocks > 0 ? (uint32_t)o.tile_max_row_blocks : TILE_MAX_SPAN;
+        host_alloc_point();
         build_tiles(H.rb_ptr, H.blk_desc, nbr, W, R, H.tiles);
         A->T = (int64_t)H.tiles.size();
         for (size_t i = 0; i < H.tiles.size(); ++i) {

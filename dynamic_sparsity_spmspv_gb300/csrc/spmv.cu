@@ -30,6 +30,7 @@
 #include <new>
 
 #include "../../include/dbspmspv.h"
+#include "internal.h"
 
 namespace {
 
@@ -388,7 +389,7 @@ template <class T>
 bool alloc0(T **p, size_t count)
 {
     const size_t bytes = std::max<size_t>(count * sizeof(T), 16);
-    if (cudaMalloc((void **)p, bytes) != cudaSuccess) { cudaGetLastError(); *p = nullptr; return false; }
+    if (dbs::dev_malloc(p, bytes) != cudaSuccess) { cudaGetLastError(); *p = nullptr; return false; }
     if (cudaMemset(*p, 0, bytes) != cudaSuccess) { cudaGetLastError(); return false; }
     return true;
 }
@@ -413,7 +414,7 @@ dbs_status dbs_spmv_plan_create(int64_t m, int64_t n, int64_t nnz, const int64_t
         return DBS_ERR_INVALID_ARG;
     // entry offsets in the row queues are 32-bit
     if (nnz >= (int64_t(1) << 32)) return DBS_ERR_UNSUPPORTED;
-    dbs_spmv_plan *p = new (std::nothrow) dbs_spmv_plan();
+    dbs_spmv_plan *p = dbs::alloc_fault() ? nullptr : new (std::nothrow) dbs_spmv_plan();
     if (!p) return DBS_ERR_OOM;
     PlanDev &D = p->D;
     D.m = m; D.n = n; D.nnz = nnz; D.rp = row_ptr; D.ci = col_idx; D.va = vals;

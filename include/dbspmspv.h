@@ -379,9 +379,31 @@ dbs_status dbs_selftest_wait_timeout(dbs_workspace *ws, void *stream);
  *   All calls share the one array: calls that may overlap on the GPU (on
  *   different streams, or from different threads) race and must be
  *   serialised by the caller.  Each call clears the state it needs.
- *   Device-side wait timeouts are not reported (y is then undefined).
+ *   A device-side wait that timed out leaves y undefined and is reported by
+ *   dbs_spmspv_dense_noalloc_check.
  * ASYNC. */
 dbs_status dbs_spmspv_dense_noalloc(const dbs_matrix *A, const float *x, float *y, void *stream);
+
+/* Status of the last dbs_spmspv_dense_noalloc call on the current device:
+ * synchronizes `stream` (the stream that call used), reads the error word of
+ * the fixed scratch array (cudaMemcpyFromSymbol, no allocation) and returns
+ * DBS_OK, or what that call latched on the device (DBS_ERR_TIMEOUT when a
+ * bounded grid-barrier wait expired; y is then undefined).  The next
+ * dbs_spmspv_dense_noalloc call clears the word, so query in between.
+ * DBS_ERR_INVALID_ARG if no call has run on this device yet. */
+dbs_status dbs_spmspv_dense_noalloc_check(void *stream);
+
+/* Test hook (the paper has no counterpart): injects one allocation failure.
+ * The k-th allocation attempt from now on (k = 0: the next one) fails as if
+ * memory were exhausted -- device allocations (cudaMalloc) and the host
+ * allocations of dbs_matrix_build_csr, dbs_workspace_create and
+ * dbs_spmv_plan_create alike.  A call that meets it returns DBS_ERR_OOM
+ * after releasing everything it had allocated.  k < 0 switches the hook
+ * off; it also switches itself off after firing.  *previous (may be NULL)
+ * receives the countdown it replaced: -1 when the last setting has fired
+ * or was off, else the attempts that were still to come.  Process-wide and
+ * not thread-safe with respect to concurrent builds; for tests. */
+dbs_status dbs_debug_fail_alloc(int64_t k, int64_t *previous);
 
 /* Human-readable name of a status. */
 const char *dbs_status_string(dbs_status s);

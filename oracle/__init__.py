@@ -35,8 +35,11 @@ def build(force: bool = False) -> str:
     os.makedirs(_OUT_DIR, exist_ok=True)
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-shared", "-fPIC",
-                               "-o", tmp, _SRC, "-lm"])
+        base = ["gcc", "-O2", "-std=c11", "-Wall", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+        # OpenMP only splits the rows of the all-cores baseline; without it
+        # those functions run on one thread
+        if subprocess.call(base + ["-fopenmp"], stderr=subprocess.DEVNULL) != 0:
+            subprocess.check_call(base)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -64,6 +67,12 @@ def _load(path: Optional[str] = None):
     lib.oracle_activation_mask.argtypes = [I64, P, ctypes.c_float, P]
     lib.oracle_spmv_csr.restype = None
     lib.oracle_spmv_csr.argtypes = [I64, I64, P, P, P, P, P, P]
+    lib.oracle_spmspv_pull_par.restype = I64
+    lib.oracle_spmspv_pull_par.argtypes = [I64, I64, P, P, P, ctypes.c_int, I64, P, P, P, P, P, P]
+    lib.oracle_bfs_pull_par.restype = I64
+    lib.oracle_bfs_pull_par.argtypes = [I64, P, P, I64, P]
+    lib.oracle_par_threads.restype = ctypes.c_int
+    lib.oracle_par_threads.argtypes = []
     lib.oracle_block_views.restype = I64
     lib.oracle_block_views.argtypes = [I64, I64, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_double, P, P, P, P, P, P, P]
@@ -213,6 +222,42 @@ def spmspv_pull(A, x, semiring: int = PLUS_TIMES, visited: Optional[np.ndarray] 
     if semiring == PLUS_TIMES:
         return y_idx[:k].copy(), y_val[:k].copy(), y_abs[:k].copy()
     return y_idx[:k].copy(), None, None
+
+
+def par_threads() -> int:
+    """Threads the all-cores baseline functions use (1 without OpenMP)."""
+    return int(_load().oracle_par_threads())
+
+
+def spmspv_pull_par(A, x, semiring: int = PLUS_TIMES, visited: Optional[np.ndarray] = None):
+    """The all-cores CPU baseline: Algorithm 1 (bottom) with the rows split
+    among OpenMP threads.  Same return shape as ``Oracle.spmspv``."""
+    rp, ci, va = _csr_arrays(A)
+    idx = np.ascontiguousarray(x.idx, dtype=np.int32)
+    val = None if x.val is None else np.ascontiguousarray(x.val, dtype=np.float32)
+    vis = None if visited is None else np.ascontiguousarray(visited, dtype=np.uint8)
+    y_idx = np.empty(max(A.m, 1), dtype=np.int32)
+    y_val = np.empty(max(A.m, 1), dtype=np.float64) if semiring == PLUS_TIMES else None
+    y_abs = np.empty(max(A.m, 1), dtype=np.float64) if semiring == PLUS_TIMES else None
+    k = _load().oracle_spmspv_pull_par(A.m, A.n, _ptr(rp), _ptr(ci), _ptr(va), semiring,
+                                       idx.shape[0], _ptr(idx), _ptr(val), _ptr(vis),
+                                       _ptr(y_idx), _ptr(y_val), _ptr(y_abs))
+    if k < 0:
+        raise MemoryError("oracle_spmspv_pull_par failed")
+    if semiring == PLUS_TIMES:
+        return y_idx[:k].copy(), y_val[:k].copy(), y_abs[:k].copy()
+    return y_idx[:k].copy(), None, None
+
+
+def bfs_pull_par(A, src: int) -> np.ndarray:
+    """The all-cores CPU baseline's BFS: level-synchronous, each level one
+    row-parallel pull.  Levels as ``Oracle.bfs_queue``."""
+    rp, ci, _ = _csr_arrays(A)
+    lev = np.empty(max(A.n, 1), dtype=np.int32)
+    r = _load().oracle_bfs_pull_par(A.n, _ptr(rp), _ptr(ci), int(src), _ptr(lev))
+    if r < 0:
+        raise MemoryError("oracle_bfs_pull_par failed")
+    return lev[:A.n].copy()
 
 
 def block_views(A, bs: int = 16, th0: int = 32, th1: int = 128, th2: float = 2.0) -> dict:

@@ -24,6 +24,11 @@
  *                          activation is sparsified by magnitude thresholding;
  *                          entry j is kept iff |x_j| > tau (NaN kept).  The
  *                          kept entries are the x of oracle_spmspv_push.
+ *   - oracle_spmspv_pull_par, oracle_bfs_pull_par : the all-cores CPU
+ *                          baseline -- Algorithm 1 (bottom) with the rows split
+ *                          among OpenMP threads, and a level-synchronous BFS
+ *                          made of such pulls; checked against the push
+ *                          oracle and the queue BFS.
  *   - oracle_block_views : Section 3.2.1 and Figure 5(b): 16x16 blocking,
  *                          block-CSR view, block-CSC view, csc2csr mapping,
  *                          per-block nnz, and the low-level format class from
@@ -384,4 +389,115 @@ void oracle_spmv_csr(int64_t m, int64_t n, const int64_t *row_ptr, const int32_t
         y[i] = acc;
         abs_out[i] = sab;
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* All-cores CPU baseline (not a pin: it is checked against the functions   */
+/* above).  Algorithm 1 (bottom), the row-wise pull, with the rows split     */
+/* among OpenMP threads; and a level-synchronous BFS whose levels are each   */
+/* one such pull (Section 4.2: next = (A or.and frontier) and not visited). */
+/* Without OpenMP both run on one thread.                                    */
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oracle_par_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Same contract as oracle_spmspv_pull.  Each thread owns a contiguous range  */
+/* of rows and writes their sums and hit flags into dense arrays; the         */
+/* ascending output is compacted afterwards.                                  */
+int64_t oracle_spmspv_pull_par(int64_t m, int64_t n, const int64_t *row_ptr,
+                               const int32_t *col_idx, const float *vals, int semiring,
+                               int64_t x_nnz, const int32_t *x_idx, const float *x_val,
+                               const uint8_t *visited,
+                               int32_t *y_idx, double *y_val, double *y_abs)
+{
+    double *xd = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    uint8_t *act = (uint8_t *)calloc((size_t)(n > 0 ? n : 1), 1);
+    double *ysum = (double *)malloc(sizeof(double) * (size_t)(m > 0 ? m : 1));
+    double *yab = (double *)malloc(sizeof(double) * (size_t)(m > 0 ? m : 1));
+    uint8_t *hit = (uint8_t *)malloc((size_t)(m > 0 ? m : 1));
+    if (!xd || !act || !ysum || !yab || !hit) {
+        free(xd); free(act); free(ysum); free(yab); free(hit);
+        return -1;
+    }
+    for (int64_t e = 0; e < x_nnz; ++e) {
+        if (x_val && !(x_val[e] != 0.0f)) continue;
+        xd[x_idx[e]] = x_val ? (double)x_val[e] : 1.0;
+        act[x_idx[e]] = 1;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < m; ++i) {
+        double sum = 0.0, sab = 0.0;
+        uint8_t h = 0;
+        for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) {
+            int64_t j = col_idx[k];
+            if (!act[j]) continue;
+            h = 1;
+            if (semiring == 0) {
+                double p = (vals ? (double)vals[k] : 1.0) * xd[j];
+                sum += p;
+                sab += fabs(p);
+            }
+        }
+        if (semiring == 1 && visited && visited[i]) h = 0;
+        hit[i] = h;
+        ysum[i] = sum;
+        yab[i] = sab;
+    }
+    int64_t t = 0;
+    for (int64_t i = 0; i < m; ++i) {
+        if (!hit[i]) continue;
+        y_idx[t] = (int32_t)i;
+        if (semiring == 0) {
+            if (y_val) y_val[t] = ysum[i];
+            if (y_abs) y_abs[t] = yab[i];
+        }
+        ++t;
+    }
+    free(xd); free(act); free(ysum); free(yab); free(hit);
+    return t;
+}
+
+/* Level-synchronous BFS over the CSR of a square matrix: at level L every   */
+/* unreached row i with a stored A(i,j) whose j was reached at level L - 1    */
+/* is reached at level L; rows are split among the threads.  Returns the     */
+/* number of levels, or -1 on allocation failure.                            */
+int64_t oracle_bfs_pull_par(int64_t n, const int64_t *row_ptr, const int32_t *col_idx, int64_t src,
+                            int32_t *levels)
+{
+    uint8_t *next = (uint8_t *)calloc((size_t)(n > 0 ? n : 1), 1);
+    if (!next) return -1;
+    for (int64_t v = 0; v < n; ++v) levels[v] = -1;
+    levels[src] = 0;
+    int64_t level = 0;
+    for (;;) {
+        int64_t found = 0;
+        /* this pass reads levels and writes only next */
+#pragma omp parallel for schedule(dynamic, 4096) reduction(+ : found)
+        for (int64_t i = 0; i < n; ++i) {
+            if (levels[i] >= 0) continue;
+            for (int64_t k = row_ptr[i]; k < row_ptr[i + 1]; ++k) {
+                if (levels[col_idx[k]] == (int32_t)level) {
+                    next[i] = 1;
+                    ++found;
+                    break;
+                }
+            }
+        }
+        if (found == 0) break;
+        ++level;
+#pragma omp parallel for schedule(static)
+        for (int64_t i = 0; i < n; ++i)
+            if (next[i]) { levels[i] = (int32_t)level; next[i] = 0; }
+    }
+    free(next);
+    return level + 1;
 }

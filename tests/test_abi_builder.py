@@ -242,3 +242,34 @@ def test_tiles_and_row_block_tile_counts(name, kw):
     for i in np.nonzero(nonempty)[0]:
         want[i // 16] |= 1 << (i % 16)
     np.testing.assert_array_equal(rows, want.astype(np.uint16))
+
+
+def _fail_alloc(k):
+    prev = ctypes.c_int64(0)
+    assert _lib.load().dbs_debug_fail_alloc(k, ctypes.byref(prev)) == 0
+    return prev.value
+
+
+def test_injected_allocation_failures_in_the_host_builder():
+    """Every host allocation point of the builder, made to fail in turn by
+    the test hook, returns DBS_ERR_OOM (and the process stays usable); with
+    the hook past the last allocation the build succeeds unchanged."""
+    A = synth.config("llm", "small")
+    ref = _host(A).export_raw("blk_desc")
+    fired = 0
+    for k in range(200):
+        _fail_alloc(k)
+        try:
+            M = _host(A, num_threads=2)
+        except dbs.DbsError as e:
+            assert e.status == 2, e              # DBS_ERR_OOM
+            assert _fail_alloc(-1) == -1         # the hook fired
+            fired += 1
+            continue
+        left = _fail_alloc(-1)
+        assert left >= 0                          # not reached: every point was covered
+        np.testing.assert_array_equal(M.export_raw("blk_desc"), ref)
+        break
+    else:
+        raise AssertionError("the build never got past the injected failures")
+    assert fired >= 4

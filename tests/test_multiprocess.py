@@ -64,6 +64,9 @@ def test_reference_arm_under_torchrun_prints_once():
         assert k in d, k
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == d["value"] and d["cpu_baseline"]["value"] == d["value"]
+    # the same workload description as the GPU arm prints
+    m = d["config"]["matrix"]
+    assert d["config"] == bench.config_dict(2, m["n"], m["nnz"], m["blocks"]) and m["blocks"] > 0
 
 
 def test_touched_nnz_counter_matches_brute_force():

@@ -259,6 +259,40 @@ def test_bfs_directed_follows_columns():
     np.testing.assert_array_equal(O.bfs_spmspv(2), [-1, -1, 0])
 
 
+# ------------------------------------------------- all-cores CPU baseline
+
+@pytest.mark.parametrize("seed", range(5))
+def test_parallel_pull_equals_push_and_serial_pull(seed):
+    """The all-cores baseline's row-parallel pull gives the push oracle's
+    pattern and the serial pull's values bit for bit (same order per row)."""
+    A = synth.random_csr(300, 250, 0.04, seed, valued=seed != 4)
+    for k in (0, 1, 60, 250):
+        x = synth.x_uniform(250, k, [seed, 5, k])
+        for sr in (oracle.PLUS_TIMES, oracle.OR_AND):
+            vis = np.random.default_rng(seed).integers(0, 2, 300).astype(np.uint8) if sr else None
+            a = oracle.Oracle(A).spmspv(x, sr, vis)
+            b = oracle.spmspv_pull(A, x, sr, vis)
+            c = oracle.spmspv_pull_par(A, x, sr, vis)
+            np.testing.assert_array_equal(c[0], a[0])
+            if sr == oracle.PLUS_TIMES:
+                np.testing.assert_array_equal(c[1], b[1])
+                np.testing.assert_array_equal(c[2], b[2])
+
+
+@pytest.mark.parametrize("name", ["rmat", "grid"])
+def test_parallel_bfs_equals_queue_bfs(name):
+    A = synth.config(name, "small")
+    O = oracle.Oracle(A)
+    for src in synth.bfs_sources(A, 3, 2):
+        np.testing.assert_array_equal(oracle.bfs_pull_par(A, int(src)), O.bfs_queue(int(src)))
+    side = 19
+    G = _grid(side)
+    src = 4 * side + 11
+    rr, cc = np.divmod(np.arange(side * side), side)
+    np.testing.assert_array_equal(oracle.bfs_pull_par(G, src), np.abs(rr - 4) + np.abs(cc - 11))
+    assert oracle.par_threads() >= 1
+
+
 # ---------------------------------------------------------------- block views
 
 def _fig5_matrix(bs):

@@ -61,3 +61,29 @@ def test_noalloc_rejects_too_many_columns():
     assert e.value.status == 1
     assert "dbs_spmspv_dense_noalloc" in _lib.PROTOTYPES
     assert ctypes.CDLL(_lib.lib_path()).dbs_spmspv_dense_noalloc is not None
+
+
+def test_noalloc_allocates_nothing_and_reports_its_status():
+    """Repeated calls leave the device's free memory unchanged (nothing is
+    allocated per call), the status query reports success, and a matrix
+    whose row count is not a multiple of 16 has its last rows written."""
+    A = synth.random_csr(1003, 517, 0.05, 7)
+    M = dbs.DBMatrix.from_csr(A)
+    xd = synth.x_relu_topk(A.n, A.n // 4, [32, 0])
+    x = _dev(xd)
+    y = torch.empty(A.m, dtype=torch.float32, device="cuda")
+    dbs.dbs_spmspv_dense_noalloc(M, x, y=y)            # first call on the device: set-up
+    assert dbs.dbs_spmspv_dense_noalloc_check() == 0
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        y.fill_(float("nan"))
+        dbs.dbs_spmspv_dense_noalloc(M, x, y=y)
+        assert dbs.dbs_spmspv_dense_noalloc_check() == 0
+    assert torch.cuda.mem_get_info()[0] == free0
+    y_na = y.cpu().numpy()
+    nz = np.nonzero(xd)[0].astype(np.int32)
+    ri, rv, rs = oracle.Oracle(A).spmspv(synth.SparseVec(A.n, nz, xd[nz]))
+    assert oracle.tolerance_ok(y_na[ri], rv, rs).all()
+    rest = np.ones(A.m, bool)
+    rest[ri] = False
+    assert (y_na[rest] == 0).all()
