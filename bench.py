@@ -81,18 +81,29 @@ def _dist():
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons of this process's GPU, matched
+    by UUID (indices differ when CUDA_VISIBLE_DEVICES remaps devices)."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, device):
+        self.uuid = None
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(device).uuid)
+            self.uuid = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
         self.p = None
 
     def start(self):
+        if self.uuid is None:
+            return
         try:
-            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                       "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.p = subprocess.Popen(["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.p = None
 
@@ -109,7 +120,7 @@ class ClockSampler:
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in out.splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9 or f[0] != str(self.gpu):
+            if len(f) < 9 or f[0].lower() != self.uuid.lower():
                 continue
             try:
                 sm.append(float(f[1]))
@@ -121,9 +132,9 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "gpu_uuid": self.uuid}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+                "samples": len(sm), "power_w_max": max(power) if power else None, "gpu_uuid": self.uuid}
 
 
 def build_workload(scale: int, seed_tag: int):
@@ -173,29 +184,43 @@ def _host_cores() -> int:
 
 def cpu_baseline(A, xs, sources, touched_x, touched_bfs, budget_s: float):
     """The oracle as it stands, single-threaded, on a bounded sample of the
-    same step (densities cycled, then BFS sources)."""
+    same step (densities cycled, then BFS sources); beside it the all-cores
+    baseline -- the row-partitioned plain pull (Algorithm 1, bottom) and a
+    pull-based level-synchronous BFS on OpenMP threads -- on its own sample
+    of the same steps."""
     import oracle
     O = oracle.Oracle(A)
-    t_total, units, calls, bfs_runs = 0.0, 0, 0, 0
-    i = 0
-    while t_total < budget_s and i < POOL:
-        for d in DENSITIES:
-            x = xs[d][i]
+
+    def run(spmspv, bfs, budget):
+        t_total, units, calls, bfs_runs, i = 0.0, 0, 0, 0, 0
+        while t_total < budget and i < POOL:
+            for d in DENSITIES:
+                x = xs[d][i]
+                t0 = time.perf_counter()
+                spmspv(x)
+                t_total += time.perf_counter() - t0
+                units += touched_x[d][i]
+                calls += 1
+            src = int(sources[i % len(sources)])
             t0 = time.perf_counter()
-            O.spmspv(x, oracle.OR_AND)
+            bfs(src)
             t_total += time.perf_counter() - t0
-            units += touched_x[d][i]
-            calls += 1
-        src = int(sources[i % len(sources)])
-        t0 = time.perf_counter()
-        O.bfs_queue(src)
-        t_total += time.perf_counter() - t0
-        units += touched_bfs[i % len(sources)]
-        bfs_runs += 1
-        i += 1
-    return {"value": units / t_total, "unit": UNIT, "cores": 1, "host_cores_available": _host_cores(), "kind": "oracle",
-            "sample": f"{i} steps: {calls} oracle SpMSpV calls (push scatter, fp64 C, 1 thread) at the 5 densities "
-                      f"+ {bfs_runs} queue BFS; {t_total:.1f} s of CPU time; units = the same touched nnz"}
+            units += touched_bfs[i % len(sources)]
+            bfs_runs += 1
+            i += 1
+        return units / t_total, i, calls, bfs_runs, t_total
+
+    v1, i1, c1, b1, t1 = run(lambda x: O.spmspv(x, oracle.OR_AND), O.bfs_queue, budget_s * 0.7)
+    threads = oracle.par_threads()
+    vp, ip, cp, bp, tp = run(lambda x: oracle.spmspv_pull_par(A, x, oracle.OR_AND),
+                             lambda s: oracle.bfs_pull_par(A, s), budget_s * 0.3)
+    return {"value": v1, "unit": UNIT, "cores": 1, "host_cores_available": _host_cores(), "kind": "oracle",
+            "sample": f"{i1} steps: {c1} oracle SpMSpV calls (push scatter, fp64 C, 1 thread) at the 5 densities "
+                      f"+ {b1} queue BFS; {t1:.1f} s of CPU time; units = the same touched nnz",
+            "all_cores": {"value": vp, "unit": UNIT, "cores": threads, "kind": "oracle pull, OpenMP rows",
+                          "sample": f"{ip} steps: {cp} row-parallel pulls (Algorithm 1 bottom, fp64 C, {threads} "
+                                    f"threads) at the 5 densities + {bp} level-synchronous pull BFS; "
+                                    f"{tp:.1f} s of wall time"}}
 
 
 def reduce_over_ranks(t_ms: float, units: float, device):
@@ -211,48 +236,52 @@ def reduce_over_ranks(t_ms: float, units: float, device):
     return float(tt.item()), float(uu.item())
 
 
+def config_dict(world: int, n: int, nnz: int, blocks: int) -> dict:
+    """The workload description both arms print (the same dict)."""
+    return {"workload": WORKLOAD, "densities": list(DENSITIES), "bfs_sources": N_SOURCES,
+            "x_pool_per_density": POOL,
+            "l2": "GPU arm: flushed (256 MiB write) before every call, outside timing",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "matrix": {"n": int(n), "nnz": int(nnz), "blocks": int(blocks)}}
+
+
 def run_reference(args):
-    """--impl reference: the CPU oracle timed on this host's cores."""
+    """--impl reference: the CPU oracle timed on this host's cores, on the
+    same step as the GPU arm (one Boolean SpMSpV at each of the five
+    densities plus one BFS from the next source)."""
     ws_, rank, _ = _dist()
     if rank != 0:
         return
     A, xs, sources = build_workload(args.scale, 0)
     import oracle
     O = oracle.Oracle(A)
-    # touched nnz per x from the block views (same definition as the GPU arm)
-    counter = TouchedCounter(oracle.block_views(A))
-    touched = lambda x: counter.spmspv(x.idx)  # noqa: E731
-    bfs_touched = counter.bfs
-
-    # A reference step is a bounded sample of the workload: the SpMSpV call at
-    # one density (cycling), plus the queue BFS every fifth step, so five
-    # consecutive steps cover one full step of the GPU arm.
+    views = oracle.block_views(A)
+    counter = TouchedCounter(views)
     steps_total = args.warmup + args.steps
     t_step, units = [], []
     for s in range(steps_total):
-        i = (s // len(DENSITIES)) % POOL
-        d = DENSITIES[s % len(DENSITIES)]
+        i = s % POOL
+        u = 0
         t0 = time.perf_counter()
-        O.spmspv(xs[d][i], oracle.OR_AND)
-        lev = None
-        if s % len(DENSITIES) == len(DENSITIES) - 1:
-            lev = O.bfs_queue(int(sources[(s // len(DENSITIES)) % len(sources)]))
+        for d in DENSITIES:
+            O.spmspv(xs[d][i], oracle.OR_AND)
+        lev = O.bfs_queue(int(sources[s % N_SOURCES]))
         dt = time.perf_counter() - t0
-        u = touched(xs[d][i]) + (bfs_touched(lev) if lev is not None else 0)
+        u = sum(counter.spmspv(xs[d][i].idx) for d in DENSITIES) + counter.bfs(lev)
         if s >= args.warmup:
             t_step.append(dt)
             units.append(u)
     T = sum(t_step)
     value = sum(units) / T
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * T / len(t_step), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bool", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "densities": list(DENSITIES), "bfs_sources": N_SOURCES},
+            "config": config_dict(ws_, A.n, A.nnz, views["B"]),
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "host_cores_available": _host_cores(),
                              "kind": "oracle",
-                             "sample": f"{args.steps} steps, each one oracle SpMSpV at one of the 5 densities "
-                                       "(cycling) plus a queue BFS every 5th step; fp64 C, 1 thread"},
+                             "sample": f"{args.steps} steps, each one oracle SpMSpV at each of the 5 densities "
+                                       "plus one queue BFS (the GPU arm's step); fp64 C, 1 thread"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -744,7 +773,7 @@ def main():
     calls_per_step = len(DENSITIES) + 1
     ev = new_events(2 * calls_per_step * args.steps)
     rec = []
-    sampler = ClockSampler(dev.index if world == 1 else local)
+    sampler = ClockSampler(dev)
     sampler.start()
     time.sleep(0.3)
     if world > 1:
@@ -829,11 +858,8 @@ def main():
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "bool", "data": "synthetic",
-           "config": {"workload": WORKLOAD, "densities": list(DENSITIES), "bfs_sources": N_SOURCES,
-                      "x_pool_per_density": POOL, "l2": "flushed (256 MiB write) before every call, outside timing",
-                      "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                      "matrix": {"n": A.n, "nnz": A.nnz, "blocks": info["nblocks"], "tiles": info["ntiles"],
-                                 "device_bytes": info["total_bytes"]}},
+           "config": config_dict(world, A.n, A.nnz, info["nblocks"]),
+           "matrix_format": {"tiles": info["ntiles"], "device_bytes": info["total_bytes"]},
            "gpu_launches": calls_per_step * args.steps,
            "roofline": roofline, "per_density": per_density, "bfs": bfs_info, "clocks": clocks,
            "wall_s_timed_region": wall}
