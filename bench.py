@@ -479,8 +479,9 @@ def run_ablation(dbs, torch, dev, stream, flush, reps: int):
 
 
 def run_spmv(dbs, torch, dev, flush, reps: int):
-    """Dense-input regime: adaptive CSR SpMV (dbs_spmv, plan built once)
-    against the DB-format pull (dbs_spmspv_dense, auto path) on the same
+    """Dense-input regime: adaptive CSR SpMV (dbs_spmv, plan built once);
+    dbs_spmspv_dense on the auto path of a matrix built with dense_spmv (which
+    hands this x to the kept SpMV); and the DB-format pull forced, on the same
     matrix with a dense x (every entry nonzero, N(0,1)).  FEM rows (27
     entries) run as warp rows, LLM rows (5,504) as block rows, the R-MAT
     graph with unit weights mixes scalar and warp rows with split hub rows.
@@ -494,7 +495,7 @@ def run_spmv(dbs, torch, dev, flush, reps: int):
         if A.vals is None:
             A = synth.CSR(A.m, A.n, A.row_ptr, A.col_idx, np.ones(A.nnz, np.float32))
         plan = dbs.SpMVPlan.from_csr(A)
-        M = dbs.DBMatrix.from_csr(A)
+        M = dbs.DBMatrix.from_csr(A, dense_spmv=1)
         ws = dbs.Workspace(M)
         x = torch.from_numpy(np.random.default_rng(17).standard_normal(A.n).astype(np.float32)).to(dev)
         y = torch.empty(A.m, dtype=torch.float32, device=dev)
@@ -513,12 +514,13 @@ def run_spmv(dbs, torch, dev, flush, reps: int):
             return float(np.median(ts))
 
         us_csr = timed(lambda: plan(x, y=y))
-        us_db = timed(lambda: dbs.spmspv_dense(M, x, y=y, ws=ws))
+        us_auto = timed(lambda: dbs.spmspv_dense(M, x, y=y, ws=ws))
+        us_db = timed(lambda: dbs.spmspv_dense(M, x, y=y, ws=ws, path="pull"))
         csr_bytes = 8 * (A.m + 1) + 8 * A.nnz + 4 * A.n + 4 * A.m
         line = {"workload": name, "nnz": int(A.nnz), "buckets": plan.info(),
                 "csr_spmv_us": round(us_csr, 2), "csr_gbs": round(csr_bytes / us_csr / 1e3, 1),
                 "csr_frac_of_measured_hbm": round(csr_bytes / us_csr / 1e3 / peak, 3),
-                "db_pull_us": round(us_db, 2)}
+                "dense_x_auto_us": round(us_auto, 2), "db_pull_us": round(us_db, 2)}
         out.append(line)
         assert ws.check() == 0
         ws.close(); M.close(); plan.close()

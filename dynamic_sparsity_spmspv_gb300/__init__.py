@@ -25,11 +25,11 @@ from . import _lib
 from ._lib import DbsError, dbs_build_opts, dbs_exec_opts, dbs_matrix_info, dbs_stats  # noqa: F401
 
 PLUS_TIMES, OR_AND = 0, 1
-PATH_AUTO, PATH_PUSH, PATH_PULL = 0, 1, 2
+PATH_AUTO, PATH_PUSH, PATH_PULL, PATH_SPMV = 0, 1, 2, 3
 FMT_AUTO, FMT_COO, FMT_DENSE, FMT_FORCE_CSR, FMT_FORCE_CSC, FMT_PATCHED_CSR = -1, 0, 1, 2, 3, 4
 FORMAT_NAMES = ("coo", "dense", "force_csr", "force_csc", "patched_csr")
 
-_PATHS = {"auto": PATH_AUTO, "push": PATH_PUSH, "pull": PATH_PULL}
+_PATHS = {"auto": PATH_AUTO, "push": PATH_PUSH, "pull": PATH_PULL, "spmv": PATH_SPMV}
 _SEMIRINGS = {"plus_times": PLUS_TIMES, "or_and": OR_AND}
 
 
@@ -61,20 +61,25 @@ def _semiring(s) -> int:
     return _SEMIRINGS[s] if isinstance(s, str) else int(s)
 
 
+def _set_fields(o, kw):
+    names = {f for f, _ in type(o)._fields_}
+    for k, v in kw.items():
+        if k not in names:
+            raise TypeError(f"{type(o).__name__} has no field {k!r}")
+        setattr(o, k, v)
+    return o
+
+
 def build_opts(**kw) -> dbs_build_opts:
     o = dbs_build_opts()
     _lib.load().dbs_build_opts_default(ctypes.byref(o))
-    for k, v in kw.items():
-        setattr(o, k, v)
-    return o
+    return _set_fields(o, kw)
 
 
 def exec_opts(**kw) -> dbs_exec_opts:
     o = dbs_exec_opts()
     _lib.load().dbs_exec_opts_default(ctypes.byref(o))
-    for k, v in kw.items():
-        setattr(o, k, v)
-    return o
+    return _set_fields(o, kw)
 
 
 class DBMatrix:

@@ -21,12 +21,12 @@ NUM_FORMATS = 5
 class dbs_build_opts(ctypes.Structure):
     _fields_ = [("th0", I32), ("th1", I32), ("th2", F64), ("force_format", I32),
                 ("tile_weight", I32), ("tile_max_row_blocks", I32), ("keep_host", I32),
-                ("host_only", I32), ("num_threads", I32), ("device_convert", I32)]
+                ("host_only", I32), ("num_threads", I32), ("device_convert", I32), ("dense_spmv", I32)]
 
 
 class dbs_exec_opts(ctypes.Structure):
     _fields_ = [("th3", F64), ("local_pull_min", I32), ("collect_stats", I32),
-                ("wait_timeout_ns", I64), ("push_work_frac", F64)]
+                ("wait_timeout_ns", I64), ("push_work_frac", F64), ("spmv_x_frac", F64)]
 
 
 class dbs_matrix_info(ctypes.Structure):
@@ -35,7 +35,7 @@ class dbs_matrix_info(ctypes.Structure):
                 ("nnz_by_format", I64 * NUM_FORMATS), ("ntiles", I64), ("payload_bytes", I64),
                 ("view_bytes", I64), ("total_bytes", I64), ("csr_bytes", I64),
                 ("csr_csc_bytes", I64), ("valued", I32), ("on_device", I32),
-                ("build_seconds", F64)]
+                ("build_seconds", F64), ("spmv_bytes", I64)]
 
 
 class dbs_stats(ctypes.Structure):

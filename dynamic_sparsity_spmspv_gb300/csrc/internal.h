@@ -43,6 +43,14 @@ inline cudaError_t dev_malloc(T **p, size_t bytes)
 // std::bad_alloc when the injection hook chooses it.
 void host_alloc_point();
 
+// Device bytes held by an SpMV plan (its queues and scratch).
+int64_t spmv_plan_bytes(const dbs_spmv_plan *p);
+// The SpMV of a dense-x SpMSpV call over a kept plan, with the caller's
+// split-row scratch; `gated`: only if x's sampled nonzero fraction reaches
+// `frac`.  Writes 3 to *path_word when it runs (may be NULL).
+dbs_status spmv_launch_dense(const dbs_spmv_plan *p, float *part, uint32_t *cnt, const float *x, float *y,
+                             double frac, bool gated, unsigned *path_word, cudaStream_t s);
+
 // Device-side conversion (build_gpu.cu): fills H.rb_ptr, H.blk_desc and
 // H.blk_ref, allocates and encodes the payload on the device.  Sets
 // *fallback (and converts nothing) when a row's columns are not ascending.
@@ -70,5 +78,10 @@ struct dbs_matrix {
     uint16_t *d_rb_rows = nullptr;
     uint32_t *d_rb_ntiles = nullptr;
     dbs::HostFormat *host = nullptr;
+    // dense_spmv: a library-owned copy of the input CSR and its SpMV plan
+    int64_t *d_csr_rp = nullptr;
+    int32_t *d_csr_ci = nullptr;
+    float *d_csr_va = nullptr;
+    dbs_spmv_plan *plan = nullptr;
     dbs_matrix_info info{};
 };

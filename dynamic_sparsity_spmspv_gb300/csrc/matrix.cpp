@@ -231,6 +231,9 @@ dbs_status upload(const std::vector<T> &h, T **d, size_t min_elems, cudaStream_t
 
 void free_device(dbs_matrix *A)
 {
+    if (A->plan) dbs_spmv_plan_destroy(A->plan);
+    cudaFree(A->d_csr_rp); cudaFree(A->d_csr_ci); cudaFree(A->d_csr_va);
+    A->plan = nullptr; A->d_csr_rp = nullptr; A->d_csr_ci = nullptr; A->d_csr_va = nullptr;
     cudaFree(A->d_rb_ptr); cudaFree(A->d_blk_desc); cudaFree(A->d_blk_ref); cudaFree(A->d_cb_ptr);
     cudaFree(A->d_csc_desc); cudaFree(A->d_csc_ref); cudaFree(A->d_payload); cudaFree(A->d_tiles);
     cudaFree(A->d_rb_rows);
@@ -304,6 +307,7 @@ void dbs_build_opts_default(dbs_build_opts *o)
     o->host_only = 0;
     o->num_threads = 0;
     o->device_convert = 0;
+    o->dense_spmv = 0;
 }
 
 const char *dbs_status_string(dbs_status s)
@@ -333,7 +337,7 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
     if (opts_in) o = *opts_in; else dbs_build_opts_default(&o);
     if (o.th0 < 0 || o.th1 < 0 || !(o.th2 > 0.0) || o.force_format < -1 || o.force_format >= DBS_NUM_FORMATS ||
         o.tile_weight < 0 || o.tile_max_row_blocks < 0 || o.tile_max_row_blocks > (int)TILE_MAX_SPAN ||
-        o.num_threads < 0)
+        o.num_threads < 0 || o.dense_spmv < 0 || o.dense_spmv > 1)
         return DBS_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     auto t_start = std::chrono::steady_clock::now();
@@ -602,6 +606,25 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         if ((st = upload(H.rb_ntiles, &A->d_rb_ntiles, (size_t)nbr + 1, s)) != DBS_OK) return fail(st);
         if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return fail(DBS_ERR_CUDA); }
         A->on_device = true;
+        if (o.dense_spmv && valued) {
+            // the input CSR, kept on the device for dense-x calls, and its plan
+            const size_t rb = sizeof(int64_t) * ((size_t)m + 1), cb = sizeof(int32_t) * (size_t)std::max<int64_t>(nnz, 1),
+                         vb = sizeof(float) * (size_t)std::max<int64_t>(nnz, 1);
+            if (dev_malloc(&A->d_csr_rp, rb) != cudaSuccess || dev_malloc(&A->d_csr_ci, cb) != cudaSuccess ||
+                dev_malloc(&A->d_csr_va, vb) != cudaSuccess) {
+                cudaGetLastError();
+                return fail(DBS_ERR_OOM);
+            }
+            if (cudaMemcpy(A->d_csr_rp, row_ptr, rb, cudaMemcpyDefault) != cudaSuccess ||
+                (nnz && cudaMemcpy(A->d_csr_ci, col_idx, sizeof(int32_t) * (size_t)nnz, cudaMemcpyDefault) != cudaSuccess) ||
+                (nnz && cudaMemcpy(A->d_csr_va, vals, sizeof(float) * (size_t)nnz, cudaMemcpyDefault) != cudaSuccess)) {
+                cudaGetLastError();
+                return fail(DBS_ERR_CUDA);
+            }
+            dbs_status st2 = dbs_spmv_plan_create(m, n, nnz, A->d_csr_rp, A->d_csr_ci, A->d_csr_va, stream, &A->plan);
+            if (st2 != DBS_OK) { A->plan = nullptr; return fail(st2); }
+            I.spmv_bytes = (int64_t)(rb + (size_t)nnz * 8) + spmv_plan_bytes(A->plan);
+        }
     }
     I.on_device = A->on_device ? 1 : 0;
     if (on_gpu && o.keep_host) {

@@ -61,7 +61,9 @@ typedef enum {
 typedef enum {
     DBS_PATH_AUTO = 0,         /* device-side choice (Section 3.3.1; see dbs_exec_opts) */
     DBS_PATH_PUSH = 1,         /* column-driven over the block-CSC view */
-    DBS_PATH_PULL = 2          /* row-driven over the block-CSR view */
+    DBS_PATH_PULL = 2,         /* row-driven over the block-CSR view */
+    DBS_PATH_SPMV = 3          /* dbs_spmspv_dense only, on a matrix built with dense_spmv:
+                                  the kept adaptive CSR SpMV (the paper's Limitations) */
 } dbs_path;
 
 /* Low-level block formats (Section 3.2.1, Figure 5(b), Figure 6). */
@@ -99,6 +101,13 @@ typedef struct {
                                   tiles) stay on the host.  Needs the columns of every
                                   row ascending, else the host converts.  Same result
                                   byte for byte.  Default 0. */
+    int32_t dense_spmv;        /* 1 with a valued matrix: also keep a device copy of the
+                                  input CSR (8 B per entry and per row) and an adaptive
+                                  CSR SpMV plan over it; dbs_spmspv_dense then hands an x
+                                  whose sampled nonzero fraction reaches
+                                  dbs_exec_opts.spmv_x_frac to that SpMV inside the same
+                                  launch (the paper's Limitations: conventional SpMV is
+                                  preferable for dense inputs).  Default 0. */
 } dbs_build_opts;
 
 void dbs_build_opts_default(dbs_build_opts *opts);
@@ -120,6 +129,10 @@ typedef struct {
                                   blocks (push's work) number fewer than push_work_frac * B
                                   (pull's scan); default 0.45, the crossover measured on
                                   GB300.  0: the paper's th3 rule. */
+    double spmv_x_frac;        /* dbs_spmspv_dense, auto path, matrix with dense_spmv: the
+                                  CSR SpMV runs when the nonzero fraction of a fixed
+                                  sample of x (8 evenly spaced runs of 32 entries, read
+                                  alike by every block) is at least this; default 0.08 */
 } dbs_exec_opts;
 
 void dbs_exec_opts_default(dbs_exec_opts *opts);
@@ -167,6 +180,8 @@ typedef struct {
     int32_t valued;                         /* 1 if built with values */
     int32_t on_device;                      /* 0 for host_only builds */
     double build_seconds;                   /* host time of the conversion */
+    int64_t spmv_bytes;                     /* dense_spmv: the kept CSR and its SpMV plan
+                                               (not in total_bytes) */
 } dbs_matrix_info;
 
 /* Fills *out.  Host-only, no synchronization. */
@@ -245,7 +260,11 @@ dbs_status dbs_spmspv(const dbs_matrix *A, dbs_semiring sr, const int32_t *x_idx
 /* Section 4.3 (DB-Decoding): x given as a dense device float32[n] whose zero
  * entries are inactive; the vector-block masks are built from it with warp
  * ballots (Section 4.1).  y is a dense device float32[m]; rows with no active
- * contribution are written as 0.  Plus-times only.  ASYNC. */
+ * contribution are written as 0.  Plus-times only.  With a matrix built with
+ * dense_spmv, path DBS_PATH_SPMV (or the auto path when the sampled nonzero
+ * fraction of x reaches spmv_x_frac) computes the same y by the kept CSR SpMV,
+ * entries whose x is zero skipped; DBS_PATH_SPMV without it is
+ * DBS_ERR_INVALID_ARG.  ASYNC. */
 dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_path path,
                             dbs_workspace *ws, void *stream);
 

@@ -43,12 +43,15 @@ def test_status_strings_and_version():
 def test_struct_layouts_match_header_sizes():
     # sizes implied by the C declarations on LP64
     assert ctypes.sizeof(_lib.dbs_build_opts) == 48
-    assert ctypes.sizeof(_lib.dbs_exec_opts) == 32
+    assert ctypes.sizeof(_lib.dbs_exec_opts) == 40
     assert ctypes.sizeof(_lib.dbs_stats) == 104
     o = dbs.build_opts()
     assert (o.th0, o.th1, o.th2, o.force_format) == (32, 128, 2.0, -1)
     e = dbs.exec_opts()
-    assert (e.th3, e.local_pull_min, e.push_work_frac) == (0.01, 0, 0.45)
+    assert (e.th3, e.local_pull_min, e.push_work_frac, e.spmv_x_frac) == (0.01, 0, 0.45, 0.08)
+    assert o.dense_spmv == 0
+    with pytest.raises(TypeError):
+        dbs.build_opts(no_such_option=1)
 
 
 def _host(A, **kw):

@@ -147,3 +147,78 @@ def test_spmv_full_size_llm_and_rmat():
         check(A, x, plan(torch.from_numpy(x).to(DEV)))
         if name == "rmat":
             assert plan.info()["split_rows"] > 0          # hub rows exercise the long-row split
+
+
+def _dense_parity(A, O, y, xd):
+    """dbs_spmspv_dense's contract: the structural product over the nonzero
+    entries of x (zeros inactive), rows nothing reaches exactly 0."""
+    nz = np.nonzero(xd)[0].astype(np.int32)
+    ri, rv, rs = O.spmspv(synth.SparseVec(A.n, nz, xd[nz]))
+    y = y.cpu().numpy()[:A.m]
+    assert oracle.tolerance_ok(y[ri], rv, rs).all()
+    rest = np.ones(A.m, bool)
+    rest[ri] = False
+    assert (y[rest] == 0).all()
+
+
+@pytest.mark.parametrize("name", ["llm", "fem", "er", "rmat"])
+def test_dense_x_handed_to_the_kept_spmv(name):
+    """The paper's Limitations (conventional SpMV suits dense inputs): with
+    dense_spmv the matrix keeps its CSR and an adaptive SpMV plan, and
+    dbs_spmspv_dense computes a dense x by that SpMV -- forced ('spmv'), or
+    on the auto path once the sampled nonzero fraction reaches spmv_x_frac --
+    with the same structural result as the blocked paths; a sparse x stays
+    on the blocked path."""
+    A = valued(synth.config(name, "small"), 2)
+    O = oracle.Oracle(A)
+    M = dbs.DBMatrix.from_csr(A, dense_spmv=1)
+    assert M.info()["spmv_bytes"] > 0
+    ws = dbs.Workspace(M, collect_stats=1)
+    rng = np.random.default_rng(5)
+    for frac in (1.0, 0.6, 0.09, 0.02, 0.0):
+        xd = rng.standard_normal(A.n).astype(np.float32)
+        xd[rng.random(A.n) >= frac] = 0.0
+        xd[:3] = [0.0, -0.0, 1.0] if A.n >= 3 else xd[:3]
+        for path in ("auto", "spmv", "pull", "push"):
+            y = dbs.spmspv_dense(M, torch.from_numpy(xd).to(DEV), ws=ws, path=path)
+            st = ws.stats()
+            assert ws.check() == 0
+            _dense_parity(A, O, y, xd)
+            if path == "spmv":
+                assert st["path"] == 3
+            if path == "auto":
+                if A.n <= 256:
+                    sample = xd
+                else:
+                    t = np.arange(256)
+                    sample = xd[(t >> 5) * (A.n // 8) + (t & 31)]
+                assert (st["path"] == 3) == (np.count_nonzero(sample) >= 0.08 * sample.size), frac
+    # integer values: the SpMV route is bit-exact like the blocked paths
+    I = synth.random_csr(300, 200, 0.2, 7, integer_values=True)
+    MI = dbs.DBMatrix.from_csr(I, dense_spmv=1)
+    wsi = dbs.Workspace(MI)
+    xi = rng.integers(-3, 4, I.n).astype(np.float32)
+    y1 = dbs.spmspv_dense(MI, torch.from_numpy(xi).to(DEV), ws=wsi, path="spmv").cpu().numpy()
+    y2 = dbs.spmspv_dense(MI, torch.from_numpy(xi).to(DEV), ws=wsi, path="pull").cpu().numpy()
+    np.testing.assert_array_equal(y1, y2)
+    # without the kept plan the spmv path is refused
+    M0 = dbs.DBMatrix.from_csr(A)
+    with pytest.raises(dbs.DbsError) as e:
+        dbs.spmspv_dense(M0, torch.zeros(A.n, device=DEV), ws=dbs.Workspace(M0), path="spmv")
+    assert e.value.status == 1
+
+
+@pytest.mark.parametrize("name", ["fem", "llm", "rmat"])
+def test_dense_x_full_size_auto_route(name):
+    """Full-size FEM, LLM and R-MAT (unit weights) with an all-nonzero x: the
+    auto path routes to the kept SpMV and matches the oracle; the
+    one-launch graph replay of the routed call stays correct."""
+    A = valued(synth.config(name, "full"), 3) if name != "rmat" else synth.CSR(
+        *(lambda G: (G.m, G.n, G.row_ptr, G.col_idx, np.ones(G.nnz, np.float32)))(synth.config("rmat", "full")))
+    O = oracle.Oracle(A)
+    M = dbs.DBMatrix.from_csr(A, dense_spmv=1)
+    ws = dbs.Workspace(M, collect_stats=1)
+    xd = np.random.default_rng(9).standard_normal(A.n).astype(np.float32)
+    y = dbs.spmspv_dense(M, torch.from_numpy(xd).to(DEV), ws=ws)
+    assert ws.stats()["path"] == 3 and ws.check() == 0
+    _dense_parity(A, O, y, xd)
