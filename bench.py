@@ -325,7 +325,7 @@ def run_configs(dbs, torch, dev, stream, flush, reps: int):
         us = float(np.median(ts))
         t_nnz, b_alg = touched / len(calls), bytes_alg / len(calls)
         line = {"workload": name, "mode": mode, "path": "/".join(sorted(paths)), "us": round(us, 2),
-                "touched_nnz_per_s": round(t_nnz / us * 1e6), "gbs": round(b_alg / us / 1e3, 1),
+                "bytes_alg": round(b_alg), "touched_nnz_per_s": round(t_nnz / us * 1e6), "gbs": round(b_alg / us / 1e3, 1),
                 "frac_of_measured_hbm": round(b_alg / us / 1e3 / peak, 4)}
         line.update(extra)
         lines.append(line)
@@ -355,6 +355,16 @@ def run_configs(dbs, torch, dev, stream, flush, reps: int):
         measure("fem", f"spmspv x {f:g}", M, ws,
                 [lambda xi=xi, xv=xv: dbs.spmspv(M, xi, xv, ws=ws, y_idx=y_idx, y_val=y_val, y_nnz=y_nnz)
                  for xi, xv in xt], {"density": f})
+    # both paths forced where each moves more than 64 MB (the size at which
+    # the roofline fraction is judged): FEM at cluster densities 10 % and 20 %
+    for f in (0.1, 0.2):
+        xs = [synth.x_clusters(A.n, f, [45, int(f * 1e4), i]) for i in range(4)]
+        xt = [(torch.from_numpy(x.idx).to(dev), torch.from_numpy(x.val).to(dev)) for x in xs]
+        for path in ("push", "pull"):
+            measure("fem", f"spmspv x {f:g}, {path} forced", M, ws,
+                    [lambda xi=xi, xv=xv, path=path: dbs.spmspv(M, xi, xv, ws=ws, path=path, y_idx=y_idx,
+                                                                y_val=y_val, y_nnz=y_nnz) for xi, xv in xt],
+                    {"density": f, "forced": path})
     ws.close(); M.close()
 
     # LLM layer: dense activations (decoding form) and the same as a sparse x
