@@ -597,7 +597,7 @@ def run_decode(dbs, torch, dev, stream, n_layers: int, tokens: int):
                        f"thresholded by magnitude at {DECODE_TAU} inside the kernel",
            "layers": n_layers, "tokens_timed": tokens, "active_fraction": round(active, 4),
            "timing": "CUDA graph of the token step, replayed per token; weights far above L2", "builds": []}
-    for name, kw in (("paper thresholds", {}), ("th1 31, tile weight 160", {"th1": 31, "tile_weight": 160})):
+    for name, kw in (("paper thresholds", {}), ("th1 31", {"th1": 31})):
         Ms = [dbs.DBMatrix.from_csr(A, **kw) for A in layers]
         wss = [dbs.Workspace(M) for M in Ms]
 
@@ -608,8 +608,7 @@ def run_decode(dbs, torch, dev, stream, n_layers: int, tokens: int):
         g = capture(step)
         us = time_tokens(g, load_dev)
         row = {"build": name, "us_per_token": round(us, 1), "us_per_layer": round(us / n_layers, 2),
-               "tokens_per_s": round(1e6 / us, 1), "payload_mb_per_layer": round(Ms[0].info()["payload_bytes"] / 1e6, 1),
-               "tiles_per_layer": Ms[0].info()["ntiles"]}
+               "tokens_per_s": round(1e6 / us, 1), "payload_mb_per_layer": round(Ms[0].info()["payload_bytes"] / 1e6, 1)}
         if kw:
             # end to end: activations from pinned host memory, outputs back to pinned host memory
             h_in = [torch.from_numpy(np.stack(tok)).pin_memory() for tok in acts]

@@ -145,7 +145,7 @@ class DBMatrix:
         return out
 
     RAW_ARRAYS = ("rb_ptr", "blk_desc", "blk_ref", "cb_ptr", "csc_desc", "csc_ref", "payload", "tiles",
-                  "rb_rows", "rb_ntiles")
+                  "rb_rows")
 
     def export_raw(self, name: str) -> np.ndarray:
         """dbs_matrix_export_raw: one internal array as raw bytes (uint8)."""

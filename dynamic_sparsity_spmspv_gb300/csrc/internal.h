@@ -26,7 +26,6 @@ struct HostFormat {
     std::vector<U4> payload;          // P
     std::vector<U4> tiles;            // T: {p0, payload offset, rb0, span | flags | count}
     std::vector<uint16_t> rb_rows;    // nbr: rows of each row block that hold an entry (bit r = row r)
-    std::vector<uint32_t> rb_ntiles;  // nbr: pull tiles whose first or last row block it is
 };
 
 // Allocation-failure injection for tests (dbs_debug_fail_alloc): true when
@@ -76,7 +75,6 @@ struct dbs_matrix {
     dbs::U4 *d_payload = nullptr;
     dbs::U4 *d_tiles = nullptr;
     uint16_t *d_rb_rows = nullptr;
-    uint32_t *d_rb_ntiles = nullptr;
     dbs::HostFormat *host = nullptr;
     // dense_spmv: a library-owned copy of the input CSR and its SpMV plan
     int64_t *d_csr_rp = nullptr;

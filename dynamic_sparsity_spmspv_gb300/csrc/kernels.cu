@@ -85,7 +85,6 @@ struct KParams {
     const uint4 *__restrict__ payload;
     const uint4 *__restrict__ tiles;
     const unsigned short *__restrict__ rb_rows;   // rows holding an entry, per row block
-    const uint32_t *__restrict__ rb_ntiles;       // pull tiles meeting a row block at an end of their span
     // call
     int path_force;
     const int32_t *x_idx;
@@ -110,7 +109,6 @@ struct KParams {
     float *y_acc;
     uint32_t *yrm32;
     unsigned long long *ctile_flag;   // per compaction tile: epoch << 34 | state << 32 | count or prefix
-    uint32_t *rb_cnt;         // decoding: tiles done per shared row block (zero between calls)
     uint32_t n_ctiles;
     uint32_t *bvis32;
     uint32_t *fm32[2];
@@ -357,6 +355,15 @@ struct RowOut {
     uint32_t touched;
 };
 
+// One 16-byte load of read-only data that asks L2 to fetch 64 bytes on a
+// miss (a Dense column is one aligned 64-byte run).
+__device__ __forceinline__ float4 ldg_l2_64(const float4 *p)
+{
+    float4 v;
+    asm("ld.global.nc.L2::64B.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
 // x values: a generic load, because push passes the vector block cached in
 // shared memory and pull passes global memory written earlier in the launch
 // (never read before that point, so no stale L1 line can exist).
@@ -566,7 +573,7 @@ __device__ __forceinline__ uint32_t pair_products(const uint8_t *__restrict__ b,
         float v[16];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float4 t = __ldg(v4 + q);
+            const float4 t = ldg_l2_64(v4 + q);
             v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
         }
 #pragma unroll
@@ -1908,15 +1915,15 @@ __global__ void __launch_bounds__(NT, 4) k_bfs(KParams P)
 // DB-Decoding layer (Section 4.3; the mask generation of Section 4.1 moved
 // into the traversal): y = A x' with x'_j = x_j where |x_j| > tau (NaN is
 // kept) and 0 elsewhere -- magnitude thresholding of the activation -- on
-// the pull path, in one ordinary launch.  Warp w takes pull tile w; each
-// lane forms the activation masks of its blocks' column blocks directly
-// from x, so neither a metadata pass nor a device-wide barrier precedes the
-// traversal.  A row block inside one tile is stored whole (rows without an
-// active entry get 0); a row block split between tiles collects their
-// partial sums in the workspace accumulator with atomics, and the tile that
-// arrives last (a counter per row block) stores it and clears accumulator
-// and counter for the next call.  Row blocks without entries belong to no
-// tile's work and are zeroed up front.
+// the pull path, in one ordinary launch.  A block of threads owns one row
+// block at a time: each thread takes blocks of it (three at a time, their
+// loads issued together), forms each block's activation mask from the 16 x
+// values of its column block, and adds the products of every (block, active
+// column) pair into its own 16 row sums; one reduction over the block then
+// gives the row block's 16 results, stored once (rows without an active
+// entry get 0).  No partial sum leaves the block, so no atomic, counter or
+// fence is needed, and no metadata pass or device-wide barrier precedes the
+// traversal.
 __device__ __forceinline__ uint32_t act_mask(const float *__restrict__ x, uint32_t col, int n, float tau)
 {
     const size_t j0 = (size_t)col * 16u;
@@ -1938,88 +1945,69 @@ __device__ __forceinline__ uint32_t act_mask(const float *__restrict__ x, uint32
     return m;
 }
 
-__global__ void __launch_bounds__(NT, 4) k_decode(KParams P)
-{
-    constexpr int WK = 8;
-    SmemT<0> &S = *reinterpret_cast<SmemT<0> *>(smem_raw);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (uint32_t rb = blockIdx.x * NT + tid; rb < (uint32_t)P.nbr; rb += gridDim.x * NT) {
-        if (__ldg(P.rb_rows + rb) != 0u) continue;
-        for (uint32_t r = 0; r < 16u; ++r) {
-            const size_t row = (size_t)rb * 16u + r;
-            if (row < (size_t)P.m) P.y_dense[row] = 0.0f;
-        }
-    }
-    const uint32_t t = blockIdx.x * NW + warp;
-    if (t >= P.T) return;
-    WarpPull<0> &W = S.wp[warp];
-    const uint4 td = __ldg(P.tiles + t);
-    const uint32_t p0 = td.x, rb0 = td.z, span = td.w & TILE_SPAN_MASK, nblk = td.w >> TILE_NBLK_SHIFT;
-    uint2 d[WK];
-    uint32_t rf[WK];
-#pragma unroll
-    for (int k = 0; k < WK; ++k) {
-        const uint32_t li = (uint32_t)(k * 32 + lane);
-        d[k] = li < nblk ? __ldcs(P.blk_desc + p0 + li) : make_uint2(0u, 0u);
-        rf[k] = li < nblk ? __ldg(P.blk_ref + p0 + li) : 0u;
-    }
-    if (lane < (int)span) W.rm[lane] = 0u;
-    for (uint32_t i = lane; i < span * 16u; i += 32) W.y[i] = 0.0f;
-    if (lane == 0) { W.nq = 0u; W.nq2 = 0u; }
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < WK; ++k) {
-        const uint32_t li = (uint32_t)(k * 32 + lane);
-        if (li >= nblk) continue;
-        const uint32_t col = d[k].x & DESC_COL_MASK, meta = d[k].y, lrb = d[k].x >> DESC_LRB_SHIFT;
-        const uint32_t a = act_mask(P.x_in, col, P.n, P.tau) & meta & 0xFFFFu;
-        if (a) {
-            const uint32_t fmt = meta_fmt(meta);
-            const uint32_t slot = fmt != FMT_COO ? TILE_MAX_BLOCKS - 1u - atomicAdd(&W.nq2, 1u) : atomicAdd(&W.nq, 1u);
-            W.qe[slot] = a | (fmt << 16) | ((meta_nnz(meta) - 1u) << 19) | (lrb << 27);
-            W.qm[slot] = col;
-            W.qr[slot] = rf[k];
-        }
-    }
-    __syncwarp();
-    uint32_t c_bytes = 0;
-    pt_drain<false>(P, S, W, warp, lane, W.nq, P.x_in, c_bytes);
-    __syncwarp();
+constexpr int DEC_NT = 512; // threads per row block
+constexpr int DEC_NW = DEC_NT / 32;
+constexpr int DEC_K = 2;    // blocks per thread per round of a row block
 
-    const uint32_t nt0 = __ldg(P.rb_ntiles + rb0), nt1 = span > 1u ? __ldg(P.rb_ntiles + rb0 + span - 1u) : nt0;
-    for (uint32_t i = lane; i < span * 16u; i += 32) {
-        const uint32_t lrb = i >> 4, r = i & 15u;
-        const size_t row = (size_t)(rb0 + lrb) * 16u + r;
-        const uint32_t nt = lrb == 0u ? nt0 : (lrb == span - 1u ? nt1 : 1u);
-        if (nt > 1u) {
-            if ((W.rm[lrb] >> r) & 1u) atomicAdd(P.y_acc + row, W.y[i]);
-        } else if (row < (size_t)P.m) {
-            P.y_dense[row] = W.y[i];
-        }
-    }
-    if (nt0 > 1u || nt1 > 1u) {
-        __threadfence();                 // every lane's partial sums before the counter
-        __syncwarp();
-        bool last = false;
-        if (lane < 2 && (lane == 0 || span > 1u)) {
-            const uint32_t nt = lane == 0 ? nt0 : nt1;
-            if (nt > 1u) last = atomicAdd(P.rb_cnt + rb0 + (lane == 0 ? 0u : span - 1u), 1u) == nt - 1u;
-        }
-        const uint32_t lm = __ballot_sync(FULL, last);
-        if (lm) {
-            __threadfence();
-            for (uint32_t h = 0; h < 2u; ++h) {
-                if (!((lm >> h) & 1u)) continue;
-                const uint32_t rb = rb0 + (h ? span - 1u : 0u);
-                if (lane < 16) {
-                    const size_t row = (size_t)rb * 16u + lane;
-                    const float v = __ldcg(P.y_acc + row);
-                    P.y_acc[row] = 0.0f;
-                    if (row < (size_t)P.m) P.y_dense[row] = v;
+__global__ void __launch_bounds__(DEC_NT, 2) k_decode(KParams P)
+{
+    constexpr int NT = DEC_NT, NW = DEC_NW;
+    __shared__ float s_part[NW][16];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float tau = P.tau;
+    const float *__restrict__ x = P.x_in;
+    for (uint32_t rb = blockIdx.x; rb < (uint32_t)P.nbr; rb += gridDim.x) {
+        const uint32_t p0 = __ldg(P.rb_ptr + rb), p1 = __ldg(P.rb_ptr + rb + 1);
+        float acc[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) acc[r] = 0.0f;
+        for (uint32_t base = p0; base < p1; base += NT * DEC_K) {
+            uint2 d[DEC_K];
+            uint32_t ref[DEC_K], am[DEC_K];
+#pragma unroll
+            for (int k = 0; k < DEC_K; ++k) {
+                const uint32_t p = base + (uint32_t)(k * NT + tid);
+                d[k] = p < p1 ? __ldg(P.blk_desc + p) : make_uint2(0u, 0u);
+                ref[k] = p < p1 ? __ldg(P.blk_ref + p) : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < DEC_K; ++k)
+                am[k] = base + (uint32_t)(k * NT + tid) < p1
+                            ? act_mask(x, d[k].x & DESC_COL_MASK, P.n, tau) & d[k].y & 0xFFFFu : 0u;
+#pragma unroll
+            for (int k = 0; k < DEC_K; ++k) {
+                if (!am[k]) continue;
+                const uint32_t meta = d[k].y, fmt = meta_fmt(meta), nnz = meta_nnz(meta), col = d[k].x & DESC_COL_MASK;
+                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + ref[k]);
+                const float *xb = x + (size_t)col * 16u;
+                if (fmt == FMT_COO) {
+                    coo_lane(b, nnz, am[k], xb, true, [&](uint32_t r, float v) {
+#pragma unroll
+                        for (int rr = 0; rr < 16; ++rr) acc[rr] += (uint32_t)rr == r ? v : 0.0f;
+                    });
+                } else {
+                    for (uint32_t a = am[k]; a; a &= a - 1u) {
+                        const uint32_t c = __ffs(a) - 1u;
+                        float t[16];
+                        pair_products(b, fmt, nnz, c, __ldg(xb + c), t);
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) acc[r] += t[r];
+                    }
                 }
-                if (lane == 0) P.rb_cnt[rb] = 0u;
             }
         }
+        // row sums over the block: warp transpose reduction, then the warps
+        const float v = warp_rows_sum(acc, true, lane);
+        if (!(lane & 1)) s_part[warp][(lane >> 1) & 15] = v;
+        __syncthreads();
+        if (tid < 16) {
+            float sum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) sum += s_part[w][tid];
+            const size_t row = (size_t)rb * 16u + tid;
+            if (row < (size_t)P.m) P.y_dense[row] = sum;
+        }
+        __syncthreads();
     }
 }
 
@@ -2051,7 +2039,6 @@ struct dbs_workspace {
     float *y_acc = nullptr;
     uint32_t *yrm32 = nullptr;
     unsigned long long *ctile_flag = nullptr;
-    uint32_t *rb_cnt = nullptr;
     uint32_t n_ctiles = 0;
     uint32_t *bvis32 = nullptr;
     uint32_t *fm32[2] = {nullptr, nullptr};
@@ -2066,7 +2053,7 @@ namespace {
 void ws_free(dbs_workspace *w)
 {
     cudaFree(w->x_dense); cudaFree(w->xm32); cudaFree(w->dxm32); cudaFree(w->y_acc); cudaFree(w->yrm32);
-    cudaFree(w->ctile_flag); cudaFree(w->rb_cnt); cudaFree(w->bvis32); cudaFree(w->fm32[0]); cudaFree(w->fm32[1]);
+    cudaFree(w->ctile_flag); cudaFree(w->bvis32); cudaFree(w->fm32[0]); cudaFree(w->fm32[1]);
     cudaFree(w->ctrl); cudaFree(w->spmv_part); cudaFree(w->spmv_cnt);
     for (int s = 0; s < 3; ++s) { cudaFree(w->act[s]); cudaFree(w->chunks[s]); }
 }
@@ -2094,11 +2081,9 @@ KParams make_params(const dbs_matrix *A, dbs_workspace *w)
     P.payload = reinterpret_cast<const uint4 *>(A->d_payload);
     P.tiles = reinterpret_cast<const uint4 *>(A->d_tiles);
     P.rb_rows = A->d_rb_rows;
-    P.rb_ntiles = A->d_rb_ntiles;
     P.x_dense = w->x_dense; P.xm32 = w->xm32; P.dxm32 = w->dxm32;
     for (int s = 0; s < 3; ++s) { P.act[s] = w->act[s]; P.chunks[s] = w->chunks[s]; }
     P.y_acc = w->y_acc; P.yrm32 = w->yrm32; P.ctile_flag = w->ctile_flag; P.n_ctiles = w->n_ctiles;
-    P.rb_cnt = w->rb_cnt;
     P.bvis32 = w->bvis32; P.fm32[0] = w->fm32[0]; P.fm32[1] = w->fm32[1];
     P.ctrl = w->ctrl;
     P.th3 = w->opts.th3;
@@ -2193,7 +2178,7 @@ dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
     bool ok = dalloc(&w->x_dense, nbc * 16 + 16) && dalloc(&w->xm32, nbc / 2 + 8) &&
               dalloc(&w->dxm32, nbc / 2 + 8) &&
               dalloc(&w->y_acc, nbr * 16 + 16) && dalloc(&w->yrm32, yrm_words) &&
-              dalloc(&w->ctile_flag, (size_t)w->n_ctiles + 1) && dalloc(&w->rb_cnt, nbr + 1) &&
+              dalloc(&w->ctile_flag, (size_t)w->n_ctiles + 1) &&
               dalloc(&w->bvis32, nbr / 2 + 8) &&
               dalloc(&w->fm32[0], nbc / 2 + 8) && dalloc(&w->fm32[1], nbc / 2 + 8) && dalloc(&w->ctrl, 1);
     for (int s = 0; s < 3 && ok; ++s) ok = dalloc(&w->act[s], nbc + 1) && dalloc(&w->chunks[s], chunk_cap);
@@ -2207,7 +2192,12 @@ dbs_status dbs_workspace_create(const dbs_matrix *A, dbs_workspace **out)
     w->grid_dense[1] = coop_grid((const void *)k_spmspv_dense<true>, w->sms, SMEM0);
     w->grid_bfs[0] = coop_grid((const void *)k_bfs<false>, w->sms, SMEM1);
     w->grid_bfs[1] = coop_grid((const void *)k_bfs<true>, w->sms, SMEM1);
-    w->decode_ok = coop_grid((const void *)k_decode, w->sms, SMEM0) > 0;   // sets its shared-memory size
+    {
+        int nb = 0;
+        w->decode_ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, (const void *)k_decode, DEC_NT, 0) ==
+                           cudaSuccess && nb > 0;
+        cudaGetLastError();
+    }
     bool grids_ok = true;
     for (int a = 0; a < 2; ++a)
         grids_ok = grids_ok && w->grid_sparse[0][a] && w->grid_sparse[1][a] && w->grid_dense[a] && w->grid_bfs[a];
@@ -2258,7 +2248,6 @@ dbs_status dbs_workspace_check(dbs_workspace *w, void *stream)
               cudaMemset(w->xm32, 0, ((size_t)A->nbc / 2 + 8) * 4) == cudaSuccess &&
               cudaMemset(w->y_acc, 0, ((size_t)A->nbr * 16 + 16) * sizeof(float)) == cudaSuccess &&
               cudaMemset(w->yrm32, 0, (std::max<size_t>(1, w->n_ctiles) * CTILE / 2 + 8) * 4) == cudaSuccess &&
-              cudaMemset(w->rb_cnt, 0, ((size_t)A->nbr + 1) * 4) == cudaSuccess &&
               cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) { cudaGetLastError(); return DBS_ERR_CUDA; }
     return (dbs_status)c.err;
@@ -2344,9 +2333,9 @@ dbs_status dbs_decode_layer(const dbs_matrix *A, const float *x, float tau, floa
     P.xv = x;
     P.tau = tau;
     P.y_dense = y;
-    const int64_t g_tiles = (A->T + NW - 1) / NW, g_rows = (A->nbr + NT - 1) / NT;
-    const int grid = (int)std::max<int64_t>(1, std::max(g_tiles, g_rows));
-    k_decode<<<grid, NT, SMEM0, (cudaStream_t)stream>>>(P);
+    // one block per row block, up to two blocks per SM (the rest loop)
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(A->nbr, 2 * (int64_t)w->sms));
+    k_decode<<<grid, DEC_NT, 0, (cudaStream_t)stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return DBS_ERR_CUDA;
     return DBS_OK;
 }

@@ -237,11 +237,9 @@ void free_device(dbs_matrix *A)
     cudaFree(A->d_rb_ptr); cudaFree(A->d_blk_desc); cudaFree(A->d_blk_ref); cudaFree(A->d_cb_ptr);
     cudaFree(A->d_csc_desc); cudaFree(A->d_csc_ref); cudaFree(A->d_payload); cudaFree(A->d_tiles);
     cudaFree(A->d_rb_rows);
-    cudaFree(A->d_rb_ntiles);
     A->d_rb_ptr = nullptr; A->d_blk_desc = nullptr; A->d_blk_ref = nullptr; A->d_cb_ptr = nullptr;
     A->d_csc_desc = nullptr; A->d_csc_ref = nullptr; A->d_payload = nullptr; A->d_tiles = nullptr;
     A->d_rb_rows = nullptr;
-    A->d_rb_ntiles = nullptr;
 }
 
 template <class T>
@@ -560,14 +558,6 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
             }
             if (next != (uint64_t)B) return fail(DBS_ERR_INTERNAL);
         }
-        // tiles meeting each row block at an end of their span (2 or more:
-        // the row block's partial sums come from several tiles)
-        H.rb_ntiles.assign((size_t)nbr, 0u);
-        for (const U4 &tl : H.tiles) {
-            const uint32_t span = tl.w & TILE_SPAN_MASK;
-            ++H.rb_ntiles[tl.z];
-            if (span > 1u) ++H.rb_ntiles[tl.z + span - 1u];
-        }
     } catch (const std::bad_alloc &) {
         return fail(DBS_ERR_OOM);
     }
@@ -603,7 +593,6 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         if (!on_gpu && (st = upload(H.payload, &A->d_payload, 1, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.tiles, &A->d_tiles, 1, s)) != DBS_OK) return fail(st);
         if ((st = upload(H.rb_rows, &A->d_rb_rows, (size_t)nbr + 2, s)) != DBS_OK) return fail(st);
-        if ((st = upload(H.rb_ntiles, &A->d_rb_ntiles, (size_t)nbr + 1, s)) != DBS_OK) return fail(st);
         if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return fail(DBS_ERR_CUDA); }
         A->on_device = true;
         if (o.dense_spmv && valued) {
@@ -716,8 +705,7 @@ dbs_status dbs_matrix_export_raw(const dbs_matrix *A, int32_t which, void *dst, 
     case DBS_RAW_CSC_REF: size = B * 4; dsrc = A->d_csc_ref; hsrc = H ? H->csc_ref.data() : nullptr; break;
     case DBS_RAW_PAYLOAD: size = (size_t)A->P * 16; dsrc = A->d_payload; hsrc = H ? H->payload.data() : nullptr; break;
     case DBS_RAW_TILES: size = (size_t)A->T * 16; dsrc = A->d_tiles; hsrc = H ? H->tiles.data() : nullptr; break;
-    case DBS_RAW_RB_ROWS: size = nbr * 2; dsrc = A->d_rb_rows; hsrc = H ? H->rb_rows.data() : nullptr; break;
-    default: size = nbr * 4; dsrc = A->d_rb_ntiles; hsrc = H ? H->rb_ntiles.data() : nullptr; break;
+    default: size = nbr * 2; dsrc = A->d_rb_rows; hsrc = H ? H->rb_rows.data() : nullptr; break;
     }
     *bytes = (int64_t)size;
     if (!dst) return DBS_OK;

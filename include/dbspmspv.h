@@ -209,12 +209,12 @@ dbs_status dbs_matrix_export_csr(const dbs_matrix *A, int64_t *row_ptr, int32_t 
  * {u32, u32}[B], payload offsets u32[B], column-block pointers u32[nbc+1],
  * block-CSC descriptors {u32, u32}[B], block-CSC payload offsets u32[B],
  * payload 16-byte units [P], pull tiles {u32 x4}[T], rows holding an entry
- * u16[nbr], tiles per row block u32[nbr]) into HOST memory.  *bytes gets
+ * u16[nbr]) into HOST memory.  *bytes gets
  * the array's size; the copy happens when dst is non-NULL and capacity is
  * large enough (else DBS_ERR_INVALID_ARG).  Synchronous. */
 typedef enum {
     DBS_RAW_RB_PTR = 0, DBS_RAW_BLK_DESC, DBS_RAW_BLK_REF, DBS_RAW_CB_PTR, DBS_RAW_CSC_DESC,
-    DBS_RAW_CSC_REF, DBS_RAW_PAYLOAD, DBS_RAW_TILES, DBS_RAW_RB_ROWS, DBS_RAW_RB_NTILES, DBS_RAW_COUNT
+    DBS_RAW_CSC_REF, DBS_RAW_PAYLOAD, DBS_RAW_TILES, DBS_RAW_RB_ROWS, DBS_RAW_COUNT
 } dbs_raw_array;
 dbs_status dbs_matrix_export_raw(const dbs_matrix *A, int32_t which, void *dst, int64_t capacity, int64_t *bytes);
 
@@ -275,15 +275,17 @@ dbs_status dbs_spmspv_dense(const dbs_matrix *A, const float *x, float *y, dbs_p
  * on the pull path.  The activation mask of each 16-entry vector block is
  * formed from x inside the traversal (Section 4.1's mask generation fused
  * into the kernel that consumes it), so the call is one ordinary kernel
- * launch with no device-wide barrier and no path decision: use it when the
- * input is known to be dense enough for pull (decoding activations at about
- * 10 % density); dbs_spmspv_dense is the general form with the selector.
+ * launch with no device-wide barrier, no path decision and no workspace
+ * scratch: one block of threads owns each row block.  Use it when the input
+ * is known to be dense enough for pull (decoding activations at about 10 %
+ * density); dbs_spmspv_dense is the general form with the selector.
  *   x    device (or host-mapped) float32[n], 16-byte aligned
  *   tau  threshold, >= 0 (tau = 0: every nonzero entry is active)
  *   y    device float32[m]; every row is written (0 where nothing is active)
- * Summation order within a row is not fixed (row blocks split between
- * pull tiles combine partial sums with atomics).  Capturable in a CUDA
- * graph.  Errors: DBS_ERR_INVALID_ARG (null pointers, tau < 0 or NaN,
+ * Summation order within a row is fixed by the matrix (each thread sums
+ * its blocks, then a fixed tree combines the threads), so repeated calls
+ * give identical bits; it is not the sequential order.  Capturable in a
+ * CUDA graph.  Errors: DBS_ERR_INVALID_ARG (null pointers, tau < 0 or NaN,
  * misaligned x), DBS_ERR_UNSUPPORTED (pattern-only matrix), DBS_ERR_CUDA.
  * ASYNC. */
 dbs_status dbs_decode_layer(const dbs_matrix *A, const float *x, float tau, float *y, dbs_workspace *ws,

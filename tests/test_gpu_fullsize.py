@@ -107,9 +107,9 @@ def test_grid_hubs_full_bfs(full):
 
 def test_llm_full_decode_layer(full):
     """The DB-Decoding layer at the workload's full size, with the paper's
-    thresholds and with the GB300 decode build (th1 = 31, tile weight 160)."""
+    thresholds and with the GB300 decode build (th1 = 31)."""
     A, O, M = full("llm")
-    for Mb in (M, dbs.DBMatrix.from_csr(A, th1=31, tile_weight=160)):
+    for Mb in (M, dbs.DBMatrix.from_csr(A, th1=31)):
         ws = dbs.Workspace(Mb)
         for t in range(4):
             xa = synth.x_activation(A.n, [90, t, 0])
