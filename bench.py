@@ -488,6 +488,38 @@ def run_ablation(dbs, torch, dev, stream, flush, reps: int):
     return rows
 
 
+def run_convert(dbs, torch, reps: int):
+    """Offline conversion (DB-SpMSpV Section 5.5) of each full-size workload
+    from a device CSR: the host builder (download, native threads, upload)
+    against the device conversion (every pass on the GPU), best wall time of
+    `reps` builds each, with the most device memory each build held
+    (`build_peak_bytes`)."""
+    import synth
+    out = []
+    for name in ("rmat", "fem", "llm", "grid"):
+        A = synth.config(name, "full")
+        rp = torch.from_numpy(A.row_ptr).cuda()
+        ci = torch.from_numpy(A.col_idx).cuda()
+        va = None if A.vals is None else torch.from_numpy(A.vals).cuda()
+        torch.cuda.synchronize()
+        line = {"workload": name, "nnz": int(A.nnz)}
+        for key, dc in (("host", 0), ("device", 1)):
+            ts, inf = [], None
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                M = dbs.DBMatrix(A.m, A.n, rp, ci, va, device_convert=dc)
+                torch.cuda.synchronize()
+                ts.append(time.perf_counter() - t0)
+                inf = M.info()
+                M.close()
+            line[key] = {"seconds": round(min(ts), 4), "build_peak_mb": round(inf["build_peak_bytes"] / 1e6, 1),
+                         "matrix_mb": round(inf["total_bytes"] / 1e6, 1)}
+        line["blocks"] = int(inf["nblocks"])
+        out.append(line)
+        del rp, ci, va
+    return out
+
+
 def run_spmv(dbs, torch, dev, flush, reps: int):
     """Dense-input regime: adaptive CSR SpMV (dbs_spmv, plan built once);
     dbs_spmspv_dense on the auto path of a matrix built with dense_spmv (which
@@ -687,6 +719,8 @@ def main():
     ap.add_argument("--decode-tokens", type=int, default=20, help="tokens timed in the decoding step")
     ap.add_argument("--spmv", type=int, default=10,
                     help="calls per point of the dense-input comparison (adaptive CSR SpMV vs DB pull; 0 = off)")
+    ap.add_argument("--convert", type=int, default=2,
+                    help="builds per point of the conversion comparison (host vs device; 0 = off)")
     ap.add_argument("--ablation", type=int, default=0,
                     help="calls per point of the format ablation (Auto / COO-only / CSR-only on the "
                          "R-MAT, FEM and LLM workloads) and per-level frontier histograms (0 = off)")
@@ -950,6 +984,9 @@ def main():
 
     if args.decode_layers > 0:
         out["decode"] = run_decode(dbs, torch, dev, stream, args.decode_layers, args.decode_tokens)
+
+    if args.convert > 0:
+        out["conversion"] = run_convert(dbs, torch, args.convert)
 
     if args.ablation > 0:
         out["ablation"] = run_ablation(dbs, torch, dev, stream, flush, args.ablation)

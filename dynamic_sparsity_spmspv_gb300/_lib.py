@@ -35,7 +35,7 @@ class dbs_matrix_info(ctypes.Structure):
                 ("nnz_by_format", I64 * NUM_FORMATS), ("ntiles", I64), ("payload_bytes", I64),
                 ("view_bytes", I64), ("total_bytes", I64), ("csr_bytes", I64),
                 ("csr_csc_bytes", I64), ("valued", I32), ("on_device", I32),
-                ("build_seconds", F64), ("spmv_bytes", I64)]
+                ("build_seconds", F64), ("spmv_bytes", I64), ("build_peak_bytes", I64)]
 
 
 class dbs_stats(ctypes.Structure):

@@ -1,22 +1,35 @@
 // Device-side conversion of a device CSR into the blocked dual-view format
-// (Section 3.2.1; the paper converts offline, Section 5.5).  The
-// entry-proportional work -- finding the nonzero 16x16 blocks, classifying
-// them, encoding their payloads -- runs on the GPU; the block-proportional
-// bookkeeping (payload offsets, block-CSC view, pull tiles) stays with the
-// host builder's code, so both builders produce the same bytes.
+// (Section 3.2.1; the paper converts offline, Section 5.5).  Every pass runs
+// on the GPU: the blocks, their formats and payloads, the payload offsets,
+// the block-CSC view, the pull tiles, the per-row-block row masks and the
+// storage counts.  The host only reads a few counts between passes to size
+// the next allocation.  The result is byte-for-byte the host builder's.
 //
-// No sort.  With the columns of every row ascending, the blocks of a row
-// block are found by a 16-way merge: one warp per row block, lane r walks
-// row r, each step takes the smallest column block at the lanes' heads and
-// every lane consumes its run of entries in that column block.  A block's
-// entries then arrive in row-major order with their row-major ranks from a
-// lane prefix, and every column-ordered position follows from the block's
-// per-column row masks.  Device memory beyond the input and the finished
-// matrix is one count per row block plus 13 bytes per block (descriptor,
-// payload units, payload offset) -- no nnz-sized temporaries, unlike a
-// sort-based converter.
+// Blocks without a sort.  With the columns of every row ascending, the
+// blocks of a row block are found by a 16-way merge: one warp per row block,
+// lane r walks row r, each step takes the smallest column block at the
+// lanes' heads and every lane consumes its run of entries in that column
+// block.  A block's entries then arrive in row-major order with their
+// row-major ranks from a lane prefix, and every column-ordered position
+// follows from the block's per-column row masks.
+//
+// Block-CSC view: blocks are counted per column block, scattered into their
+// column block's range with atomic cursors, and each range is then sorted
+// by primary block id (one warp for ranges of up to 32 blocks, a CTA's
+// bitonic sort in shared memory for longer ones, and sorted 4096-block
+// chunks merged by rank for the longest), which is the stable order of the
+// host's counting sort.
+//
+// Pull tiles: the greedy cut of Section 3.3.2 depends on where the previous
+// tile ended, so the end of a tile starting at each block is computed in
+// parallel first, and one CTA then follows the chain of tile starts from
+// block 0 through windows of those ends staged in shared memory.
+//
+// Device memory beyond the input CSR and the finished matrix: 4 bytes per
+// block and 12 per column block, plus scan partials.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "internal.h"
@@ -29,21 +42,19 @@ constexpr int CT = 256;                 // threads per block: 8 warps, one row b
 constexpr uint32_t NO_CB = 0xFFFFFFFFu;
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
-enum : unsigned { ERR_RANGE = 1u, ERR_DUP = 2u, ERR_ORDER = 4u };
+enum : unsigned { ERR_RANGE = 1u, ERR_DUP = 2u, ERR_ORDER = 4u, ERR_PTR = 8u, ERR_INTERNAL = 16u, ERR_SIZE = 32u };
 
 struct ConvParams {
-    int64_t m, n, nbr;
+    int64_t m, n, nnz, nbr, nbc, B;
     const int64_t *rp;
     const int32_t *ci;
     const float *va;        // NULL: pattern only
     int th0, th1;
     double th2;
     int force_format;       // -1 automatic
-    uint32_t *rb_count;     // blocks per row block
-    const uint32_t *rb_ptr; // block-CSR row-block pointers
+    uint32_t *rb_ptr;       // block-CSR row-block pointers (counts before the scan)
     uint2 *desc;            // per block {column block, meta}
-    uint8_t *units;         // per block payload units
-    const uint32_t *ref;    // per block payload offset
+    uint32_t *ref;          // per block payload offset
     uint4 *payload;
     unsigned *err;
 };
@@ -74,6 +85,7 @@ __device__ __forceinline__ uint32_t cb_at(const ConvParams &C, const RowCursor &
     return r.pos < r.end ? (uint32_t)__ldg(C.ci + r.pos) >> 4 : NO_CB;
 }
 
+// A row's cursor; only after the row pointers were validated (pass 1).
 __device__ __forceinline__ RowCursor open_row(const ConvParams &C, int64_t rb, int lane)
 {
     RowCursor r{0, 0, NO_CB};
@@ -102,14 +114,28 @@ __device__ __forceinline__ uint32_t merge_step(const ConvParams &C, RowCursor &r
     return mn;
 }
 
-// Pass 1: validate the rows and count the blocks of every row block.
+// Pass 1: validate the row pointers (before any entry is read) and the
+// rows, and count the blocks of every row block.
 __global__ void __launch_bounds__(CT) k_conv_count(ConvParams C)
 {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && (__ldg(C.rp) != 0 || __ldg(C.rp + C.m) != C.nnz))
+        atomicOr(C.err, ERR_PTR);
     const int lane = threadIdx.x & 31;
     const int64_t rb = (int64_t)blockIdx.x * (CT / 32) + (threadIdx.x >> 5);
     if (rb >= C.nbr) return;
-    RowCursor r = open_row(C, rb, lane);
+    RowCursor r{0, 0, NO_CB};
     unsigned bad = 0;
+    const int64_t row = rb * BS + lane;
+    if (lane < BS && row < C.m) {
+        const int64_t a = __ldg(C.rp + row), b = __ldg(C.rp + row + 1);
+        if (a < 0 || b < a || b > C.nnz) bad = ERR_PTR;
+        else { r.pos = a; r.end = b; }
+    }
+    if (__reduce_or_sync(FULL, bad)) {
+        if (lane == 0) atomicOr(C.err, ERR_PTR);
+        return;
+    }
+    r.head = cb_at(C, r);
     for (int64_t k = r.pos; k < r.end; ++k) {
         const int32_t c = __ldg(C.ci + k);
         if (c < 0 || (int64_t)c >= C.n) bad |= ERR_RANGE;
@@ -131,7 +157,7 @@ __global__ void __launch_bounds__(CT) k_conv_count(ConvParams C)
         if (merge_step(C, r, &s, &cnt) == NO_CB) break;
         ++nb;
     }
-    if (lane == 0) C.rb_count[rb] = nb;
+    if (lane == 0) C.rb_ptr[rb] = nb;
 }
 
 // Statistics of the block of the current merge step, on every lane.
@@ -166,14 +192,14 @@ __device__ __forceinline__ BlockStats block_stats(const ConvParams &C, int64_t s
     return b;
 }
 
-// Pass 2: descriptor and payload size of every block.
+// Pass 2: the descriptor of every block.
 __global__ void __launch_bounds__(CT) k_conv_desc(ConvParams C)
 {
     const int lane = threadIdx.x & 31;
     const int64_t rb = (int64_t)blockIdx.x * (CT / 32) + (threadIdx.x >> 5);
     if (rb >= C.nbr) return;
     RowCursor r = open_row(C, rb, lane);
-    uint32_t p = __ldg(C.rb_ptr + rb);
+    uint32_t p = C.rb_ptr[rb];
     const bool valued = C.va != nullptr;
     for (;; ++p) {
         int64_t s;
@@ -182,7 +208,7 @@ __global__ void __launch_bounds__(CT) k_conv_desc(ConvParams C)
         if (cb == NO_CB) break;
         const BlockStats b = block_stats(C, s, cnt, lane);
         const uint32_t fmt = classify_dev(C, (int)b.nnz, (int)b.maxr, (int)b.maxc);
-        uint32_t meta, units;
+        uint32_t meta;
         if (fmt == FMT_COO && !valued && b.nnz <= INLINE_MAX_NNZ) {
             // inline block: coordinate bytes of row-major entries 0..nnz-1,
             // unused bytes repeating entry 0
@@ -195,15 +221,10 @@ __global__ void __launch_bounds__(CT) k_conv_desc(ConvParams C)
             }
             w = __reduce_or_sync(FULL, w);
             meta = META_INLINE | ((b.nnz - 1u) << 24) | w;
-            units = 0;
         } else {
             meta = meta_pack(b.cm, fmt, b.nnz);
-            units = payload_units(fmt, b.nnz, valued);
         }
-        if (lane == 0) {
-            C.desc[p] = make_uint2(cb, meta);
-            C.units[p] = (uint8_t)units;
-        }
+        if (lane == 0 && p < (uint64_t)C.B) C.desc[p] = make_uint2(cb, meta);
     }
 }
 
@@ -216,7 +237,7 @@ __global__ void __launch_bounds__(CT) k_conv_encode(ConvParams C)
     const int64_t rb = (int64_t)blockIdx.x * (CT / 32) + w;
     if (rb >= C.nbr) return;
     RowCursor r = open_row(C, rb, lane);
-    uint32_t p = __ldg(C.rb_ptr + rb);
+    uint32_t p = C.rb_ptr[rb];
     const bool valued = C.va != nullptr;
     for (;; ++p) {
         int64_t s;
@@ -281,141 +302,714 @@ __global__ void __launch_bounds__(CT) k_conv_encode(ConvParams C)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Scans.  Three passes over tiles of SCAN_TILE items: per-tile aggregates,
+// one CTA scanning the aggregates, then each tile scanned from its prefix.
+// An operation supplies the element type T, identity(), combine(a, b) (a
+// before b), load(i), store(i, exclusive prefix, element) and finish(total).
+
+constexpr int SCAN_T = 256, SCAN_V = 16, SCAN_TILE = SCAN_T * SCAN_V, SCAN_W = SCAN_T / 32;
+
+template <class T>
+__device__ __forceinline__ T shfl_up_any(const T &v, int o)
+{
+    static_assert(sizeof(T) % 4 == 0, "32-bit words");
+    T r;
+    const uint32_t *a = reinterpret_cast<const uint32_t *>(&v);
+    uint32_t *b = reinterpret_cast<uint32_t *>(&r);
+#pragma unroll
+    for (int k = 0; k < (int)(sizeof(T) / 4); ++k) b[k] = __shfl_up_sync(FULL, a[k], o);
+    return r;
+}
+
+// Exclusive scan of one value per thread over the CTA; *total gets the
+// combination of all of them.  s_w holds SCAN_W values.
+template <class Op>
+__device__ typename Op::T block_exclusive(typename Op::T v, typename Op::T *s_w, typename Op::T *total)
+{
+    using T = typename Op::T;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    T inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const T t = shfl_up_any(inc, o);
+        if (lane >= o) inc = Op::combine(t, inc);
+    }
+    T ex = shfl_up_any(inc, 1);
+    if (lane == 0) ex = Op::identity();
+    if (lane == 31) s_w[warp] = inc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        T run = Op::identity();
+        for (int w = 0; w < SCAN_W; ++w) {
+            const T t = s_w[w];
+            s_w[w] = run;
+            run = Op::combine(run, t);
+        }
+        s_w[SCAN_W] = run;
+    }
+    __syncthreads();
+    const T res = Op::combine(s_w[warp], ex);
+    *total = s_w[SCAN_W];
+    __syncthreads();
+    return res;
+}
+
+template <class Op>
+__global__ void __launch_bounds__(SCAN_T) k_scan_reduce(Op op, int64_t n, typename Op::T *agg)
+{
+    using T = typename Op::T;
+    __shared__ T s_w[SCAN_W + 1];
+    const int64_t base = (int64_t)blockIdx.x * SCAN_TILE + (int64_t)threadIdx.x * SCAN_V;
+    T a = Op::identity();
+    for (int k = 0; k < SCAN_V; ++k)
+        if (base + k < n) a = Op::combine(a, op.load(base + k));
+    T tot;
+    block_exclusive<Op>(a, s_w, &tot);
+    if (threadIdx.x == 0) agg[blockIdx.x] = tot;
+}
+
+template <class Op>
+__global__ void __launch_bounds__(SCAN_T) k_scan_aggs(Op op, int64_t ntiles, typename Op::T *agg)
+{
+    using T = typename Op::T;
+    __shared__ T s_w[SCAN_W + 1];
+    T carry = Op::identity();
+    for (int64_t b = 0; b < ntiles; b += SCAN_T) {
+        const int64_t i = b + threadIdx.x;
+        const T v = i < ntiles ? agg[i] : Op::identity();
+        T tot;
+        const T ex = block_exclusive<Op>(v, s_w, &tot);
+        if (i < ntiles) agg[i] = Op::combine(carry, ex);
+        carry = Op::combine(carry, tot);
+    }
+    if (threadIdx.x == 0) op.finish(carry);
+}
+
+template <class Op>
+__global__ void __launch_bounds__(SCAN_T) k_scan_down(Op op, int64_t n, const typename Op::T *agg)
+{
+    using T = typename Op::T;
+    __shared__ T s_w[SCAN_W + 1];
+    const int64_t base = (int64_t)blockIdx.x * SCAN_TILE + (int64_t)threadIdx.x * SCAN_V;
+    T v[SCAN_V];
+    T a = Op::identity();
+#pragma unroll
+    for (int k = 0; k < SCAN_V; ++k) {
+        v[k] = base + k < n ? op.load(base + k) : Op::identity();
+        a = Op::combine(a, v[k]);
+    }
+    T tot;
+    T run = Op::combine(agg[blockIdx.x], block_exclusive<Op>(a, s_w, &tot));
+#pragma unroll
+    for (int k = 0; k < SCAN_V; ++k)
+        if (base + k < n) {
+            op.store(base + k, run, v[k]);
+            run = Op::combine(run, v[k]);
+        }
+}
+
+// Exclusive prefix sums of n counts in place, the total stored at a[n] and
+// (64-bit) at *total; totals of 2^32 or more set ERR_SIZE.
+struct CountScan {
+    using T = unsigned long long;
+    uint32_t *a;
+    int64_t n;
+    unsigned long long *total;
+    unsigned *err;
+    __device__ static T identity() { return 0ull; }
+    __device__ static T combine(T x, T y) { return x + y; }
+    __device__ T load(int64_t i) const { return a[i]; }
+    __device__ void store(int64_t i, T ex, T) const { a[i] = (uint32_t)ex; }
+    __device__ void finish(T t) const
+    {
+        *total = t;
+        if (t >= (1ull << 32)) atomicOr(err, ERR_SIZE);
+        a[n] = (uint32_t)t;
+    }
+};
+
+// Payload offsets: block p's payload starts where block p-1's ended,
+// rounded up to DENSE_ALIGN_UNITS for a valued Dense block.  The running
+// end offset after a range of blocks is a function x -> f(x) of the offset
+// before it, of the form x + b or align(x + a) + b; these compose in closed
+// form (align(align(x + a1) + b1 + a2) = align(x + a1) + align(b1 + a2)
+// since align(x + a1) is a multiple of the alignment), so the offsets are a
+// scan over that composition.
+struct Shift {
+    uint32_t al, pad;
+    unsigned long long a, b;
+};
+__device__ __forceinline__ unsigned long long align_units(unsigned long long x)
+{
+    return (x + DENSE_ALIGN_UNITS - 1) / DENSE_ALIGN_UNITS * DENSE_ALIGN_UNITS;
+}
+struct OffsetScan {
+    using T = Shift;
+    const uint2 *desc;
+    uint32_t *ref;
+    bool valued;
+    unsigned long long *total;
+    unsigned *err;
+    __device__ static T identity() { return Shift{0u, 0u, 0ull, 0ull}; }
+    __device__ static T combine(const T &g, const T &h)
+    {
+        if (!h.al) return Shift{g.al, 0u, g.a, g.b + h.b};
+        if (!g.al) return Shift{1u, 0u, g.b + h.a, h.b};
+        return Shift{1u, 0u, g.a, align_units(g.b + h.a) + h.b};
+    }
+    __device__ T load(int64_t p) const
+    {
+        const uint32_t meta = desc[p].y;
+        const bool al = valued && !meta_inline(meta) && meta_fmt(meta) == FMT_DENSE;
+        return Shift{al ? 1u : 0u, 0u, 0ull, (unsigned long long)meta_units(meta, valued)};
+    }
+    __device__ static unsigned long long apply0(const T &f) { return f.al ? align_units(f.a) + f.b : f.b; }
+    __device__ void store(int64_t p, const T &ex, const T &e) const
+    {
+        unsigned long long start = apply0(ex);
+        if (e.al) start = align_units(start);
+        if (start + e.b >= (1ull << 32)) atomicOr(err, ERR_SIZE);
+        ref[p] = (uint32_t)start;
+    }
+    __device__ void finish(const T &t) const
+    {
+        *total = apply0(t);
+        if (*total >= (1ull << 32)) atomicOr(err, ERR_SIZE);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Block-CSC view.
+
+// Row block holding primary block p (the largest rb with rb_ptr[rb] <= p).
+__device__ __forceinline__ uint32_t row_block_of(const uint32_t *rb_ptr, int64_t nbr, uint32_t p)
+{
+    uint32_t lo = 0, hi = (uint32_t)nbr;
+    while (hi - lo > 1u) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (__ldg(rb_ptr + mid) <= p) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+constexpr uint32_t SORT_CHUNK = 4096;   // blocks sorted at once in shared memory
+
+struct CscParams {
+    int64_t nbr, nbc, B;
+    const uint32_t *rb_ptr;
+    const uint2 *desc;
+    const uint32_t *ref;
+    uint32_t *cb_ptr;       // counts, then pointers (nbc + 1)
+    uint32_t *cur;          // per column block: next free position
+    uint32_t *pos;          // B: primary ids in CSC order (the csc_ref array until filled)
+    uint32_t *tmp;          // B: chunk-sorted ranges
+    uint32_t *lists;        // [nbc] ranges over 32 blocks, [nbc] ranges over SORT_CHUNK
+    unsigned *nlists;       // their counts
+    uint2 *csc_desc;
+    unsigned *err;
+};
+
+__global__ void k_csc_count(CscParams P)
+{
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < P.B; p += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t c = P.desc[p].x & DESC_COL_MASK;
+        if (c < (uint64_t)P.nbc) atomicAdd(P.cb_ptr + c, 1u);
+        else atomicOr(P.err, ERR_INTERNAL);
+    }
+}
+
+__global__ void k_csc_scatter(CscParams P)
+{
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < P.B; p += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t c = P.desc[p].x & DESC_COL_MASK;
+        if (c >= (uint64_t)P.nbc) continue;
+        const uint32_t q = atomicAdd(P.cur + c, 1u);
+        if (q < P.cb_ptr[c + 1]) P.pos[q] = (uint32_t)p;
+        else atomicOr(P.err, ERR_INTERNAL);
+    }
+}
+
+// One warp per column block: ranges of up to 32 blocks are ranked in place
+// (ids are distinct); longer ranges are listed for the CTA sorts.
+__global__ void __launch_bounds__(CT) k_csc_small(CscParams P)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t c = (int64_t)blockIdx.x * (CT / 32) + (threadIdx.x >> 5);
+    if (c >= P.nbc) return;
+    const uint32_t s = P.cb_ptr[c], len = P.cb_ptr[c + 1] - s;
+    if (len <= 1u) return;
+    if (len <= 32u) {
+        const uint32_t v = (uint32_t)lane < len ? P.pos[s + lane] : 0xFFFFFFFFu;
+        uint32_t rank = 0;
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t t = __shfl_sync(FULL, v, j);
+            rank += ((uint32_t)j < len && t < v) ? 1u : 0u;
+        }
+        __syncwarp();
+        if ((uint32_t)lane < len) P.pos[s + rank] = v;
+        return;
+    }
+    if (lane == 0) {
+        P.lists[atomicAdd(P.nlists, 1u)] = (uint32_t)c;
+        if (len > SORT_CHUNK) P.lists[P.nbc + atomicAdd(P.nlists + 1, 1u)] = (uint32_t)c;
+    }
+}
+
+// Bitonic sort, ascending, of s[0..np) (np a power of two) by the CTA.
+__device__ void bitonic_sort(uint32_t *s, uint32_t np)
+{
+    for (uint32_t k = 2; k <= np; k <<= 1)
+        for (uint32_t j = k >> 1; j > 0; j >>= 1) {
+            for (uint32_t i = threadIdx.x; i < np; i += blockDim.x) {
+                const uint32_t l = i ^ j;
+                if (l > i) {
+                    const uint32_t a = s[i], b = s[l];
+                    if ((a > b) == ((i & k) == 0u)) { s[i] = b; s[l] = a; }
+                }
+            }
+            __syncthreads();
+        }
+}
+
+// One CTA per listed range: each chunk of up to SORT_CHUNK blocks sorted in
+// shared memory, in place when the range is one chunk, else into tmp.
+__global__ void __launch_bounds__(CT) k_csc_sort(CscParams P)
+{
+    __shared__ uint32_t s_v[SORT_CHUNK];
+    const uint32_t nl = *P.nlists;
+    for (uint32_t e = blockIdx.x; e < nl; e += gridDim.x) {
+        const uint32_t c = P.lists[e];
+        const uint32_t s = P.cb_ptr[c], len = P.cb_ptr[c + 1] - s;
+        uint32_t *dst = len > SORT_CHUNK ? P.tmp : P.pos;
+        for (uint32_t c0 = 0; c0 < len; c0 += SORT_CHUNK) {
+            const uint32_t cl = min(SORT_CHUNK, len - c0);
+            uint32_t np = 2;
+            while (np < cl) np <<= 1;
+            for (uint32_t i = threadIdx.x; i < np; i += blockDim.x)
+                s_v[i] = i < cl ? P.pos[s + c0 + i] : 0xFFFFFFFFu;
+            __syncthreads();
+            bitonic_sort(s_v, np);
+            for (uint32_t i = threadIdx.x; i < cl; i += blockDim.x) dst[s + c0 + i] = s_v[i];
+            __syncthreads();
+        }
+    }
+}
+
+// Ranges of several chunks: an id's final rank is its rank in its own
+// sorted chunk plus the count of smaller ids in each other chunk.
+__global__ void __launch_bounds__(CT) k_csc_merge(CscParams P)
+{
+    const uint32_t nh = P.nlists[1];
+    for (uint32_t e = blockIdx.x; e < nh; e += gridDim.x) {
+        const uint32_t c = P.lists[P.nbc + e];
+        const uint32_t s = P.cb_ptr[c], len = P.cb_ptr[c + 1] - s;
+        const uint32_t nch = (len + SORT_CHUNK - 1) / SORT_CHUNK;
+        for (uint32_t i = threadIdx.x; i < len; i += blockDim.x) {
+            const uint32_t v = P.tmp[s + i], own = i / SORT_CHUNK;
+            uint32_t rank = i - own * SORT_CHUNK;
+            for (uint32_t k = 0; k < nch; ++k) {
+                if (k == own) continue;
+                const uint32_t *ch = P.tmp + s + k * SORT_CHUNK;
+                uint32_t lo = 0, hi = min(SORT_CHUNK, len - k * SORT_CHUNK);
+                while (lo < hi) {
+                    const uint32_t mid = (lo + hi) >> 1;
+                    if (ch[mid] < v) lo = mid + 1;
+                    else hi = mid;
+                }
+                rank += lo;
+            }
+            P.pos[s + rank] = v;
+        }
+    }
+}
+
+// CSC position q: {row block, meta} and the payload offset of its block.
+__global__ void k_csc_fill(CscParams P)
+{
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < P.B; q += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t p = P.pos[q];
+        if (p >= (uint64_t)P.B) {
+            atomicOr(P.err, ERR_INTERNAL);
+            continue;
+        }
+        P.csc_desc[q] = make_uint2(row_block_of(P.rb_ptr, P.nbr, p), P.desc[p].y);
+        P.pos[q] = __ldg(P.ref + p);
+    }
+}
+
+// Rows of each row block that hold an entry.
+__global__ void k_rb_rows(const int64_t *rp, int64_t m, int64_t nbr, uint16_t *rows)
+{
+    for (int64_t rb = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; rb < nbr; rb += (int64_t)gridDim.x * blockDim.x) {
+        uint32_t bits = 0;
+        for (int r = 0; r < BS; ++r) {
+            const int64_t i = rb * BS + r;
+            if (i < m && __ldg(rp + i + 1) > __ldg(rp + i)) bits |= 1u << r;
+        }
+        rows[rb] = (uint16_t)bits;
+    }
+}
+
+// Blocks and entries per format, and the total tile weight.
+__global__ void k_format_counts(const uint2 *desc, int64_t B, unsigned long long *out)
+{
+    __shared__ unsigned long long s_c[2 * DBS_NUM_FORMATS + 1];
+    if (threadIdx.x < 2 * DBS_NUM_FORMATS + 1) s_c[threadIdx.x] = 0;
+    __syncthreads();
+    unsigned long long nb[DBS_NUM_FORMATS] = {}, nz[DBS_NUM_FORMATS] = {}, w = 0;
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < B; p += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t meta = desc[p].y, f = meta_fmt(meta);
+        if (f >= (uint32_t)DBS_NUM_FORMATS) continue;
+        nb[f] += 1;
+        nz[f] += meta_nnz(meta);
+        w += fmt_weight(f);
+    }
+    for (int f = 0; f < DBS_NUM_FORMATS; ++f) {
+        if (nb[f]) atomicAdd(s_c + f, nb[f]);
+        if (nz[f]) atomicAdd(s_c + DBS_NUM_FORMATS + f, nz[f]);
+    }
+    if (w) atomicAdd(s_c + 2 * DBS_NUM_FORMATS, w);
+    __syncthreads();
+    if (threadIdx.x < 2 * DBS_NUM_FORMATS + 1 && s_c[threadIdx.x]) atomicAdd(out + threadIdx.x, s_c[threadIdx.x]);
+}
+
+// ---------------------------------------------------------------------------
+// Pull tiles (Section 3.3.2 segments, generalised as in the host builder: a
+// tile closes once its weight reaches W or its count reaches the block cap,
+// and before a block whose row block is R or more past the tile's first).
+
+struct TileParams {
+    int64_t nbr, B;
+    uint32_t W, R;
+    const uint32_t *rb_ptr;
+    uint2 *desc;
+    const uint32_t *ref;
+    uint32_t *next;         // B: end of the tile starting at each block; then the tile starts
+    uint4 *tiles;
+    unsigned long long *count;
+    unsigned *err;
+};
+
+constexpr int NEXT_SPAN = 32 + (int)TILE_MAX_BLOCKS;   // blocks a warp's 32 starts can reach
+
+// One warp per 32 consecutive starts: block weights over the reachable
+// window, their prefix sums, and per start the first block where the weight
+// reaches W (a binary search; every weight is at least 1 and W <= 256).
+__global__ void __launch_bounds__(CT) k_tile_next(TileParams P)
+{
+    __shared__ uint32_t s_pre[CT / 32][NEXT_SPAN];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t base = ((int64_t)blockIdx.x * (CT / 32) + warp) * 32;
+    if (base >= P.B) return;
+    uint32_t *pre = s_pre[warp];
+    const int64_t kmax = min((int64_t)NEXT_SPAN, P.B - base);
+    constexpr int PER = NEXT_SPAN / 32;
+    uint32_t loc[PER], sum = 0;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        const int64_t i = (int64_t)lane * PER + k;
+        loc[k] = i < kmax ? fmt_weight(meta_fmt(P.desc[base + i].y)) : 0u;
+        sum += loc[k];
+    }
+    uint32_t inc = sum;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(FULL, inc, o);
+        if (lane >= o) inc += t;
+    }
+    uint32_t run = inc - sum;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+        run += loc[k];
+        pre[lane * PER + k] = run;
+    }
+    __syncwarp();
+    const int64_t p = base + lane;
+    if (p >= P.B) return;
+    const uint32_t target = (lane ? pre[lane - 1] : 0u) + P.W;
+    uint32_t lo = (uint32_t)lane, hi = (uint32_t)kmax;
+    while (lo < hi) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (pre[mid] >= target) hi = mid;
+        else lo = mid + 1;
+    }
+    int64_t e = lo < (uint32_t)kmax ? base + lo + 1 : P.B;
+    e = min(e, p + (int64_t)TILE_MAX_BLOCKS - (int64_t)(p & 1));
+    const uint32_t rb = row_block_of(P.rb_ptr, P.nbr, (uint32_t)p);
+    e = min(e, (int64_t)P.rb_ptr[min((int64_t)rb + P.R, P.nbr)]);
+    e = min(e, P.B);
+    P.next[p] = (uint32_t)e;
+}
+
+constexpr int CHAIN_T = 1024;
+constexpr uint32_t CHAIN_WIN = 11264;   // ends staged per window (44 KB)
+
+// One CTA: the tile starts are the chain 0 -> next[0] -> ... < B.  Windows
+// of next[] are staged in shared memory and thread 0 walks them, writing the
+// t-th start over next[t] (t never exceeds the start, and every entry at
+// or past the window's end is still unread).
+__global__ void __launch_bounds__(CHAIN_T) k_tile_chain(TileParams P)
+{
+    __shared__ uint32_t s_next[CHAIN_WIN];
+    __shared__ uint32_t s_p, s_t;
+    if (threadIdx.x == 0) { s_p = 0; s_t = 0; }
+    __syncthreads();
+    for (;;) {
+        const uint32_t w0 = s_p;
+        if ((int64_t)w0 >= P.B) break;
+        const uint32_t wl = (uint32_t)min((int64_t)CHAIN_WIN, P.B - (int64_t)w0);
+        for (uint32_t i = threadIdx.x; i < wl; i += blockDim.x) s_next[i] = P.next[w0 + i];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            uint32_t p = w0, t = s_t;
+            while (p < w0 + wl) {
+                const uint32_t e = s_next[p - w0];
+                P.next[t++] = p;
+                if (e <= p || (int64_t)e > P.B) {
+                    atomicOr(P.err, ERR_INTERNAL);
+                    p = (uint32_t)P.B;
+                    break;
+                }
+                p = e;
+            }
+            s_p = p;
+            s_t = t;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *P.count = s_t;
+}
+
+// One thread per tile: its kernel form, and each block's local row block.
+__global__ void k_tile_build(TileParams P, uint32_t T)
+{
+    for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) {
+        const uint32_t p0 = P.next[t], p1 = t + 1 < T ? P.next[t + 1] : (uint32_t)P.B;
+        const uint32_t nb = p1 - p0;
+        if (p1 <= p0 || (int64_t)p1 > P.B || (p0 & 1u) + nb > TILE_MAX_BLOCKS) {
+            atomicOr(P.err, ERR_INTERNAL);
+            continue;
+        }
+        const uint32_t rb0 = row_block_of(P.rb_ptr, P.nbr, p0), rbl = row_block_of(P.rb_ptr, P.nbr, p1 - 1);
+        const uint32_t span = rbl - rb0 + 1u;
+        if (span > TILE_MAX_SPAN || (int64_t)rb0 + span > P.nbr) {
+            atomicOr(P.err, ERR_INTERNAL);
+            continue;
+        }
+        uint32_t w = span | (nb << TILE_NBLK_SHIFT);
+        if (P.rb_ptr[rb0] < p0) w |= TILE_FIRST_SHARED;
+        if (P.rb_ptr[rb0 + span] > p1) w |= TILE_LAST_SHARED;
+        P.tiles[t] = make_uint4(p0, P.ref[p0], rb0, w);
+        uint32_t rb = rb0;
+        for (uint32_t p = p0; p < p1; ++p) {
+            while (P.rb_ptr[rb + 1] <= p) ++rb;
+            P.desc[p].x |= (rb - rb0) << DESC_LRB_SHIFT;
+        }
+    }
+}
+
+// Counts the host reads between passes.
+struct Small {
+    unsigned err;
+    unsigned nlists[2];
+    unsigned pad;
+    unsigned long long B, P, B_csc, T;
+    unsigned long long fmt[2 * DBS_NUM_FORMATS + 1];   // blocks, entries per format; total weight
+};
+
+// The device allocations of one conversion: every one not handed to the
+// matrix is released when this goes out of scope.
+struct Slots {
+    static constexpr int N = 24;
+    void *p[N] = {};
+    template <class T>
+    bool alloc(T **q, size_t bytes)
+    {
+        *q = nullptr;
+        for (int i = 0; i < N; ++i)
+            if (!p[i]) {
+                if (dev_malloc(q, std::max<size_t>(bytes, 16)) != cudaSuccess) { cudaGetLastError(); *q = nullptr; return false; }
+                p[i] = *q;
+                return true;
+            }
+        return false;
+    }
+    void release(void *q)
+    {
+        for (int i = 0; i < N; ++i)
+            if (q && p[i] == q) { dev_free(q); p[i] = nullptr; }
+    }
+    void keep(void *q)
+    {
+        for (int i = 0; i < N; ++i)
+            if (q && p[i] == q) p[i] = nullptr;
+    }
+    ~Slots()
+    {
+        for (int i = 0; i < N; ++i) dev_free(p[i]);
+    }
+};
+
+unsigned grid_for(int64_t n, int sms)
+{
+    return (unsigned)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)sms * 32));
+}
+
+template <class Op>
+bool run_scan(const Op &op, int64_t n, typename Op::T *agg, cudaStream_t s)
+{
+    const int64_t ntiles = (n + SCAN_TILE - 1) / SCAN_TILE;
+    if (ntiles) k_scan_reduce<Op><<<(unsigned)ntiles, SCAN_T, 0, s>>>(op, n, agg);
+    k_scan_aggs<Op><<<1, SCAN_T, 0, s>>>(op, ntiles, agg);
+    if (ntiles) k_scan_down<Op><<<(unsigned)ntiles, SCAN_T, 0, s>>>(op, n, agg);
+    return cudaGetLastError() == cudaSuccess;
+}
+
 }  // namespace
 
 namespace dbs {
 
-// Runs the conversion on the device.  On return (DBS_OK): H.rb_ptr,
-// H.blk_desc (local row blocks not yet set) and H.blk_ref are filled on the
-// host, *B and *P hold the block and payload-unit counts, and *d_payload is
-// a device allocation holding the encoded payload (P units).  `fallback`
-// is set when a row's columns are not ascending (the host builder handles
-// any order).  Validation failures return DBS_ERR_INVALID_ARG.
-static dbs_status device_convert_impl(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp, const int32_t *d_ci,
-                                      const float *d_va, const dbs_build_opts &o, cudaStream_t s, HostFormat &H,
-                                      int64_t *B, int64_t *P, uint4 **d_payload, bool *fallback,
-                                      void *(&scratch)[6]);
-
 dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp, const int32_t *d_ci,
-                          const float *d_va, const dbs_build_opts &o, cudaStream_t s, HostFormat &H, int64_t *B,
-                          int64_t *P, uint4 **d_payload, bool *fallback)
-{
-    // the device scratch of a conversion that a host allocation failure
-    // interrupts is released here
-    void *scratch[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
-    try {
-        return device_convert_impl(m, n, nnz, d_rp, d_ci, d_va, o, s, H, B, P, d_payload, fallback, scratch);
-    } catch (const std::bad_alloc &) {
-        for (void *q : scratch) cudaFree(q);
-        *d_payload = nullptr;
-        return DBS_ERR_OOM;
-    }
-}
-
-static dbs_status device_convert_impl(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp, const int32_t *d_ci,
-                                      const float *d_va, const dbs_build_opts &o, cudaStream_t s, HostFormat &H,
-                                      int64_t *B, int64_t *P, uint4 **d_payload, bool *fallback,
-                                      void *(&scratch)[6])
+                          const float *d_va, const dbs_build_opts &o, cudaStream_t s, DeviceFormat *F,
+                          bool *fallback)
 {
     *fallback = false;
-    *d_payload = nullptr;
-    const int64_t nbr = (m + BS - 1) / BS;
+    *F = DeviceFormat{};
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return DBS_ERR_CUDA;
+    }
+    const int64_t nbr = (m + BS - 1) / BS, nbc = (n + BS - 1) / BS;
+    Slots S;
+    Small h{};
+    Small *d_small = nullptr;
+    auto oom = []() { return DBS_ERR_OOM; };
+    auto cuda_fail = [&]() { cudaGetLastError(); return DBS_ERR_CUDA; };
+    auto read_small = [&]() {
+        return cudaMemcpyAsync(&h, d_small, sizeof(Small), cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+               cudaStreamSynchronize(s) == cudaSuccess;
+    };
     ConvParams C{};
-    C.m = m; C.n = n; C.nbr = nbr;
+    C.m = m; C.n = n; C.nnz = nnz; C.nbr = nbr; C.nbc = nbc;
     C.rp = d_rp; C.ci = d_ci; C.va = d_va;
     C.th0 = o.th0; C.th1 = o.th1; C.th2 = o.th2; C.force_format = o.force_format;
-    uint32_t *d_count = nullptr, *d_rb_ptr = nullptr, *d_ref = nullptr;
-    unsigned *d_err = nullptr;
-    uint2 *d_desc = nullptr;
-    uint8_t *d_units = nullptr;
-    auto cleanup = [&]() {
-        cudaFree(d_count); cudaFree(d_rb_ptr); cudaFree(d_ref); cudaFree(d_err); cudaFree(d_desc); cudaFree(d_units);
-        for (void *&q : scratch) q = nullptr;
-    };
-    // what the caller frees if a host allocation throws
-    auto track = [&]() {
-        scratch[0] = d_count; scratch[1] = d_rb_ptr; scratch[2] = d_ref; scratch[3] = d_err; scratch[4] = d_desc;
-        scratch[5] = d_units;
-    };
-    auto cuda_fail = [&]() { cudaGetLastError(); cleanup(); return DBS_ERR_CUDA; };
-    const unsigned grid = (unsigned)((nbr + CT / 32 - 1) / (CT / 32));
-    if (dev_malloc(&d_count, sizeof(uint32_t) * (size_t)(nbr + 1)) != cudaSuccess ||
-        dev_malloc(&d_err, sizeof(unsigned)) != cudaSuccess) { cudaGetLastError(); cleanup(); return DBS_ERR_OOM; }
-    if (cudaMemsetAsync(d_err, 0, sizeof(unsigned), s) != cudaSuccess ||
-        cudaMemsetAsync(d_count, 0, sizeof(uint32_t) * (size_t)(nbr + 1), s) != cudaSuccess) return cuda_fail();
-    track();
-    C.rb_count = d_count;
-    C.err = d_err;
-    if (grid) k_conv_count<<<grid, CT, 0, s>>>(C);
-    host_alloc_point();
-    std::vector<uint32_t> cnt((size_t)nbr);
-    unsigned err = 0;
-    if (cudaGetLastError() != cudaSuccess ||
-        cudaMemcpyAsync(&err, d_err, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        (nbr && cudaMemcpyAsync(cnt.data(), d_count, sizeof(uint32_t) * (size_t)nbr, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
-        cudaStreamSynchronize(s) != cudaSuccess) return cuda_fail();
-    if (err & (ERR_RANGE | ERR_DUP)) { cleanup(); return DBS_ERR_INVALID_ARG; }
-    if (err & ERR_ORDER) { cleanup(); *fallback = true; return DBS_OK; }
-
-    // block-CSR pointers
-    H.rb_ptr.assign((size_t)nbr + 1, 0u);
-    uint64_t tot = 0;
-    for (int64_t rb = 0; rb < nbr; ++rb) {
-        tot += cnt[(size_t)rb];
-        if (tot >= (uint64_t(1) << 32)) { cleanup(); return DBS_ERR_UNSUPPORTED; }
-        H.rb_ptr[(size_t)rb + 1] = (uint32_t)tot;
-    }
-    *B = (int64_t)tot;
-    const size_t nB = (size_t)tot;
-    if (dev_malloc(&d_rb_ptr, sizeof(uint32_t) * (size_t)(nbr + 1)) != cudaSuccess ||
-        dev_malloc(&d_desc, sizeof(uint2) * (nB + 1)) != cudaSuccess ||
-        dev_malloc(&d_units, nB + 16) != cudaSuccess ||
-        dev_malloc(&d_ref, sizeof(uint32_t) * (nB + 1)) != cudaSuccess) { cudaGetLastError(); cleanup(); return DBS_ERR_OOM; }
-    track();
-    if (cudaMemcpyAsync(d_rb_ptr, H.rb_ptr.data(), sizeof(uint32_t) * (size_t)(nbr + 1), cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return cuda_fail();
-    C.rb_ptr = d_rb_ptr;
-    C.desc = d_desc;
-    C.units = d_units;
-    if (grid) k_conv_desc<<<grid, CT, 0, s>>>(C);
-    host_alloc_point();
-    std::vector<uint8_t> units(nB);
-    H.blk_desc.resize(nB);
-    if (cudaGetLastError() != cudaSuccess ||
-        (nB && cudaMemcpyAsync(H.blk_desc.data(), d_desc, sizeof(uint2) * nB, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
-        (nB && cudaMemcpyAsync(units.data(), d_units, nB, cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
-        cudaStreamSynchronize(s) != cudaSuccess) return cuda_fail();
-
-    // payload offsets, with the host builder's alignment rule
-    H.blk_ref.resize(nB);
     const bool valued = d_va != nullptr;
-    uint64_t pu = 0;
-    for (size_t p = 0; p < nB; ++p) {
-        const uint32_t meta = H.blk_desc[p].y;
-        if (valued && !meta_inline(meta) && meta_fmt(meta) == FMT_DENSE)
-            pu = (pu + DENSE_ALIGN_UNITS - 1) / DENSE_ALIGN_UNITS * DENSE_ALIGN_UNITS;
-        H.blk_ref[p] = (uint32_t)pu;
-        pu += units[p];
-        if (pu >= (uint64_t(1) << 32)) { cleanup(); return DBS_ERR_UNSUPPORTED; }
+    const unsigned grid_rb = (unsigned)((nbr + CT / 32 - 1) / (CT / 32));
+
+    // 1. validation and blocks per row block; block-CSR pointers
+    if (!S.alloc(&d_small, sizeof(Small)) || !S.alloc(&C.rb_ptr, sizeof(uint32_t) * (size_t)(nbr + 1))) return oom();
+    if (cudaMemsetAsync(d_small, 0, sizeof(Small), s) != cudaSuccess ||
+        cudaMemsetAsync(C.rb_ptr, 0, sizeof(uint32_t) * (size_t)(nbr + 1), s) != cudaSuccess) return cuda_fail();
+    C.err = &d_small->err;
+    k_conv_count<<<std::max(grid_rb, 1u), CT, 0, s>>>(C);
+    if (cudaGetLastError() != cudaSuccess || !read_small()) return cuda_fail();
+    if (h.err & (ERR_PTR | ERR_RANGE | ERR_DUP)) return DBS_ERR_INVALID_ARG;
+    if (h.err & ERR_ORDER) { *fallback = true; return DBS_OK; }
+    // scan partials: one per tile of the scanned array
+    auto agg_bytes = [](int64_t len) { return sizeof(Shift) * (size_t)((len + SCAN_TILE - 1) / SCAN_TILE + 1); };
+    char *d_agg = nullptr;
+    if (!S.alloc(&d_agg, agg_bytes(nbr))) return oom();
+    {
+        CountScan op{C.rb_ptr, nbr, &d_small->B, C.err};
+        if (!run_scan(op, nbr, reinterpret_cast<unsigned long long *>(d_agg), s) || !read_small()) return cuda_fail();
     }
-    *P = (int64_t)pu;
-    uint4 *d_pay = nullptr;
-    const size_t pay_bytes = std::max<size_t>((size_t)pu * 16, 16);
-    if (dev_malloc(&d_pay, pay_bytes) != cudaSuccess) { cudaGetLastError(); cleanup(); return DBS_ERR_OOM; }
-    if (cudaMemsetAsync(d_pay, 0, pay_bytes, s) != cudaSuccess ||
-        (nB && cudaMemcpyAsync(d_ref, H.blk_ref.data(), sizeof(uint32_t) * nB, cudaMemcpyHostToDevice, s) != cudaSuccess)) {
-        cudaFree(d_pay);
+    if (h.err & ERR_SIZE) return DBS_ERR_UNSUPPORTED;
+    const int64_t B = (int64_t)h.B;
+    C.B = B;
+
+    // 2. descriptors, storage counts and payload offsets
+    if (!S.alloc(&C.desc, sizeof(uint2) * (size_t)(B + 8)) || !S.alloc(&C.ref, sizeof(uint32_t) * (size_t)(B + 8)))
+        return oom();
+    if (cudaMemsetAsync(C.desc, 0, sizeof(uint2) * (size_t)(B + 8), s) != cudaSuccess ||
+        cudaMemsetAsync(C.ref, 0, sizeof(uint32_t) * (size_t)(B + 8), s) != cudaSuccess) return cuda_fail();
+    if (grid_rb) k_conv_desc<<<grid_rb, CT, 0, s>>>(C);
+    k_format_counts<<<grid_for(B, sms), 256, 0, s>>>(C.desc, B, d_small->fmt);
+    S.release(d_agg);
+    if (!S.alloc(&d_agg, agg_bytes(std::max(B, nbc)))) return oom();
+    {
+        OffsetScan op{C.desc, C.ref, valued, &d_small->P, C.err};
+        if (!run_scan(op, B, reinterpret_cast<Shift *>(d_agg), s) || !read_small()) return cuda_fail();
+    }
+    if (h.err & ERR_SIZE) return DBS_ERR_UNSUPPORTED;
+    const int64_t P = (int64_t)h.P;
+
+    // 3. payload
+    if (!S.alloc(&C.payload, (size_t)P * 16)) return oom();
+    if (cudaMemsetAsync(C.payload, 0, std::max<size_t>((size_t)P * 16, 16), s) != cudaSuccess) return cuda_fail();
+    if (grid_rb) k_conv_encode<<<grid_rb, CT, 0, s>>>(C);
+    if (cudaGetLastError() != cudaSuccess) return cuda_fail();
+
+    // 4. block-CSC view
+    CscParams Q{};
+    Q.nbr = nbr; Q.nbc = nbc; Q.B = B;
+    Q.rb_ptr = C.rb_ptr; Q.desc = C.desc; Q.ref = C.ref;
+    Q.nlists = d_small->nlists;
+    Q.err = C.err;
+    if (!S.alloc(&Q.cb_ptr, sizeof(uint32_t) * (size_t)(nbc + 1)) || !S.alloc(&Q.cur, sizeof(uint32_t) * (size_t)nbc) ||
+        !S.alloc(&Q.lists, sizeof(uint32_t) * 2 * (size_t)nbc) || !S.alloc(&Q.csc_desc, sizeof(uint2) * (size_t)(B + 8)) ||
+        !S.alloc(&Q.pos, sizeof(uint32_t) * (size_t)(B + 8)) || !S.alloc(&Q.tmp, sizeof(uint32_t) * (size_t)B))
+        return oom();
+    if (cudaMemsetAsync(Q.cb_ptr, 0, sizeof(uint32_t) * (size_t)(nbc + 1), s) != cudaSuccess ||
+        cudaMemsetAsync(Q.csc_desc, 0, sizeof(uint2) * (size_t)(B + 8), s) != cudaSuccess ||
+        cudaMemsetAsync(Q.pos, 0, sizeof(uint32_t) * (size_t)(B + 8), s) != cudaSuccess) return cuda_fail();
+    k_csc_count<<<grid_for(B, sms), 256, 0, s>>>(Q);
+    {
+        CountScan op{Q.cb_ptr, nbc, &d_small->B_csc, C.err};
+        if (!run_scan(op, nbc, reinterpret_cast<unsigned long long *>(d_agg), s)) return cuda_fail();
+    }
+    if (nbc && cudaMemcpyAsync(Q.cur, Q.cb_ptr, sizeof(uint32_t) * (size_t)nbc, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
         return cuda_fail();
+    k_csc_scatter<<<grid_for(B, sms), 256, 0, s>>>(Q);
+    if (nbc) k_csc_small<<<(unsigned)((nbc + CT / 32 - 1) / (CT / 32)), CT, 0, s>>>(Q);
+    k_csc_sort<<<(unsigned)sms * 4, CT, 0, s>>>(Q);
+    k_csc_merge<<<(unsigned)sms * 4, CT, 0, s>>>(Q);
+    k_csc_fill<<<grid_for(B, sms), 256, 0, s>>>(Q);
+    if (cudaGetLastError() != cudaSuccess) return cuda_fail();
+    S.release(Q.cur);
+    S.release(Q.lists);
+
+    // 5. rows holding an entry, per row block
+    uint16_t *d_rows = nullptr;
+    if (!S.alloc(&d_rows, sizeof(uint16_t) * (size_t)(nbr + 2))) return oom();
+    if (cudaMemsetAsync(d_rows, 0, sizeof(uint16_t) * (size_t)(nbr + 2), s) != cudaSuccess) return cuda_fail();
+    k_rb_rows<<<grid_for(nbr, sms), 256, 0, s>>>(d_rp, m, nbr, d_rows);
+    if (cudaGetLastError() != cudaSuccess || !read_small()) return cuda_fail();
+    if (h.err || h.B_csc != (unsigned long long)B) return DBS_ERR_INTERNAL;
+
+    // 6. pull tiles
+    TileParams T{};
+    T.nbr = nbr; T.B = B;
+    T.W = tile_weight_cap(o, h.fmt[2 * DBS_NUM_FORMATS]);
+    T.R = o.tile_max_row_blocks > 0 ? (uint32_t)o.tile_max_row_blocks : TILE_MAX_SPAN;
+    T.rb_ptr = C.rb_ptr; T.desc = C.desc; T.ref = C.ref;
+    T.next = Q.tmp;
+    T.count = &d_small->T;
+    T.err = C.err;
+    const int64_t warps = (B + 31) / 32;
+    if (warps) k_tile_next<<<(unsigned)((warps + CT / 32 - 1) / (CT / 32)), CT, 0, s>>>(T);
+    k_tile_chain<<<1, CHAIN_T, 0, s>>>(T);
+    if (cudaGetLastError() != cudaSuccess || !read_small()) return cuda_fail();
+    if (h.err) return DBS_ERR_INTERNAL;
+    const int64_t NT = (int64_t)h.T;
+    if (!S.alloc(&T.tiles, sizeof(uint4) * (size_t)NT)) return oom();
+    k_tile_build<<<grid_for(NT, sms), 256, 0, s>>>(T, (uint32_t)NT);
+    if (cudaGetLastError() != cudaSuccess || !read_small()) return cuda_fail();
+    if (h.err) return DBS_ERR_INTERNAL;
+
+    // hand the matrix's arrays over; the rest is released with S
+    F->rb_ptr = C.rb_ptr; F->blk_desc = reinterpret_cast<U2 *>(C.desc); F->blk_ref = C.ref;
+    F->cb_ptr = Q.cb_ptr; F->csc_desc = reinterpret_cast<U2 *>(Q.csc_desc); F->csc_ref = Q.pos;
+    F->payload = reinterpret_cast<U4 *>(C.payload); F->tiles = reinterpret_cast<U4 *>(T.tiles); F->rb_rows = d_rows;
+    for (void *q : {(void *)C.rb_ptr, (void *)C.desc, (void *)C.ref, (void *)Q.cb_ptr, (void *)Q.csc_desc, (void *)Q.pos,
+                    (void *)C.payload, (void *)T.tiles, (void *)d_rows})
+        S.keep(q);
+    F->B = B; F->P = P; F->T = NT;
+    for (int f = 0; f < DBS_NUM_FORMATS; ++f) {
+        F->blocks_by_format[f] = (int64_t)h.fmt[f];
+        F->nnz_by_format[f] = (int64_t)h.fmt[DBS_NUM_FORMATS + f];
     }
-    C.ref = d_ref;
-    C.payload = d_pay;
-    if (grid) k_conv_encode<<<grid, CT, 0, s>>>(C);
-    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
-        cudaFree(d_pay);
-        return cuda_fail();
-    }
-    cleanup();
-    *d_payload = d_pay;
     return DBS_OK;
 }
 

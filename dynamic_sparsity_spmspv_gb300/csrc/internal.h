@@ -22,7 +22,6 @@ struct HostFormat {
     std::vector<uint32_t> cb_ptr;     // nbc + 1
     std::vector<U2> csc_desc;         // B: {row block, meta}
     std::vector<uint32_t> csc_ref;    // B
-    std::vector<uint32_t> csc2csr;    // B (host only)
     std::vector<U4> payload;          // P
     std::vector<U4> tiles;            // T: {p0, payload offset, rb0, span | flags | count}
     std::vector<uint16_t> rb_rows;    // nbr: rows of each row block that hold an entry (bit r = row r)
@@ -31,13 +30,26 @@ struct HostFormat {
 // Allocation-failure injection for tests (dbs_debug_fail_alloc): true when
 // this allocation attempt is the one chosen to fail.
 bool alloc_fault();
-// cudaMalloc behind the injection hook.
+// Every device allocation of the library: cudaMalloc behind the injection
+// hook, with its size recorded for dev_free and the calling thread's
+// MemWatch.
+cudaError_t dev_malloc_bytes(void **p, size_t bytes);
 template <class T>
 inline cudaError_t dev_malloc(T **p, size_t bytes)
 {
-    if (alloc_fault()) { *p = nullptr; return cudaErrorMemoryAllocation; }
-    return cudaMalloc((void **)p, bytes);
+    void *q = nullptr;
+    const cudaError_t e = dev_malloc_bytes(&q, bytes);
+    *p = static_cast<T *>(q);
+    return e;
 }
+// Frees a dev_malloc allocation (NULL is ignored).
+void dev_free(void *p);
+// Live and peak device bytes allocated and freed by one thread while the
+// watch is installed (a matrix build).
+struct MemWatch {
+    int64_t live = 0, peak = 0;
+};
+void mem_watch(MemWatch *w);   // NULL removes it
 // A host allocation of the builder, workspace or plan: throws
 // std::bad_alloc when the injection hook chooses it.
 void host_alloc_point();
@@ -50,12 +62,32 @@ int64_t spmv_plan_bytes(const dbs_spmv_plan *p);
 dbs_status spmv_launch_dense(const dbs_spmv_plan *p, float *part, uint32_t *cnt, const float *x, float *y,
                              double frac, bool gated, unsigned *path_word, cudaStream_t s);
 
-// Device-side conversion (build_gpu.cu): fills H.rb_ptr, H.blk_desc and
-// H.blk_ref, allocates and encodes the payload on the device.  Sets
-// *fallback (and converts nothing) when a row's columns are not ascending.
+// Pull-tile weight cap W (Section 3.3.2 segments): the option, or by
+// default about 64 tiles per SM, within [16, TILE_MAX_BLOCKS].
+uint32_t tile_weight_cap(const dbs_build_opts &o, uint64_t total_weight);
+
+// The device arrays of a matrix converted on the GPU, and its counts.
+struct DeviceFormat {
+    uint32_t *rb_ptr = nullptr;
+    U2 *blk_desc = nullptr;
+    uint32_t *blk_ref = nullptr;
+    uint32_t *cb_ptr = nullptr;
+    U2 *csc_desc = nullptr;
+    uint32_t *csc_ref = nullptr;
+    U4 *payload = nullptr;
+    U4 *tiles = nullptr;
+    uint16_t *rb_rows = nullptr;
+    int64_t B = 0, P = 0, T = 0;
+    int64_t blocks_by_format[DBS_NUM_FORMATS] = {}, nnz_by_format[DBS_NUM_FORMATS] = {};
+};
+
+// Device-side conversion (build_gpu.cu) of a device CSR: every array of the
+// matrix is built on the GPU, byte for byte the host builder's.  Sets
+// *fallback (and converts nothing) when a row's columns are not ascending;
+// invalid row pointers or columns return DBS_ERR_INVALID_ARG.
 dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp, const int32_t *d_ci,
-                          const float *d_va, const dbs_build_opts &o, cudaStream_t s, HostFormat &H, int64_t *B,
-                          int64_t *P, uint4 **d_payload, bool *fallback);
+                          const float *d_va, const dbs_build_opts &o, cudaStream_t s, DeviceFormat *F,
+                          bool *fallback);
 
 }  // namespace dbs
 

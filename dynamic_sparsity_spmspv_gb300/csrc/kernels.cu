@@ -2052,10 +2052,10 @@ namespace {
 
 void ws_free(dbs_workspace *w)
 {
-    cudaFree(w->x_dense); cudaFree(w->xm32); cudaFree(w->dxm32); cudaFree(w->y_acc); cudaFree(w->yrm32);
-    cudaFree(w->ctile_flag); cudaFree(w->bvis32); cudaFree(w->fm32[0]); cudaFree(w->fm32[1]);
-    cudaFree(w->ctrl); cudaFree(w->spmv_part); cudaFree(w->spmv_cnt);
-    for (int s = 0; s < 3; ++s) { cudaFree(w->act[s]); cudaFree(w->chunks[s]); }
+    dbs::dev_free(w->x_dense); dbs::dev_free(w->xm32); dbs::dev_free(w->dxm32); dbs::dev_free(w->y_acc); dbs::dev_free(w->yrm32);
+    dbs::dev_free(w->ctile_flag); dbs::dev_free(w->bvis32); dbs::dev_free(w->fm32[0]); dbs::dev_free(w->fm32[1]);
+    dbs::dev_free(w->ctrl); dbs::dev_free(w->spmv_part); dbs::dev_free(w->spmv_cnt);
+    for (int s = 0; s < 3; ++s) { dbs::dev_free(w->act[s]); dbs::dev_free(w->chunks[s]); }
 }
 
 template <class T>

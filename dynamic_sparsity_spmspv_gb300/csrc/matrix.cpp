@@ -7,8 +7,10 @@
 //                   directional skew (th2), patched CSR with row_idx_csc2csr;
 //   Section 3.3.2 - load-weighted pull segments (Dense 4, Force/CSR 2, COO 1);
 //   Section 5.5   - conversion is offline and reused across calls.
-// The conversion runs once per matrix on the host threads; the result is
-// uploaded to HBM and every later call runs on the GPU.
+// The conversion runs once per matrix, on the host threads with one upload
+// to HBM, or with device_convert on the GPU (build_gpu.cu); every later call
+// runs on the GPU.  All device memory of the library is allocated here
+// (dev_malloc / dev_free), which lets a build report its peak.
 #include <cuda_runtime_api.h>
 
 #include <algorithm>
@@ -16,8 +18,10 @@
 #include <chrono>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <thread>
+#include <unordered_map>
 
 #include "internal.h"
 
@@ -179,6 +183,16 @@ void convert_chunk(Chunk &ch, int64_t m, int64_t n, const int64_t *rp, const int
 // allocation attempt that fails; -1 when off.
 std::atomic<int64_t> g_fail_countdown{-1};
 
+// Sizes of the live device allocations (dev_free), and the calling thread's
+// build watch.
+std::mutex g_alloc_mu;
+std::unordered_map<void *, size_t> &alloc_sizes()
+{
+    static std::unordered_map<void *, size_t> sizes;
+    return sizes;
+}
+thread_local MemWatch *t_watch = nullptr;
+
 int num_sms_or_default()
 {
     int dev = 0, sms = 0;
@@ -232,11 +246,11 @@ dbs_status upload(const std::vector<T> &h, T **d, size_t min_elems, cudaStream_t
 void free_device(dbs_matrix *A)
 {
     if (A->plan) dbs_spmv_plan_destroy(A->plan);
-    cudaFree(A->d_csr_rp); cudaFree(A->d_csr_ci); cudaFree(A->d_csr_va);
+    dev_free(A->d_csr_rp); dev_free(A->d_csr_ci); dev_free(A->d_csr_va);
     A->plan = nullptr; A->d_csr_rp = nullptr; A->d_csr_ci = nullptr; A->d_csr_va = nullptr;
-    cudaFree(A->d_rb_ptr); cudaFree(A->d_blk_desc); cudaFree(A->d_blk_ref); cudaFree(A->d_cb_ptr);
-    cudaFree(A->d_csc_desc); cudaFree(A->d_csc_ref); cudaFree(A->d_payload); cudaFree(A->d_tiles);
-    cudaFree(A->d_rb_rows);
+    dev_free(A->d_rb_ptr); dev_free(A->d_blk_desc); dev_free(A->d_blk_ref); dev_free(A->d_cb_ptr);
+    dev_free(A->d_csc_desc); dev_free(A->d_csc_ref); dev_free(A->d_payload); dev_free(A->d_tiles);
+    dev_free(A->d_rb_rows);
     A->d_rb_ptr = nullptr; A->d_blk_desc = nullptr; A->d_blk_ref = nullptr; A->d_cb_ptr = nullptr;
     A->d_csc_desc = nullptr; A->d_csc_ref = nullptr; A->d_payload = nullptr; A->d_tiles = nullptr;
     A->d_rb_rows = nullptr;
@@ -268,6 +282,217 @@ dbs_status host_view(const dbs_matrix *A, HostFormat &tmp, const HostFormat **ou
     return DBS_OK;
 }
 
+// The host conversion (Section 3.2.1) on the builder's threads, then one
+// upload unless host_only.  Inputs are host arrays, or device arrays
+// downloaded first.
+dbs_status host_convert(dbs_matrix *A, const int64_t *row_ptr, const int32_t *col_idx, const float *vals,
+                        bool inputs_on_device, const dbs_build_opts &o, cudaStream_t s)
+{
+    const int64_t m = A->m, n = A->n, nnz = A->nnz, nbr = A->nbr, nbc = A->nbc;
+    HostFormat &H = *A->host;
+    std::vector<int64_t> h_rp;
+    std::vector<int32_t> h_ci;
+    std::vector<float> h_va;
+    const int64_t *rp = row_ptr;
+    const int32_t *ci = col_idx;
+    const float *va = vals;
+    try {
+        if (inputs_on_device) {
+            host_alloc_point();
+            h_rp.resize((size_t)m + 1);
+            if (cudaMemcpy(h_rp.data(), row_ptr, sizeof(int64_t) * ((size_t)m + 1), cudaMemcpyDeviceToHost) != cudaSuccess) {
+                cudaGetLastError();
+                return DBS_ERR_CUDA;
+            }
+            rp = h_rp.data();
+        }
+    } catch (const std::bad_alloc &) {
+        return DBS_ERR_OOM;
+    }
+    if (rp[0] != 0 || rp[m] != nnz) return DBS_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < m; ++i)
+        if (rp[i + 1] < rp[i]) return DBS_ERR_INVALID_ARG;
+    if (inputs_on_device) {
+        try {
+            h_ci.resize((size_t)nnz);
+            if (vals) h_va.resize((size_t)nnz);
+        } catch (const std::bad_alloc &) {
+            return DBS_ERR_OOM;
+        }
+        if ((nnz && cudaMemcpy(h_ci.data(), col_idx, sizeof(int32_t) * (size_t)nnz, cudaMemcpyDeviceToHost) != cudaSuccess) ||
+            (vals && nnz && cudaMemcpy(h_va.data(), vals, sizeof(float) * (size_t)nnz, cudaMemcpyDeviceToHost) != cudaSuccess)) {
+            cudaGetLastError();
+            return DBS_ERR_CUDA;
+        }
+        ci = h_ci.data();
+        va = vals ? h_va.data() : nullptr;
+    }
+
+    try {
+      {
+        // 1. Row-block chunks converted in parallel.
+        int nthreads = o.num_threads > 0 ? o.num_threads : (int)std::max(1u, std::thread::hardware_concurrency());
+        const int64_t chunk_rb = std::max<int64_t>(1, std::min<int64_t>(4096, nbr / (int64_t)(8 * nthreads) + 1));
+        std::vector<Chunk> chunks((size_t)((nbr + chunk_rb - 1) / chunk_rb));
+        for (size_t c = 0; c < chunks.size(); ++c) {
+            chunks[c].rb0 = (int64_t)c * chunk_rb;
+            chunks[c].rb1 = std::min(nbr, chunks[c].rb0 + chunk_rb);
+        }
+        std::atomic<size_t> next{0};
+        std::atomic<bool> oom{false};
+        auto worker = [&]() {
+            std::vector<Entry> ents;
+            try {
+                host_alloc_point();
+                for (size_t c; (c = next.fetch_add(1)) < chunks.size();)
+                    convert_chunk(chunks[c], m, n, rp, ci, va, o, ents);
+            } catch (const std::bad_alloc &) {
+                oom = true;
+            }
+        };
+        std::vector<std::thread> pool;
+        for (int t = 1; t < nthreads && (size_t)t < chunks.size(); ++t) pool.emplace_back(worker);
+        worker();
+        for (auto &t : pool) t.join();
+        if (oom) return DBS_ERR_OOM;
+        for (auto &c : chunks)
+            if (c.error != DBS_OK) return (dbs_status)c.error;
+
+        // 2. Concatenate: primary block order, payload offsets (a valued
+        // Dense block starts on a 64-byte boundary).
+        const bool valued_m = va != nullptr;
+        auto aligned = [&](const U2 &d) { return valued_m && !meta_inline(d.y) && meta_fmt(d.y) == FMT_DENSE; };
+        auto align_up = [](int64_t u) { return (u + DENSE_ALIGN_UNITS - 1) / DENSE_ALIGN_UNITS * DENSE_ALIGN_UNITS; };
+        int64_t B = 0, P = 0;
+        for (auto &c : chunks) {
+            B += (int64_t)c.desc.size();
+            for (size_t i = 0; i < c.units.size(); ++i) {
+                if (aligned(c.desc[i])) P = align_up(P);
+                P += c.units[i];
+            }
+        }
+        if (B >= (int64_t(1) << 32) || P >= (int64_t(1) << 32)) return DBS_ERR_UNSUPPORTED;
+        A->B = B; A->P = P;
+        host_alloc_point();
+        H.rb_ptr.resize((size_t)nbr + 1);
+        H.blk_desc.resize((size_t)B);
+        H.blk_ref.resize((size_t)B);
+        H.payload.resize((size_t)P);
+        {
+            uint32_t pb = 0, pu = 0;
+            H.rb_ptr[0] = 0;
+            for (auto &c : chunks) {
+                for (size_t i = 0; i < c.rb_count.size(); ++i)
+                    H.rb_ptr[(size_t)c.rb0 + i + 1] = H.rb_ptr[(size_t)c.rb0 + i] + c.rb_count[i];
+                std::copy(c.desc.begin(), c.desc.end(), H.blk_desc.begin() + pb);
+                size_t lo = 0;
+                for (size_t i = 0; i < c.units.size(); ++i) {
+                    if (aligned(c.desc[i])) pu = (uint32_t)align_up(pu);
+                    std::copy(c.payload.begin() + lo, c.payload.begin() + lo + c.units[i], H.payload.begin() + pu);
+                    H.blk_ref[pb + i] = pu;
+                    pu += c.units[i];
+                    lo += c.units[i];
+                }
+                pb += (uint32_t)c.desc.size();
+                std::vector<U2>().swap(c.desc);
+                std::vector<U4>().swap(c.payload);
+            }
+        }
+      }
+      const int64_t B = A->B;
+
+        // 3. Block-CSC view: counting sort of primary blocks by column block;
+        //    row blocks stay ascending within a column block.
+        host_alloc_point();
+        H.cb_ptr.assign((size_t)nbc + 1, 0);
+        for (int64_t p = 0; p < B; ++p) H.cb_ptr[H.blk_desc[(size_t)p].x + 1]++;
+        for (int64_t c = 0; c < nbc; ++c) H.cb_ptr[(size_t)c + 1] += H.cb_ptr[(size_t)c];
+        H.csc_desc.resize((size_t)B);
+        H.csc_ref.resize((size_t)B);
+        {
+            std::vector<uint32_t> fill(H.cb_ptr.begin(), H.cb_ptr.end() - 1);
+            for (int64_t rb = 0; rb < nbr; ++rb)
+                for (uint32_t p = H.rb_ptr[(size_t)rb]; p < H.rb_ptr[(size_t)rb + 1]; ++p) {
+                    uint32_t q = fill[H.blk_desc[p].x]++;
+                    H.csc_desc[q] = U2{(uint32_t)rb, H.blk_desc[p].y};
+                    H.csc_ref[q] = H.blk_ref[p];
+                }
+        }
+
+        // Rows that hold an entry, per row block (a row without one can
+        // never be reached or touched).
+        H.rb_rows.assign((size_t)nbr, 0);
+        for (int64_t i = 0; i < m; ++i)
+            if (rp[i + 1] > rp[i]) H.rb_rows[(size_t)(i / BS)] |= (uint16_t)(1u << (i % BS));
+
+        // 4. Pull tiles.
+        uint64_t total_w = 0;
+        for (int64_t p = 0; p < B; ++p) total_w += fmt_weight(meta_fmt(H.blk_desc[(size_t)p].y));
+        const uint32_t W = tile_weight_cap(o, total_w);
+        uint32_t R = o.tile_max_row_blocks > 0 ? (uint32_t)o.tile_max_row_blocks : TILE_MAX_SPAN;
+        host_alloc_point();
+        build_tiles(H.rb_ptr, H.blk_desc, nbr, W, R, H.tiles);
+        A->T = (int64_t)H.tiles.size();
+        for (size_t i = 0; i < H.tiles.size(); ++i) {
+            // local row block of each block into blk_desc.x bits 27-31; flags
+            // for row blocks shared with the neighbouring tiles
+            U4 &tl = H.tiles[i];
+            uint32_t rb = tl.z;
+            for (uint32_t p = tl.x; p < tl.y; ++p) {
+                while (H.rb_ptr[rb + 1] <= p) ++rb;
+                H.blk_desc[p].x |= (rb - tl.z) << DESC_LRB_SHIFT;
+            }
+            if (H.rb_ptr[tl.z] < tl.x) tl.w |= TILE_FIRST_SHARED;
+            if (H.rb_ptr[tl.z + (tl.w & TILE_SPAN_MASK)] > tl.y) tl.w |= TILE_LAST_SHARED;
+            // kernel form: the block count joins w, the payload offset of
+            // the first block replaces the end index
+            tl.w |= (tl.y - tl.x) << TILE_NBLK_SHIFT;
+            tl.y = tl.x < (uint32_t)B ? H.blk_ref[tl.x] : 0u;
+        }
+        // the pull kernel's copy and queue bounds rely on these
+        {
+            uint64_t next = 0;
+            for (const U4 &tl : H.tiles) {
+                const uint32_t nb = tl.w >> TILE_NBLK_SHIFT, span = tl.w & TILE_SPAN_MASK;
+                if (tl.x != next || nb == 0 || (tl.x & 1u) + nb > TILE_MAX_BLOCKS || span == 0 ||
+                    span > TILE_MAX_SPAN || (int64_t)tl.z + span > nbr)
+                    return DBS_ERR_INTERNAL;
+                next += nb;
+            }
+            if (next != (uint64_t)B) return DBS_ERR_INTERNAL;
+        }
+    } catch (const std::bad_alloc &) {
+        return DBS_ERR_OOM;
+    }
+
+
+    dbs_matrix_info &I = A->info;
+    for (int64_t p = 0; p < A->B; ++p) {
+        uint32_t meta = H.blk_desc[(size_t)p].y;
+        I.blocks_by_format[meta_fmt(meta)] += 1;
+        I.nnz_by_format[meta_fmt(meta)] += meta_nnz(meta);
+    }
+
+    // Upload.
+    if (!o.host_only) {
+        if (cudaGetDevice(&A->device) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+        dbs_status st;
+        if ((st = upload(H.rb_ptr, &A->d_rb_ptr, 1, s)) != DBS_OK) return st;
+        // blk_desc is padded with 8 zero entries so vector loads may run past B.
+        if ((st = upload(H.blk_desc, &A->d_blk_desc, (size_t)A->B + 8, s)) != DBS_OK) return st;
+        if ((st = upload(H.blk_ref, &A->d_blk_ref, (size_t)A->B + 8, s)) != DBS_OK) return st;
+        if ((st = upload(H.cb_ptr, &A->d_cb_ptr, 1, s)) != DBS_OK) return st;
+        if ((st = upload(H.csc_desc, &A->d_csc_desc, (size_t)A->B + 8, s)) != DBS_OK) return st;
+        if ((st = upload(H.csc_ref, &A->d_csc_ref, (size_t)A->B + 8, s)) != DBS_OK) return st;
+        if ((st = upload(H.payload, &A->d_payload, 1, s)) != DBS_OK) return st;
+        if ((st = upload(H.tiles, &A->d_tiles, 1, s)) != DBS_OK) return st;
+        if ((st = upload(H.rb_rows, &A->d_rb_rows, (size_t)nbr + 2, s)) != DBS_OK) return st;
+        if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return DBS_ERR_CUDA; }
+        A->on_device = true;
+    }
+    return DBS_OK;
+}
+
 }  // namespace
 
 bool dbs::alloc_fault()
@@ -281,6 +506,58 @@ bool dbs::alloc_fault()
 void dbs::host_alloc_point()
 {
     if (alloc_fault()) throw std::bad_alloc();
+}
+
+cudaError_t dbs::dev_malloc_bytes(void **p, size_t bytes)
+{
+    *p = nullptr;
+    if (alloc_fault()) return cudaErrorMemoryAllocation;
+    void *q = nullptr;
+    const cudaError_t e = cudaMalloc(&q, bytes);
+    if (e != cudaSuccess) return e;
+    try {
+        std::lock_guard<std::mutex> g(g_alloc_mu);
+        alloc_sizes()[q] = bytes;
+    } catch (...) {
+        cudaFree(q);
+        return cudaErrorMemoryAllocation;
+    }
+    if (t_watch) {
+        t_watch->live += (int64_t)bytes;
+        t_watch->peak = std::max(t_watch->peak, t_watch->live);
+    }
+    *p = q;
+    return cudaSuccess;
+}
+
+void dbs::dev_free(void *p)
+{
+    if (!p) return;
+    size_t bytes = 0;
+    {
+        std::lock_guard<std::mutex> g(g_alloc_mu);
+        auto &sizes = alloc_sizes();
+        auto it = sizes.find(p);
+        if (it != sizes.end()) {
+            bytes = it->second;
+            sizes.erase(it);
+        }
+    }
+    cudaFree(p);
+    if (t_watch) t_watch->live -= (int64_t)bytes;
+}
+
+void dbs::mem_watch(MemWatch *w) { t_watch = w; }
+
+uint32_t dbs::tile_weight_cap(const dbs_build_opts &o, uint64_t total_weight)
+{
+    uint32_t W = (uint32_t)o.tile_weight;
+    if (W == 0) {
+        // about 64 tiles per SM, within [16, TILE_MAX_BLOCKS]
+        const uint64_t target = (uint64_t)num_sms_or_default() * 64u;
+        W = (uint32_t)std::min<uint64_t>(TILE_MAX_BLOCKS, std::max<uint64_t>(16, (total_weight + target - 1) / target));
+    }
+    return std::min<uint32_t>(W, TILE_MAX_BLOCKS);
 }
 
 extern "C" {
@@ -337,37 +614,18 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
         o.tile_weight < 0 || o.tile_max_row_blocks < 0 || o.tile_max_row_blocks > (int)TILE_MAX_SPAN ||
         o.num_threads < 0 || o.dense_spmv < 0 || o.dense_spmv > 1)
         return DBS_ERR_INVALID_ARG;
+    if (inputs_on_device && o.host_only) return DBS_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     auto t_start = std::chrono::steady_clock::now();
-
-    // Inputs to host memory (with device conversion, only the row pointers:
-    // the entries stay on the GPU).
-    std::vector<int64_t> h_rp;
-    std::vector<int32_t> h_ci;
-    std::vector<float> h_va;
-    const int64_t *rp = row_ptr;
-    const int32_t *ci = col_idx;
-    const float *va = vals;
-    bool on_gpu = inputs_on_device && o.device_convert && !o.host_only;
-    try {
-        if (inputs_on_device) {
-            if (o.host_only) return DBS_ERR_INVALID_ARG;
-            h_rp.resize((size_t)m + 1);
-            if (cudaMemcpy(h_rp.data(), row_ptr, sizeof(int64_t) * ((size_t)m + 1), cudaMemcpyDeviceToHost) != cudaSuccess) {
-                cudaGetLastError();
-                return DBS_ERR_CUDA;
-            }
-            rp = h_rp.data();
-        }
-    } catch (const std::bad_alloc &) {
-        return DBS_ERR_OOM;
-    }
-    if (rp[0] != 0 || rp[m] != nnz) return DBS_ERR_INVALID_ARG;
-    for (int64_t i = 0; i < m; ++i)
-        if (rp[i + 1] < rp[i]) return DBS_ERR_INVALID_ARG;
+    // the build's own device allocations, for build_peak_bytes
+    MemWatch watch;
+    mem_watch(&watch);
+    struct Unwatch {
+        ~Unwatch() { mem_watch(nullptr); }
+    } unwatch;
 
     const int64_t nbr = (m + BS - 1) / BS, nbc = (n + BS - 1) / BS;
-    const bool valued = va != nullptr;
+    const bool valued = vals != nullptr;
     dbs_matrix *A = nullptr;
     try {
         host_alloc_point();
@@ -379,256 +637,96 @@ dbs_status dbs_matrix_build_csr(int64_t m, int64_t n, int64_t nnz, const int64_t
     }
     A->m = m; A->n = n; A->nnz = nnz; A->nbr = nbr; A->nbc = nbc; A->valued = valued;
     HostFormat &H = *A->host;
+    dbs_matrix_info &I = A->info;
     auto fail = [&](dbs_status st) { free_device(A); delete A->host; delete A; return st; };
 
+    bool on_gpu = inputs_on_device && o.device_convert;
     if (on_gpu) {
-        // 1-2 on the device: blocks, formats and payload; the host gets the
-        // block-proportional arrays (Section 3.2.1 conversion without a sort)
-        int64_t B = 0, P = 0;
+        // the whole conversion on the device (Section 3.2.1 without a sort)
+        DeviceFormat D;
         bool fallback = false;
-        uint4 *d_pay = nullptr;
-        dbs_status st;
-        try {
-            st = device_convert(m, n, nnz, row_ptr, col_idx, vals, o, s, H, &B, &P, &d_pay, &fallback);
-        } catch (const std::bad_alloc &) {
-            st = DBS_ERR_OOM;
-        }
+        const dbs_status st = device_convert(m, n, nnz, row_ptr, col_idx, vals, o, s, &D, &fallback);
         if (st != DBS_OK) return fail(st);
         if (fallback) {
             on_gpu = false;                 // a row's columns are not ascending: host conversion
         } else {
-            A->B = B; A->P = P;
-            A->d_payload = reinterpret_cast<U4 *>(d_pay);
+            if (cudaGetDevice(&A->device) != cudaSuccess) {
+                cudaGetLastError();
+                for (void *q : {(void *)D.rb_ptr, (void *)D.blk_desc, (void *)D.blk_ref, (void *)D.cb_ptr,
+                                (void *)D.csc_desc, (void *)D.csc_ref, (void *)D.payload, (void *)D.tiles,
+                                (void *)D.rb_rows})
+                    dev_free(q);
+                return fail(DBS_ERR_CUDA);
+            }
+            A->d_rb_ptr = D.rb_ptr; A->d_blk_desc = D.blk_desc; A->d_blk_ref = D.blk_ref; A->d_cb_ptr = D.cb_ptr;
+            A->d_csc_desc = D.csc_desc; A->d_csc_ref = D.csc_ref; A->d_payload = D.payload; A->d_tiles = D.tiles;
+            A->d_rb_rows = D.rb_rows;
+            A->B = D.B; A->P = D.P; A->T = D.T;
+            A->on_device = true;
+            for (int f = 0; f < DBS_NUM_FORMATS; ++f) {
+                I.blocks_by_format[f] = D.blocks_by_format[f];
+                I.nnz_by_format[f] = D.nnz_by_format[f];
+            }
         }
     }
-    if (!on_gpu && inputs_on_device) {
-        try {
-            h_ci.resize((size_t)nnz);
-            if (vals) h_va.resize((size_t)nnz);
-        } catch (const std::bad_alloc &) {
-            return fail(DBS_ERR_OOM);
-        }
-        if ((nnz && cudaMemcpy(h_ci.data(), col_idx, sizeof(int32_t) * (size_t)nnz, cudaMemcpyDeviceToHost) != cudaSuccess) ||
-            (vals && nnz && cudaMemcpy(h_va.data(), vals, sizeof(float) * (size_t)nnz, cudaMemcpyDeviceToHost) != cudaSuccess)) {
-            cudaGetLastError();
-            return fail(DBS_ERR_CUDA);
-        }
-        ci = h_ci.data();
-        va = vals ? h_va.data() : nullptr;
+
+    if (!on_gpu) {
+        dbs_status st = host_convert(A, row_ptr, col_idx, vals, inputs_on_device != 0, o, s);
+        if (st != DBS_OK) return fail(st);
     }
 
-    try {
-      if (!on_gpu) {
-        // 1. Row-block chunks converted in parallel.
-        int nthreads = o.num_threads > 0 ? o.num_threads : (int)std::max(1u, std::thread::hardware_concurrency());
-        const int64_t chunk_rb = std::max<int64_t>(1, std::min<int64_t>(4096, nbr / (int64_t)(8 * nthreads) + 1));
-        std::vector<Chunk> chunks((size_t)((nbr + chunk_rb - 1) / chunk_rb));
-        for (size_t c = 0; c < chunks.size(); ++c) {
-            chunks[c].rb0 = (int64_t)c * chunk_rb;
-            chunks[c].rb1 = std::min(nbr, chunks[c].rb0 + chunk_rb);
-        }
-        std::atomic<size_t> next{0};
-        std::atomic<bool> oom{false};
-        auto worker = [&]() {
-            std::vector<Entry> ents;
-            try {
-                host_alloc_point();
-                for (size_t c; (c = next.fetch_add(1)) < chunks.size();)
-                    convert_chunk(chunks[c], m, n, rp, ci, va, o, ents);
-            } catch (const std::bad_alloc &) {
-                oom = true;
-            }
-        };
-        std::vector<std::thread> pool;
-        for (int t = 1; t < nthreads && (size_t)t < chunks.size(); ++t) pool.emplace_back(worker);
-        worker();
-        for (auto &t : pool) t.join();
-        if (oom) return fail(DBS_ERR_OOM);
-        for (auto &c : chunks)
-            if (c.error != DBS_OK) return fail((dbs_status)c.error);
-
-        // 2. Concatenate: primary block order, payload offsets (a valued
-        // Dense block starts on a 64-byte boundary).
-        const bool valued_m = va != nullptr;
-        auto aligned = [&](const U2 &d) { return valued_m && !meta_inline(d.y) && meta_fmt(d.y) == FMT_DENSE; };
-        auto align_up = [](int64_t u) { return (u + DENSE_ALIGN_UNITS - 1) / DENSE_ALIGN_UNITS * DENSE_ALIGN_UNITS; };
-        int64_t B = 0, P = 0;
-        for (auto &c : chunks) {
-            B += (int64_t)c.desc.size();
-            for (size_t i = 0; i < c.units.size(); ++i) {
-                if (aligned(c.desc[i])) P = align_up(P);
-                P += c.units[i];
-            }
-        }
-        if (B >= (int64_t(1) << 32) || P >= (int64_t(1) << 32)) return fail(DBS_ERR_UNSUPPORTED);
-        A->B = B; A->P = P;
-        host_alloc_point();
-        H.rb_ptr.resize((size_t)nbr + 1);
-        H.blk_desc.resize((size_t)B);
-        H.blk_ref.resize((size_t)B);
-        H.payload.resize((size_t)P);
-        {
-            uint32_t pb = 0, pu = 0;
-            H.rb_ptr[0] = 0;
-            for (auto &c : chunks) {
-                for (size_t i = 0; i < c.rb_count.size(); ++i)
-                    H.rb_ptr[(size_t)c.rb0 + i + 1] = H.rb_ptr[(size_t)c.rb0 + i] + c.rb_count[i];
-                std::copy(c.desc.begin(), c.desc.end(), H.blk_desc.begin() + pb);
-                size_t lo = 0;
-                for (size_t i = 0; i < c.units.size(); ++i) {
-                    if (aligned(c.desc[i])) pu = (uint32_t)align_up(pu);
-                    std::copy(c.payload.begin() + lo, c.payload.begin() + lo + c.units[i], H.payload.begin() + pu);
-                    H.blk_ref[pb + i] = pu;
-                    pu += c.units[i];
-                    lo += c.units[i];
-                }
-                pb += (uint32_t)c.desc.size();
-                std::vector<U2>().swap(c.desc);
-                std::vector<U4>().swap(c.payload);
-            }
-        }
-      }
-      const int64_t B = A->B;
-
-        // 3. Block-CSC view: counting sort of primary blocks by column block;
-        //    row blocks stay ascending within a column block.
-        host_alloc_point();
-        H.cb_ptr.assign((size_t)nbc + 1, 0);
-        for (int64_t p = 0; p < B; ++p) H.cb_ptr[H.blk_desc[(size_t)p].x + 1]++;
-        for (int64_t c = 0; c < nbc; ++c) H.cb_ptr[(size_t)c + 1] += H.cb_ptr[(size_t)c];
-        H.csc_desc.resize((size_t)B);
-        H.csc_ref.resize((size_t)B);
-        H.csc2csr.resize((size_t)B);
-        {
-            std::vector<uint32_t> fill(H.cb_ptr.begin(), H.cb_ptr.end() - 1);
-            for (int64_t rb = 0; rb < nbr; ++rb)
-                for (uint32_t p = H.rb_ptr[(size_t)rb]; p < H.rb_ptr[(size_t)rb + 1]; ++p) {
-                    uint32_t q = fill[H.blk_desc[p].x]++;
-                    H.csc_desc[q] = U2{(uint32_t)rb, H.blk_desc[p].y};
-                    H.csc_ref[q] = H.blk_ref[p];
-                    H.csc2csr[q] = p;
-                }
-        }
-
-        // Rows that hold an entry, per row block (a row without one can
-        // never be reached or touched).
-        H.rb_rows.assign((size_t)nbr, 0);
-        for (int64_t i = 0; i < m; ++i)
-            if (rp[i + 1] > rp[i]) H.rb_rows[(size_t)(i / BS)] |= (uint16_t)(1u << (i % BS));
-
-        // 4. Pull tiles.
-        uint64_t total_w = 0;
-        for (int64_t p = 0; p < B; ++p) total_w += fmt_weight(meta_fmt(H.blk_desc[(size_t)p].y));
-        uint32_t W = (uint32_t)o.tile_weight;
-        if (W == 0) {
-            // about 64 tiles per SM, within [16, TILE_MAX_BLOCKS]
-            uint64_t target = (uint64_t)num_sms_or_default() * 64u;
-            W = (uint32_t)std::min<uint64_t>(TILE_MAX_BLOCKS, std::max<uint64_t>(16, (total_w + target - 1) / target));
-        }
-        W = std::min<uint32_t>(W, TILE_MAX_BLOCKS);
-        uint32_t R = o.tile_max_row_blocks > 0 ? (uint32_t)o.tile_max_row_blocks : TILE_MAX_SPAN;
-        host_alloc_point();
-        build_tiles(H.rb_ptr, H.blk_desc, nbr, W, R, H.tiles);
-        A->T = (int64_t)H.tiles.size();
-        for (size_t i = 0; i < H.tiles.size(); ++i) {
-            // local row block of each block into blk_desc.x bits 27-31; flags
-            // for row blocks shared with the neighbouring tiles
-            U4 &tl = H.tiles[i];
-            uint32_t rb = tl.z;
-            for (uint32_t p = tl.x; p < tl.y; ++p) {
-                while (H.rb_ptr[rb + 1] <= p) ++rb;
-                H.blk_desc[p].x |= (rb - tl.z) << DESC_LRB_SHIFT;
-            }
-            if (H.rb_ptr[tl.z] < tl.x) tl.w |= TILE_FIRST_SHARED;
-            if (H.rb_ptr[tl.z + (tl.w & TILE_SPAN_MASK)] > tl.y) tl.w |= TILE_LAST_SHARED;
-            // kernel form: the block count joins w, the payload offset of
-            // the first block replaces the end index
-            tl.w |= (tl.y - tl.x) << TILE_NBLK_SHIFT;
-            tl.y = tl.x < (uint32_t)B ? H.blk_ref[tl.x] : 0u;
-        }
-        // the pull kernel's copy and queue bounds rely on these
-        {
-            uint64_t next = 0;
-            for (const U4 &tl : H.tiles) {
-                const uint32_t nb = tl.w >> TILE_NBLK_SHIFT, span = tl.w & TILE_SPAN_MASK;
-                if (tl.x != next || nb == 0 || (tl.x & 1u) + nb > TILE_MAX_BLOCKS || span == 0 ||
-                    span > TILE_MAX_SPAN || (int64_t)tl.z + span > nbr)
-                    return fail(DBS_ERR_INTERNAL);
-                next += nb;
-            }
-            if (next != (uint64_t)B) return fail(DBS_ERR_INTERNAL);
-        }
-    } catch (const std::bad_alloc &) {
-        return fail(DBS_ERR_OOM);
-    }
-
-    // 5. Info (Table 4 style storage report).
-    dbs_matrix_info &I = A->info;
+    // Info (Table 4 style storage report).
     I.m = m; I.n = n; I.nnz = nnz; I.nbr = nbr; I.nbc = nbc; I.nblocks = A->B;
-    for (int64_t p = 0; p < A->B; ++p) {
-        uint32_t meta = H.blk_desc[(size_t)p].y;
-        I.blocks_by_format[meta_fmt(meta)] += 1;
-        I.nnz_by_format[meta_fmt(meta)] += meta_nnz(meta);
-    }
     I.ntiles = A->T;
     I.payload_bytes = A->P * 16;
     I.view_bytes = (nbr + 1) * 4 + A->B * 8 + A->B * 4 + (nbc + 1) * 4 + A->B * 8 + A->B * 4 + A->T * 16 +
-                   nbr * (2 + 4);   // + per row block: rows holding entries, tiles meeting it
+                   nbr * 2;   // + per row block: rows holding entries
     I.total_bytes = I.payload_bytes + I.view_bytes;
     I.csr_bytes = (m + 1) * 4 + nnz * 4 + (valued ? nnz * 4 : 0);
     I.csr_csc_bytes = I.csr_bytes + (n + 1) * 4 + nnz * 4 + (valued ? nnz * 4 : 0);
     I.valued = valued ? 1 : 0;
 
-    // 6. Upload.
-    if (!o.host_only) {
-        if (cudaGetDevice(&A->device) != cudaSuccess) { cudaGetLastError(); return fail(DBS_ERR_CUDA); }
-        dbs_status st;
-        if ((st = upload(H.rb_ptr, &A->d_rb_ptr, 1, s)) != DBS_OK) return fail(st);
-        // blk_desc is padded with 8 zero entries so vector loads may run past B.
-        if ((st = upload(H.blk_desc, &A->d_blk_desc, (size_t)A->B + 8, s)) != DBS_OK) return fail(st);
-        if ((st = upload(H.blk_ref, &A->d_blk_ref, (size_t)A->B + 8, s)) != DBS_OK) return fail(st);
-        if ((st = upload(H.cb_ptr, &A->d_cb_ptr, 1, s)) != DBS_OK) return fail(st);
-        if ((st = upload(H.csc_desc, &A->d_csc_desc, (size_t)A->B + 8, s)) != DBS_OK) return fail(st);
-        if ((st = upload(H.csc_ref, &A->d_csc_ref, (size_t)A->B + 8, s)) != DBS_OK) return fail(st);
-        if (!on_gpu && (st = upload(H.payload, &A->d_payload, 1, s)) != DBS_OK) return fail(st);
-        if ((st = upload(H.tiles, &A->d_tiles, 1, s)) != DBS_OK) return fail(st);
-        if ((st = upload(H.rb_rows, &A->d_rb_rows, (size_t)nbr + 2, s)) != DBS_OK) return fail(st);
-        if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return fail(DBS_ERR_CUDA); }
-        A->on_device = true;
-        if (o.dense_spmv && valued) {
-            // the input CSR, kept on the device for dense-x calls, and its plan
-            const size_t rb = sizeof(int64_t) * ((size_t)m + 1), cb = sizeof(int32_t) * (size_t)std::max<int64_t>(nnz, 1),
-                         vb = sizeof(float) * (size_t)std::max<int64_t>(nnz, 1);
-            if (dev_malloc(&A->d_csr_rp, rb) != cudaSuccess || dev_malloc(&A->d_csr_ci, cb) != cudaSuccess ||
-                dev_malloc(&A->d_csr_va, vb) != cudaSuccess) {
-                cudaGetLastError();
-                return fail(DBS_ERR_OOM);
-            }
-            if (cudaMemcpy(A->d_csr_rp, row_ptr, rb, cudaMemcpyDefault) != cudaSuccess ||
-                (nnz && cudaMemcpy(A->d_csr_ci, col_idx, sizeof(int32_t) * (size_t)nnz, cudaMemcpyDefault) != cudaSuccess) ||
-                (nnz && cudaMemcpy(A->d_csr_va, vals, sizeof(float) * (size_t)nnz, cudaMemcpyDefault) != cudaSuccess)) {
-                cudaGetLastError();
-                return fail(DBS_ERR_CUDA);
-            }
-            dbs_status st2 = dbs_spmv_plan_create(m, n, nnz, A->d_csr_rp, A->d_csr_ci, A->d_csr_va, stream, &A->plan);
-            if (st2 != DBS_OK) { A->plan = nullptr; return fail(st2); }
-            I.spmv_bytes = (int64_t)(rb + (size_t)nnz * 8) + spmv_plan_bytes(A->plan);
-        }
-    }
-    I.on_device = A->on_device ? 1 : 0;
-    if (on_gpu && o.keep_host) {
-        // the host copy holds the payload too
-        try {
-            H.payload.resize((size_t)A->P);
-        } catch (const std::bad_alloc &) {
+    if (A->on_device && o.dense_spmv && valued) {
+        // the input CSR, kept on the device for dense-x calls, and its plan
+        const size_t rb = sizeof(int64_t) * ((size_t)m + 1), cb = sizeof(int32_t) * (size_t)std::max<int64_t>(nnz, 1),
+                     vb = sizeof(float) * (size_t)std::max<int64_t>(nnz, 1);
+        if (dev_malloc(&A->d_csr_rp, rb) != cudaSuccess || dev_malloc(&A->d_csr_ci, cb) != cudaSuccess ||
+            dev_malloc(&A->d_csr_va, vb) != cudaSuccess) {
+            cudaGetLastError();
             return fail(DBS_ERR_OOM);
         }
-        if (A->P && cudaMemcpy(H.payload.data(), A->d_payload, (size_t)A->P * 16, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        if (cudaMemcpy(A->d_csr_rp, row_ptr, rb, cudaMemcpyDefault) != cudaSuccess ||
+            (nnz && cudaMemcpy(A->d_csr_ci, col_idx, sizeof(int32_t) * (size_t)nnz, cudaMemcpyDefault) != cudaSuccess) ||
+            (nnz && cudaMemcpy(A->d_csr_va, vals, sizeof(float) * (size_t)nnz, cudaMemcpyDefault) != cudaSuccess)) {
             cudaGetLastError();
             return fail(DBS_ERR_CUDA);
         }
+        dbs_status st2 = dbs_spmv_plan_create(m, n, nnz, A->d_csr_rp, A->d_csr_ci, A->d_csr_va, stream, &A->plan);
+        if (st2 != DBS_OK) { A->plan = nullptr; return fail(st2); }
+        I.spmv_bytes = (int64_t)(rb + (size_t)nnz * 8) + spmv_plan_bytes(A->plan);
+    }
+    I.on_device = A->on_device ? 1 : 0;
+    if (on_gpu && o.keep_host) {
+        // the host copy of a device conversion: every array downloaded
+        bool ok = false;
+        try {
+            host_alloc_point();
+            ok = copy_from_device(H.rb_ptr, A->d_rb_ptr, (size_t)nbr + 1) &&
+                 copy_from_device(H.blk_desc, A->d_blk_desc, (size_t)A->B) &&
+                 copy_from_device(H.blk_ref, A->d_blk_ref, (size_t)A->B) &&
+                 copy_from_device(H.cb_ptr, A->d_cb_ptr, (size_t)nbc + 1) &&
+                 copy_from_device(H.csc_desc, A->d_csc_desc, (size_t)A->B) &&
+                 copy_from_device(H.csc_ref, A->d_csc_ref, (size_t)A->B) &&
+                 copy_from_device(H.payload, A->d_payload, (size_t)A->P) &&
+                 copy_from_device(H.tiles, A->d_tiles, (size_t)A->T) &&
+                 copy_from_device(H.rb_rows, A->d_rb_rows, (size_t)nbr);
+        } catch (const std::bad_alloc &) {
+            return fail(DBS_ERR_OOM);
+        }
+        if (!ok) { cudaGetLastError(); return fail(DBS_ERR_CUDA); }
     }
     if (!o.keep_host && !o.host_only) { delete A->host; A->host = nullptr; }
+    I.build_peak_bytes = watch.peak;
     I.build_seconds = std::chrono::duration<double>(std::chrono::steady_clock::now() - t_start).count();
     *out = A;
     return DBS_OK;

@@ -149,9 +149,9 @@ bool alloc0(T **p, size_t count)
 void plan_free(dbs_spmv_plan *p)
 {
     PlanDev &D = p->D;
-    for (int k = 0; k < B_SPLIT; ++k) cudaFree(D.rows[k]);
-    cudaFree(D.split); cudaFree(D.chunks); cudaFree(D.part); cudaFree(D.cnt);
-    cudaFree(D.blk_counts); cudaFree(D.blk_offs); cudaFree(D.tot);
+    for (int k = 0; k < B_SPLIT; ++k) dbs::dev_free(D.rows[k]);
+    dbs::dev_free(D.split); dbs::dev_free(D.chunks); dbs::dev_free(D.part); dbs::dev_free(D.cnt);
+    dbs::dev_free(D.blk_counts); dbs::dev_free(D.blk_offs); dbs::dev_free(D.tot);
 }
 
 }  // namespace

@@ -94,20 +94,22 @@ typedef struct {
                                   is touched (the matrix can be inspected and exported
                                   but not multiplied).  For CPU-side checks. */
     int32_t num_threads;       /* host builder threads; 0 = all hardware threads */
-    int32_t device_convert;    /* 1 with inputs_on_device: find, classify and encode the
-                                  blocks on the GPU (no sort; device memory beyond input
-                                  and result: 4 B per row block + 13 B per block); the
-                                  block-proportional steps (offsets, block-CSC view,
-                                  tiles) stay on the host.  Needs the columns of every
-                                  row ascending, else the host converts.  Same result
-                                  byte for byte.  Default 0. */
+    int32_t device_convert;    /* 1 with inputs_on_device: the whole conversion runs on
+                                  the GPU (validation, blocks, formats, payload, offsets,
+                                  block-CSC view, tiles); nothing proportional to the
+                                  matrix crosses to the host.  Device memory beyond the
+                                  input and the result: 4 B per block + 12 B per column
+                                  block (see build_peak_bytes).  Needs the columns of
+                                  every row ascending, else the host converts.  Same
+                                  result byte for byte.  Default 0. */
     int32_t dense_spmv;        /* 1 with a valued matrix: also keep a device copy of the
                                   input CSR (8 B per entry and per row) and an adaptive
                                   CSR SpMV plan over it; dbs_spmspv_dense then hands an x
                                   whose sampled nonzero fraction reaches
-                                  dbs_exec_opts.spmv_x_frac to that SpMV inside the same
-                                  launch (the paper's Limitations: conventional SpMV is
-                                  preferable for dense inputs).  Default 0. */
+                                  dbs_exec_opts.spmv_x_frac to that SpMV, which runs
+                                  first and makes the blocked kernel return at once (the
+                                  paper's Limitations: conventional SpMV is preferable
+                                  for dense inputs).  Default 0. */
 } dbs_build_opts;
 
 void dbs_build_opts_default(dbs_build_opts *opts);
@@ -182,6 +184,10 @@ typedef struct {
     double build_seconds;                   /* host time of the conversion */
     int64_t spmv_bytes;                     /* dense_spmv: the kept CSR and its SpMV plan
                                                (not in total_bytes) */
+    int64_t build_peak_bytes;               /* most device memory the build held at once
+                                               (library allocations only: the matrix,
+                                               its SpMV plan and all scratch; not the
+                                               caller's input) */
 } dbs_matrix_info;
 
 /* Fills *out.  Host-only, no synchronization. */

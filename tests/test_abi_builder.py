@@ -45,6 +45,7 @@ def test_struct_layouts_match_header_sizes():
     assert ctypes.sizeof(_lib.dbs_build_opts) == 48
     assert ctypes.sizeof(_lib.dbs_exec_opts) == 40
     assert ctypes.sizeof(_lib.dbs_stats) == 104
+    assert ctypes.sizeof(_lib.dbs_matrix_info) == 8 * 15 + 8 * 2 * 5 + 4 * 2   # 64-bit scalars, formats, 2 int32
     o = dbs.build_opts()
     assert (o.th0, o.th1, o.th2, o.force_format) == (32, 128, 2.0, -1)
     e = dbs.exec_opts()
@@ -136,6 +137,7 @@ def test_storage_report():
     assert inf["csr_csc_bytes"] == 2 * inf["csr_bytes"] - (A.m + 1) * 4 + (A.n + 1) * 4
     assert inf["total_bytes"] == inf["payload_bytes"] + inf["view_bytes"]
     assert inf["valued"] == 1 and inf["on_device"] == 0
+    assert inf["build_peak_bytes"] == 0          # a host-only build touches no device memory
 
 
 @pytest.mark.parametrize("bad", ["dup", "range", "rowptr", "neg"])

@@ -1,9 +1,12 @@
-"""Device-side conversion (device_convert = 1): the blocks are found,
-classified and encoded on the GPU, and the matrix must equal the host
+"""Device-side conversion (device_convert = 1): every pass of the conversion
+runs on the GPU -- blocks, formats, payloads, payload offsets, the block-CSC
+view, the pull tiles and the row masks -- and the matrix must equal the host
 builder's byte for byte -- every internal array -- for every workload,
-forced format, pattern-only and valued inputs, ragged sizes and empty rows.
-Rows whose columns are not ascending fall back to the host conversion;
-out-of-range or repeated columns are rejected like on the host."""
+forced format, pattern-only and valued inputs, ragged sizes and empty rows,
+block-CSC column ranges on each side of the sort's size classes, and tile
+options.  Rows whose columns are not ascending fall back to the host
+conversion; bad row pointers and out-of-range or repeated columns are
+rejected like on the host."""
 import numpy as np
 import pytest
 
@@ -64,6 +67,92 @@ def test_device_conversion_thresholds_ragged_and_empty():
     assert_same(E)
 
 
+def test_device_conversion_csc_size_classes_and_tile_windows():
+    """Column blocks holding 1, 32, 33, 4096, 4097 and 9000 blocks (the
+    warp rank, one shared-memory sort, and sorted chunks merged by rank),
+    and more blocks than one window of the tile-start walk."""
+    rng = np.random.default_rng(31)
+    nrb = 9000
+    m, n = 16 * nrb, 4096
+    rows, cols = [], []
+    for c, k in ((3, nrb), (20, 4096), (40, 4097), (60, 33), (80, 32), (100, 1)):
+        rbs = np.sort(rng.choice(nrb, k, replace=False))
+        rows.append(rbs * 16 + rng.integers(0, 16, k))
+        cols.append(np.full(k, c))
+    rr = rng.integers(0, m, 60000)
+    rows.append(rr)
+    cols.append(rng.integers(128, n, rr.size))
+    rows, cols = np.concatenate(rows), np.concatenate(cols)
+    key = np.unique(rows.astype(np.int64) * n + cols)
+    rows, cols = key // n, (key % n).astype(np.int32)
+    vals = rng.standard_normal(rows.size).astype(np.float32)
+    A = synth.csr_from_coo(m, n, rows, cols, vals)
+    M = assert_same(A)
+    assert M.info()["nblocks"] > 11264
+    assert_same(synth.CSR(A.m, A.n, A.row_ptr, A.col_idx, None))
+    assert_same(A, tile_weight=256)
+    assert_same(A, tile_weight=16, tile_max_row_blocks=1)
+
+
+def test_device_conversion_rejects_bad_row_pointers():
+    """The device validates the row pointers before reading any entry:
+    rp[0] != 0, rp[m] != nnz, a decreasing pair and a pointer past nnz are
+    DBS_ERR_INVALID_ARG, as on the host."""
+    import ctypes
+    from dynamic_sparsity_spmspv_gb300 import _lib
+
+    A = synth.random_csr(300, 200, 0.05, 29)
+    for mutate in ("first", "decreasing", "past_end"):
+        rp = A.row_ptr.copy()
+        if mutate == "first":
+            rp[0] = 1
+        elif mutate == "decreasing":
+            rp[100] = rp[101] + 1
+        else:
+            rp[150] = A.nnz + 1000
+        r, c, v = _dev(synth.CSR(A.m, A.n, rp, A.col_idx, A.vals))
+        with pytest.raises(dbs.DbsError):
+            dbs.DBMatrix(A.m, A.n, r, c, v, device_convert=1)
+        with pytest.raises(dbs.DbsError):
+            dbs.DBMatrix(A.m, A.n, r, c, v)
+    # nnz other than rp[m] (the entry arrays are padded, so nothing is out of bounds)
+    r, _, _ = _dev(A)
+    c = torch.zeros(A.nnz + 8, dtype=torch.int32, device=DEV)
+    v = torch.zeros(A.nnz + 8, dtype=torch.float32, device=DEV)
+    c[:A.nnz] = torch.from_numpy(A.col_idx).to(DEV)
+    lib = _lib.load()
+    for dc in (1, 0):
+        o = _lib.dbs_build_opts()
+        lib.dbs_build_opts_default(ctypes.byref(o))
+        o.device_convert = dc
+        h = ctypes.c_void_p()
+        st = lib.dbs_matrix_build_csr(A.m, A.n, A.nnz + 5, ctypes.c_void_p(r.data_ptr()),
+                                      ctypes.c_void_p(c.data_ptr()), ctypes.c_void_p(v.data_ptr()), 1,
+                                      ctypes.byref(o), None, ctypes.byref(h))
+        assert st == 1 and not h.value
+
+
+@pytest.mark.parametrize("name", ["rmat", "llm"])
+def test_build_peak_device_memory(name):
+    """build_peak_bytes: the host build holds the uploaded matrix alone; the
+    device conversion holds the matrix plus 4 bytes per block, 12 per column
+    block and the scan partials, within the bound the header states."""
+    A = synth.config(name, "full")
+    rp, ci, va = _dev(A)
+    for dc in (0, 1):
+        M = dbs.DBMatrix(A.m, A.n, rp, ci, va, device_convert=dc)
+        inf = M.info()
+        B, nbr, nbc = inf["nblocks"], inf["nbr"], inf["nbc"]
+        padded = inf["total_bytes"] + 4 * 8 * 16 + 8 * 16
+        assert inf["build_peak_bytes"] >= inf["total_bytes"]
+        if dc == 0:
+            assert inf["build_peak_bytes"] <= padded + 4096
+        else:
+            scan = 24 * ((max(B, nbc, nbr) + 4095) // 4096 + 1)
+            assert inf["build_peak_bytes"] <= padded + 4 * B + 12 * nbc + scan + 4096, inf
+        M.close()
+
+
 def test_device_conversion_then_multiply_and_keep_host():
     """A device-converted matrix multiplies like the host one, and keep_host
     holds its payload too (export round trip)."""
@@ -107,7 +196,7 @@ def test_device_conversion_unsorted_rows_fall_back_and_bad_columns_fail():
         dbs.DBMatrix(A.m, A.n, rp, c, v, device_convert=1)
 
 
-@pytest.mark.parametrize("name", ["rmat", "llm", "fem"])
+@pytest.mark.parametrize("name", ["rmat", "llm", "fem", "grid"])
 def test_device_conversion_full_size(name):
     M = assert_same(synth.config(name, "full"))
     assert M.info()["build_seconds"] > 0
