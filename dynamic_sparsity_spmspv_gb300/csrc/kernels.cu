@@ -686,12 +686,14 @@ __device__ __forceinline__ uint32_t coo_unit(uint4 u, uint32_t nnz, uint32_t act
 // the Boolean variant does not.
 template <int SR>
 struct WarpPull {
-    // Queued hits with a payload.  Boolean pull: qe = li | lrb << 8 | act << 16,
-    // qm = meta.  Plus-times pull: qe = act | fmt << 16 | (nnz - 1) << 19 |
-    // lrb << 27, qm = column block, qr = payload offset.  Push: see push_tasks.
-    uint32_t qe[TILE_MAX_BLOCKS];
-    uint32_t qm[TILE_MAX_BLOCKS];
-    uint32_t qr[TILE_MAX_BLOCKS];
+    // Queued hits with a payload.  Boolean pull (kept across tiles, up to 31
+    // carried over): qe = block id, qm = meta with the active columns in
+    // its low 16 bits, qr = row block.  Plus-times pull: qe = act | fmt << 16 |
+    // (nnz - 1) << 19 | lrb << 27, qm = column block, qr = payload offset.
+    // Push: see push_tasks.
+    uint32_t qe[TILE_MAX_BLOCKS + 32];
+    uint32_t qm[TILE_MAX_BLOCKS + 32];
+    uint32_t qr[TILE_MAX_BLOCKS + 32];
     uint32_t rm[TILE_MAX_SPAN];       // touched (Boolean: found) rows per row block
     uint32_t nq;                      // queued COO hits, from the front
     uint32_t nq2;                     // queued hits of the other formats, from the back
@@ -1098,8 +1100,12 @@ __device__ void pull_tiles(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
 // come from its coordinate bytes in registers, and a lane ORs them into one
 // register while its blocks stay in one row block (blocks are in row-block
 // order), so shared memory sees one OR per row-block change instead of one
-// per found block.  Stored blocks that meet an active column are queued and
-// decoded from their payload after the scan.
+// per found block.  Stored blocks that meet an active column are queued
+// across tiles and decoded in full rounds of 32 (one block per lane); the
+// lanes' found rows are combined per row block (match and reduce) and
+// OR-ed into the output, since a queued block's tile has been flushed by
+// then.  Visited rows are not removed from those: every consumer of a
+// Boolean pull's output applies the visited mask itself.
 template <bool ST>
 __device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, const uint32_t *vis,
                           uint32_t *out_rm, int tslot)
@@ -1140,12 +1146,34 @@ __device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, con
             dd[j] = 2u * u < end ? __ldcs(desc4 + u) : z4;
         }
     };
+    // queued entries [0, n) decoded, one per lane, their rows combined per
+    // row block across the warp and OR-ed into the output
+    auto drain = [&](uint32_t n, uint32_t &c_bytes) {
+        for (uint32_t i0 = 0; i0 < n; i0 += 32) {
+            const uint32_t i = i0 + (uint32_t)lane;
+            uint32_t r = 0, rb = 0xFFFFFFFFu;
+            if (i < n) {
+                const uint32_t qm = W.qm[i], fmt = meta_fmt(qm), nnz = meta_nnz(qm);
+                const uint4 *b = P.payload + __ldg(P.blk_ref + W.qe[i]);
+                uint4 u0, u1;
+                bool_load(b, fmt, nnz, P.valued != 0, u0, u1);
+                r = bool_found_units(fmt, nnz, qm & 0xFFFFu, u0, u1, b);
+                rb = W.qr[i];
+                if (ST) c_bytes += 4u + (fmt == FMT_COO ? nnz : 32u);
+            }
+            const uint32_t grp = __match_any_sync(FULL, rb);
+            const uint32_t rr = __reduce_or_sync(grp, r);
+            if (rr && rb != 0xFFFFFFFFu && lane == __ffs(grp) - 1) or16(out_rm, rb, rr);
+        }
+    };
 
     uint32_t t = blockIdx.x * NW + warp;
     if (t >= T0) {
         const uint32_t v = lane == 0 ? T0 + atomicAdd(ctr, 1u) : 0u;
         t = __shfl_sync(FULL, v, 0);
     }
+    if (lane == 0) W.nq = 0u;
+    __syncwarp();
     uint4 td = t < P.T ? __ldg(P.tiles + t) : z4;
     uint32_t vrow = 0;
     if (vis) settle(t, td, vrow);
@@ -1159,7 +1187,6 @@ __device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, con
         // block k of this lane (k = 2j + h) is tile block li = 2 (32 j + lane) + h - (p0 & 1)
         const int lbase = 2 * lane - (int)(p0 & 1u);
         if (lane < (int)span) W.rm[lane] = 0u;
-        if (lane == 0) { W.nq = 0u; W.nq2 = 0u; }
         uint32_t mp[WU];   // the eight column-block masks, two per register
 #pragma unroll
         for (int j = 0; j < WU; ++j) {
@@ -1192,10 +1219,10 @@ __device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, con
             acc |= f;
             const uint32_t a = inl ? 0u : mk & meta & 0xFFFFu;
             if (a) {
-                const bool coo = meta_fmt(meta) == FMT_COO;
-                const uint32_t slot = coo ? atomicAdd(&W.nq, 1u) : TILE_MAX_BLOCKS - 1u - atomicAdd(&W.nq2, 1u);
-                W.qe[slot] = (uint32_t)li | (lrb << 8) | (a << 16);
-                W.qm[slot] = meta;
+                const uint32_t slot = atomicAdd(&W.nq, 1u);
+                W.qe[slot] = p0 + (uint32_t)li;
+                W.qm[slot] = (meta & 0xFFFF0000u) | a;
+                W.qr[slot] = rb0 + lrb;
             }
             if (ST) {
                 if (mk) { ++c_vis; c_touch += meta_nnz(meta); }
@@ -1212,35 +1239,21 @@ __device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, con
         }
         __syncwarp();
 
-        // stored blocks meeting an active column: COO (front of the queue),
-        // then the mask formats (back)
-        const uint32_t nq = W.nq, nq2 = W.nq2;
-        if (nq | nq2) {
-            for (uint32_t i = lane; i < nq; i += 32) {
-                const uint32_t e = W.qe[i], nnz = meta_nnz(W.qm[i]);
-                const uint4 *b = P.payload + __ldg(P.blk_ref + p0 + (e & 0xFFu));
-                const uint4 u0 = __ldg(b);
-                const uint4 u1 = nnz > 16u ? __ldg(b + 1) : z4;
-                const uint32_t r = bool_found_units(FMT_COO, nnz, e >> 16, u0, u1, b);
-                if (r) atomicOr(&W.rm[(e >> 8) & 0xFFu], r);
-                if (ST) c_bytes += 4u + nnz;
-            }
-            for (uint32_t i = lane; i < nq2; i += 32) {
-                const uint32_t k = TILE_MAX_BLOCKS - 1u - i;
-                const uint32_t e = W.qe[k], meta = W.qm[k];
-                const uint4 *b = P.payload + __ldg(P.blk_ref + p0 + (e & 0xFFu));
-                const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
-                uint4 u0, u1;
-                bool_load(b, fmt, nnz, P.valued != 0, u0, u1);
-                const uint32_t r = bool_found_units(fmt, nnz, e >> 16, u0, u1, b);
-                if (r) atomicOr(&W.rm[(e >> 8) & 0xFFu], r);
-                if (ST) c_bytes += 4u + 32u;
-            }
-            __syncwarp();
-        }
         if (lane < (int)span) {
             const uint32_t f = W.rm[lane] & ~vrow;
             if (f) or16(out_rm, rb0 + lane, f);
+        }
+        // stored blocks meeting an active column, in full rounds; at most 31
+        // stay queued, so the next tile's 256 fit
+        const uint32_t nq = W.nq;
+        if (nq >= 32u) {
+            const uint32_t nfull = nq & ~31u, rem = nq - nfull;
+            drain(nfull, c_bytes);
+            uint32_t e0 = 0, e1 = 0, e2 = 0;
+            if ((uint32_t)lane < rem) { e0 = W.qe[nfull + lane]; e1 = W.qm[nfull + lane]; e2 = W.qr[nfull + lane]; }
+            __syncwarp();
+            if ((uint32_t)lane < rem) { W.qe[lane] = e0; W.qm[lane] = e1; W.qr[lane] = e2; }
+            if (lane == 0) W.nq = rem;
         }
         if (ST) {
             if (lane == 0) c_bytes += 8u * nblk + 16u;
@@ -1256,6 +1269,10 @@ __device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, con
 #pragma unroll
         for (int j = 0; j < WU; ++j) d[j] = d_n[j];
     }
+    uint32_t c_bytes = 0;
+    drain(W.nq, c_bytes);
+    if (ST) stat_add(S, 3, c_bytes);
+    __syncwarp();
 }
 
 // Push (Section 3.3.2): warps take tasks of up to 256 consecutive CSC
