@@ -292,7 +292,8 @@ ABLATION_FORMATS = (("auto", -1), ("coo", 0), ("force_csr", 2))
 def run_configs(dbs, torch, dev, stream, flush, reps: int):
     """The other workloads at full size, default options (auto path): ER and
     FEM plus-times SpMSpV, the LLM layer with dense and sparse activations,
-    and BFS on the grid with hubs.  Per line: median kernel µs over `reps`
+    FEM and LLM density sweeps with each path forced, and BFS on the grid
+    with hubs and on the grid without hubs.  Per line: median kernel µs over `reps`
     calls (L2 flushed before each), touched nnz and algorithmic bytes from
     one statistics call per input, touched-nnz/s, GB/s, share of HBM."""
     import synth
@@ -355,9 +356,10 @@ def run_configs(dbs, torch, dev, stream, flush, reps: int):
         measure("fem", f"spmspv x {f:g}", M, ws,
                 [lambda xi=xi, xv=xv: dbs.spmspv(M, xi, xv, ws=ws, y_idx=y_idx, y_val=y_val, y_nnz=y_nnz)
                  for xi, xv in xt], {"density": f})
-    # both paths forced where each moves more than 64 MB (the size at which
-    # the roofline fraction is judged): FEM at cluster densities 10 % and 20 %
-    for f in (0.1, 0.2):
+    # density sweep with both paths forced (blocks of ~3 stored entries with
+    # values, against R-MAT's inline pattern blocks); from 10 % up each path
+    # moves more than 64 MB, the size at which the roofline fraction is judged
+    for f in (0.001, 0.01, 0.1, 0.2, 0.5):
         xs = [synth.x_clusters(A.n, f, [45, int(f * 1e4), i]) for i in range(4)]
         xt = [(torch.from_numpy(x.idx).to(dev), torch.from_numpy(x.val).to(dev)) for x in xs]
         for path in ("push", "pull"):
@@ -384,6 +386,16 @@ def run_configs(dbs, torch, dev, stream, flush, reps: int):
     measure("llm", "sparse x (1,101 entries)", M, ws,
             [lambda xi=xi, xv=xv: dbs.spmspv(M, xi, xv, ws=ws, y_idx=y_idx, y_val=y_val, y_nnz=y_nnz)
              for xi, xv in sp], {})
+    # density sweep of uniform sparse x with both paths forced (Dense and
+    # patched-CSR blocks of ~128 entries)
+    for f in (0.001, 0.01, 0.1, 0.5):
+        xs = [synth.x_uniform(A.n, max(1, int(round(f * A.n))), [47, int(f * 1e4), i]) for i in range(4)]
+        xt = [(torch.from_numpy(x.idx).to(dev), torch.from_numpy(x.val).to(dev)) for x in xs]
+        for path in ("push", "pull"):
+            measure("llm", f"spmspv x {f:g}, {path} forced", M, ws,
+                    [lambda xi=xi, xv=xv, path=path: dbs.spmspv(M, xi, xv, ws=ws, path=path, y_idx=y_idx,
+                                                                y_val=y_val, y_nnz=y_nnz) for xi, xv in xt],
+                    {"density": f, "forced": path})
     ws.close(); M.close()
 
     # grid with hubs: BFS
