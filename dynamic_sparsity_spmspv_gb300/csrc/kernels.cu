@@ -480,51 +480,6 @@ __device__ __forceinline__ RowOut mk_pcsr_col(const uint8_t *__restrict__ b, uin
     return RowOut{s, (rows >> (lane & 15)) & 1u};
 }
 
-// Half-warp forms of the fp32 microkernels: lane l (0..15) of a half-warp
-// computes row l of one block, so a warp works on two blocks at once.  The
-// loads of one step do not depend on each other (Dense: value and column
-// mask together; row-wise: row mask and row pointer together, then the
-// values), which keeps each block to one or two memory round trips.
-// Returns the row's sum and whether the row met an active column; *nread
-// counts the values read.
-__device__ __forceinline__ RowOut hw_heavy(const uint8_t *__restrict__ b, uint32_t meta, uint32_t act,
-                                           const float *xb, uint32_t l, uint32_t *nread)
-{
-    const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
-    const float *vals = reinterpret_cast<const float *>(b + val_offset(fmt, nnz));
-    float sum = 0.0f;
-    uint32_t t = 0, cnt = 0;
-    if (fmt == FMT_DENSE || fmt == FMT_FCSC) {
-        const uint16_t *cmask = reinterpret_cast<const uint16_t *>(b + (fmt == FMT_DENSE ? dense_mask_off(true) : OFF_MASK));
-        uint32_t a = act;
-        while (a) {
-            const uint32_t c = __ffs(a) - 1u;
-            a &= a - 1u;
-            const uint32_t cm = __ldg(cmask + c);
-            float v;
-            if (fmt == FMT_DENSE) v = __ldg(vals + c * 16u + l);
-            else v = ((cm >> l) & 1u) ? __ldg(vals + (uint32_t)__ldg(b + OFF_PTR + c) + __popc(cm & ((1u << l) - 1u))) : 0.0f;
-            if ((cm >> l) & 1u) {
-                sum = fmaf(v, xval(xb, c), sum);
-                t = 1u;
-                ++cnt;
-            }
-        }
-    } else {                                               // ForceCSR, patched CSR (row mode)
-        const uint32_t rm = __ldg(reinterpret_cast<const uint16_t *>(b + OFF_MASK) + l);
-        const uint32_t base = __ldg(b + OFF_PTR + l);
-        uint32_t a = rm & act;
-        t = a != 0u;
-        while (a) {
-            const uint32_t c = __ffs(a) - 1u;
-            a &= a - 1u;
-            sum = fmaf(__ldg(vals + base + __popc(rm & ((1u << c) - 1u))), xval(xb, c), sum);
-            ++cnt;
-        }
-    }
-    *nread = cnt;
-    return RowOut{sum, t};
-}
 // Whether a block needs the whole-warp patched-CSR column mode.
 __device__ __forceinline__ bool needs_col_mode(const KParams &P, uint32_t meta, uint32_t act)
 {
@@ -559,7 +514,9 @@ __device__ __forceinline__ RowOut mk_heavy(const KParams &P, const uint8_t *b, u
 // (acc[r], 0 for the other rows); returns those rows.  None of a pair's loads
 // depends on another, so a warp has the payload reads of 32 pairs in flight
 // together instead of walking a block's active columns one after another
-// (Algorithms 2-4 restated per (block, column) pair).
+// (Algorithms 2-4 restated per (block, column) pair).  ADD: the products are
+// added to acc instead of replacing it.
+template <bool ADD = false>
 __device__ __forceinline__ uint32_t pair_products(const uint8_t *__restrict__ b, uint32_t fmt, uint32_t nnz, uint32_t c,
                                                   float xc, float (&acc)[16])
 {
@@ -577,13 +534,14 @@ __device__ __forceinline__ uint32_t pair_products(const uint8_t *__restrict__ b,
             v[4 * q] = t.x; v[4 * q + 1] = t.y; v[4 * q + 2] = t.z; v[4 * q + 3] = t.w;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) acc[r] = ((rows >> r) & 1u) ? v[r] * xc : 0.0f;
+        for (int r = 0; r < 16; ++r) acc[r] = (ADD ? acc[r] : 0.0f) + (((rows >> r) & 1u) ? v[r] * xc : 0.0f);
     } else if (fmt == FMT_FCSC) {
         rows = __ldg(reinterpret_cast<const uint16_t *>(b + OFF_MASK) + c);
         const uint32_t cp = __ldg(b + OFF_PTR + c);
 #pragma unroll
         for (int r = 0; r < 16; ++r)
-            acc[r] = ((rows >> r) & 1u) ? __ldg(vals + cp + __popc(rows & ((1u << r) - 1u))) * xc : 0.0f;
+            acc[r] = (ADD ? acc[r] : 0.0f) +
+                     (((rows >> r) & 1u) ? __ldg(vals + cp + __popc(rows & ((1u << r) - 1u))) * xc : 0.0f);
     } else {
         // row layouts: row_ptr u8[16] at 0, row_mask u16[16] at 16
         const uint4 *b4 = reinterpret_cast<const uint4 *>(b);
@@ -597,7 +555,7 @@ __device__ __forceinline__ uint32_t pair_products(const uint8_t *__restrict__ b,
             const uint32_t base = (rpw[r >> 2] >> ((r & 3) * 8)) & 0xFFu;
             const bool has = (rm >> c) & 1u;
             rows |= (has ? 1u : 0u) << r;
-            acc[r] = has ? __ldg(vals + base + __popc(rm & below)) * xc : 0.0f;
+            acc[r] = (ADD ? acc[r] : 0.0f) + (has ? __ldg(vals + base + __popc(rm & below)) * xc : 0.0f);
         }
     }
     return rows;
@@ -1400,8 +1358,11 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
             }
             // the other hits: payload offsets first (independent loads; the
             // offset replaces the position and the active columns replace
-            // the meta word's column mask), then two blocks at a time, one
-            // per half-warp (a patched-CSR block in column mode takes the warp)
+            // the meta word's column mask), then one block per lane, 32 at
+            // a time: the lane adds up the row products of the block's
+            // active columns in registers and adds each touched row to y
+            // once (every block lies in its own row block).  A patched-CSR
+            // block in column mode takes the whole warp after.
             for (uint32_t i = lane; i < nq2; i += 32) {
                 const uint32_t k = TILE_MAX_BLOCKS - 1u - i;
                 const uint32_t e = W.qe[k];
@@ -1409,38 +1370,45 @@ __device__ void push_tasks(const KParams &P, SmemT<SR> &S, const uint32_t *xm, c
                 W.qm[k] = (W.qm[k] & ~0xFFFFu) | (e >> 16);
             }
             __syncwarp();
-            const uint32_t l = lane & 15u, h = lane >> 4;
-            for (uint32_t i = 0; i < nq2; i += 2) {
-                const bool two = i + 1u < nq2;
-                const uint32_t k = TILE_MAX_BLOCKS - 1u - i - (h & (two ? 1u : 0u));
+            bool any_col_mode = false;
+            for (uint32_t i = lane; i < nq2; i += 32) {
+                const uint32_t k = TILE_MAX_BLOCKS - 1u - i;
                 const uint32_t meta = W.qm[k], act = meta & 0xFFFFu, rb = W.qr[k];
+                if (needs_col_mode(P, meta, act)) { any_col_mode = true; continue; }
+                const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
                 const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + W.qe[k]);
-                if (__any_sync(FULL, needs_col_mode(P, meta, act))) {
-                    for (uint32_t j = 0; j < (two ? 2u : 1u); ++j) {
-                        const uint32_t kj = TILE_MAX_BLOCKS - 1u - i - j;
-                        const uint32_t mj = W.qm[kj], rj = W.qr[kj];
-                        uint32_t by = 0;
-                        RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + W.qe[kj]), mj, mj & 0xFFFFu,
-                                            wx, lane, S.wacc[warp], &by);
-                        if (lane < 16 && o.touched) atomicAdd(y + (size_t)rj * 16u + lane, o.sum);
-                        const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
-                        if (lane == 0) {
-                            if (!DOUT && bits) or16(out_rm, rj, bits);
-                            if (ST) c_bytes += 4u + by;
-                        }
-                        __syncwarp();
-                    }
-                    continue;
+                float acc[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) acc[r] = 0.0f;
+                uint32_t rows = 0;
+                for (uint32_t a = act; a; a &= a - 1u) {
+                    const uint32_t c = __ffs(a) - 1u;
+                    const uint32_t rc = pair_products<true>(b, fmt, nnz, c, wx[c], acc);
+                    rows |= rc;
+                    if (ST) c_bytes += fmt == FMT_DENSE ? 64u : 4u * __popc(rc);
                 }
-                uint32_t nr = 0;
-                const RowOut o = hw_heavy(b, meta, act, wx, l, &nr);
-                const bool mine = two || h == 0u;
-                if (mine && o.touched) atomicAdd(y + (size_t)rb * 16u + l, o.sum);
-                const uint32_t bits = __ballot_sync(FULL, mine && o.touched);
-                if (!DOUT && l == 0 && mine && ((bits >> (16u * h)) & 0xFFFFu)) or16(out_rm, rb, (bits >> (16u * h)) & 0xFFFFu);
-                if (ST) {
-                    const uint32_t tot = __reduce_add_sync(FULL, mine ? nr : 0u);
-                    if (lane == 0) c_bytes += 8u + 32u + 4u * tot;
+                float *yr = y + (size_t)rb * 16u;
+#pragma unroll
+                for (int r = 0; r < 16; ++r)
+                    if ((rows >> r) & 1u) atomicAdd(yr + r, acc[r]);
+                if (!DOUT && rows) or16(out_rm, rb, rows);
+                if (ST) c_bytes += 4u + (fmt == FMT_DENSE ? 32u : 48u);
+            }
+            if (__any_sync(FULL, any_col_mode)) {
+                for (uint32_t i = 0; i < nq2; ++i) {
+                    const uint32_t k = TILE_MAX_BLOCKS - 1u - i;
+                    const uint32_t mj = W.qm[k], rj = W.qr[k];
+                    if (!needs_col_mode(P, mj, mj & 0xFFFFu)) continue;
+                    uint32_t by = 0;
+                    RowOut o = mk_heavy(P, reinterpret_cast<const uint8_t *>(P.payload + W.qe[k]), mj, mj & 0xFFFFu, wx,
+                                        lane, S.wacc[warp], &by);
+                    if (lane < 16 && o.touched) atomicAdd(y + (size_t)rj * 16u + lane, o.sum);
+                    const uint32_t bits = __ballot_sync(FULL, lane < 16 && o.touched) & 0xFFFFu;
+                    if (lane == 0) {
+                        if (!DOUT && bits) or16(out_rm, rj, bits);
+                        if (ST) c_bytes += 4u + by;
+                    }
+                    __syncwarp();
                 }
             }
         }
