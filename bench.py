@@ -595,8 +595,7 @@ def run_decode(dbs, torch, dev, stream, n_layers: int, tokens: int):
     activations in and outputs out as well).  The weights total several GB,
     far above L2, so every layer streams its blocks cold.  Two builds: the
     paper's format thresholds, and th1 = 31 (every block with 32 or more
-    entries Dense, column-major) with tile weight 160 (about one pull tile
-    per resident warp) -- the setting measured fastest on GB300.  cuBLAS
+    entries Dense, column-major) -- the setting measured fastest on GB300.  cuBLAS
     dense GEMV of the same layers (fp32 and bf16, dense weights) is timed
     the same way as context."""
     import synth

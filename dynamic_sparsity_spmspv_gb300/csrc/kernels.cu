@@ -8,17 +8,19 @@
 //   3.3.1    high-level path: push iff N_nzblk / N_blk < th3, decided on the
 //            device; low-level microkernel from block type and blk_x_mask;
 //   3.3.2    push: matrix-block tasks flattened over the active column blocks
-//            (a warp takes 32 CSC positions); pull: load-weighted tiles of
-//            consecutive primary blocks, one CTA each;
+//            (a warp takes 32 to 256 CSC positions, sized per call); pull:
+//            load-weighted tiles of consecutive primary blocks, one warp each;
 //   3.3.3    hierarchical writeback: microkernel registers / warp shuffles ->
 //            shared-memory row accumulators -> global;
-//   Alg. 2   ForceCSR row-wise microkernel (two lanes per row);
-//   Alg. 3   ForceCSC column-wise microkernel (half-warps over column ranges);
-//   Alg. 4   Dense microkernel -- here over a column-major block, so pull and
-//            push both read only the active columns' 64-byte runs;
+//   Alg. 2-4 fp32 microkernels per (block, active column) pair: Dense over a
+//            column-major block (only the active columns' 64-byte runs are
+//            read), ForceCSC over a column's run, ForceCSR and patched CSR
+//            by row lookups; patched CSR in column mode through
+//            row_idx_csc2csr with the whole warp;
 //   Alg. 5   Boolean reachability with the visited mask; here one lane per
 //            block computes the found-row mask with bit operations;
-//   4.2      DB-BFS: the level loop runs inside one cooperative launch.
+//   4.2      DB-BFS: the level loop runs inside one cooperative launch;
+//   4.3      DB-Decoding layer: one ordinary launch, one CTA per row block.
 //
 // Every device-side wait is a grid barrier with a time bound; on expiry the
 // kernel latches DBS_ERR_TIMEOUT in the workspace and returns.
@@ -369,81 +371,10 @@ __device__ __forceinline__ float4 ldg_l2_64(const float4 *p)
 // (never read before that point, so no stale L1 line can exist).
 __device__ __forceinline__ float xval(const float *xb, uint32_t c) { return xb[c]; }
 
-// Algorithm 3 structure (column-organised payloads: Dense, ForceCSC): lane
-// (row r, half h) walks the active columns of its half.
-template <uint32_t FMT>
-__device__ __forceinline__ RowOut mk_colwise(const uint8_t *__restrict__ b, uint32_t nnz, uint32_t act,
-                                             const float *xb, int lane, uint32_t *nread)
-{
-    const uint32_t r = lane & 15, h = lane >> 4;
-    const uint16_t *cmask = reinterpret_cast<const uint16_t *>(b + (FMT == FMT_DENSE ? dense_mask_off(true) : OFF_MASK));
-    const float *vals = reinterpret_cast<const float *>(b + val_offset(FMT, nnz));
-    uint32_t a = act & (h ? 0xFF00u : 0x00FFu);
-    float sum = 0.0f;
-    uint32_t t = 0, cnt = 0;
-    while (a) {
-        uint32_t c = __ffs(a) - 1u;
-        a &= a - 1u;
-        if (FMT == FMT_DENSE) {
-            // column-major with zeros for absent entries: the value's address
-            // does not depend on the mask, so both loads go out together
-            const float v = __ldg(vals + c * 16u + r);
-            const uint32_t cm = __ldg(cmask + c);
-            if ((cm >> r) & 1u) {
-                sum = fmaf(v, xval(xb, c), sum);
-                t = 1u;
-                ++cnt;
-            }
-        } else {
-            uint32_t cm = __ldg(cmask + c);
-            if ((cm >> r) & 1u) {
-                uint32_t idx = (uint32_t)__ldg(b + OFF_PTR + c) + __popc(cm & ((1u << r) - 1u));
-                sum = fmaf(__ldg(vals + idx), xval(xb, c), sum);
-                t = 1u;
-                ++cnt;
-            }
-        }
-    }
-    sum += __shfl_xor_sync(FULL, sum, 16);
-    t |= __shfl_xor_sync(FULL, t, 16);
-    *nread = cnt;
-    return RowOut{sum, t};
-}
-
-// Algorithm 2 (row-organised payloads: ForceCSR, patched CSR in pull mode):
-// two lanes per row take alternate active entries; results move to lane r.
-template <uint32_t FMT>
-__device__ __forceinline__ RowOut mk_rowwise(const uint8_t *__restrict__ b, uint32_t nnz, uint32_t act,
-                                             const float *xb, int lane, uint32_t *nread)
-{
-    const uint32_t row = lane >> 1, sub = lane & 1;
-    const uint32_t rm = __ldg(reinterpret_cast<const uint16_t *>(b + OFF_MASK) + row);
-    const uint32_t base = __ldg(b + OFF_PTR + row);
-    const float *vals = reinterpret_cast<const float *>(b + val_offset(FMT, nnz));
-    uint32_t a = rm & act, k = 0, cnt = 0;
-    float sum = 0.0f;
-    while (a) {
-        uint32_t c = __ffs(a) - 1u;
-        if ((k & 1u) == sub) {
-            uint32_t off = __popc(rm & ((1u << c) - 1u));
-            sum = fmaf(__ldg(vals + base + off), xval(xb, c), sum);
-            ++cnt;
-        }
-        a &= a - 1u;
-        ++k;
-    }
-    sum += __shfl_xor_sync(FULL, sum, 1);
-    uint32_t t = (rm & act) != 0u;
-    const int src = (lane & 15) << 1;
-    float s2 = __shfl_sync(FULL, sum, src);
-    uint32_t t2 = __shfl_sync(FULL, t, src);
-    *nread = cnt;
-    return RowOut{s2, t2};
-}
-
-// Patched CSR in push mode (Section 3.3.3): for each active column walk its
+// Patched CSR in column mode (Section 3.3.3, the local push paradigm of a
+// patched block with few active columns): for each active column walk its
 // row_idx_csc2csr bytes (row, offset within the row) and read the value from
-// the row-ordered array; two columns per step (one per half-warp).
+// the row-ordered array; two columns per step, one per 16 lanes.
 __device__ __forceinline__ RowOut mk_pcsr_col(const uint8_t *__restrict__ b, uint32_t nnz, uint32_t act,
                                               const float *xb, int lane, float *wacc, uint32_t *nread)
 {
@@ -486,25 +417,15 @@ __device__ __forceinline__ bool needs_col_mode(const KParams &P, uint32_t meta, 
     return meta_fmt(meta) == FMT_PCSR && (int)__popc(act) < P.local_pull_min;
 }
 
-// Dispatch of the fp32 warp microkernel for a non-COO block (Section 3.3.1:
-// by blocks_type and blk_x_mask).
+// The whole-warp microkernel of a patched-CSR block in column mode (Section
+// 3.3.1: chosen by the block type and its active columns); *bytes gets the
+// algorithmic bytes when statistics are on.
 __device__ __forceinline__ RowOut mk_heavy(const KParams &P, const uint8_t *b, uint32_t meta, uint32_t act,
                                            const float *xb, int lane, float *wacc, uint32_t *bytes)
 {
-    const uint32_t fmt = meta_fmt(meta), nnz = meta_nnz(meta);
     uint32_t nr = 0;
-    RowOut o;
-    uint32_t fixed;
-    if (fmt == FMT_DENSE) { o = mk_colwise<FMT_DENSE>(b, nnz, act, xb, lane, &nr); fixed = 32; }
-    else if (fmt == FMT_FCSC) { o = mk_colwise<FMT_FCSC>(b, nnz, act, xb, lane, &nr); fixed = 48; }
-    else if (fmt == FMT_FCSR) { o = mk_rowwise<FMT_FCSR>(b, nnz, act, xb, lane, &nr); fixed = 48; }
-    else if ((int)__popc(act) >= P.local_pull_min) { o = mk_rowwise<FMT_PCSR>(b, nnz, act, xb, lane, &nr); fixed = 48; }
-    else { o = mk_pcsr_col(b, nnz, act, xb, lane, wacc, &nr); fixed = 64; nr *= 2; /* rcsc byte + value */ }
-    if (P.stats) {
-        uint32_t tot = __reduce_add_sync(FULL, nr);
-        // Dense reads whole 64-byte column runs; the others read values and codes
-        *bytes = fixed + (fmt == FMT_DENSE ? 64u * __popc(act) : 4u * tot);
-    }
+    const RowOut o = mk_pcsr_col(b, meta_nnz(meta), act, xb, lane, wacc, &nr);
+    if (P.stats) *bytes = 64u + 8u * __reduce_add_sync(FULL, nr);   // structure, then a code byte + value per entry
     return o;
 }
 
