@@ -243,19 +243,20 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane)
 
 // Block-wide exclusive scan of one value per thread; returns the prefix and
 // stores the total in *total.  All threads must call it.
+template <int NWB = NW>
 __device__ uint32_t block_excl_scan(uint32_t v, uint32_t *total)
 {
-    __shared__ uint32_t s_w[NW];
+    __shared__ uint32_t s_w[NWB];
     __shared__ uint32_t s_tot;
     int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     uint32_t inc = warp_incl_scan(v, lane);
     if (lane == 31) s_w[w] = inc;
     __syncthreads();
     if (w == 0) {
-        uint32_t x = lane < NW ? s_w[lane] : 0u;
+        uint32_t x = lane < NWB ? s_w[lane] : 0u;
         uint32_t xi = warp_incl_scan(x, lane);
-        if (lane < NW) s_w[lane] = xi - x;
-        if (lane == NW - 1) s_tot = xi;
+        if (lane < NWB) s_w[lane] = xi - x;
+        if (lane == NWB - 1) s_tot = xi;
     }
     __syncthreads();
     uint32_t r = s_w[w] + inc - v;
@@ -1854,11 +1855,21 @@ __device__ __forceinline__ uint32_t act_mask(const float *__restrict__ x, uint32
 constexpr int DEC_NT = 512; // threads per row block
 constexpr int DEC_NW = DEC_NT / 32;
 constexpr int DEC_K = 2;    // blocks per thread per round of a row block
+constexpr int DEC_SLOTS = DEC_NT * DEC_K;
 
+// The CTA owns one row block.  Per round of up to DEC_SLOTS blocks: each
+// thread loads its blocks' descriptors and forms their activation masks;
+// COO blocks are done by the thread at once, the other blocks' (block,
+// active column) pairs are listed in shared memory and shared out evenly,
+// so the round ends after about pairs / DEC_NT column reads per thread
+// whatever the mix of active columns per block.  Every pair adds into the
+// same 16 rows, kept in registers until the row block's reduction.
 __global__ void __launch_bounds__(DEC_NT, 2) k_decode(KParams P)
 {
     constexpr int NT = DEC_NT, NW = DEC_NW;
     __shared__ float s_part[NW][16];
+    __shared__ uint32_t s_ref[DEC_SLOTS], s_meta[DEC_SLOTS], s_col[DEC_SLOTS];
+    __shared__ uint16_t s_pair[DEC_SLOTS * 16];   // slot << 4 | column
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float tau = P.tau;
     const float *__restrict__ x = P.x_in;
@@ -1867,7 +1878,7 @@ __global__ void __launch_bounds__(DEC_NT, 2) k_decode(KParams P)
         float acc[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) acc[r] = 0.0f;
-        for (uint32_t base = p0; base < p1; base += NT * DEC_K) {
+        for (uint32_t base = p0; base < p1; base += DEC_SLOTS) {
             uint2 d[DEC_K];
             uint32_t ref[DEC_K], am[DEC_K];
 #pragma unroll
@@ -1876,31 +1887,48 @@ __global__ void __launch_bounds__(DEC_NT, 2) k_decode(KParams P)
                 d[k] = p < p1 ? __ldg(P.blk_desc + p) : make_uint2(0u, 0u);
                 ref[k] = p < p1 ? __ldg(P.blk_ref + p) : 0u;
             }
-#pragma unroll
-            for (int k = 0; k < DEC_K; ++k)
-                am[k] = base + (uint32_t)(k * NT + tid) < p1
-                            ? act_mask(x, d[k].x & DESC_COL_MASK, P.n, tau) & d[k].y & 0xFFFFu : 0u;
+            uint32_t np = 0;
 #pragma unroll
             for (int k = 0; k < DEC_K; ++k) {
-                if (!am[k]) continue;
-                const uint32_t meta = d[k].y, fmt = meta_fmt(meta), nnz = meta_nnz(meta), col = d[k].x & DESC_COL_MASK;
-                const uint8_t *b = reinterpret_cast<const uint8_t *>(P.payload + ref[k]);
-                const float *xb = x + (size_t)col * 16u;
-                if (fmt == FMT_COO) {
-                    coo_lane(b, nnz, am[k], xb, true, [&](uint32_t r, float v) {
+                am[k] = base + (uint32_t)(k * NT + tid) < p1
+                            ? act_mask(x, d[k].x & DESC_COL_MASK, P.n, tau) & d[k].y & 0xFFFFu : 0u;
+                const uint32_t meta = d[k].y, col = d[k].x & DESC_COL_MASK;
+                if (am[k] && meta_fmt(meta) == FMT_COO) {
+                    coo_lane(reinterpret_cast<const uint8_t *>(P.payload + ref[k]), meta_nnz(meta), am[k],
+                             x + (size_t)col * 16u, true, [&](uint32_t r, float v) {
 #pragma unroll
-                        for (int rr = 0; rr < 16; ++rr) acc[rr] += (uint32_t)rr == r ? v : 0.0f;
-                    });
-                } else {
-                    for (uint32_t a = am[k]; a; a &= a - 1u) {
-                        const uint32_t c = __ffs(a) - 1u;
-                        float t[16];
-                        pair_products(b, fmt, nnz, c, __ldg(xb + c), t);
-#pragma unroll
-                        for (int r = 0; r < 16; ++r) acc[r] += t[r];
-                    }
+                                 for (int rr = 0; rr < 16; ++rr) acc[rr] += (uint32_t)rr == r ? v : 0.0f;
+                             });
+                    am[k] = 0u;
+                }
+                if (am[k]) {
+                    const uint32_t slot = (uint32_t)(k * NT + tid);
+                    s_ref[slot] = ref[k];
+                    s_meta[slot] = meta;
+                    s_col[slot] = col;
+                    np += __popc(am[k]);
                 }
             }
+            uint32_t tot;
+            uint32_t o = block_excl_scan<NW>(np, &tot);
+#pragma unroll
+            for (int k = 0; k < DEC_K; ++k)
+                for (uint32_t a = am[k]; a; a &= a - 1u)
+                    s_pair[o++] = (uint16_t)(((uint32_t)(k * NT + tid) << 4) | (__ffs(a) - 1u));
+            __syncthreads();
+            // two pairs per step, their loads issued together
+            for (uint32_t i = tid; i < tot; i += 2 * NT) {
+                const uint32_t e0 = s_pair[i], s0 = e0 >> 4, c0 = e0 & 15u, m0 = s_meta[s0];
+                const bool two = i + NT < tot;
+                const uint32_t e1 = two ? s_pair[i + NT] : e0, s1 = e1 >> 4, c1 = e1 & 15u, m1 = s_meta[s1];
+                const float x0 = __ldg(x + (size_t)s_col[s0] * 16u + c0), x1 = __ldg(x + (size_t)s_col[s1] * 16u + c1);
+                pair_products<true>(reinterpret_cast<const uint8_t *>(P.payload + s_ref[s0]), meta_fmt(m0),
+                                    meta_nnz(m0), c0, x0, acc);
+                if (two)
+                    pair_products<true>(reinterpret_cast<const uint8_t *>(P.payload + s_ref[s1]), meta_fmt(m1),
+                                        meta_nnz(m1), c1, x1, acc);
+            }
+            __syncthreads();
         }
         // row sums over the block: warp transpose reduction, then the warps
         const float v = warp_rows_sum(acc, true, lane);
