@@ -79,8 +79,8 @@ def test_decode_every_block_mask():
 @pytest.mark.parametrize("m,n", [(1, 1), (17, 33), (250, 1000), (1000, 250), (4099, 4111)])
 def test_decode_ragged_and_empty_rows(m, n):
     """Sizes that are not multiples of 16 (ragged row and column tails),
-    empty rows and empty row blocks; repeated calls reuse the same
-    workspace (the shared-row-block counters reset themselves)."""
+    empty rows and empty row blocks; repeated calls into the same output
+    (every row is rewritten on every call, stale values included)."""
     rng = np.random.default_rng(m * 7 + n)
     A = synth.random_csr(m, n, 0.05, m + n)
     keep = rng.random(m) < 0.7
@@ -96,6 +96,25 @@ def test_decode_ragged_and_empty_rows(m, n):
         dbs.decode_layer(M, torch.from_numpy(x).to(DEV), 0.7, y=y, ws=ws)
         assert ws.check() == 0
         check(O, x, 0.7, y)
+
+
+@pytest.mark.parametrize("fmt", [-1, 0, 1, 2, 3, 4])
+def test_decode_long_row_blocks(fmt):
+    """Row blocks of more than one round of the kernel (over 1,024 blocks:
+    the (block, column) pair list is refilled per round) with every column
+    of a block active (16 pairs per block at tau = 0), in every format."""
+    rng = np.random.default_rng(40 + fmt)
+    m, n = 45, 16 * 2100 + 5
+    dense = rng.random((m, n)) < 0.35
+    rows, cols = np.nonzero(dense)
+    A = synth.csr_from_coo(m, n, rows, cols.astype(np.int32), rng.standard_normal(rows.size).astype(np.float32))
+    O = oracle.Oracle(A)
+    M = dbs.DBMatrix.from_csr(A, force_format=fmt)
+    ws = dbs.Workspace(M)
+    assert M.info()["nblocks"] > 3 * 2 * 1024
+    for tau in (0.0, 0.9):
+        x = rng.standard_normal(n).astype(np.float32)
+        check(O, x, tau, run(M, ws, x, tau))
 
 
 def test_decode_interleaved_with_other_calls():
