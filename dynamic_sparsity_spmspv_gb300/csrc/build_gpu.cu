@@ -25,8 +25,13 @@
 // parallel first, and one CTA then follows the chain of tile starts from
 // block 0 through windows of those ends staged in shared memory.
 //
+// Row blocks with many entries (hub rows) are split into several merge
+// tasks over equal shares of the column blocks, one warp each.
+//
 // Device memory beyond the input CSR and the finished matrix: 4 bytes per
-// block and 12 per column block, plus scan partials.
+// block and 12 per column block, or, while the blocks are found, 4 per row
+// block and 8 per merge task (one per row block plus one per 4,096 entries
+// of a long one), whichever is more; plus scan partials.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -45,19 +50,29 @@ constexpr unsigned FULL = 0xFFFFFFFFu;
 enum : unsigned { ERR_RANGE = 1u, ERR_DUP = 2u, ERR_ORDER = 4u, ERR_PTR = 8u, ERR_INTERNAL = 16u, ERR_SIZE = 32u };
 
 struct ConvParams {
-    int64_t m, n, nnz, nbr, nbc, B;
+    int64_t m, n, nnz, nbr, nbc, B, ntasks;
     const int64_t *rp;
     const int32_t *ci;
     const float *va;        // NULL: pattern only
     int th0, th1;
     double th2;
     int force_format;       // -1 automatic
-    uint32_t *rb_ptr;       // block-CSR row-block pointers (counts before the scan)
+    uint32_t *rb_ptr;       // block-CSR row-block pointers
+    uint32_t *rb_t0;        // first merge task of each row block (counts before the scan)
+    uint32_t *t_rb;         // row block of each merge task
+    uint32_t *t_off;        // blocks of each merge task, then its first block (after the scan)
     uint2 *desc;            // per block {column block, meta}
     uint32_t *ref;          // per block payload offset
     uint4 *payload;
     unsigned *err;
 };
+
+// Merge tasks: a row block's blocks are found by one warp, or, for a row
+// block with many entries (a hub row of a power-law graph), by several
+// warps, each over an equal share of the column blocks, so no warp walks
+// tens of thousands of column blocks alone.
+constexpr int64_t TASK_ENTRIES = 4096;   // entries of a row block per merge task
+constexpr int64_t TASK_MIN_CBS = 16;     // column blocks per task at least
 
 // Section 3.2.1 classification with the host builder's fp64 operations,
 // each rounded on its own (no fused multiply-add), so both builders agree.
@@ -85,14 +100,32 @@ __device__ __forceinline__ uint32_t cb_at(const ConvParams &C, const RowCursor &
     return r.pos < r.end ? (uint32_t)__ldg(C.ci + r.pos) >> 4 : NO_CB;
 }
 
-// A row's cursor; only after the row pointers were validated (pass 1).
-__device__ __forceinline__ RowCursor open_row(const ConvParams &C, int64_t rb, int lane)
+// First position in ci[lo, hi) (ascending) whose column block is >= cb.
+__device__ __forceinline__ int64_t first_at_or_after(const ConvParams &C, int64_t lo, int64_t hi, uint32_t cb)
 {
+    while (lo < hi) {
+        const int64_t mid = lo + ((hi - lo) >> 1);
+        if (((uint32_t)__ldg(C.ci + mid) >> 4) < cb) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// A lane's cursor over its row's entries in merge task t's column blocks;
+// only after the rows were validated.  Sets *rb and the task's column-block
+// range.
+__device__ __forceinline__ RowCursor open_task(const ConvParams &C, int64_t t, int lane, int64_t *rb_out)
+{
+    const uint32_t rb = __ldg(C.t_rb + t);
+    const uint32_t t0 = __ldg(C.rb_t0 + rb), nt = __ldg(C.rb_t0 + rb + 1) - t0, k = (uint32_t)t - t0;
+    const uint32_t c_lo = (uint32_t)((uint64_t)C.nbc * k / nt), c_hi = (uint32_t)((uint64_t)C.nbc * (k + 1u) / nt);
+    *rb_out = rb;
     RowCursor r{0, 0, NO_CB};
-    const int64_t row = rb * BS + lane;
+    const int64_t row = (int64_t)rb * BS + lane;
     if (lane < BS && row < C.m) {
-        r.pos = __ldg(C.rp + row);
-        r.end = __ldg(C.rp + row + 1);
+        const int64_t a = __ldg(C.rp + row), b = __ldg(C.rp + row + 1);
+        r.pos = k == 0u ? a : first_at_or_after(C, a, b, c_lo);
+        r.end = k + 1u == nt ? b : first_at_or_after(C, r.pos, b, c_hi);
         r.head = cb_at(C, r);
     }
     return r;
@@ -115,41 +148,58 @@ __device__ __forceinline__ uint32_t merge_step(const ConvParams &C, RowCursor &r
 }
 
 // Pass 1: validate the row pointers (before any entry is read) and the
-// rows, and count the blocks of every row block.
-__global__ void __launch_bounds__(CT) k_conv_count(ConvParams C)
+// rows' columns (range, repeats, order); one warp per row.
+__global__ void __launch_bounds__(CT) k_conv_validate(ConvParams C)
 {
     if (blockIdx.x == 0 && threadIdx.x == 0 && (__ldg(C.rp) != 0 || __ldg(C.rp + C.m) != C.nnz))
         atomicOr(C.err, ERR_PTR);
     const int lane = threadIdx.x & 31;
-    const int64_t rb = (int64_t)blockIdx.x * (CT / 32) + (threadIdx.x >> 5);
-    if (rb >= C.nbr) return;
-    RowCursor r{0, 0, NO_CB};
     unsigned bad = 0;
-    const int64_t row = rb * BS + lane;
-    if (lane < BS && row < C.m) {
+    for (int64_t row = (int64_t)blockIdx.x * (CT / 32) + (threadIdx.x >> 5); row < C.m;
+         row += (int64_t)gridDim.x * (CT / 32)) {
         const int64_t a = __ldg(C.rp + row), b = __ldg(C.rp + row + 1);
-        if (a < 0 || b < a || b > C.nnz) bad = ERR_PTR;
-        else { r.pos = a; r.end = b; }
-    }
-    if (__reduce_or_sync(FULL, bad)) {
-        if (lane == 0) atomicOr(C.err, ERR_PTR);
-        return;
-    }
-    r.head = cb_at(C, r);
-    for (int64_t k = r.pos; k < r.end; ++k) {
-        const int32_t c = __ldg(C.ci + k);
-        if (c < 0 || (int64_t)c >= C.n) bad |= ERR_RANGE;
-        else if (k > r.pos) {
-            const int32_t p = __ldg(C.ci + k - 1);
-            if (c == p) bad |= ERR_DUP;
-            else if (c < p) bad |= ERR_ORDER;
+        if (a < 0 || b < a || b > C.nnz) {
+            bad |= ERR_PTR;
+            continue;
+        }
+        for (int64_t k = a + lane; k < b; k += 32) {
+            const int32_t c = __ldg(C.ci + k);
+            if (c < 0 || (int64_t)c >= C.n) bad |= ERR_RANGE;
+            else if (k > a) {
+                const int32_t p = __ldg(C.ci + k - 1);
+                if (c == p) bad |= ERR_DUP;
+                else if (c < p) bad |= ERR_ORDER;
+            }
         }
     }
     bad = __reduce_or_sync(FULL, bad);
-    if (bad) {
-        if (lane == 0) atomicOr(C.err, bad);
-        return;
+    if (bad && lane == 0) atomicOr(C.err, bad);
+}
+
+// Merge tasks per row block, from its entry count.
+__global__ void k_task_counts(ConvParams C)
+{
+    for (int64_t rb = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; rb < C.nbr; rb += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e = __ldg(C.rp + min(C.m, (rb + 1) * BS)) - __ldg(C.rp + rb * BS);
+        const int64_t cap = max((int64_t)1, C.nbc / TASK_MIN_CBS);
+        C.rb_t0[rb] = (uint32_t)min(cap, max((int64_t)1, (e + TASK_ENTRIES - 1) / TASK_ENTRIES));
     }
+}
+
+__global__ void k_task_fill(ConvParams C)
+{
+    for (int64_t rb = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; rb < C.nbr; rb += (int64_t)gridDim.x * blockDim.x)
+        for (uint32_t t = C.rb_t0[rb]; t < C.rb_t0[rb + 1]; ++t) C.t_rb[t] = (uint32_t)rb;
+}
+
+// Pass 2: blocks of every merge task.
+__global__ void __launch_bounds__(CT) k_conv_count(ConvParams C)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * (CT / 32) + (threadIdx.x >> 5);
+    if (t >= C.ntasks) return;
+    int64_t rb;
+    RowCursor r = open_task(C, t, lane, &rb);
     uint32_t nb = 0;
     for (;;) {
         int64_t s;
@@ -157,7 +207,14 @@ __global__ void __launch_bounds__(CT) k_conv_count(ConvParams C)
         if (merge_step(C, r, &s, &cnt) == NO_CB) break;
         ++nb;
     }
-    if (lane == 0) C.rb_ptr[rb] = nb;
+    if (lane == 0) C.t_off[t] = nb;
+}
+
+// Row-block pointers from the tasks' first blocks.
+__global__ void k_rb_ptr_from_tasks(ConvParams C)
+{
+    for (int64_t rb = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; rb <= C.nbr; rb += (int64_t)gridDim.x * blockDim.x)
+        C.rb_ptr[rb] = rb < C.nbr ? C.t_off[C.rb_t0[rb]] : (uint32_t)C.B;
 }
 
 // Statistics of the block of the current merge step, on every lane.
@@ -169,7 +226,9 @@ struct BlockStats {
     uint32_t rbase;                 // row-major rank of this lane's first entry
 };
 
-__device__ __forceinline__ BlockStats block_stats(const ConvParams &C, int64_t s, uint32_t cnt, int lane)
+// The per-column fields (maxc, cmask_own, cc_own: a 16 x 16 bit transpose)
+// are formed only when `cols` (warp-uniform) asks for them.
+__device__ __forceinline__ BlockStats block_stats(const ConvParams &C, int64_t s, uint32_t cnt, int lane, bool cols)
 {
     BlockStats b{};
     for (uint32_t i = 0; i < cnt; ++i) b.rmask |= 1u << ((uint32_t)__ldg(C.ci + s + i) & 15u);
@@ -177,10 +236,12 @@ __device__ __forceinline__ BlockStats block_stats(const ConvParams &C, int64_t s
     b.maxr = __reduce_max_sync(FULL, cnt);
     b.cm = __reduce_or_sync(FULL, b.rmask);
     uint32_t maxc = 0;
-    for (int c = 0; c < 16; ++c) {
-        const uint32_t rows = __ballot_sync(FULL, (b.rmask >> c) & 1u) & 0xFFFFu;
-        maxc = max(maxc, (uint32_t)__popc(rows));
-        if (lane == c) { b.cmask_own = rows; b.cc_own = __popc(rows); }
+    if (cols) {
+        for (int c = 0; c < 16; ++c) {
+            const uint32_t rows = __ballot_sync(FULL, (b.rmask >> c) & 1u) & 0xFFFFu;
+            maxc = max(maxc, (uint32_t)__popc(rows));
+            if (lane == c) { b.cmask_own = rows; b.cc_own = __popc(rows); }
+        }
     }
     b.maxc = maxc;
     uint32_t inc = cnt;
@@ -192,21 +253,25 @@ __device__ __forceinline__ BlockStats block_stats(const ConvParams &C, int64_t s
     return b;
 }
 
-// Pass 2: the descriptor of every block.
+// Pass 3: the descriptor of every block.
 __global__ void __launch_bounds__(CT) k_conv_desc(ConvParams C)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t rb = (int64_t)blockIdx.x * (CT / 32) + (threadIdx.x >> 5);
-    if (rb >= C.nbr) return;
-    RowCursor r = open_row(C, rb, lane);
-    uint32_t p = C.rb_ptr[rb];
+    const int64_t t = (int64_t)blockIdx.x * (CT / 32) + (threadIdx.x >> 5);
+    if (t >= C.ntasks) return;
+    int64_t rb;
+    RowCursor r = open_task(C, t, lane, &rb);
+    uint32_t p = C.t_off[t];
     const bool valued = C.va != nullptr;
     for (;; ++p) {
         int64_t s;
         uint32_t cnt;
         const uint32_t cb = merge_step(C, r, &s, &cnt);
         if (cb == NO_CB) break;
-        const BlockStats b = block_stats(C, s, cnt, lane);
+        // the column counts matter only for the skew rule (th0 <= nnz <= th1)
+        const uint32_t nnz_w = __reduce_add_sync(FULL, cnt);
+        const bool skew = C.force_format < 0 && (int)nnz_w >= C.th0 && (int)nnz_w <= C.th1;
+        const BlockStats b = block_stats(C, s, cnt, lane, skew);
         const uint32_t fmt = classify_dev(C, (int)b.nnz, (int)b.maxr, (int)b.maxc);
         uint32_t meta;
         if (fmt == FMT_COO && !valued && b.nnz <= INLINE_MAX_NNZ) {
@@ -228,16 +293,17 @@ __global__ void __launch_bounds__(CT) k_conv_desc(ConvParams C)
     }
 }
 
-// Pass 3: encode every stored block's payload at its offset (the payload
+// Pass 4: encode every stored block's payload at its offset (the payload
 // array is zero-filled first, so padding bytes stay 0).
 __global__ void __launch_bounds__(CT) k_conv_encode(ConvParams C)
 {
     __shared__ uint32_t s_cp[CT / 32][16], s_cm[CT / 32][16];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t rb = (int64_t)blockIdx.x * (CT / 32) + w;
-    if (rb >= C.nbr) return;
-    RowCursor r = open_row(C, rb, lane);
-    uint32_t p = C.rb_ptr[rb];
+    const int64_t t = (int64_t)blockIdx.x * (CT / 32) + w;
+    if (t >= C.ntasks) return;
+    int64_t rb;
+    RowCursor r = open_task(C, t, lane, &rb);
+    uint32_t p = C.t_off[t];
     const bool valued = C.va != nullptr;
     for (;; ++p) {
         int64_t s;
@@ -247,7 +313,8 @@ __global__ void __launch_bounds__(CT) k_conv_encode(ConvParams C)
         const uint2 d = C.desc[p];
         if (meta_inline(d.y)) continue;
         const uint32_t fmt = meta_fmt(d.y);
-        const BlockStats b = block_stats(C, s, cnt, lane);
+        // column masks and pointers: Dense masks, ForceCSC and patched-CSR layouts
+        const BlockStats b = block_stats(C, s, cnt, lane, fmt == FMT_DENSE || fmt == FMT_FCSC || fmt == FMT_PCSR);
         uint8_t *out = reinterpret_cast<uint8_t *>(C.payload + __ldg(C.ref + p));
         float *vals = reinterpret_cast<float *>(out + val_offset(fmt, b.nnz));
         // column pointers (exclusive prefix of the column counts) and masks
@@ -743,29 +810,59 @@ __global__ void __launch_bounds__(CT) k_tile_next(TileParams P)
 }
 
 constexpr int CHAIN_T = 1024;
-constexpr uint32_t CHAIN_WIN = 11264;   // ends staged per window (44 KB)
+constexpr uint32_t CHAIN_WIN = 12288;   // ends staged per window (a multiple of 4: 16-byte loads)
+constexpr size_t CHAIN_SMEM = 4u * CHAIN_WIN * sizeof(uint32_t);   // two windows of ends, two of starts
 
-// One CTA: the tile starts are the chain 0 -> next[0] -> ... < B.  Windows
-// of next[] are staged in shared memory and thread 0 walks them, writing the
-// t-th start over next[t] (t never exceeds the start, and every entry at
-// or past the window's end is still unread).
+// One CTA: the tile starts are the chain 0 -> next[0] -> ... < B.  The ends
+// are staged in shared memory in fixed windows of CHAIN_WIN blocks, two
+// buffers deep: while thread 0 walks window k (a walk leaves a window at
+// most 256 blocks past its end, inside the next one), the other warps stage
+// window k + 1 and copy window k - 1's starts, which the walk collects in
+// shared memory, to next[t] with coalesced stores (t never exceeds the
+// start, so those entries were staged and read already).
 __global__ void __launch_bounds__(CHAIN_T) k_tile_chain(TileParams P)
 {
-    __shared__ uint32_t s_next[CHAIN_WIN];
-    __shared__ uint32_t s_p, s_t;
-    if (threadIdx.x == 0) { s_p = 0; s_t = 0; }
+    extern __shared__ __align__(16) uint32_t chain_smem[];
+    uint32_t *s_next[2] = {chain_smem, chain_smem + CHAIN_WIN};
+    uint32_t *s_st[2] = {chain_smem + 2 * CHAIN_WIN, chain_smem + 3 * CHAIN_WIN};
+    __shared__ uint32_t s_p, s_t, s_n[2], s_t0[2];
+    const uint32_t nwin = (uint32_t)((P.B + CHAIN_WIN - 1) / CHAIN_WIN);
+    // window k into dst: 16-byte loads, all of a thread's in flight together
+    auto stage = [&](uint32_t k, uint32_t *dst, uint32_t tid0, uint32_t nthr) {
+        const int64_t w0 = (int64_t)k * CHAIN_WIN, wl = min((int64_t)CHAIN_WIN, P.B - w0);
+        const uint4 *src4 = reinterpret_cast<const uint4 *>(P.next + w0);
+        uint4 *dst4 = reinterpret_cast<uint4 *>(dst);
+        const int64_t n4 = wl >> 2;
+        constexpr int U = (int)(CHAIN_WIN / 4 / (CHAIN_T - 32)) + 1;
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = (int64_t)(threadIdx.x - tid0) + (int64_t)u * nthr;
+            if (i < n4) v[u] = src4[i];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = (int64_t)(threadIdx.x - tid0) + (int64_t)u * nthr;
+            if (i < n4) dst4[i] = v[u];
+        }
+        for (int64_t i = 4 * n4 + (threadIdx.x - tid0); i < wl; i += nthr) dst[i] = P.next[w0 + i];
+    };
+    auto flush = [&](uint32_t buf, uint32_t tid0, uint32_t nthr) {
+        for (uint32_t i = threadIdx.x - tid0; i < s_n[buf]; i += nthr) P.next[s_t0[buf] + i] = s_st[buf][i];
+    };
+    if (threadIdx.x == 0) { s_p = 0; s_t = 0; s_n[0] = s_n[1] = 0; s_t0[0] = s_t0[1] = 0; }
+    if (nwin) stage(0, s_next[0], 0, blockDim.x);
     __syncthreads();
-    for (;;) {
-        const uint32_t w0 = s_p;
-        if ((int64_t)w0 >= P.B) break;
-        const uint32_t wl = (uint32_t)min((int64_t)CHAIN_WIN, P.B - (int64_t)w0);
-        for (uint32_t i = threadIdx.x; i < wl; i += blockDim.x) s_next[i] = P.next[w0 + i];
-        __syncthreads();
+    uint32_t k = 0;
+    for (; k < nwin; ++k) {
+        const uint32_t *cur = s_next[k & 1];
         if (threadIdx.x == 0) {
-            uint32_t p = w0, t = s_t;
-            while (p < w0 + wl) {
-                const uint32_t e = s_next[p - w0];
-                P.next[t++] = p;
+            const int64_t w0 = (int64_t)k * CHAIN_WIN, w1 = min(w0 + (int64_t)CHAIN_WIN, P.B);
+            uint32_t p = s_p, n = 0;
+            uint32_t *st = s_st[k & 1];
+            while ((int64_t)p < w1) {
+                const uint32_t e = cur[p - (uint32_t)w0];
+                st[n++] = p;
                 if (e <= p || (int64_t)e > P.B) {
                     atomicOr(P.err, ERR_INTERNAL);
                     p = (uint32_t)P.B;
@@ -773,11 +870,19 @@ __global__ void __launch_bounds__(CHAIN_T) k_tile_chain(TileParams P)
                 }
                 p = e;
             }
+            s_t0[k & 1] = s_t;
+            s_n[k & 1] = n;
+            s_t += n;
             s_p = p;
-            s_t = t;
+        } else if (threadIdx.x >= 32) {
+            if (k + 1 < nwin) stage(k + 1, s_next[(k + 1) & 1], 32, blockDim.x - 32);
+            if (k > 0) flush((k - 1) & 1, 32, blockDim.x - 32);
         }
         __syncthreads();
+        if ((int64_t)s_p >= P.B) break;
     }
+    // the walk ends in window k: its starts are still in shared memory
+    if (nwin) flush(min(k, nwin - 1) & 1, 0, blockDim.x);
     if (threadIdx.x == 0) *P.count = s_t;
 }
 
@@ -896,14 +1001,15 @@ dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp
     C.rp = d_rp; C.ci = d_ci; C.va = d_va;
     C.th0 = o.th0; C.th1 = o.th1; C.th2 = o.th2; C.force_format = o.force_format;
     const bool valued = d_va != nullptr;
-    const unsigned grid_rb = (unsigned)((nbr + CT / 32 - 1) / (CT / 32));
 
-    // 1. validation and blocks per row block; block-CSR pointers
-    if (!S.alloc(&d_small, sizeof(Small)) || !S.alloc(&C.rb_ptr, sizeof(uint32_t) * (size_t)(nbr + 1))) return oom();
+    // 1. validation; merge tasks; blocks per task; block-CSR pointers
+    if (!S.alloc(&d_small, sizeof(Small)) || !S.alloc(&C.rb_ptr, sizeof(uint32_t) * (size_t)(nbr + 1)) ||
+        !S.alloc(&C.rb_t0, sizeof(uint32_t) * (size_t)(nbr + 1))) return oom();
     if (cudaMemsetAsync(d_small, 0, sizeof(Small), s) != cudaSuccess ||
-        cudaMemsetAsync(C.rb_ptr, 0, sizeof(uint32_t) * (size_t)(nbr + 1), s) != cudaSuccess) return cuda_fail();
+        cudaMemsetAsync(C.rb_ptr, 0, sizeof(uint32_t) * (size_t)(nbr + 1), s) != cudaSuccess ||
+        cudaMemsetAsync(C.rb_t0, 0, sizeof(uint32_t) * (size_t)(nbr + 1), s) != cudaSuccess) return cuda_fail();
     C.err = &d_small->err;
-    k_conv_count<<<std::max(grid_rb, 1u), CT, 0, s>>>(C);
+    k_conv_validate<<<(unsigned)std::max<int64_t>(1, std::min<int64_t>((m + 7) / 8, (int64_t)sms * 64)), CT, 0, s>>>(C);
     if (cudaGetLastError() != cudaSuccess || !read_small()) return cuda_fail();
     if (h.err & (ERR_PTR | ERR_RANGE | ERR_DUP)) return DBS_ERR_INVALID_ARG;
     if (h.err & ERR_ORDER) { *fallback = true; return DBS_OK; }
@@ -911,20 +1017,36 @@ dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp
     auto agg_bytes = [](int64_t len) { return sizeof(Shift) * (size_t)((len + SCAN_TILE - 1) / SCAN_TILE + 1); };
     char *d_agg = nullptr;
     if (!S.alloc(&d_agg, agg_bytes(nbr))) return oom();
+    k_task_counts<<<grid_for(nbr, sms), 256, 0, s>>>(C);
     {
-        CountScan op{C.rb_ptr, nbr, &d_small->B, C.err};
+        CountScan op{C.rb_t0, nbr, &d_small->T, C.err};
         if (!run_scan(op, nbr, reinterpret_cast<unsigned long long *>(d_agg), s) || !read_small()) return cuda_fail();
+    }
+    const int64_t ntasks = (int64_t)h.T;
+    C.ntasks = ntasks;
+    if (!S.alloc(&C.t_rb, sizeof(uint32_t) * (size_t)ntasks) || !S.alloc(&C.t_off, sizeof(uint32_t) * (size_t)(ntasks + 1)))
+        return oom();
+    if (cudaMemsetAsync(C.t_off, 0, sizeof(uint32_t) * (size_t)(ntasks + 1), s) != cudaSuccess) return cuda_fail();
+    k_task_fill<<<grid_for(nbr, sms), 256, 0, s>>>(C);
+    const unsigned grid_t = (unsigned)((ntasks + CT / 32 - 1) / (CT / 32));
+    if (grid_t) k_conv_count<<<grid_t, CT, 0, s>>>(C);
+    S.release(d_agg);
+    if (!S.alloc(&d_agg, agg_bytes(ntasks))) return oom();
+    {
+        CountScan op{C.t_off, ntasks, &d_small->B, C.err};
+        if (!run_scan(op, ntasks, reinterpret_cast<unsigned long long *>(d_agg), s) || !read_small()) return cuda_fail();
     }
     if (h.err & ERR_SIZE) return DBS_ERR_UNSUPPORTED;
     const int64_t B = (int64_t)h.B;
     C.B = B;
+    k_rb_ptr_from_tasks<<<grid_for(nbr + 1, sms), 256, 0, s>>>(C);
 
     // 2. descriptors, storage counts and payload offsets
     if (!S.alloc(&C.desc, sizeof(uint2) * (size_t)(B + 8)) || !S.alloc(&C.ref, sizeof(uint32_t) * (size_t)(B + 8)))
         return oom();
     if (cudaMemsetAsync(C.desc, 0, sizeof(uint2) * (size_t)(B + 8), s) != cudaSuccess ||
         cudaMemsetAsync(C.ref, 0, sizeof(uint32_t) * (size_t)(B + 8), s) != cudaSuccess) return cuda_fail();
-    if (grid_rb) k_conv_desc<<<grid_rb, CT, 0, s>>>(C);
+    if (grid_t) k_conv_desc<<<grid_t, CT, 0, s>>>(C);
     k_format_counts<<<grid_for(B, sms), 256, 0, s>>>(C.desc, B, d_small->fmt);
     S.release(d_agg);
     if (!S.alloc(&d_agg, agg_bytes(std::max(B, nbc)))) return oom();
@@ -938,8 +1060,11 @@ dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp
     // 3. payload
     if (!S.alloc(&C.payload, (size_t)P * 16)) return oom();
     if (cudaMemsetAsync(C.payload, 0, std::max<size_t>((size_t)P * 16, 16), s) != cudaSuccess) return cuda_fail();
-    if (grid_rb) k_conv_encode<<<grid_rb, CT, 0, s>>>(C);
+    if (grid_t) k_conv_encode<<<grid_t, CT, 0, s>>>(C);
     if (cudaGetLastError() != cudaSuccess) return cuda_fail();
+    S.release(C.rb_t0);
+    S.release(C.t_rb);
+    S.release(C.t_off);
 
     // 4. block-CSC view
     CscParams Q{};
@@ -989,7 +1114,9 @@ dbs_status device_convert(int64_t m, int64_t n, int64_t nnz, const int64_t *d_rp
     T.err = C.err;
     const int64_t warps = (B + 31) / 32;
     if (warps) k_tile_next<<<(unsigned)((warps + CT / 32 - 1) / (CT / 32)), CT, 0, s>>>(T);
-    k_tile_chain<<<1, CHAIN_T, 0, s>>>(T);
+    if (cudaFuncSetAttribute(k_tile_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CHAIN_SMEM) != cudaSuccess)
+        return cuda_fail();
+    k_tile_chain<<<1, CHAIN_T, CHAIN_SMEM, s>>>(T);
     if (cudaGetLastError() != cudaSuccess || !read_small()) return cuda_fail();
     if (h.err) return DBS_ERR_INTERNAL;
     const int64_t NT = (int64_t)h.T;

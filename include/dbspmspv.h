@@ -99,7 +99,8 @@ typedef struct {
                                   block-CSC view, tiles); nothing proportional to the
                                   matrix crosses to the host.  Device memory beyond the
                                   input and the result: 4 B per block + 12 B per column
-                                  block (see build_peak_bytes).  Needs the columns of
+                                  block, or 12 B per row block + 8 B per 4,096 entries
+                                  if more (see build_peak_bytes).  Needs the columns of
                                   every row ascending, else the host converts.  Same
                                   result byte for byte.  Default 0. */
     int32_t dense_spmv;        /* 1 with a valued matrix: also keep a device copy of the
