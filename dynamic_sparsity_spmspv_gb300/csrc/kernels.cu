@@ -426,7 +426,7 @@ __device__ __forceinline__ RowOut mk_heavy(const KParams &P, const uint8_t *b, u
 {
     uint32_t nr = 0;
     const RowOut o = mk_pcsr_col(b, meta_nnz(meta), act, xb, lane, wacc, &nr);
-    if (P.stats) *bytes = 64u + 8u * __reduce_add_sync(FULL, nr);   // structure, then a code byte + value per entry
+    if (P.stats) *bytes = 64u + 5u * __reduce_add_sync(FULL, nr);   // structure, then a code byte + value per entry
     return o;
 }
 
