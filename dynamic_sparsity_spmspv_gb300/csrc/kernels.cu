@@ -513,7 +513,8 @@ __device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint
 {
     const float *vals = reinterpret_cast<const float *>(b + val_offset(FMT_COO, nnz));
     const uint4 *c4 = reinterpret_cast<const uint4 *>(b);
-    uint32_t rows = 0;
+    uint32_t rows = 0, cur = 16u;
+    float acc = 0.0f;
     for (uint32_t base = 0; base < nnz; base += 16u) {
         const uint4 v = __ldg(c4 + (base >> 4));
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
@@ -535,10 +536,22 @@ __device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint
                 if (!((hit >> j) & 1u)) continue;
                 const uint32_t r = ((wv[g] >> (8u * j)) >> 4) & 15u;
                 rows |= 1u << r;
-                if (valued) add(r, av[j] * xx[j]);
+                // entries are in row-major order: a row's run of products is
+                // summed first and handed to `add` once
+                if (valued) {
+                    const float p = av[j] * xx[j];
+                    if (r == cur) {
+                        acc += p;
+                    } else {
+                        if (cur < 16u) add(cur, acc);
+                        cur = r;
+                        acc = p;
+                    }
+                }
             }
         }
     }
+    if (valued && cur < 16u) add(cur, acc);
     return rows;
 }
 
@@ -548,15 +561,26 @@ __device__ __forceinline__ uint32_t coo_lane(const uint8_t *__restrict__ b, uint
 __device__ __forceinline__ uint32_t coo_unit(uint4 u, uint32_t nnz, uint32_t act, const float *xb, float *yr)
 {
     const float v[3] = {__uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
-    uint32_t rows = 0;
+    uint32_t rows = 0, cur = 16u;
+    float acc = 0.0f;
 #pragma unroll
     for (uint32_t j = 0; j < 3u; ++j) {
         const uint32_t e = (u.x >> (8u * j)) & 0xFFu, c = e & 15u, r = e >> 4;
         if (j < nnz && ((act >> c) & 1u)) {
             rows |= 1u << r;
-            atomicAdd(yr + r, v[j] * xval(xb, c));
+            // entries are in row-major order: a row's products are summed
+            // first and added to y once
+            const float p = v[j] * xval(xb, c);
+            if (r == cur) {
+                acc += p;
+            } else {
+                if (cur < 16u) atomicAdd(yr + cur, acc);
+                cur = r;
+                acc = p;
+            }
         }
     }
+    if (cur < 16u) atomicAdd(yr + cur, acc);
     return rows;
 }
 
