@@ -524,7 +524,8 @@ def run_convert(dbs, torch, reps: int):
                 ts.append(time.perf_counter() - t0)
                 inf = M.info()
                 M.close()
-            line[key] = {"seconds": round(min(ts), 4), "build_peak_mb": round(inf["build_peak_bytes"] / 1e6, 1),
+            line[key] = {"seconds": round(min(ts), 4), "seconds_each": [round(t, 4) for t in ts],
+                         "build_peak_mb": round(inf["build_peak_bytes"] / 1e6, 1),
                          "matrix_mb": round(inf["total_bytes"] / 1e6, 1)}
         line["blocks"] = int(inf["nblocks"])
         out.append(line)
@@ -990,14 +991,14 @@ def main():
     if not args.no_configs:
         out["other_workloads"] = run_configs(dbs, torch, dev, stream, flush, 10)
 
+    if args.convert > 0:
+        out["conversion"] = run_convert(dbs, torch, args.convert)
+
     if args.spmv > 0:
         out["dense_input"] = run_spmv(dbs, torch, dev, flush, args.spmv)
 
     if args.decode_layers > 0:
         out["decode"] = run_decode(dbs, torch, dev, stream, args.decode_layers, args.decode_tokens)
-
-    if args.convert > 0:
-        out["conversion"] = run_convert(dbs, torch, args.convert)
 
     if args.ablation > 0:
         out["ablation"] = run_ablation(dbs, torch, dev, stream, flush, args.ablation)
