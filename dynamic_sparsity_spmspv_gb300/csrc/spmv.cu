@@ -189,6 +189,7 @@ dbs_status dbs_spmv_plan_create(int64_t m, int64_t n, int64_t nnz, const int64_t
     if (!p) return DBS_ERR_OOM;
     PlanDev &D = p->D;
     D.m = m; D.n = n; D.nnz = nnz; D.rp = row_ptr; D.ci = col_idx; D.va = vals;
+    D.vec16 = ((reinterpret_cast<uintptr_t>(col_idx) | reinterpret_cast<uintptr_t>(vals)) & 15u) == 0;
     int sms = 0;
     if (cudaGetDevice(&p->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
@@ -196,7 +197,22 @@ dbs_status dbs_spmv_plan_create(int64_t m, int64_t n, int64_t nnz, const int64_t
         delete p;
         return DBS_ERR_CUDA;
     }
-    p->grid = std::max(1, sms * 8);
+    // persistent grid: as many blocks as stay resident together (the items
+    // are dealt out by block index, so a block that waits for a slot would
+    // add its items to the end of the launch)
+    int per_sm = 8;
+    {
+        int o[3] = {0, 0, 0};
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o[0], k_spmv, NT, 0) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o[1], k_spmv_dense<true>, NT, 0) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o[2], k_spmv_dense<false>, NT, 0) != cudaSuccess) {
+            cudaGetLastError();
+            delete p;
+            return DBS_ERR_CUDA;
+        }
+        per_sm = std::min(o[0], std::min(o[1], o[2]));
+    }
+    p->grid = std::max(1, sms * std::max(1, per_sm));
     p->nplan = (uint32_t)((m + PLAN_ROWS - 1) / PLAN_ROWS);
     const size_t max_chunks = (size_t)(nnz / SPMV_CHUNK) + (size_t)(nnz / (LEN_CTA + 1)) + 2;
     const size_t max_split = (size_t)(nnz / (LEN_CTA + 1)) + 1;

@@ -85,6 +85,36 @@ def test_spmv_every_bucket_and_boundary():
         check(A, x, y)
 
 
+@pytest.mark.parametrize("b", range(5))
+def test_spmv_short_row_buckets(b):
+    """Thousands of rows of the 2^b-lane bucket (lengths in (2^(b+1),
+    2^(b+2)], 1 to 4 entries for b = 0), every alignment of a row's first
+    entry, empty rows among them, rows of wider buckets in between, columns
+    outside [0, n) on some entries and a row count that leaves a ragged last
+    item; integer values make the sums exact, so y must equal the oracle's
+    and the plan's bucket count must follow the lengths."""
+    rng = np.random.default_rng(40 + b)
+    lo, hi = (1, 4) if b == 0 else ((4 << b) // 2 + 1, 4 << b)
+    m, n = 5000 + 37 * b, 4096
+    lengths = rng.integers(lo, hi + 1, m)
+    lengths[rng.random(m) < 0.03] = 0
+    other = rng.random(m) < 0.01
+    lengths[other] = rng.integers(hi + 1, 2 * hi + 40, int(other.sum()))
+    A = _shaped(list(lengths), n, 50 + b)
+    vals = rng.integers(-3, 4, A.nnz).astype(np.float32)
+    ci = A.col_idx.copy()
+    ci[rng.random(A.nnz) < 0.01] = n + 3
+    A = synth.CSR(A.m, A.n, A.row_ptr, ci, vals)
+    below = 0 if b == 0 else hi // 2
+    want = int(((lengths > below) & (lengths <= hi)).sum() + (b == 0) * (lengths == 0).sum())
+    assert dbs.SpMVPlan.from_csr(A).info()["lane_group_rows"][str(1 << b)] == want
+    x = rng.integers(-3, 4, n).astype(np.float32)
+    y = torch.full((A.m,), 7.0, dtype=torch.float32, device=DEV)
+    dbs.SpMVPlan.from_csr(A)(torch.from_numpy(x).to(DEV), y=y)
+    ref, _ = oracle.spmv_csr(A, x)
+    np.testing.assert_array_equal(y.cpu().numpy(), ref.astype(np.float32))
+
+
 def test_spmv_integer_values_bit_exact():
     A = synth.random_csr(300, 300, 0.1, 9, integer_values=True)
     x = np.random.default_rng(9).integers(-3, 4, 300).astype(np.float32)
