@@ -189,7 +189,6 @@ dbs_status dbs_spmv_plan_create(int64_t m, int64_t n, int64_t nnz, const int64_t
     if (!p) return DBS_ERR_OOM;
     PlanDev &D = p->D;
     D.m = m; D.n = n; D.nnz = nnz; D.rp = row_ptr; D.ci = col_idx; D.va = vals;
-    D.vec16 = ((reinterpret_cast<uintptr_t>(col_idx) | reinterpret_cast<uintptr_t>(vals)) & 15u) == 0;
     int sms = 0;
     if (cudaGetDevice(&p->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
