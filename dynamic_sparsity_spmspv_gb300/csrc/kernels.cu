@@ -647,6 +647,19 @@ __device__ __forceinline__ uint32_t inline_found(uint32_t meta, uint32_t mm)
     return coord_found(mm, meta) | coord_found(mm, meta >> 8) | coord_found(mm, meta >> 16);
 }
 
+// inline_found without the row extraction: coordinate byte s's found bit
+// goes to bit ((s >> 4) & 31), i.e. row or row + 16 depending on the low bit
+// of the next byte; fold16 brings the two halves together once per run.
+__device__ __forceinline__ uint32_t coord_found_w(uint32_t mm, uint32_t s)
+{
+    return __funnelshift_l(0u, __funnelshift_r(mm, mm, s) & 1u, s >> 4);
+}
+__device__ __forceinline__ uint32_t inline_found_w(uint32_t meta, uint32_t mm)
+{
+    return coord_found_w(mm, meta) | coord_found_w(mm, meta >> 8) | coord_found_w(mm, meta >> 16);
+}
+__device__ __forceinline__ uint32_t fold16(uint32_t f) { return (f | (f >> 16)) & 0xFFFFu; }
+
 // Rows of a COO block reached from its active columns: 16 coordinates per
 // 16-byte unit, the first `cnt` of them valid.
 __device__ __forceinline__ uint32_t coo_found16(uint4 v, uint32_t mm, uint32_t cnt)
@@ -1041,13 +1054,18 @@ __device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, con
     };
     // units holding at least one block of the tile (block 2u < p0 + count);
     // the descriptor array has padding past B, so a unit's second block may
-    // lie one past the last block
+    // lie one past the last block.  A unit's block outside the tile (the one
+    // before an odd p0, the one after the last block) is zeroed: column
+    // block 0, local row block 0, a stored block with no columns, so it
+    // finds nothing and the loop needs no range test per block.
     auto load_desc = [&](const uint4 &tdd, uint4 (&dd)[WU]) {
         const uint32_t u0 = tdd.x >> 1, end = tdd.x + (tdd.w >> TILE_NBLK_SHIFT);
 #pragma unroll
         for (int j = 0; j < WU; ++j) {
             const uint32_t u = u0 + (uint32_t)(j * 32 + lane);
             dd[j] = 2u * u < end ? __ldcs(desc4 + u) : z4;
+            if (2u * u < tdd.x) { dd[j].x = 0u; dd[j].y = 0u; }
+            if (2u * u + 1u >= end) { dd[j].z = 0u; dd[j].w = 0u; }
         }
     };
     // queued entries [0, n) decoded, one per lane, their rows combined per
@@ -1094,9 +1112,8 @@ __device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, con
         uint32_t mp[WU];   // the eight column-block masks, two per register
 #pragma unroll
         for (int j = 0; j < WU; ++j) {
-            const int li = lbase + 64 * j;
-            const uint32_t a = li >= 0 && li < (int)nblk ? (uint32_t)__ldca(xm16 + (d[j].x & DESC_COL_MASK)) : 0u;
-            const uint32_t b = li + 1 < (int)nblk ? (uint32_t)__ldca(xm16 + (d[j].z & DESC_COL_MASK)) : 0u;
+            const uint32_t a = (uint32_t)__ldca(xm16 + (d[j].x & DESC_COL_MASK));
+            const uint32_t b = (uint32_t)__ldca(xm16 + (d[j].z & DESC_COL_MASK));
             mp[j] = a | (b << 16);
         }
         uint32_t vrow_n = 0;
@@ -1105,23 +1122,25 @@ __device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, con
         load_desc(td_n, d_n);
         __syncwarp();
 
+        // acc holds found rows at row or row + 16 (inline_found_w), folded
+        // when a run ends
         uint32_t acc = 0, cur = 0;
 #pragma unroll
         for (int k = 0; k < 2 * WU; ++k) {
             const int li = lbase + 64 * (k >> 1) + (k & 1);
-            const bool valid = li >= 0 && li < (int)nblk;
             const uint32_t dx = (k & 1) ? d[k >> 1].z : d[k >> 1].x;
             const uint32_t meta = (k & 1) ? d[k >> 1].w : d[k >> 1].y;
-            const uint32_t mk = (mp[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu, lrb = dx >> DESC_LRB_SHIFT;
+            // the block's column mask held twice (both 16-bit halves)
+            const uint32_t mm = __byte_perm(mp[k >> 1], 0u, (k & 1) ? 0x3232u : 0x1010u), lrb = dx >> DESC_LRB_SHIFT;
             const bool inl = meta_inline(meta);
-            const uint32_t f = inl ? inline_found(meta, dup16(mk)) : 0u;
-            if (valid && lrb != cur) {
-                if (acc) atomicOr(&W.rm[cur], acc);
+            const uint32_t f = inl ? inline_found_w(meta, mm) : 0u;
+            if (lrb != cur) {
+                if (acc) atomicOr(&W.rm[cur], fold16(acc));
                 acc = 0u;
                 cur = lrb;
             }
             acc |= f;
-            const uint32_t a = inl ? 0u : mk & meta & 0xFFFFu;
+            const uint32_t a = inl ? 0u : mm & meta & 0xFFFFu;
             if (a) {
                 const uint32_t slot = atomicAdd(&W.nq, 1u);
                 W.qe[slot] = p0 + (uint32_t)li;
@@ -1129,17 +1148,18 @@ __device__ void pull_bool(const KParams &P, SmemT<1> &S, const uint32_t *xm, con
                 W.qr[slot] = rb0 + lrb;
             }
             if (ST) {
-                if (mk) { ++c_vis; c_touch += meta_nnz(meta); }
+                const bool valid = li >= 0 && li < (int)nblk;
+                if (valid && (mm & 0xFFFFu)) { ++c_vis; c_touch += meta_nnz(meta); }
                 if (f || a) ++c_hit;
             }
         }
         // the lanes' last runs: one OR for the warp when they share a row block
         const uint32_t c0 = __shfl_sync(FULL, cur, 0);
         if (__all_sync(FULL, cur == c0 || acc == 0u)) {
-            const uint32_t r = __reduce_or_sync(FULL, acc);
+            const uint32_t r = fold16(__reduce_or_sync(FULL, acc));
             if (lane == 0 && r) atomicOr(&W.rm[c0], r);
         } else if (acc) {
-            atomicOr(&W.rm[cur], acc);
+            atomicOr(&W.rm[cur], fold16(acc));
         }
         __syncwarp();
 
