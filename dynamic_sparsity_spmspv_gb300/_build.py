@@ -21,12 +21,14 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 SOURCES_CU = ["kernels.cu", "spmv.cu", "build_gpu.cu"]
 SOURCES_CPP = ["matrix.cpp"]
-HEADERS = ["format.h", "internal.h"]
 
 
 def _newest_input() -> float:
-    paths = [os.path.join(CSRC, f) for f in SOURCES_CU + SOURCES_CPP + HEADERS]
-    paths.append(os.path.join(INCLUDE, "dbspmspv.h"))
+    """Latest modification time over every source and header the library is
+    built from (all of csrc/ and include/), so that an edited header always
+    triggers a rebuild."""
+    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp", ".h", ".cuh"))]
+    paths += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return max(os.path.getmtime(p) for p in paths)
 
 
