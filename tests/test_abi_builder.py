@@ -34,6 +34,24 @@ def test_library_exports_every_declared_function():
         assert name in _lib.PROTOTYPES, f"binding lacks {name}"
 
 
+def test_library_is_rebuilt_after_any_source_or_header_changes(monkeypatch):
+    """The in-tree build is redone when any file under csrc/ or include/ is
+    newer than the library: a later modification time faked for each file in
+    turn (the files themselves are not touched) must make the library stale."""
+    from dynamic_sparsity_spmspv_gb300 import _build
+    lib_t = os.path.getmtime(_build.LIB)
+    files = [os.path.join(_build.CSRC, f) for f in os.listdir(_build.CSRC)
+             if f.endswith((".cu", ".cpp", ".h", ".cuh"))]
+    files += [os.path.join(_build.INCLUDE, f) for f in os.listdir(_build.INCLUDE) if f.endswith(".h")]
+    assert any(f.endswith("spmv_dev.h") for f in files)
+    real = os.path.getmtime
+    for f in files:
+        monkeypatch.setattr(os.path, "getmtime", lambda p, f=f: lib_t + 10.0 if p == f else real(p))
+        assert _build._newest_input() > lib_t, f
+    monkeypatch.setattr(os.path, "getmtime", real)
+    assert _build._newest_input() <= lib_t
+
+
 def test_status_strings_and_version():
     lib = _lib.load()
     assert lib.dbs_status_string(4) == b"DBS_ERR_TIMEOUT"
